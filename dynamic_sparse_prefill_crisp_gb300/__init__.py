@@ -1,0 +1,215 @@
+"""Python binding of the CRISP sparse-prefill C ABI (``include/crisp.h``).
+
+Argument marshalling only: every step runs in the CUDA kernels of
+``libcrisp.so``. Tensors are passed by ``data_ptr()``; PyTorch provides the
+device memory and the stream. Each wrapper raises :class:`CrispError` when the
+library returns a non-OK status. Importing succeeds without a GPU; calling a
+step without the built library raises immediately (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcrisp.so")
+_lib = None
+
+B = 128
+D = 128
+
+STATUS_NAMES = {0: "CRISP_OK", 1: "CRISP_ERR_INVALID_ARG", 2: "CRISP_ERR_SHAPE", 3: "CRISP_ERR_ALIGN",
+                4: "CRISP_ERR_WORKSPACE", 5: "CRISP_ERR_CUDA", 6: "CRISP_ERR_TIMEOUT", 7: "CRISP_ERR_DEVICE"}
+PE_GAMMA, PE_NOISE = 0, 1
+
+
+class CrispError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("hq", ctypes.c_int32), ("hkv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("seq_len", ctypes.c_int32), ("block", ctypes.c_int32),
+                ("q_head_stride", ctypes.c_int64), ("q_tok_stride", ctypes.c_int64),
+                ("kv_head_stride", ctypes.c_int64), ("kv_tok_stride", ctypes.c_int64),
+                ("o_head_stride", ctypes.c_int64), ("o_tok_stride", ctypes.c_int64),
+                ("scale", ctypes.c_float)]
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("tau_num", ctypes.c_uint32), ("tau_den", ctypes.c_uint32),
+                ("alpha_num", ctypes.c_uint32), ("alpha_den", ctypes.c_uint32),
+                ("gamma_num", ctypes.c_uint32), ("gamma_den", ctypes.c_uint32),
+                ("kmin_blocks", ctypes.c_int32), ("pe_mode", ctypes.c_int32)]
+
+
+class LayerViews(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in
+                ("pmap", "vmass", "smass", "cstruct", "total", "route", "vbits", "sbits", "pbar", "pebits",
+                 "rowbits", "counts")]
+
+
+def lib():
+    """The loaded libcrisp.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with dynamic_sparse_prefill_crisp_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
+        P = ctypes.POINTER
+        L.crisp_params_default.argtypes = [P(Params)]
+        L.crisp_params_default.restype = None
+        L.crisp_workspace_size.argtypes = [P(Shape), P(sz)]
+        L.crisp_layer_workspace_size.argtypes = [P(Shape), P(sz)]
+        L.crisp_workspace_init.argtypes = [vp, sz, st]
+        L.crisp_proxy_map.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
+        L.crisp_block_masses.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
+        L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
+        L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
+        L.crisp_pe_map.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
+        L.crisp_select_pe.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, sz, st]
+        L.crisp_build_mask.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, st]
+        L.crisp_sparse_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, st]
+        L.crisp_dense_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
+        L.crisp_layer_views_get.argtypes = [P(Shape), vp, P(LayerViews)]
+        L.crisp_prefill_layer.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, sz, st]
+        L.crisp_read_status.argtypes = [vp, st, P(ctypes.c_int)]
+        L.crisp_status_string.argtypes = [ctypes.c_int]
+        L.crisp_status_string.restype = ctypes.c_char_p
+        for name in ("crisp_workspace_size", "crisp_layer_workspace_size", "crisp_workspace_init", "crisp_proxy_map",
+                     "crisp_block_masses", "crisp_route_cstruct", "crisp_select_vs", "crisp_pe_map",
+                     "crisp_select_pe", "crisp_build_mask", "crisp_sparse_prefill", "crisp_dense_prefill",
+                     "crisp_layer_views_get", "crisp_prefill_layer", "crisp_read_status"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().crisp_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise CrispError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr() if hasattr(t, "data_ptr") else int(t))
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def make_shape(hq, hkv, n, q=None, k=None, out=None, scale=0.0) -> Shape:
+    """Shape for [heads][tokens][128] tensors; strides are taken from the
+    tensors when given (any layout with the 128 features contiguous)."""
+    def strides(t, heads):
+        if t is None:
+            return n * D, D
+        assert t.dim() == 3 and t.shape[0] == heads and t.shape[1] == n and t.shape[2] == D and t.stride(2) == 1
+        return t.stride(0), t.stride(1)
+    qs, ks, os_ = strides(q, hq), strides(k, hkv), strides(out, hq)
+    return Shape(hq, hkv, D, n, B, qs[0], qs[1], ks[0], ks[1], os_[0], os_[1], scale)
+
+
+def params_default(**overrides) -> Params:
+    p = Params()
+    lib().crisp_params_default(ctypes.byref(p))
+    for key, val in overrides.items():
+        if key in ("alpha", "tau", "gamma"):
+            setattr(p, f"{key}_num", val[0])
+            setattr(p, f"{key}_den", val[1])
+        else:
+            setattr(p, key, val)
+    return p
+
+
+def workspace_size(shape: Shape) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().crisp_workspace_size(ctypes.byref(shape), ctypes.byref(n)), "crisp_workspace_size")
+    return n.value
+
+
+def layer_workspace_size(shape: Shape) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().crisp_layer_workspace_size(ctypes.byref(shape), ctypes.byref(n)), "crisp_layer_workspace_size")
+    return n.value
+
+
+def workspace_init(ws, stream=None):
+    _check(lib().crisp_workspace_init(_ptr(ws), _nbytes(ws), _stream(stream)), "crisp_workspace_init")
+
+
+def proxy_map(shape, q, k, pmap, ws, stream=None):
+    _check(lib().crisp_proxy_map(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(pmap), _ptr(ws), _nbytes(ws),
+                                 _stream(stream)), "crisp_proxy_map")
+
+
+def block_masses(shape, pmap, vmass, smass, ws, stream=None):
+    _check(lib().crisp_block_masses(ctypes.byref(shape), _ptr(pmap), _ptr(vmass), _ptr(smass), _ptr(ws), _nbytes(ws),
+                                    _stream(stream)), "crisp_block_masses")
+
+
+def route_cstruct(shape, params, vmass, cstruct, total, route, stream=None):
+    _check(lib().crisp_route_cstruct(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(cstruct),
+                                     _ptr(total), _ptr(route), _stream(stream)), "crisp_route_cstruct")
+
+
+def select_vs(shape, params, vmass, smass, route, vbits, sbits, ws, stream=None):
+    _check(lib().crisp_select_vs(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(smass), _ptr(route),
+                                 _ptr(vbits), _ptr(sbits), _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_select_vs")
+
+
+def pe_map(shape, q, k, route, pbar, ws, stream=None):
+    _check(lib().crisp_pe_map(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(route), _ptr(pbar), _ptr(ws), _nbytes(ws),
+                              _stream(stream)), "crisp_pe_map")
+
+
+def select_pe(shape, params, pbar, route, pebits, ws, stream=None):
+    _check(lib().crisp_select_pe(ctypes.byref(shape), ctypes.byref(params), _ptr(pbar), _ptr(route), _ptr(pebits),
+                                 _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_select_pe")
+
+
+def build_mask(shape, route, vbits, sbits, pebits, rowbits, counts, ws, stream=None):
+    _check(lib().crisp_build_mask(ctypes.byref(shape), _ptr(route), _ptr(vbits), _ptr(sbits), _ptr(pebits),
+                                  _ptr(rowbits), _ptr(counts), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "crisp_build_mask")
+
+
+def sparse_prefill(shape, q, k, v, rowbits, counts, out, ws, stream=None):
+    _check(lib().crisp_sparse_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(rowbits), _ptr(counts),
+                                      _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_sparse_prefill")
+
+
+def dense_prefill(shape, q, k, v, out, ws, stream=None):
+    _check(lib().crisp_dense_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(ws),
+                                     _nbytes(ws), _stream(stream)), "crisp_dense_prefill")
+
+
+def layer_views(shape, ws) -> dict:
+    v = LayerViews()
+    _check(lib().crisp_layer_views_get(ctypes.byref(shape), _ptr(ws), ctypes.byref(v)), "crisp_layer_views_get")
+    return {name: getattr(v, name) for name, _ in LayerViews._fields_}
+
+
+def prefill_layer(shape, params, q, k, v, out, ws, stream=None):
+    _check(lib().crisp_prefill_layer(ctypes.byref(shape), ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                     _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_prefill_layer")
+
+
+def read_status(ws, stream=None) -> int:
+    s = ctypes.c_int()
+    _check(lib().crisp_read_status(_ptr(ws), _stream(stream), ctypes.byref(s)), "crisp_read_status")
+    return s.value

@@ -1,0 +1,378 @@
+// Host side of the C ABI declared in include/crisp.h: argument validation,
+// workspace layout, TMA descriptors and the launch sequence of each step.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace crisp {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+crisp_status check_shape(const crisp_shape* s) {
+  if (!s) return CRISP_ERR_INVALID_ARG;
+  if (s->hq <= 0 || s->hkv <= 0 || s->hq % s->hkv != 0) return CRISP_ERR_SHAPE;
+  if (s->head_dim != kD || s->block != kB) return CRISP_ERR_SHAPE;
+  if (s->seq_len < 2 * kB || s->seq_len > kMaxSeq || s->seq_len % kB != 0) return CRISP_ERR_SHAPE;
+  if (s->hq > 4096) return CRISP_ERR_SHAPE;
+  const int64_t strides[6] = {s->q_head_stride, s->q_tok_stride, s->kv_head_stride,
+                              s->kv_tok_stride, s->o_head_stride, s->o_tok_stride};
+  for (int64_t st : strides)
+    if (st <= 0 || st % 8 != 0 || st > (int64_t(1) << 38)) return CRISP_ERR_ALIGN;
+  if (s->q_tok_stride < kD || s->kv_tok_stride < kD || s->o_tok_stride < kD) return CRISP_ERR_SHAPE;
+  if (!(s->scale >= 0.f) || std::isinf(s->scale)) return CRISP_ERR_INVALID_ARG;
+  return CRISP_OK;
+}
+
+crisp_status check_params(const crisp_params* p) {
+  if (!p) return CRISP_ERR_INVALID_ARG;
+  if (p->tau_den == 0 || p->tau_num > p->tau_den) return CRISP_ERR_INVALID_ARG;
+  if (p->alpha_den == 0 || p->alpha_den > 65535u || p->alpha_num > 65535u) return CRISP_ERR_INVALID_ARG;
+  if (p->gamma_den == 0 || p->gamma_num > p->gamma_den) return CRISP_ERR_INVALID_ARG;
+  if (p->kmin_blocks < 0 || p->kmin_blocks > kMaxBlocks) return CRISP_ERR_INVALID_ARG;
+  if (p->pe_mode != CRISP_PE_GAMMA && p->pe_mode != CRISP_PE_NOISE) return CRISP_ERR_INVALID_ARG;
+  return CRISP_OK;
+}
+
+crisp_shape normalised(const crisp_shape& s) {
+  crisp_shape t = s;
+  if (t.scale == 0.f) t.scale = 1.0f / std::sqrt(static_cast<float>(kD));
+  return t;
+}
+
+crisp_status check_device() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CRISP_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return CRISP_ERR_CUDA;
+  return (major == 10 && minor == 3) ? CRISP_OK : CRISP_ERR_DEVICE;
+}
+
+crisp_status check_ws(const crisp_shape& s, const void* ws, size_t ws_bytes) {
+  if (!ws || !aligned(ws, kAlign)) return ws ? CRISP_ERR_ALIGN : CRISP_ERR_WORKSPACE;
+  return ws_bytes >= scratch_layout(s).total ? CRISP_OK : CRISP_ERR_WORKSPACE;
+}
+
+typedef CUresult (*EncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver entry point is looked up once; it is a constant afterwards.
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// bf16 [heads][n][128] with element strides; boxes of 64 features x 128 tokens
+// (one 128-byte swizzle row per token).
+crisp_status make_map(CUtensorMap* m, const void* ptr, int heads, int n, int64_t hs, int64_t ts) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return CRISP_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ts) * 2, static_cast<cuuint64_t>(hs) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kB), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CRISP_OK : CRISP_ERR_ALIGN;
+}
+
+crisp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CRISP_OK : CRISP_ERR_CUDA; }
+
+}  // namespace
+
+ScratchLayout scratch_layout(const crisp_shape& s) {
+  const size_t hq = s.hq, hkv = s.hkv, nb = num_blocks(s.seq_len), W = bit_words(static_cast<int>(nb));
+  const size_t chunks = proxy_chunks(static_cast<int>(nb));
+  ScratchLayout L{};
+  size_t o = 0;
+  L.status = o;      o = up(o + sizeof(DevStatus));
+  L.proxy_part = o;  o = up(o + hq * kB * 2 * chunks * sizeof(float2));
+  L.proxy_stats = o; o = up(o + hq * kB * sizeof(float2));
+  L.mass_lower = o;  o = up(o + hq * nb * 8);
+  L.mass_upper = o;  o = up(o + hq * nb * 8);
+  L.qbar = o;        o = up(o + hq * nb * kD * 4);
+  L.kbar = o;        o = up(o + hkv * nb * kD * 4);
+  L.srev = o;        o = up(o + hq * (W + 2) * 4);
+  L.order = o;       o = up(o + hq * nb * 4);
+  L.bucket = o;      o = up(o + (nb + 2) * 4);
+  L.total = o;
+  return L;
+}
+
+LayerLayout layer_layout(const crisp_shape& s) {
+  const size_t hq = s.hq, n = s.seq_len, nb = num_blocks(s.seq_len), W = bit_words(static_cast<int>(nb));
+  LayerLayout L{};
+  size_t o = scratch_layout(s).total;
+  L.pmap = o;       o = up(o + hq * kB * n * 4);
+  L.vmass = o;      o = up(o + hq * nb * 8);
+  L.smass = o;      o = up(o + hq * nb * 8);
+  L.cstruct = o;    o = up(o + hq * 8);
+  L.total_mass = o; o = up(o + hq * 8);
+  L.route = o;      o = up(o + hq);
+  L.vbits = o;      o = up(o + hq * W * 4);
+  L.sbits = o;      o = up(o + hq * W * 4);
+  L.pbar = o;       o = up(o + hq * nb * nb * 4);
+  L.pebits = o;     o = up(o + hq * nb * W * 4);
+  L.rowbits = o;    o = up(o + hq * nb * W * 4);
+  L.counts = o;     o = up(o + hq * nb * 4);
+  L.total = o;
+  return L;
+}
+
+}  // namespace crisp
+
+using namespace crisp;
+
+extern "C" {
+
+void crisp_params_default(crisp_params* p) {
+  if (!p) return;
+  p->tau_num = 1;
+  p->tau_den = 5;
+  p->alpha_num = 1;
+  p->alpha_den = 1;
+  p->gamma_num = 19;
+  p->gamma_den = 20;
+  p->kmin_blocks = 8;
+  p->pe_mode = CRISP_PE_GAMMA;
+}
+
+crisp_status crisp_workspace_size(const crisp_shape* shape, size_t* bytes) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!bytes) return CRISP_ERR_INVALID_ARG;
+  *bytes = scratch_layout(*shape).total;
+  return CRISP_OK;
+}
+
+crisp_status crisp_layer_workspace_size(const crisp_shape* shape, size_t* bytes) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!bytes) return CRISP_ERR_INVALID_ARG;
+  *bytes = layer_layout(*shape).total;
+  return CRISP_OK;
+}
+
+crisp_status crisp_workspace_init(void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  if (!ws) return CRISP_ERR_WORKSPACE;
+  if (ws_bytes < sizeof(DevStatus)) return CRISP_ERR_WORKSPACE;
+  return from_cuda(cudaMemsetAsync(ws, 0, sizeof(DevStatus), stream));
+}
+
+crisp_status crisp_proxy_map(const crisp_shape* shape, const void* q, const void* k, float* pmap, void* ws,
+                             size_t ws_bytes, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!q || !k || !pmap) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(pmap)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  TmaMaps maps;
+  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  maps.v = maps.k;
+  return from_cuda(launch_proxy(s, maps, pmap, static_cast<char*>(ws), stream));
+}
+
+crisp_status crisp_block_masses(const crisp_shape* shape, const float* pmap, uint64_t* vmass, uint64_t* smass,
+                                void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!pmap || !vmass || !smass) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(pmap) || !aligned(vmass, 8) || !aligned(smass, 8)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  return from_cuda(launch_block_masses(s, pmap, vmass, smass, static_cast<char*>(ws), stream));
+}
+
+crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
+                                 uint64_t* cstruct, uint64_t* total, uint8_t* route, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if ((st = check_params(params)) != CRISP_OK) return st;
+  if (!vmass || !cstruct || !total || !route) return CRISP_ERR_INVALID_ARG;
+  if (!aligned(vmass, 8) || !aligned(cstruct, 8) || !aligned(total, 8)) return CRISP_ERR_ALIGN;
+  if ((st = check_device()) != CRISP_OK) return st;
+  return from_cuda(launch_route(normalised(*shape), *params, vmass, cstruct, total, route, stream));
+}
+
+crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
+                             const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
+                             void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if ((st = check_params(params)) != CRISP_OK) return st;
+  if (!vmass || !smass || !route || !vbits || !sbits) return CRISP_ERR_INVALID_ARG;
+  if (!aligned(vmass, 8) || !aligned(smass, 8) || !aligned(vbits, 4) || !aligned(sbits, 4)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, stream));
+}
+
+crisp_status crisp_pe_map(const crisp_shape* shape, const void* q, const void* k, const uint8_t* route, float* pbar,
+                          void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!q || !k || !route || !pbar) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(pbar)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  return from_cuda(launch_pe_map(s, q, k, route, pbar, static_cast<char*>(ws), stream));
+}
+
+crisp_status crisp_select_pe(const crisp_shape* shape, const crisp_params* params, const float* pbar,
+                             const uint8_t* route, uint32_t* pebits, void* ws, size_t ws_bytes,
+                             crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if ((st = check_params(params)) != CRISP_OK) return st;
+  if (!pbar || !route || !pebits) return CRISP_ERR_INVALID_ARG;
+  if (!aligned(pbar, 4) || !aligned(pebits, 4)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  return from_cuda(launch_select_pe(s, *params, pbar, route, pebits, stream));
+}
+
+crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t* route, const uint32_t* vbits,
+                              const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits, int32_t* counts,
+                              void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!route || !vbits || !sbits || !pebits || !rowbits || !counts) return CRISP_ERR_INVALID_ARG;
+  if (!aligned(vbits, 4) || !aligned(sbits, 4) || !aligned(pebits, 4) || !aligned(rowbits, 4) || !aligned(counts, 4))
+    return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  return from_cuda(launch_build_mask(s, route, vbits, sbits, pebits, rowbits, counts, static_cast<char*>(ws), stream));
+}
+
+static crisp_status attention_common(const crisp_shape* shape, const void* q, const void* k, const void* v,
+                                     const uint32_t* rowbits, const int32_t* counts, void* out, void* ws,
+                                     size_t ws_bytes, crisp_stream_t stream, bool dense) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!q || !k || !v || !out || (!dense && (!rowbits || !counts))) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
+  if (!dense && (!aligned(rowbits, 4) || !aligned(counts, 4))) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  TmaMaps maps;
+  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  return from_cuda(launch_attention(s, maps, rowbits, counts, out, static_cast<char*>(ws), dense, stream));
+}
+
+crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v,
+                                  const uint32_t* rowbits, const int32_t* counts, void* out, void* ws,
+                                  size_t ws_bytes, crisp_stream_t stream) {
+  return attention_common(shape, q, k, v, rowbits, counts, out, ws, ws_bytes, stream, false);
+}
+
+crisp_status crisp_dense_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v, void* out,
+                                 void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  return attention_common(shape, q, k, v, nullptr, nullptr, out, ws, ws_bytes, stream, true);
+}
+
+crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws, crisp_layer_views* views) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!ws || !views) return CRISP_ERR_INVALID_ARG;
+  const LayerLayout L = layer_layout(*shape);
+  char* b = static_cast<char*>(ws);
+  views->pmap = reinterpret_cast<float*>(b + L.pmap);
+  views->vmass = reinterpret_cast<uint64_t*>(b + L.vmass);
+  views->smass = reinterpret_cast<uint64_t*>(b + L.smass);
+  views->cstruct = reinterpret_cast<uint64_t*>(b + L.cstruct);
+  views->total = reinterpret_cast<uint64_t*>(b + L.total_mass);
+  views->route = reinterpret_cast<uint8_t*>(b + L.route);
+  views->vbits = reinterpret_cast<uint32_t*>(b + L.vbits);
+  views->sbits = reinterpret_cast<uint32_t*>(b + L.sbits);
+  views->pbar = reinterpret_cast<float*>(b + L.pbar);
+  views->pebits = reinterpret_cast<uint32_t*>(b + L.pebits);
+  views->rowbits = reinterpret_cast<uint32_t*>(b + L.rowbits);
+  views->counts = reinterpret_cast<int32_t*>(b + L.counts);
+  return CRISP_OK;
+}
+
+crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* params, const void* q, const void* k,
+                                 const void* v, void* out, void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if ((st = check_params(params)) != CRISP_OK) return st;
+  if (!q || !k || !v || !out) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if (!ws) return CRISP_ERR_WORKSPACE;
+  if (!aligned(ws, kAlign)) return CRISP_ERR_ALIGN;
+  if (ws_bytes < layer_layout(s).total) return CRISP_ERR_WORKSPACE;
+  if ((st = check_device()) != CRISP_OK) return st;
+  crisp_layer_views w;
+  crisp_layer_views_get(&s, ws, &w);
+  TmaMaps maps;
+  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  char* wsb = static_cast<char*>(ws);
+  if (launch_proxy(s, maps, w.pmap, wsb, stream) != cudaSuccess ||
+      launch_block_masses(s, w.pmap, w.vmass, w.smass, wsb, stream) != cudaSuccess ||
+      launch_route(s, *params, w.vmass, w.cstruct, w.total, w.route, stream) != cudaSuccess ||
+      launch_select_vs(s, *params, w.vmass, w.smass, w.route, w.vbits, w.sbits, stream) != cudaSuccess ||
+      launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess ||
+      launch_select_pe(s, *params, w.pbar, w.route, w.pebits, stream) != cudaSuccess ||
+      launch_build_mask(s, w.route, w.vbits, w.sbits, w.pebits, w.rowbits, w.counts, wsb, stream) != cudaSuccess ||
+      launch_attention(s, maps, w.rowbits, w.counts, out, wsb, false, stream) != cudaSuccess)
+    return CRISP_ERR_CUDA;
+  return CRISP_OK;
+}
+
+crisp_status crisp_read_status(const void* ws, crisp_stream_t stream, crisp_status* status) {
+  if (!ws || !status) return CRISP_ERR_INVALID_ARG;
+  DevStatus host{};
+  if (cudaMemcpyAsync(&host, ws, sizeof(host), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return CRISP_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CRISP_ERR_CUDA;
+  *status = static_cast<crisp_status>(host.code);
+  return CRISP_OK;
+}
+
+const char* crisp_status_string(crisp_status status) {
+  switch (status) {
+    case CRISP_OK: return "ok";
+    case CRISP_ERR_INVALID_ARG: return "invalid argument";
+    case CRISP_ERR_SHAPE: return "unsupported shape";
+    case CRISP_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case CRISP_ERR_WORKSPACE: return "workspace missing or too small";
+    case CRISP_ERR_CUDA: return "CUDA runtime error";
+    case CRISP_ERR_TIMEOUT: return "device wait timed out";
+    case CRISP_ERR_DEVICE: return "device is not sm_103";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,347 @@
+// A8/A9. Causal GQA block-sparse (or dense) attention on the 5th-generation
+// tensor cores (CRISP paper page on ai.info, "Why This Matters": exact
+// softmax attention over the blocks the method selects; the dense path is the
+// exact FlashAttention-style baseline the paper measures against).
+//
+// One CTA per (head h, query block qb), two CTAs per SM so that one CTA's
+// softmax overlaps the other's matrix products. Per selected key block kb:
+//   S  = Q K_kb^T        tcgen05.mma, A = Q (smem), B = K (smem), D = S (TMEM)
+//   P  = 2^(S*c - m)     softmax warps: TMEM -> registers -> bf16 -> TMEM (over S)
+//   O += P V_kb          tcgen05.mma, A = P (TMEM), B = V (smem, MN-major), D = O (TMEM)
+// K and V tiles arrive by TMA at row coordinate kb*128 (gather by block index).
+// The running max m is raised lazily: O and the row sum are rescaled only when
+// a block's max exceeds m by more than 2^8, which keeps every exponent <= 2^8
+// and leaves O/l exact.
+//
+// Warp roles: 0-3 softmax + epilogue (warp w owns TMEM lanes / rows 32w..32w+31),
+// 4 TMA producer, 5 MMA issuer (and TMEM owner).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace crisp {
+using namespace ptx;
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTmaWarp = 4, kMmaWarp = 5;
+constexpr uint32_t kTile = kB * kD * 2;  // 32 KB bf16 tile
+constexpr uint32_t kHalf = kTile / 2;
+constexpr uint32_t kSmemBytes = 1024 + 3 * kTile;  // Q, K, V (+ alignment slack)
+constexpr uint32_t kTmemCols = 256;                // S/P [0,128), O [128,256)
+constexpr float kRescaleLog2 = 8.0f;
+
+struct Bars {
+  uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, o_full, drain;
+  uint32_t tmem_base;
+  int count;
+  int has_diag;
+  int abort;
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* abort) {
+  const bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void fail(int* abort, DevStatus* st, uint32_t where) {
+  *reinterpret_cast<volatile int*>(abort) = 1;
+  report_error(st, CRISP_ERR_TIMEOUT, where);
+}
+
+// Bits of row word w restricted to key blocks <= qb.
+__device__ __forceinline__ uint32_t row_word(const uint32_t* row, bool dense, int w, int qb) {
+  uint32_t bits = dense ? 0xffffffffu : row[w];
+  if (w == (qb >> 5) && (qb & 31) != 31) bits &= (1u << ((qb & 31) + 1)) - 1u;
+  return bits;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    attention_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tv, int n, int hq, int group, float c_log2,
+                     const uint32_t* __restrict__ rowbits, const int32_t* __restrict__ order, int dense,
+                     __nv_bfloat16* __restrict__ out, int64_t o_hs, int64_t o_ts, DevStatus* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* sK = base + kTile;
+  uint8_t* sV = base + 2 * kTile;
+  __shared__ Bars bars;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = n / kB, W = (nb + 31) / 32;
+  // Work item: rows in order[] (longest first) or, dense, qb descending.
+  int item;
+  if (order != nullptr) {
+    item = order[blockIdx.x];
+  } else {
+    const int qb_desc = nb - 1 - static_cast<int>(blockIdx.x) / hq;
+    item = (static_cast<int>(blockIdx.x) % hq) * nb + qb_desc;
+  }
+  const int h = item / nb, qb = item % nb;
+  const int g = h / group;
+  const uint32_t* row = rowbits ? rowbits + static_cast<size_t>(item) * W : nullptr;
+  const bool is_dense = dense != 0;
+
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.k_full, 1);
+    mbar_init(&bars.k_empty, 1);
+    mbar_init(&bars.v_full, 1);
+    mbar_init(&bars.v_empty, 1);
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.p_full, 4);
+    mbar_init(&bars.pv_done, 1);
+    mbar_init(&bars.o_full, 1);
+    mbar_init(&bars.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kTmaWarp) {
+    int cnt = 0;
+    for (int w = lane; w <= (qb >> 5); w += 32) cnt += __popc(row_word(row, is_dense, w, qb));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0) {
+      bars.count = cnt;
+      bars.has_diag = (row_word(row, is_dense, qb >> 5, qb) >> (qb & 31)) & 1u;
+    }
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const int count = bars.count;
+
+  if (warp == kTmaWarp) {
+    if (lane == 0 && count > 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      mbar_arrive_expect_tx(&bars.q_full, kTile);
+      tma_load_3d(sQ, &tq, &bars.q_full, 0, qb * kB, h);
+      tma_load_3d(sQ + kHalf, &tq, &bars.q_full, 64, qb * kB, h);
+      int j = 0;
+      bool ok = true;
+      for (int w = 0; ok && w <= (qb >> 5); ++w) {
+        uint32_t bits = row_word(row, is_dense, w, qb);
+        while (bits) {
+          const int kb = w * 32 + __ffs(bits) - 1;
+          bits &= bits - 1;
+          const uint32_t par = (static_cast<uint32_t>(j) & 1u) ^ 1u;
+          if (!mbar_wait(&bars.k_empty, par, &bars.abort)) {
+            fail(&bars.abort, status, 0x201);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars.k_full, kTile);
+          tma_load_3d(sK, &tk, &bars.k_full, 0, kb * kB, g);
+          tma_load_3d(sK + kHalf, &tk, &bars.k_full, 64, kb * kB, g);
+          if (!mbar_wait(&bars.v_empty, par, &bars.abort)) {
+            fail(&bars.abort, status, 0x202);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars.v_full, kTile);
+          tma_load_3d(sV, &tv, &bars.v_full, 0, kb * kB, g);
+          tma_load_3d(sV + kHalf, &tv, &bars.v_full, 64, kb * kB, g);
+          ++j;
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && count > 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
+      bool ok = mbar_wait(&bars.q_full, 0, &bars.abort);
+      if (!ok) fail(&bars.abort, status, 0x203);
+      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
+      for (int j = 0; ok && j < count; ++j) {
+        const uint32_t par = static_cast<uint32_t>(j) & 1u;
+        // S (aliased by P_{j-1}) is free once PV_{j-1} has completed.
+        if ((j > 0 && !mbar_wait(&bars.pv_done, par ^ 1u, &bars.abort)) ||
+            !mbar_wait(&bars.k_full, par, &bars.abort)) {
+          fail(&bars.abort, status, 0x204);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma_ss(tmem, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_qk, kk > 0);
+        }
+        umma_commit(&bars.k_empty);
+        umma_commit(&bars.s_full);
+        if (!mbar_wait(&bars.p_full, par, &bars.abort) || !mbar_wait(&bars.v_full, par, &bars.abort)) {
+          fail(&bars.abort, status, 0x205);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // A = P rows in TMEM (bf16 pairs, 8 columns per 16 keys);
+          // B = V, 16 keys x 128 features, MN-major: 16 rows of 128 B per
+          // step, the second 64-feature half kHalf bytes further.
+          umma_ts(tmem + 128, tmem + kk * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), idesc_pv,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars.v_empty);
+        umma_commit(&bars.pv_done);
+      }
+      umma_commit(&bars.o_full);
+      umma_commit(&bars.drain);
+      if (!mbar_wait(&bars.drain, 0, &bars.abort)) fail(&bars.abort, status, 0x206);
+    }
+  } else {
+    // Softmax warps: thread owns query row r of the block.
+    const int r = threadIdx.x;
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t s_addr = tmem + lane_addr, o_addr = tmem + lane_addr + 128;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < count; ++j) {
+      if (!warp_wait(&bars.s_full, static_cast<uint32_t>(j) & 1u, &bars.abort)) {
+        if (lane == 0) fail(&bars.abort, status, 0x207);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool diag = bars.has_diag && j == count - 1;  // ascending order: qb is last
+      float x[128];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(s_addr + cc * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float val = __uint_as_float(v[e]) * c_log2;
+          x[cc * 32 + e] = (diag && cc * 32 + e > r) ? -INFINITY : val;
+        }
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int e = 1; e < 128; ++e) mx = fmaxf(mx, x[e]);
+      if (j == 0) {
+        m_ref = mx;
+      } else if (__any_sync(0xffffffffu, mx > m_ref + kRescaleLog2)) {
+        // Warp-uniform branch (TMEM loads/stores are warp-collective); each
+        // row moves to its own new max, f = 1 where it did not grow.
+        // PV_{j-1} is complete (QK_j was issued after it), so O is stable.
+        const float m_new = fmaxf(m_ref, mx);
+        const float f = ex2_approx(m_ref - m_new);
+        l *= f;
+        m_ref = m_new;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(o_addr + cc * 32, v);
+          uint32_t a[16], b[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            a[e] = __float_as_uint(__uint_as_float(v[e]) * f);
+            b[e] = __float_as_uint(__uint_as_float(v[16 + e]) * f);
+          }
+          tmem_st16(o_addr + cc * 32, a);
+          tmem_st16(o_addr + cc * 32 + 16, b);
+        }
+      }
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        const float p0 = ex2_approx(x[2 * e] - m_ref);
+        const float p1 = ex2_approx(x[2 * e + 1] - m_ref);
+        sum += p0 + p1;
+        pk[e] = pack_bf16x2(p0, p1);
+      }
+      l += sum;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t a[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) a[e] = pk[cc * 16 + e];
+        tmem_st16(s_addr + cc * 16, a);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full);
+    }
+    // Epilogue: O / l -> bf16, staged per warp through shared memory (the
+    // K/V tiles are no longer needed) so that each store is two full rows.
+    bool have = ok && count > 0;
+    if (have && !warp_wait(&bars.o_full, 0, &bars.abort)) {
+      if (lane == 0) fail(&bars.abort, status, 0x208);
+      have = false;
+    }
+    tc_fence_after();
+    uint4* stg = reinterpret_cast<uint4*>(sK + warp * (32 * 256));  // 32 rows x 256 B
+    const float inv_l = have && l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld32(o_addr + cc * 32, v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint4 u;
+        u.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * inv_l, __uint_as_float(v[q4 * 8 + 1]) * inv_l);
+        u.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * inv_l, __uint_as_float(v[q4 * 8 + 3]) * inv_l);
+        u.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * inv_l, __uint_as_float(v[q4 * 8 + 5]) * inv_l);
+        u.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * inv_l, __uint_as_float(v[q4 * 8 + 7]) * inv_l);
+        const int chunk = cc * 4 + q4;  // 16-byte chunk of the 256-byte row
+        stg[lane * 16 + (chunk ^ (lane & 15))] = u;
+      }
+    }
+    __syncwarp();
+    const int chunk = lane & 15;
+#pragma unroll 4
+    for (int it = 0; it < 16; ++it) {
+      const int R = it * 2 + (lane >> 4);
+      const uint4 u = stg[R * 16 + (chunk ^ (R & 15))];
+      const int tok = qb * kB + warp * 32 + R;
+      uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * o_hs + static_cast<int64_t>(tok) * o_ts);
+      dst[chunk] = u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const crisp_shape& s, const TmaMaps& maps, const uint32_t* rowbits,
+                             const int32_t* counts, void* out, char* ws, bool dense, cudaStream_t st) {
+  const ScratchLayout L = scratch_layout(s);
+  const int nb = num_blocks(s.seq_len);
+  auto* status = reinterpret_cast<DevStatus*>(ws + L.status);
+  const int32_t* order = nullptr;
+  if (!dense) {
+    cudaError_t e = launch_row_order(s, counts, ws, st);
+    if (e != cudaSuccess) return e;
+    order = reinterpret_cast<const int32_t*>(ws + L.order);
+  }
+  cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int items = s.hq * nb;
+  attention_kernel<<<items, kThreads, kSmemBytes, st>>>(
+      maps.q, maps.k, maps.v, s.seq_len, s.hq, s.hq / s.hkv, s.scale * 1.4426950408889634f,
+      dense ? nullptr : rowbits, order, dense ? 1 : 0, static_cast<__nv_bfloat16*>(out), s.o_head_stride,
+      s.o_tok_stride, status);
+  return cudaGetLastError();
+}
+
+}  // namespace crisp

@@ -1,0 +1,85 @@
+// Internal declarations shared by the CRISP CUDA translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/crisp.h"
+
+namespace crisp {
+
+constexpr int kB = 128;  // block size (tokens), "block size B=128"
+constexpr int kD = 128;  // head dimension
+constexpr int kMaxSeq = 1 << 20;
+constexpr int kMaxBlocks = kMaxSeq / kB;  // 8192
+constexpr int kProxyChunk = 16;           // key blocks per proxy CTA
+
+// Device status word at offset 0 of every workspace: first error wins.
+struct DevStatus {
+  uint32_t code;
+  uint32_t detail;
+};
+
+__device__ __forceinline__ void report_error(DevStatus* st, uint32_t code, uint32_t detail) {
+  if (atomicCAS(&st->code, 0u, code) == 0u) atomicExch(&st->detail, detail);
+}
+
+// Q32 quantum of a probability: round-half-even(p * 2^32). p * 2^32 is exact
+// in fp32 for p in [0, 1]; the conversion rounds to nearest even.
+__device__ __forceinline__ uint64_t q32(float p) { return __float2ull_rn(p * 4294967296.0f); }
+
+inline int num_blocks(int n) { return n / kB; }
+inline int bit_words(int nb) { return (nb + 31) / 32; }
+inline int proxy_chunks(int nb) { return (nb + kProxyChunk - 1) / kProxyChunk; }
+
+// Scratch part of every workspace (offsets in bytes, each 256-aligned).
+struct ScratchLayout {
+  size_t status;       // DevStatus
+  size_t proxy_part;   // float2 [hq][128][chunks]  per-chunk (max, sum) in log2 units
+  size_t proxy_stats;  // float2 [hq][128]          (row max, 1/row sum)
+  size_t mass_lower;   // uint64 [hq][nb]  lower-triangle slash part of tile c
+  size_t mass_upper;   // uint64 [hq][nb]  strict-upper slash part of tile c
+  size_t qbar;         // float  [hq][nb][128]
+  size_t kbar;         // float  [hkv][nb][128]
+  size_t srev;         // uint32 [hq][W + 2]  slash bits reversed
+  size_t order;        // int32  [hq * nb]    attention work order
+  size_t bucket;       // int32  [nb + 2]     counting-sort buckets
+  size_t total;
+};
+
+// Intermediates of crisp_prefill_layer, placed after the scratch.
+struct LayerLayout {
+  size_t pmap, vmass, smass, cstruct, total_mass, route, vbits, sbits, pbar, pebits, rowbits, counts;
+  size_t total;
+};
+
+ScratchLayout scratch_layout(const crisp_shape& s);
+LayerLayout layer_layout(const crisp_shape& s);
+
+struct TmaMaps {
+  CUtensorMap q, k, v;
+};
+
+// ---- launchers (one per translation unit); return cudaSuccess or the launch error
+cudaError_t launch_proxy(const crisp_shape& s, const TmaMaps& maps, float* pmap, char* ws, cudaStream_t st);
+cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_t* vmass, uint64_t* smass, char* ws,
+                                cudaStream_t st);
+cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, uint64_t* cstruct,
+                         uint64_t* total, uint8_t* route, cudaStream_t st);
+cudaError_t launch_select_vs(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass,
+                             const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
+                             cudaStream_t st);
+cudaError_t launch_pe_map(const crisp_shape& s, const void* q, const void* k, const uint8_t* route, float* pbar,
+                          char* ws, cudaStream_t st);
+cudaError_t launch_select_pe(const crisp_shape& s, const crisp_params& p, const float* pbar, const uint8_t* route,
+                             uint32_t* pebits, cudaStream_t st);
+cudaError_t launch_build_mask(const crisp_shape& s, const uint8_t* route, const uint32_t* vbits,
+                              const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits, int32_t* counts,
+                              char* ws, cudaStream_t st);
+cudaError_t launch_row_order(const crisp_shape& s, const int32_t* counts, char* ws, cudaStream_t st);
+cudaError_t launch_attention(const crisp_shape& s, const TmaMaps& maps, const uint32_t* rowbits,
+                             const int32_t* counts, void* out, char* ws, bool dense, cudaStream_t st);
+
+}  // namespace crisp

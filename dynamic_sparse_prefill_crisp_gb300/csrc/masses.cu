@@ -1,0 +1,182 @@
+// A3 block masses, A2 C_struct routing and A4 Vertical-Slash noise-floor
+// selection (CRISP paper page on ai.info, "Key Contributions" 2 and
+// "Methodology in Plain English"; ai-feeds page, "方法").
+//
+// Every mass is an integer sum of Q32 quanta q(p) = round-half-even(p * 2^32),
+// so the result does not depend on the order of the reduction and matches an
+// element-by-element statement bit for bit.
+#include "common.cuh"
+#include "reduce.cuh"
+
+namespace crisp {
+
+namespace {
+
+constexpr int kMassThreads = 256;
+
+// One CTA per 128x128 tile (key block c, head h) of the proxy map. Thread t
+// reads columns 4*(t%32)..+3 of rows 16*(t/32)..+15 (coalesced 512-byte rows)
+// and sums the quanta three ways: the whole tile (vertical mass of block c),
+// the lower triangle r >= jj (slash offset block nb-1-c) and the strict upper
+// triangle r < jj (slash offset block nb-2-c).
+__global__ void __launch_bounds__(kMassThreads) mass_tiles(const float* __restrict__ pmap, int n,
+                                                           uint64_t* __restrict__ vmass,
+                                                           uint64_t* __restrict__ lower,
+                                                           uint64_t* __restrict__ upper) {
+  __shared__ uint64_t red[3][kMassThreads / 32];
+  const int c = blockIdx.x, h = blockIdx.y, nb = gridDim.x;
+  const int cq = threadIdx.x & 31, rg = threadIdx.x >> 5;
+  const float* base = pmap + static_cast<size_t>(h) * kB * n + static_cast<size_t>(c) * kB + cq * 4;
+  float4 p[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+    p[k] = __ldcs(reinterpret_cast<const float4*>(base + static_cast<size_t>(rg * 16 + k) * n));
+  uint64_t all = 0, lo = 0;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int r = rg * 16 + k;
+    const int jj = cq * 4;
+    const uint64_t a = q32(p[k].x), b = q32(p[k].y), d = q32(p[k].z), e = q32(p[k].w);
+    all += a + b + d + e;
+    lo += (r >= jj ? a : 0) + (r >= jj + 1 ? b : 0) + (r >= jj + 2 ? d : 0) + (r >= jj + 3 ? e : 0);
+  }
+  uint64_t v[3] = {all, lo, all - lo};
+#pragma unroll
+  for (int t = 0; t < 3; ++t) v[t] = warp_sum(v[t]);
+  if ((threadIdx.x & 31) == 0)
+    for (int t = 0; t < 3; ++t) red[t][threadIdx.x >> 5] = v[t];
+  __syncthreads();
+  if (threadIdx.x < 3) {
+    uint64_t s = 0;
+    for (int w = 0; w < kMassThreads / 32; ++w) s += red[threadIdx.x][w];
+    uint64_t* out = threadIdx.x == 0 ? vmass : (threadIdx.x == 1 ? lower : upper);
+    out[static_cast<size_t>(h) * nb + c] = s;
+  }
+}
+
+// smass[h][s] = lower[nb-1-s] (tile nb-1-s >= 1) + upper[nb-2-s] (tile >= 1).
+// Tile 0 holds the sink columns j < 128, which the slash direction leaves out.
+__global__ void assemble_slash(const uint64_t* __restrict__ lower, const uint64_t* __restrict__ upper, int nb,
+                               uint64_t* __restrict__ smass) {
+  const int h = blockIdx.y;
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= nb) return;
+  const uint64_t* lo = lower + static_cast<size_t>(h) * nb;
+  const uint64_t* up = upper + static_cast<size_t>(h) * nb;
+  const int cl = nb - 1 - s, cu = nb - 2 - s;
+  smass[static_cast<size_t>(h) * nb + s] = (cl >= 1 ? lo[cl] : 0ull) + (cu >= 1 ? up[cu] : 0ull);
+}
+
+// C_struct = vmass[0] + vmass[nb-1] (columns [0,128) and [n-128,n)), total =
+// sum of vmass; VS iff tau_den * C_struct >= tau_num * total.
+__global__ void route_kernel(const uint64_t* __restrict__ vmass, int nb, uint32_t tau_num, uint32_t tau_den,
+                             uint64_t* __restrict__ cstruct, uint64_t* __restrict__ total,
+                             uint8_t* __restrict__ route) {
+  __shared__ uint64_t scratch[32];
+  const int h = blockIdx.x;
+  const uint64_t* v = vmass + static_cast<size_t>(h) * nb;
+  uint64_t s = 0;
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) s += v[c];
+  const uint64_t T = block_sum(s, scratch);
+  if (threadIdx.x == 0) {
+    const uint64_t S = v[0] + v[nb - 1];
+    cstruct[h] = S;
+    total[h] = T;
+    route[h] = static_cast<unsigned __int128>(tau_den) * S >= static_cast<unsigned __int128>(tau_num) * T ? 1 : 0;
+  }
+}
+
+// A4 for one (head, direction): direction 0 = vertical (always keeps {0,
+// nb-1}), 1 = slash (always keeps {0}); candidates [1, nb-2].
+constexpr int kSelThreads = 512;
+__global__ void __launch_bounds__(kSelThreads) select_vs_kernel(const uint64_t* __restrict__ vmass,
+                                                                const uint64_t* __restrict__ smass,
+                                                                const uint8_t* __restrict__ route, int nb,
+                                                                uint32_t alpha_num, uint32_t alpha_den, int kmin,
+                                                                uint32_t* __restrict__ vbits,
+                                                                uint32_t* __restrict__ sbits) {
+  __shared__ uint32_t chosen[kMaxBlocks / 32];
+  __shared__ uint64_t scratch64[32];
+  __shared__ int scratch32[32];
+  const int h = blockIdx.x, dir = blockIdx.y;
+  const int W = (nb + 31) / 32;
+  uint32_t* out = (dir == 0 ? vbits : sbits) + static_cast<size_t>(h) * W;
+  for (int w = threadIdx.x; w < W; w += blockDim.x) chosen[w] = 0u;
+  __syncthreads();
+  if (!route[h]) {
+    for (int w = threadIdx.x; w < W; w += blockDim.x) out[w] = 0u;
+    return;
+  }
+  const uint64_t* m = (dir == 0 ? vmass : smass) + static_cast<size_t>(h) * nb;
+  const int c_lo = 1, c_hi = nb - 2;  // candidates [c_lo, c_hi]
+  const int N = max(0, c_hi - c_lo + 1);
+  const int nforced = (dir == 0 && nb >= 2) ? 2 : 1;
+  if (threadIdx.x == 0) {
+    chosen[0] |= 1u;
+    if (dir == 0) chosen[(nb - 1) >> 5] |= 1u << ((nb - 1) & 31);
+  }
+  uint64_t part = 0;
+  for (int c = c_lo + threadIdx.x; c <= c_hi; c += blockDim.x) part += m[c];
+  const uint64_t sum = block_sum(part, scratch64);
+  int mine = 0;
+  if (N > 0) {
+    const unsigned __int128 rhs = static_cast<unsigned __int128>(alpha_num) * sum;
+    for (int c = c_lo + threadIdx.x; c <= c_hi; c += blockDim.x) {
+      const unsigned __int128 lhs = static_cast<unsigned __int128>(m[c]) * static_cast<unsigned>(N) * alpha_den;
+      if (lhs > rhs) {
+        atomicOr(&chosen[c >> 5], 1u << (c & 31));
+        ++mine;
+      }
+    }
+  }
+  const int count = nforced + block_sum(mine, scratch32);
+  const int target = min(kmin, nforced + N);
+  int need = target - count;
+  if (need > 0) {
+    // Largest key x with #{unchosen candidates: key >= x} >= need; keys are
+    // unique, so exactly `need` candidates reach it: the (mass desc, index
+    // asc) order of the k_min fill.
+    uint64_t x = 0;
+    for (int bit = kKeyBits - 1; bit >= 0; --bit) {
+      const uint64_t cand = x | (1ull << bit);
+      int cnt = 0;
+      for (int c = c_lo + threadIdx.x; c <= c_hi; c += blockDim.x)
+        if (!((chosen[c >> 5] >> (c & 31)) & 1u) && sel_key(m[c], c) >= cand) ++cnt;
+      if (block_sum(cnt, scratch32) >= need) x = cand;
+    }
+    __syncthreads();
+    for (int c = c_lo + threadIdx.x; c <= c_hi; c += blockDim.x)
+      if (!((chosen[c >> 5] >> (c & 31)) & 1u) && sel_key(m[c], c) >= x) atomicOr(&chosen[c >> 5], 1u << (c & 31));
+  }
+  __syncthreads();
+  for (int w = threadIdx.x; w < W; w += blockDim.x) out[w] = chosen[w];
+}
+
+}  // namespace
+
+cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_t* vmass, uint64_t* smass, char* ws,
+                                cudaStream_t st) {
+  const ScratchLayout L = scratch_layout(s);
+  const int nb = num_blocks(s.seq_len);
+  auto* lower = reinterpret_cast<uint64_t*>(ws + L.mass_lower);
+  auto* upper = reinterpret_cast<uint64_t*>(ws + L.mass_upper);
+  mass_tiles<<<dim3(nb, s.hq), kMassThreads, 0, st>>>(pmap, s.seq_len, vmass, lower, upper);
+  assemble_slash<<<dim3((nb + 255) / 256, s.hq), 256, 0, st>>>(lower, upper, nb, smass);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, uint64_t* cstruct,
+                         uint64_t* total, uint8_t* route, cudaStream_t st) {
+  route_kernel<<<s.hq, 256, 0, st>>>(vmass, num_blocks(s.seq_len), p.tau_num, p.tau_den, cstruct, total, route);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select_vs(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass,
+                             const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
+                             cudaStream_t st) {
+  select_vs_kernel<<<dim3(s.hq, 2), kSelThreads, 0, st>>>(vmass, smass, route, num_blocks(s.seq_len), p.alpha_num,
+                                                          p.alpha_den, p.kmin_blocks, vbits, sbits);
+  return cudaGetLastError();
+}
+
+}  // namespace crisp

@@ -1,0 +1,233 @@
+/*
+ * crisp.h -- C ABI of the CRISP sparse-prefill library (GB300, sm_103a).
+ *
+ * CRISP ("CRISP: Cliff-awaRe Input-adaptive Sparse Prefilling with
+ * Structural-Mass-Motivated Routing", arXiv 2609.01925) decides, per layer and
+ * per attention head, which 128x128 blocks of the causal attention matrix to
+ * compute, then computes exact softmax attention over those blocks:
+ *
+ *   A1 crisp_proxy_map       proxy attention map of the last query block
+ *   A3 crisp_block_masses    vertical / slash block masses of that map
+ *   A2 crisp_route_cstruct   C_struct routing: Vertical-Slash or Pooled-Estimation
+ *   A4 crisp_select_vs       sink-aware noise-floor selection (VS heads)
+ *   A5 crisp_pe_map          pooled attention estimate (PE heads)
+ *   A6 crisp_select_pe       PE block selection (gamma coverage or noise floor)
+ *   A7 crisp_build_mask      per-head sparse block mask
+ *   A8 crisp_sparse_prefill  causal GQA block-sparse attention
+ *   A9 crisp_dense_prefill   the same kernel over every causal block
+ *   crisp_prefill_layer      A1..A8 in order, intermediates in the workspace
+ *
+ * Conventions (every function):
+ *  - Pointers are DEVICE pointers unless marked "host". The caller owns and
+ *    allocates every buffer, including the workspace; the library allocates
+ *    and frees nothing and keeps no mutable global state.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream); calls return without synchronising, except crisp_read_status.
+ *  - Argument errors are detected on the host, returned synchronously, and
+ *    nothing is launched. Errors found on the device (a bounded wait that ran
+ *    out) are recorded in the workspace status word; read it with
+ *    crisp_read_status. No C++ exception crosses this boundary.
+ *  - Fixed sizes: head_dim = 128, block = 128 tokens, batch 1 (a batch is a
+ *    loop over calls). seq_len is a multiple of 128, 256 <= seq_len <= 2^20.
+ *  - bf16 tensors are [heads][tokens][128] with element strides per head and
+ *    per token (the 128 features contiguous). For the TMA copies every
+ *    pointer must be 16-byte aligned and every stride a multiple of 8
+ *    elements.
+ *  - Bitsets: bit c of a row is (word[c >> 5] >> (c & 31)) & 1; a row of nb
+ *    bits takes W = ceil(nb / 32) uint32 words.
+ *  - Rational parameters (tau, alpha, gamma) are compared exactly in integer
+ *    arithmetic; masses are integer sums of Q32 quanta, q(p) = round-half-
+ *    even(p * 2^32), so index sets do not depend on summation order.
+ */
+#ifndef CRISP_H_
+#define CRISP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CRISP_API __attribute__((visibility("default")))
+#else
+#define CRISP_API
+#endif
+
+typedef struct CUstream_st* crisp_stream_t; /* same type as cudaStream_t */
+
+typedef enum crisp_status {
+  CRISP_OK = 0,
+  CRISP_ERR_INVALID_ARG = 1, /* null pointer or parameter out of range */
+  CRISP_ERR_SHAPE = 2,       /* unsupported shape (see limits above) */
+  CRISP_ERR_ALIGN = 3,       /* pointer or stride not 16-byte aligned */
+  CRISP_ERR_WORKSPACE = 4,   /* workspace null or smaller than required */
+  CRISP_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, copy) */
+  CRISP_ERR_TIMEOUT = 6,     /* device: a bounded wait inside a kernel ran out */
+  CRISP_ERR_DEVICE = 7       /* the current device is not sm_103 */
+} crisp_status;
+
+typedef enum crisp_pe_mode {
+  CRISP_PE_GAMMA = 0, /* cumulative coverage gamma (the paper's PE rule) */
+  CRISP_PE_NOISE = 1  /* the noise-floor rule applied to each pooled row */
+} crisp_pe_mode;
+
+/* Problem shape. Strides are in elements. scale = 0 selects 1/sqrt(128). */
+typedef struct crisp_shape {
+  int32_t hq;       /* query heads */
+  int32_t hkv;      /* key/value heads; hq % hkv == 0 (GQA group G = hq/hkv) */
+  int32_t head_dim; /* must be 128 */
+  int32_t seq_len;  /* n */
+  int32_t block;    /* must be 128 */
+  int64_t q_head_stride, q_tok_stride;
+  int64_t kv_head_stride, kv_tok_stride; /* shared by K and V */
+  int64_t o_head_stride, o_tok_stride;
+  float scale;
+} crisp_shape;
+
+/* Method parameters; crisp_params_default gives the paper's universal
+ * configuration: tau_proxy = 1/5, alpha = 1, gamma = 19/20 (PE only),
+ * k_min = 8 blocks (1024 tokens) per direction, pe_mode = CRISP_PE_GAMMA. */
+typedef struct crisp_params {
+  uint32_t tau_num, tau_den;     /* 0 <= tau <= 1, tau_den > 0 */
+  uint32_t alpha_num, alpha_den; /* alpha_num, alpha_den <= 65535, alpha_den > 0 */
+  uint32_t gamma_num, gamma_den; /* 0 <= gamma <= 1, gamma_den > 0 */
+  int32_t kmin_blocks;           /* 0 <= kmin_blocks <= 8192 */
+  int32_t pe_mode;               /* crisp_pe_mode */
+} crisp_params;
+
+/* Fills *p (host) with the defaults above. */
+CRISP_API void crisp_params_default(crisp_params* p);
+
+/* Bytes of workspace the step functions need (status word and scratch). */
+CRISP_API crisp_status crisp_workspace_size(const crisp_shape* shape, size_t* bytes /* host */);
+
+/* Bytes of workspace crisp_prefill_layer needs (scratch + every intermediate). */
+CRISP_API crisp_status crisp_layer_workspace_size(const crisp_shape* shape, size_t* bytes /* host */);
+
+/* Clears the status word at the start of `ws` (asynchronously on `stream`).
+ * Call once after allocating a workspace and after reading an error. */
+CRISP_API crisp_status crisp_workspace_init(void* ws, size_t ws_bytes, crisp_stream_t stream);
+
+/* A1. Proxy attention map of the last query block (ai.info page, "Key
+ * Contributions" 2 and "Methodology": routing reads the proxy attention map
+ * the method already computes). For q-head h (kv head h/G) and the last
+ * block's rows i = n-128+r, r in [0,128):
+ *   pmap[h][r][j] = softmax_j(scale * q_i . k_j) over j <= i, and 0 for j > i.
+ * q: bf16 [hq][n][128] (only the last 128 rows are read); k: bf16
+ * [hkv][n][128]; pmap: fp32 [hq][128][n] contiguous, 16-byte aligned. */
+CRISP_API crisp_status crisp_proxy_map(const crisp_shape* shape, const void* q, const void* k, float* pmap, void* ws,
+                             size_t ws_bytes, crisp_stream_t stream);
+
+/* A3. Block masses of the proxy map ("mass at Vertical-Slash compatible
+ * positions", ai-feeds page, "方法"). With q(p) the Q32 quantum:
+ *   vmass[h][c] = sum over rows r and key columns j of block c of q(pmap[h][r][j])
+ *   smass[h][s] = sum over (r, j) with j <= i, j >= 128 and
+ *                 floor((i - j)/128) == s of q(pmap[h][r][j])
+ * Sink columns (j < 128) are left out of the slash masses, so the sink cannot
+ * raise the slash noise floor. pmap fp32 [hq][128][n]; vmass, smass: uint64
+ * [hq][nb]. */
+CRISP_API crisp_status crisp_block_masses(const crisp_shape* shape, const float* pmap, uint64_t* vmass, uint64_t* smass,
+                                void* ws, size_t ws_bytes, crisp_stream_t stream);
+
+/* A2. C_struct routing (ai.info page, "Key Contributions" 2: mass at the
+ * first 128 and the last 128 tokens of the proxy map; tau_proxy = 0.2). With
+ * B = 128 those slices are key blocks 0 and nb-1, so
+ *   cstruct[h] = vmass[h][0] + vmass[h][nb-1],  total[h] = sum_c vmass[h][c],
+ *   route[h]   = 1 (Vertical-Slash) iff tau_den * cstruct >= tau_num * total,
+ *                0 (Pooled-Estimation) otherwise.
+ * vmass uint64 [hq][nb]; cstruct, total uint64 [hq]; route uint8 [hq]. */
+CRISP_API crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
+                                 uint64_t* cstruct, uint64_t* total, uint8_t* route, crisp_stream_t stream);
+
+/* A4. Sink-aware noise-floor selection for VS heads (ai.info page,
+ * "Methodology in Plain English": keep each block whose mass exceeds alpha
+ * times the expected background mass of the blocks that are not always
+ * retained; "k_min=1024 tokens (8 blocks) per direction"). Per direction:
+ * always-retained vertical {0, nb-1}, slash {0}; candidates [1, nb-2], N of
+ * them, mass sum M; keep c iff m[c]*N*alpha_den > alpha_num*M; then fill to
+ * min(kmin, available) by (mass desc, index asc). PE heads get empty rows.
+ * vbits, sbits: uint32 [hq][W]. */
+CRISP_API crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
+                             const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
+                             void* ws, size_t ws_bytes, crisp_stream_t stream);
+
+/* A5. Pooled attention estimate for PE heads (the Pooled-Estimation route
+ * CRISP keeps from FlexPrefill; ai.info page, "Overview"): block means of q
+ * and k, pbar[h][b][c] = softmax over c <= b of scale * qbar_b . kbar_c, and 0
+ * for c > b. Rows of VS heads are not written. q, k bf16; pbar fp32
+ * [hq][nb][nb], 16-byte aligned. */
+CRISP_API crisp_status crisp_pe_map(const crisp_shape* shape, const void* q, const void* k, const uint8_t* route, float* pbar,
+                          void* ws, size_t ws_bytes, crisp_stream_t stream);
+
+/* A6. PE block selection per query block b from pbar (ai.info page,
+ * "Methodology in Plain English": gamma = 0.95 for the PE path only).
+ * CRISP_PE_GAMMA: the shortest prefix of [0, b] ordered by (mass desc, index
+ * asc) whose mass reaches gamma of the row (gamma_den*prefix >= gamma_num*
+ * total), plus {0, b}. CRISP_PE_NOISE: forced {0, b}, candidates [1, b-1],
+ * the A4 rule. Both fill to min(kmin, b+1). VS heads get empty rows.
+ * pebits: uint32 [hq][nb][W]. */
+CRISP_API crisp_status crisp_select_pe(const crisp_shape* shape, const crisp_params* params, const float* pbar,
+                             const uint8_t* route, uint32_t* pebits, void* ws, size_t ws_bytes,
+                             crisp_stream_t stream);
+
+/* A7. The per-head sparse mask (ai-feeds page, "方法": the output is a
+ * per-head sparse attention mask) as key-block sets per query block qb:
+ *   VS head: {kb <= qb : kb in V} U {qb-s, qb-s-1 : s in S} within [0, qb]
+ *            (a 128-wide diagonal band at offset block s crosses key blocks
+ *            qb-s and qb-s-1);
+ *   PE head: pebits row qb within [0, qb].
+ * rowbits: uint32 [hq][nb][W]; counts: int32 [hq][nb] = blocks per row. */
+CRISP_API crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t* route, const uint32_t* vbits,
+                              const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits, int32_t* counts,
+                              void* ws, size_t ws_bytes, crisp_stream_t stream);
+
+/* A8. Exact causal GQA softmax attention over the selected blocks (ai.info
+ * page, "Why This Matters": exact softmax attention over the blocks it
+ * selects): for token i in query block qb of head h,
+ *   out_i = sum_{j in A(i)} softmax_j(scale * q_i . k_j) v_j,
+ *   A(i) = { j <= i : block(j) in rowbits[h][qb] }.
+ * Rows with an empty A(i) are written as zeros. q bf16 [hq][n][128]; k, v
+ * bf16 [hkv][n][128]; rowbits, counts from crisp_build_mask; out bf16
+ * [hq][n][128] (o strides). */
+CRISP_API crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v,
+                                  const uint32_t* rowbits, const int32_t* counts, void* out, void* ws,
+                                  size_t ws_bytes, crisp_stream_t stream);
+
+/* A9. Dense causal attention (A(i) = [0, i]): the exact baseline the paper
+ * compares against ("FlashAttention (exact dense)", ai.info page). */
+CRISP_API crisp_status crisp_dense_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v, void* out,
+                                 void* ws, size_t ws_bytes, crisp_stream_t stream);
+
+/* Device views of the intermediates crisp_prefill_layer leaves in `ws`. */
+typedef struct crisp_layer_views {
+  float* pmap;
+  uint64_t *vmass, *smass, *cstruct, *total;
+  uint8_t* route;
+  uint32_t *vbits, *sbits;
+  float* pbar;
+  uint32_t *pebits, *rowbits;
+  int32_t* counts;
+} crisp_layer_views;
+
+/* Fills *views (host) with pointers into `ws` for this shape. */
+CRISP_API crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws, crisp_layer_views* views /* host */);
+
+/* A1..A8 for one layer: proxy map, masses, routing, VS and PE selection,
+ * mask, sparse attention. ws must hold crisp_layer_workspace_size bytes. */
+CRISP_API crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* params, const void* q, const void* k,
+                                 const void* v, void* out, void* ws, size_t ws_bytes, crisp_stream_t stream);
+
+/* Synchronises `stream` and copies the workspace status word to *status
+ * (host). Returns CRISP_ERR_CUDA if the stream or the copy failed. */
+CRISP_API crisp_status crisp_read_status(const void* ws, crisp_stream_t stream, crisp_status* status /* host */);
+
+/* Static description of a status code (never NULL). */
+CRISP_API const char* crisp_status_string(crisp_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CRISP_H_ */

@@ -1,0 +1,79 @@
+"""Shared plumbing for the GPU parity tests: move synthetic inputs to the
+device, run the C-ABI steps one by one and bring every result back."""
+import numpy as np
+import torch
+
+import dynamic_sparse_prefill_crisp_gb300 as crisp
+
+B = 128
+
+
+def to_dev(a_u16):
+    return torch.from_numpy(np.ascontiguousarray(a_u16).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def bf16_to_u16(t):
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def empty(shape, dtype):
+    return torch.empty(shape, dtype=dtype, device="cuda")
+
+
+def new_workspace(shape, layer=False):
+    n = crisp.layer_workspace_size(shape) if layer else crisp.workspace_size(shape)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    crisp.workspace_init(ws)
+    return ws
+
+
+def assert_status_ok(ws):
+    st = crisp.read_status(ws)
+    assert st == 0, crisp.status_string(st)
+
+
+def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_only=True):
+    """Runs A1..A8 through the step entry points; returns numpy copies."""
+    hq, n, _ = q.shape
+    hkv = k.shape[0]
+    nb = n // B
+    W = (nb + 31) // 32
+    qd = to_dev(q) if q_dev is None else q_dev
+    kd = to_dev(k) if k_dev is None else k_dev
+    vd = to_dev(v) if v_dev is None else v_dev
+    out = empty((hq, n, 128), torch.bfloat16)
+    s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+    ws = new_workspace(s)
+    pmap = empty((hq, B, n), torch.float32)
+    vmass = empty((hq, nb), torch.int64)
+    smass = empty((hq, nb), torch.int64)
+    cstruct = empty((hq,), torch.int64)
+    total = empty((hq,), torch.int64)
+    route = empty((hq,), torch.uint8)
+    vbits = empty((hq, W), torch.int32)
+    sbits = empty((hq, W), torch.int32)
+    pbar = torch.zeros((hq, nb, nb), dtype=torch.float32, device="cuda")
+    pebits = empty((hq, nb, W), torch.int32)
+    rowbits = empty((hq, nb, W), torch.int32)
+    counts = empty((hq, nb), torch.int32)
+    crisp.proxy_map(s, qd, kd, pmap, ws)
+    crisp.block_masses(s, pmap, vmass, smass, ws)
+    crisp.route_cstruct(s, params, vmass, cstruct, total, route)
+    crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws)
+    crisp.pe_map(s, qd, kd, route, pbar, ws)
+    crisp.select_pe(s, params, pbar, route, pebits, ws)
+    crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, ws)
+    crisp.sparse_prefill(s, qd, kd, vd, rowbits, counts, out, ws)
+    torch.cuda.synchronize()
+    assert_status_ok(ws)
+    u64 = lambda t: t.cpu().numpy().view(np.uint64)
+    u32 = lambda t: t.cpu().numpy().view(np.uint32)
+    return dict(pmap=pmap.cpu().numpy(), vmass=u64(vmass), smass=u64(smass), cstruct=u64(cstruct), total=u64(total),
+                route=route.cpu().numpy(), vbits=u32(vbits), sbits=u32(sbits), pbar=pbar.cpu().numpy(),
+                pebits=u32(pebits), rowbits=u32(rowbits), counts=counts.cpu().numpy(), out=out)
+
+
+def attn_error(out_dev_or_np, ref):
+    o = out_dev_or_np.float().cpu().numpy() if hasattr(out_dev_or_np, "cpu") else out_dev_or_np
+    d = np.abs(o.astype(np.float64) - ref)
+    return float(d.max()), float(d.mean())

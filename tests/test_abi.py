@@ -1,0 +1,113 @@
+"""The C ABI library loads without a GPU, exports every declared symbol and
+rejects bad arguments on the host (no kernel launch, no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import dynamic_sparse_prefill_crisp_gb300 as crisp
+from dynamic_sparse_prefill_crisp_gb300 import build as crisp_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    crisp_build.build()
+    return crisp.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "crisp.h")).read()
+    return sorted(set(re.findall(r"CRISP_API\s+[\w\s\*]*?\b(crisp_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_steps():
+    names = declared_functions()
+    for want in ("crisp_proxy_map", "crisp_route_cstruct", "crisp_select_vs", "crisp_select_pe",
+                 "crisp_sparse_prefill", "crisp_dense_prefill", "crisp_block_masses", "crisp_pe_map",
+                 "crisp_build_mask", "crisp_prefill_layer", "crisp_read_status", "crisp_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", crisp.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (crisp_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert getattr(L, n) is not None
+
+
+def test_params_default_is_the_universal_configuration(L):
+    p = crisp.params_default()
+    assert (p.tau_num, p.tau_den) == (1, 5)
+    assert (p.alpha_num, p.alpha_den) == (1, 1)
+    assert (p.gamma_num, p.gamma_den) == (19, 20)
+    assert p.kmin_blocks == 8 and p.pe_mode == crisp.PE_GAMMA
+
+
+def test_status_strings(L):
+    for code in range(8):
+        assert crisp.status_string(code)
+    assert crisp.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(L):
+    s = crisp.make_shape(32, 8, 524288)
+    small = crisp.workspace_size(s)
+    layer = crisp.layer_workspace_size(s)
+    assert 0 < small < layer
+    # the layer workspace holds the fp32 proxy map of the last block
+    assert layer > 4 * 32 * 128 * 524288
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("hq", 6, 2), ("hkv", 0, 2), ("head_dim", 64, 2), ("block", 64, 2), ("seq_len", 200, 2),
+    ("seq_len", 128, 2), ("seq_len", (1 << 20) + 128, 2), ("q_tok_stride", 100, 3), ("kv_head_stride", 0, 3),
+    ("scale", float("nan"), 1), ("scale", -1.0, 1)])
+def test_shape_validation(L, field, value, code):
+    s = crisp.make_shape(8, 4, 1024)
+    setattr(s, field, value)
+    n = ctypes.c_size_t()
+    assert L.crisp_workspace_size(ctypes.byref(s), ctypes.byref(n)) == code
+    # a step rejects the shape before touching any pointer or the device
+    rc = L.crisp_proxy_map(ctypes.byref(s), ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                           ctypes.c_void_p(256), 1 << 30, None)
+    assert rc == code
+
+
+@pytest.mark.parametrize("field,value", [("tau_den", 0), ("tau_num", 6), ("alpha_den", 0), ("alpha_num", 70000),
+                                         ("gamma_num", 21), ("kmin_blocks", -1), ("kmin_blocks", 9000),
+                                         ("pe_mode", 2)])
+def test_params_validation(L, field, value):
+    s = crisp.make_shape(8, 4, 1024)
+    p = crisp.params_default()
+    setattr(p, field, value)
+    rc = L.crisp_route_cstruct(ctypes.byref(s), ctypes.byref(p), ctypes.c_void_p(256), ctypes.c_void_p(256),
+                               ctypes.c_void_p(256), ctypes.c_void_p(256), None)
+    assert rc == 1
+
+
+def test_null_and_misaligned_pointers(L):
+    s = crisp.make_shape(8, 4, 1024)
+    vp = ctypes.c_void_p
+    assert L.crisp_proxy_map(ctypes.byref(s), None, vp(16), vp(16), vp(256), 1 << 30, None) == 1
+    assert L.crisp_proxy_map(ctypes.byref(s), vp(8), vp(16), vp(16), vp(256), 1 << 30, None) == 3
+    assert L.crisp_sparse_prefill(ctypes.byref(s), vp(16), vp(16), vp(16), None, vp(16), vp(16), vp(256), 1 << 30,
+                                  None) == 1
+    # workspace missing / misaligned / too small
+    assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), None, 1 << 30, None) == 4
+    assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), vp(272), 1 << 30, None) == 3
+    assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), vp(256), 64, None) == 4
+    assert L.crisp_prefill_layer(ctypes.byref(s), ctypes.byref(crisp.params_default()), vp(16), vp(16), vp(16),
+                                 vp(16), vp(256), 1024, None) == 4
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(crisp, "_lib", None)
+    monkeypatch.setattr(crisp, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        crisp.lib()

@@ -1,0 +1,243 @@
+"""CUDA path vs the CPU oracle, step by step, through the C ABI.
+
+Acceptance (stated once, used throughout):
+  * index sets, masses, C_struct, routes, bitsets, counts: bit-exact, with the
+    oracle run on the GPU's own fp32 proxy / pooled maps;
+  * proxy and pooled maps: |gpu - oracle| <= 1e-6 + 1e-3 * oracle element-wise
+    (fp32 accumulate and base-2 exponent vs fp64);
+  * attention output (bf16): max |err| <= 2e-2 and mean |err| <= 2e-3 against
+    fp64 attention over the same blocks.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dynamic_sparse_prefill_crisp_gb300 as crisp
+import oracle
+import synth
+from gpu_helpers import (B, assert_status_ok, attn_error, bf16_to_u16, empty, new_workspace, run_steps, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+MAP_ATOL, MAP_RTOL = 1e-6, 1e-3
+ATT_MAX, ATT_MEAN = 2e-2, 2e-3
+
+
+def check_map(gpu, ref):
+    bad = np.abs(gpu.astype(np.float64) - ref) > MAP_ATOL + MAP_RTOL * np.abs(ref)
+    assert not bad.any(), f"{bad.sum()} entries out of tolerance, max err {np.abs(gpu - ref).max()}"
+
+
+def check_index_sets(r, params):
+    """Oracle A2..A7 from the GPU's own fp32 maps; every integer result equal."""
+    vm, sm = oracle.vs_masses(r["pmap"])
+    assert np.array_equal(vm, r["vmass"])
+    assert np.array_equal(sm, r["smass"])
+    S, T, route = oracle.route(r["pmap"], tau=(params.tau_num, params.tau_den))
+    assert np.array_equal(S, r["cstruct"]) and np.array_equal(T, r["total"])
+    assert np.array_equal(route, r["route"])
+    vb, sb = oracle.select_vs(vm, sm, route, alpha=(params.alpha_num, params.alpha_den), kmin=params.kmin_blocks)
+    assert np.array_equal(vb, r["vbits"])
+    assert np.array_equal(sb, r["sbits"])
+    pbar = r["pbar"].copy()
+    pbar[route == 1] = 0.0  # VS heads' pooled rows are not written
+    pe = oracle.select_pe(pbar, route, pe_mode=params.pe_mode, gamma=(params.gamma_num, params.gamma_den),
+                          alpha=(params.alpha_num, params.alpha_den), kmin=params.kmin_blocks)
+    assert np.array_equal(pe, r["pebits"])
+    rb = oracle.build_mask(route, vb, sb, pe)
+    assert np.array_equal(rb, r["rowbits"])
+    pop = np.unpackbits(rb.view(np.uint8), axis=-1).sum(-1)
+    assert np.array_equal(pop, r["counts"])
+    return rb, route
+
+
+def sample_rows(hq, n, count, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 127, 128, n - 129, n - 128, n - 1]
+    heads, toks = [], []
+    for h in range(hq):
+        ts = sorted(set(fixed + rng.integers(0, n, count).tolist()))
+        heads += [h] * len(ts)
+        toks += ts
+    return np.array(heads, np.int32), np.array(toks, np.int32)
+
+
+def check_attention(q, k, v, out, rowbits, rows=None):
+    hq, n, _ = q.shape
+    if rows is None:
+        h, t = np.meshgrid(np.arange(hq), np.arange(n), indexing="ij")
+        h, t = h.ravel().astype(np.int32), t.ravel().astype(np.int32)
+    else:
+        h, t = rows
+    ref = oracle.attention_rows(q, k, v, h, t, rowbits=rowbits)
+    got = out.float().cpu().numpy()[h, t]
+    mx, mean = attn_error(got, ref)
+    assert mx <= ATT_MAX and mean <= ATT_MEAN, (mx, mean)
+
+
+CASES = [
+    # name, hq, hkv, n, seed, vs_heads
+    ("gqa4-1k", 4, 1, 1024, 1, None),
+    ("mixed-2k", 8, 2, 2048, 2, None),
+    ("nb2-256", 2, 1, 256, 3, None),
+    ("nb3-384", 2, 2, 384, 4, None),
+    ("nb5-640", 4, 2, 640, 5, [0]),
+    ("gqa7-1152", 7, 1, 1152, 6, [0, 3, 6]),
+    ("nb33-4224", 4, 2, 4224, 7, None),
+    ("all-pe-2k", 4, 2, 2048, 8, []),
+]
+
+
+@pytest.mark.parametrize("name,hq,hkv,n,seed,vs", CASES, ids=[c[0] for c in CASES])
+def test_pipeline_steps_match_oracle(name, hq, hkv, n, seed, vs):
+    w = synth.small(name, hq, hkv, n, seed, vs_heads=vs)
+    q, k, v = w.generate()
+    params = crisp.params_default()
+    r = run_steps(q, k, v, params)
+    check_map(r["pmap"], oracle.proxy_map(q, k))
+    rb, route = check_index_sets(r, params)
+    if (route == 0).any():
+        ref = oracle.pe_map(q, k)
+        check_map(r["pbar"][route == 0], ref[route == 0])
+    check_attention(q, k, v, r["out"], rb, rows=None if n <= 2048 else sample_rows(hq, n, 48, seed))
+
+
+@pytest.mark.parametrize("overrides", [dict(alpha=(5, 4)), dict(alpha=(0, 1)), dict(alpha=(3, 1), kmin_blocks=0),
+                                       dict(kmin_blocks=64), dict(pe_mode=crisp.PE_NOISE),
+                                       dict(pe_mode=crisp.PE_NOISE, alpha=(5, 4), kmin_blocks=2),
+                                       dict(gamma=(1, 1)), dict(gamma=(1, 2)), dict(tau=(1, 1)), dict(tau=(0, 1))],
+                         ids=lambda d: "-".join(f"{k}{v}" for k, v in d.items()))
+def test_parameter_variants(overrides):
+    w = synth.small("params", 8, 2, 4096, 11)
+    q, k, v = w.generate()
+    params = crisp.params_default(**overrides)
+    r = run_steps(q, k, v, params)
+    rb, _ = check_index_sets(r, params)
+    check_attention(q, k, v, r["out"], rb, rows=sample_rows(8, 4096, 24, 11))
+
+
+def test_dense_prefill_matches_oracle():
+    for hq, hkv, n, seed in ((4, 1, 1024, 21), (6, 2, 640, 22), (2, 2, 256, 23)):
+        w = synth.small("dense", hq, hkv, n, seed)
+        q, k, v = w.generate()
+        qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+        out = empty((hq, n, 128), torch.bfloat16)
+        s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+        ws = new_workspace(s)
+        crisp.dense_prefill(s, qd, kd, vd, out, ws)
+        torch.cuda.synchronize()
+        assert_status_ok(ws)
+        check_attention(q, k, v, out, None)
+
+
+def test_sparse_prefill_arbitrary_masks():
+    # Masks not produced by the selection: rows without their diagonal block,
+    # empty rows (zeros out), single far blocks, full rows.
+    hq, hkv, n = 3, 1, 1536
+    nb = n // B
+    rng = np.random.default_rng(31)
+    w = synth.small("masks", hq, hkv, n, 31)
+    q, k, v = w.generate()
+    rb = np.zeros((hq, nb, 1), np.uint32)
+    for h in range(hq):
+        for qb in range(nb):
+            kind = rng.integers(0, 4)
+            if kind == 0:
+                bits = 0
+            elif kind == 1:
+                bits = (1 << (qb + 1)) - 1
+            elif kind == 2:
+                bits = 1 << int(rng.integers(0, qb + 1))
+            else:
+                bits = int(rng.integers(0, 1 << (qb + 1))) & ~(1 << qb)
+            rb[h, qb, 0] = bits
+    # stray bits above the diagonal must be ignored
+    rb[0, 2, 0] |= np.uint32(1 << 9)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    out = empty((hq, n, 128), torch.bfloat16)
+    s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+    ws = new_workspace(s)
+    rbd = torch.from_numpy(rb.view(np.int32)).cuda()
+    cnt = torch.from_numpy(np.unpackbits(rb.view(np.uint8), axis=-1).sum(-1).astype(np.int32)).cuda()
+    crisp.sparse_prefill(s, qd, kd, vd, rbd, cnt, out, ws)
+    torch.cuda.synchronize()
+    assert_status_ok(ws)
+    rb_causal = rb.copy()
+    for qb in range(nb):
+        rb_causal[:, qb, 0] &= np.uint32((1 << (qb + 1)) - 1)
+    check_attention(q, k, v, out, rb_causal)
+    # empty rows are exactly zero
+    o = out.float().cpu().numpy()
+    for h in range(hq):
+        for qb in range(nb):
+            if rb_causal[h, qb, 0] == 0:
+                assert np.all(o[h, qb * B:(qb + 1) * B] == 0.0)
+
+
+def test_strided_token_major_layout():
+    # [n][heads][128] storage (token-major), viewed as [heads][n][128]: head
+    # stride 128, token stride heads*128. Results must equal the contiguous run.
+    hq, hkv, n = 4, 2, 1024
+    w = synth.small("strided", hq, hkv, n, 41)
+    q, k, v = w.generate()
+    params = crisp.params_default()
+    ref = run_steps(q, k, v, params)
+    qt = to_dev(np.ascontiguousarray(q.transpose(1, 0, 2))).permute(1, 0, 2)
+    kt = to_dev(np.ascontiguousarray(k.transpose(1, 0, 2))).permute(1, 0, 2)
+    vt = to_dev(np.ascontiguousarray(v.transpose(1, 0, 2))).permute(1, 0, 2)
+    got = run_steps(q, k, v, params, q_dev=qt, k_dev=kt, v_dev=vt)
+    assert np.array_equal(got["pmap"], ref["pmap"])
+    assert np.array_equal(got["rowbits"], ref["rowbits"])
+    assert torch.equal(got["out"], ref["out"])
+
+
+def test_prefill_layer_matches_steps():
+    for hq, hkv, n, seed in ((8, 2, 2048, 51), (4, 1, 640, 52)):
+        w = synth.small("layer", hq, hkv, n, seed)
+        q, k, v = w.generate()
+        params = crisp.params_default()
+        steps = run_steps(q, k, v, params)
+        qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+        out = empty((hq, n, 128), torch.bfloat16)
+        s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+        ws = new_workspace(s, layer=True)
+        crisp.prefill_layer(s, params, qd, kd, vd, out, ws)
+        torch.cuda.synchronize()
+        assert_status_ok(ws)
+        views = crisp.layer_views(s, ws)
+        nb, W = n // B, (n // B + 31) // 32
+
+        def grab(name, shape, dtype):
+            t = torch.empty(shape, dtype=dtype, device="cuda")
+            base = ws.data_ptr()
+            off = views[name] - base
+            nbytes = t.numel() * t.element_size()
+            t.view(torch.uint8).view(-1).copy_(ws[off:off + nbytes])
+            return t.cpu().numpy()
+
+        assert np.array_equal(grab("pmap", (hq, B, n), torch.float32), steps["pmap"])
+        assert np.array_equal(grab("route", (hq,), torch.uint8), steps["route"])
+        assert np.array_equal(grab("rowbits", (hq, nb, W), torch.int32).view(np.uint32), steps["rowbits"])
+        assert torch.equal(out, steps["out"])
+
+
+def test_cfg1_full_layer():
+    w = synth.WORKLOADS["cfg1"]
+    q, k, v = w.generate()
+    params = crisp.params_default()
+    r = run_steps(q, k, v, params)
+    check_map(r["pmap"], oracle.proxy_map(q, k))
+    rb, route = check_index_sets(r, params)
+    assert route.tolist() == [1, 1, 1, 1]
+    check_attention(q, k, v, r["out"], rb)
+
+
+def test_repeat_calls_are_deterministic():
+    w = synth.small("repeat", 8, 2, 2048, 61)
+    q, k, v = w.generate()
+    params = crisp.params_default()
+    a = run_steps(q, k, v, params)
+    b = run_steps(q, k, v, params)
+    for key in ("pmap", "vmass", "smass", "rowbits", "pbar"):
+        assert np.array_equal(a[key], b[key]), key
+    assert torch.equal(a["out"], b["out"])
