@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""CRISP sparse prefill benchmark on one synthetic Llama-3.1-8B-shaped layer.
+
+Workload (default): 32 query / 8 kv heads, head_dim 128, 524,288 tokens,
+bf16, every head sink-type with 2 slashes and 32 needle columns (seed 5).
+One step = one pass of the whole hot path over the layer: proxy map, block
+masses, C_struct routing, VS selection, pooled estimate and PE selection,
+mask + schedule, block-sparse attention. Inputs (6 GiB) are larger than L2,
+so no flush between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl crisp|reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own replica
+of the layer on its own GPU (no data-path collective; the path shards by kv
+head group with no exchange); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B = 128
+METRIC = "sparse prefill ms/layer"
+UNIT = "ms/layer"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["crisp", "reference"], default="crisp")
+    ap.add_argument("--config", default="cfg5")
+    ap.add_argument("--alpha", default="1/1")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention baseline launch")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------- distributed
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a host float over all ranks (NCCL with a device, else gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running (SM clock, reasons)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- accounting
+def selected_pairs(rowbits: np.ndarray, nb: int) -> int:
+    """(row, key) pairs of the selected blocks: B*B off the diagonal block,
+    B(B+1)/2 on it (the causal half)."""
+    hq = rowbits.shape[0]
+    bits = np.unpackbits(rowbits.view(np.uint8), axis=-1, bitorder="little")[..., :nb]  # [hq][nb][nb]
+    total = int(bits.sum())
+    diag = int(bits[:, np.arange(nb), np.arange(nb)].sum())
+    return (total - diag) * B * B + diag * B * (B + 1) // 2
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p.get("hbm_gbs", 6800.0), p.get("bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------ CPU baseline
+def cpu_sample(w, q, k, v, params_alpha, nthreads=None):
+    """The fp64 oracle on a bounded sample of the layer: the full proxy /
+    route / selection for the query heads of kv group 0 and attention for 128
+    query rows of each of those heads; extrapolated to the whole layer."""
+    import oracle
+    G = w.hq // w.hkv
+    heads = list(range(G))
+    nb = w.n // B
+    t0 = time.perf_counter()
+    P = oracle.proxy_map(q[heads], k[:1], nthreads=nthreads).astype(np.float32)
+    vm, sm = oracle.vs_masses(P)
+    _, _, route = oracle.route(P)
+    vb, sb = oracle.select_vs(vm, sm, route, alpha=params_alpha)
+    if (route == 0).any():
+        pbar = oracle.pe_map(q[heads], k[:1], nthreads=nthreads).astype(np.float32)
+    else:
+        pbar = np.zeros((len(heads), nb, nb), np.float32)
+    pe = oracle.select_pe(pbar, route)
+    rb = oracle.build_mask(route, vb, sb, pe)
+    t_select = time.perf_counter() - t0
+    rng = np.random.default_rng(0)
+    rows = 128
+    hh = np.repeat(np.arange(len(heads)), rows).astype(np.int32)
+    tt = rng.integers(0, w.n, hh.size).astype(np.int32)
+    t1 = time.perf_counter()
+    oracle.attention_rows(q[heads], k[:1], v[:1], hh, tt, rowbits=rb, nthreads=nthreads)
+    t_attn = time.perf_counter() - t1
+    # Pairs visited by the sampled rows vs by every row of the sampled heads.
+    counts = np.unpackbits(rb.view(np.uint8), axis=-1, bitorder="little")[..., :nb]
+    sampled_keys = sum(int(counts[h, t // B, : t // B].sum()) * B + (t % B + 1) for h, t in zip(hh, tt))
+    all_pairs = selected_pairs(rb, nb)
+    layer_s = (t_select + t_attn * all_pairs / max(sampled_keys, 1)) * (w.hq / len(heads))
+    return {
+        "layer_ms": layer_s * 1e3,
+        "sample": (f"oracle proxy map, C_struct route, VS/PE selection and mask for the {len(heads)} query heads of "
+                   f"kv head 0 over all {w.n} keys ({t_select:.2f} s), plus fp64 attention for {hh.size} random query "
+                   f"rows of those heads ({t_attn:.2f} s); scaled by selected (row,key) pairs to all rows and by "
+                   f"{w.hq}/{len(heads)} to all heads"),
+        "seconds": t_select + t_attn,
+    }
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    import synth
+    w = synth.WORKLOADS[args.config]
+    alpha = tuple(int(x) for x in args.alpha.split("/"))
+    q, k, v = w.generate()
+    cores = os.cpu_count() or 1
+    times = []
+    sample = None
+    for i in range(args.warmup + args.steps):
+        r = cpu_sample(w, q, k, v, alpha, nthreads=cores)
+        sample = r["sample"]
+        if i >= args.warmup:
+            times.append(r["layer_ms"])
+    ms = statistics.mean(times)
+    line = {"impl": "reference", "metric": METRIC, "value": ms, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "hq": w.hq, "hkv": w.hkv, "seq_len": w.n, "head_dim": 128,
+                       "alpha": args.alpha},
+            "cpu_baseline": {"value": ms, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": ms, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- GPU arm
+def run_crisp(args):
+    import torch
+    import dynamic_sparse_prefill_crisp_gb300 as crisp
+    import synth
+    from dynamic_sparse_prefill_crisp_gb300 import build as crisp_build
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    if rank == 0:
+        crisp_build.build()
+    barrier(world)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.config]
+    alpha = tuple(int(x) for x in args.alpha.split("/"))
+    hq, hkv, n = w.hq, w.hkv, w.n
+    nb, W = n // B, (n // B + 31) // 32
+
+    # Inputs: generated on the host into pinned buffers (also the e2e source).
+    qh = torch.empty((hq, n, 128), dtype=torch.int16, pin_memory=True)
+    kh = torch.empty((hkv, n, 128), dtype=torch.int16, pin_memory=True)
+    vh = torch.empty((hkv, n, 128), dtype=torch.int16, pin_memory=True)
+    t0 = time.perf_counter()
+    w.generate(qh.numpy().view(np.uint16), kh.numpy().view(np.uint16), vh.numpy().view(np.uint16))
+    gen_s = time.perf_counter() - t0
+    qd = qh.to(dev).view(torch.bfloat16)
+    kd = kh.to(dev).view(torch.bfloat16)
+    vd = vh.to(dev).view(torch.bfloat16)
+    out = torch.empty((hq, n, 128), dtype=torch.bfloat16, device=dev)
+    s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+    params = crisp.params_default(alpha=alpha)
+    ws = torch.empty(crisp.workspace_size(s), dtype=torch.uint8, device=dev)
+    crisp.workspace_init(ws)
+    E = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+    pmap = E((hq, B, n), torch.float32)
+    vmass, smass = E((hq, nb), torch.int64), E((hq, nb), torch.int64)
+    cstruct, total, route = E((hq,), torch.int64), E((hq,), torch.int64), E((hq,), torch.uint8)
+    vbits, sbits = E((hq, W), torch.int32), E((hq, W), torch.int32)
+    pbar = E((hq, nb, nb), torch.float32)
+    pebits, rowbits = E((hq, nb, W), torch.int32), E((hq, nb, W), torch.int32)
+    counts, order = E((hq, nb), torch.int32), E((hq * nb,), torch.int32)
+    stream = torch.cuda.current_stream()
+
+    stages = ["proxy", "masses", "route", "select_vs", "pe_map", "select_pe", "mask", "attention"]
+    calls = [
+        lambda: crisp.proxy_map(s, qd, kd, pmap, ws, stream),
+        lambda: crisp.block_masses(s, pmap, vmass, smass, ws, stream),
+        lambda: crisp.route_cstruct(s, params, vmass, cstruct, total, route, stream),
+        lambda: crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws, stream),
+        lambda: crisp.pe_map(s, qd, kd, route, pbar, ws, stream),
+        lambda: crisp.select_pe(s, params, pbar, route, pebits, ws, stream),
+        lambda: crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, ws, stream),
+        lambda: crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws, stream),
+    ]
+    # our kernel launches per step: proxy 3, masses 2, route 1, select_vs 1,
+    # pe_map 3, select_pe 1, mask+schedule 6, attention 1
+    launches_per_step = 18
+
+    def step(events=None):
+        for i, c in enumerate(calls):
+            if events is not None:
+                events[i].record(stream)
+            c()
+        if events is not None:
+            events[-1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = crisp.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {crisp.status_string(st)}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, world, dev)
+    ms_per_step = ms_total / args.steps
+    stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                for j, name in enumerate(stages)}
+    st = crisp.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {crisp.status_string(st)}")
+
+    # Algorithmic work of the step's results.
+    rb = rowbits.cpu().numpy().view(np.uint32)
+    pairs = selected_pairs(rb, nb)
+    flops = 4 * 128 * pairs
+    dense_pairs = hq * n * (n + 1) // 2
+    routes = route.cpu().numpy()
+    hbm_peak, tf_peak, peak_kind = measured_peaks()
+    attn_ms = stage_ms["attention"]
+    achieved_tf = flops / (attn_ms * 1e-3) / 1e12
+    proxy_bytes = 4 * hq * B * n + 2 * (2 * hkv * n * 128) + 2 * hq * B * 128
+    masses_bytes = 4 * hq * B * n
+
+    # Dense attention over every causal block, same inputs, same run.
+    dense = None
+    if not args.no_dense:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        crisp.dense_prefill(s, qd, kd, vd, out, ws, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        d_ms = e0.elapsed_time(e1)
+        dense = {"ms": d_ms, "tflops": 4 * 128 * dense_pairs / (d_ms * 1e-3) / 1e12,
+                 "attention_speedup": d_ms / attn_ms, "layer_speedup": d_ms / ms_per_step}
+        crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws, stream)
+
+    # End to end through the public API: pinned host -> device, the whole
+    # layer (crisp_prefill_layer), device -> pinned host of the output.
+    e2e = None
+    if not args.no_e2e:
+        lws = torch.empty(crisp.layer_workspace_size(s), dtype=torch.uint8, device=dev)
+        crisp.workspace_init(lws)
+        oh = torch.empty((hq, n, 128), dtype=torch.int16, pin_memory=True)
+        qx, kx, vx = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        ox = torch.empty_like(out)
+
+        def e2e_step():
+            qx.view(torch.int16).copy_(qh, non_blocking=True)
+            kx.view(torch.int16).copy_(kh, non_blocking=True)
+            vx.view(torch.int16).copy_(vh, non_blocking=True)
+            crisp.prefill_layer(s, params, qx, kx, vx, ox, lws, stream)
+            oh.copy_(ox.view(torch.int16), non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, dev)
+        if crisp.read_status(lws) != 0:
+            raise RuntimeError("device status after e2e")
+        assert torch.equal(oh.view(torch.bfloat16).to(dev), out), "e2e output differs from the device-resident run"
+        h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
+        e2e = {"value": e2e_ms / world, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": oh.numel() * 2}
+        del lws, qx, kx, vx, ox
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        r = cpu_sample(w, qh.numpy().view(np.uint16), kh.numpy().view(np.uint16), vh.numpy().view(np.uint16), alpha,
+                       nthreads=os.cpu_count())
+        cpu = {"value": r["layer_ms"], "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": r["sample"]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": ms_per_step / world, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, planted sink/slash/needle structure)",
+            "config": {"workload": w.name, "hq": hq, "hkv": hkv, "seq_len": n, "head_dim": 128, "block": B,
+                       "alpha": args.alpha, "tau": "1/5", "gamma": "19/20", "kmin_blocks": 8,
+                       "l2": "inputs (6 GiB) larger than L2; no flush", "parallelism": f"replicas x{world}"},
+            "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "routes": {"vs": int(routes.sum()), "pe": int((routes == 0).sum())},
+            "density": pairs / dense_pairs,
+            "eff_tflops": achieved_tf,
+            "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": achieved_tf, "peak": tf_peak,
+                         "unit": "TFLOP/s", "frac": achieved_tf / tf_peak, "traffic": None,
+                         "peak_kind": f"bf16 dense, {peak_kind} (sustained)"},
+            "hbm": {"proxy_gbs": proxy_bytes / (stage_ms["proxy"] * 1e-3) / 1e9,
+                    "masses_gbs": masses_bytes / (stage_ms["masses"] * 1e-3) / 1e9, "peak_gbs": hbm_peak,
+                    "route_select_frac": (masses_bytes / ((stage_ms["masses"] + stage_ms["route"] +
+                                                           stage_ms["select_vs"]) * 1e-3) / 1e9) / hbm_peak},
+            "dense": dense,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "gen_seconds": gen_s,
+        }
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_crisp(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -46,8 +46,12 @@ def check_index_sets(r, params):
     assert np.array_equal(pe, r["pebits"])
     rb = oracle.build_mask(route, vb, sb, pe)
     assert np.array_equal(rb, r["rowbits"])
-    pop = np.unpackbits(rb.view(np.uint8), axis=-1).sum(-1)
+    pop = np.unpackbits(rb.view(np.uint8), axis=-1).sum(-1).astype(np.int64)
     assert np.array_equal(pop, r["counts"])
+    # schedule: a permutation of the rows with non-increasing counts
+    order = r["order"]
+    assert np.array_equal(np.sort(order), np.arange(order.size))
+    assert np.all(np.diff(pop.reshape(-1)[order]) <= 0)
     return rb, route
 
 
@@ -158,8 +162,7 @@ def test_sparse_prefill_arbitrary_masks():
     s = crisp.make_shape(hq, hkv, n, qd, kd, out)
     ws = new_workspace(s)
     rbd = torch.from_numpy(rb.view(np.int32)).cuda()
-    cnt = torch.from_numpy(np.unpackbits(rb.view(np.uint8), axis=-1).sum(-1).astype(np.int32)).cuda()
-    crisp.sparse_prefill(s, qd, kd, vd, rbd, cnt, out, ws)
+    crisp.sparse_prefill(s, qd, kd, vd, rbd, None, out, ws)  # default order: query blocks descending
     torch.cuda.synchronize()
     assert_status_ok(ws)
     rb_causal = rb.copy()
