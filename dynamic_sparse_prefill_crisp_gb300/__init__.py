@@ -48,7 +48,7 @@ class Params(ctypes.Structure):
 class LayerViews(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in
                 ("pmap", "vmass", "smass", "cstruct", "total", "route", "vbits", "sbits", "pbar", "pebits",
-                 "rowbits", "counts")]
+                 "rowbits", "counts", "order")]
 
 
 def lib():
@@ -66,12 +66,13 @@ def lib():
         L.crisp_layer_workspace_size.argtypes = [P(Shape), P(sz)]
         L.crisp_workspace_init.argtypes = [vp, sz, st]
         L.crisp_proxy_map.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
+        L.crisp_proxy_map_noalloc.argtypes = [P(Shape), vp, vp, vp, st]
         L.crisp_block_masses.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
         L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
         L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
         L.crisp_pe_map.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
         L.crisp_select_pe.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, sz, st]
-        L.crisp_build_mask.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, st]
+        L.crisp_build_mask.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, vp, sz, st]
         L.crisp_sparse_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, st]
         L.crisp_dense_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
         L.crisp_layer_views_get.argtypes = [P(Shape), vp, P(LayerViews)]
@@ -80,6 +81,7 @@ def lib():
         L.crisp_status_string.argtypes = [ctypes.c_int]
         L.crisp_status_string.restype = ctypes.c_char_p
         for name in ("crisp_workspace_size", "crisp_layer_workspace_size", "crisp_workspace_init", "crisp_proxy_map",
+                     "crisp_proxy_map_noalloc",
                      "crisp_block_masses", "crisp_route_cstruct", "crisp_select_vs", "crisp_pe_map",
                      "crisp_select_pe", "crisp_build_mask", "crisp_sparse_prefill", "crisp_dense_prefill",
                      "crisp_layer_views_get", "crisp_prefill_layer", "crisp_read_status"):
@@ -157,6 +159,13 @@ def proxy_map(shape, q, k, pmap, ws, stream=None):
                                  _stream(stream)), "crisp_proxy_map")
 
 
+def proxy_map_noalloc(shape, q, k, pmap, stream=None):
+    """crisp_proxy_map with the library's static scratch instead of a workspace
+    (for callers that cannot allocate device memory; see include/crisp.h)."""
+    _check(lib().crisp_proxy_map_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(pmap), _stream(stream)),
+           "crisp_proxy_map_noalloc")
+
+
 def block_masses(shape, pmap, vmass, smass, ws, stream=None):
     _check(lib().crisp_block_masses(ctypes.byref(shape), _ptr(pmap), _ptr(vmass), _ptr(smass), _ptr(ws), _nbytes(ws),
                                     _stream(stream)), "crisp_block_masses")
@@ -182,14 +191,15 @@ def select_pe(shape, params, pbar, route, pebits, ws, stream=None):
                                  _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_select_pe")
 
 
-def build_mask(shape, route, vbits, sbits, pebits, rowbits, counts, ws, stream=None):
+def build_mask(shape, route, vbits, sbits, pebits, rowbits, counts, order, ws, stream=None):
     _check(lib().crisp_build_mask(ctypes.byref(shape), _ptr(route), _ptr(vbits), _ptr(sbits), _ptr(pebits),
-                                  _ptr(rowbits), _ptr(counts), _ptr(ws), _nbytes(ws), _stream(stream)),
+                                  _ptr(rowbits), _ptr(counts), _ptr(order), _ptr(ws), _nbytes(ws), _stream(stream)),
            "crisp_build_mask")
 
 
-def sparse_prefill(shape, q, k, v, rowbits, counts, out, ws, stream=None):
-    _check(lib().crisp_sparse_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(rowbits), _ptr(counts),
+def sparse_prefill(shape, q, k, v, rowbits, order, out, ws, stream=None):
+    """order: the schedule from build_mask, or None (query blocks descending)."""
+    _check(lib().crisp_sparse_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(rowbits), _ptr(order),
                                       _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_sparse_prefill")
 
 

@@ -112,7 +112,6 @@ ScratchLayout scratch_layout(const crisp_shape& s) {
   L.qbar = o;        o = up(o + hq * nb * kD * 4);
   L.kbar = o;        o = up(o + hkv * nb * kD * 4);
   L.srev = o;        o = up(o + hq * (W + 2) * 4);
-  L.order = o;       o = up(o + hq * nb * 4);
   L.bucket = o;      o = up(o + (nb + 2) * 4);
   L.total = o;
   return L;
@@ -134,6 +133,7 @@ LayerLayout layer_layout(const crisp_shape& s) {
   L.pebits = o;     o = up(o + hq * nb * W * 4);
   L.rowbits = o;    o = up(o + hq * nb * W * 4);
   L.counts = o;     o = up(o + hq * nb * 4);
+  L.order = o;      o = up(o + hq * nb * 4);
   L.total = o;
   return L;
 }
@@ -192,6 +192,66 @@ crisp_status crisp_proxy_map(const crisp_shape* shape, const void* q, const void
   if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
   maps.v = maps.k;
   return from_cuda(launch_proxy(s, maps, pmap, static_cast<char*>(ws), stream));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Proxy map for callers that cannot allocate: the scratch of the proxy
+// kernels (status word + per-chunk statistics, the first regions of the
+// workspace layout) lives in this static device array instead of a caller
+// workspace. Every GPU that loads the library holds it until exit.
+namespace crisp {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) unsigned char g_proxy_scratch[kNoAllocScratchBytes];
+
+// Device address of g_proxy_scratch on the current device; looked up once per
+// device (host code only sees a host-side stand-in for the symbol).
+crisp_status noalloc_scratch(char** out) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CRISP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return CRISP_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_proxy_scratch) != cudaSuccess || p == nullptr) return CRISP_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = static_cast<char*>(addr[dev]);
+  return CRISP_OK;
+}
+
+}  // namespace
+}  // namespace crisp
+
+extern "C" {
+
+crisp_status crisp_proxy_map_noalloc(const crisp_shape* shape, const void* q, const void* k, float* pmap,
+                                     crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!q || !k || !pmap) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(pmap)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  // The proxy kernels touch only the status word and the two statistics
+  // regions, which end where the mass scratch begins.
+  const ScratchLayout L = scratch_layout(s);
+  if (L.mass_lower > kNoAllocScratchBytes) return CRISP_ERR_WORKSPACE;
+  if ((st = check_device()) != CRISP_OK) return st;
+  char* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != CRISP_OK) return st;
+  TmaMaps maps;
+  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  maps.v = maps.k;
+  // The array keeps the previous call's contents: start from a clear status.
+  if (cudaMemsetAsync(scratch + L.status, 0, sizeof(DevStatus), stream) != cudaSuccess) return CRISP_ERR_CUDA;
+  return from_cuda(launch_proxy(s, maps, pmap, scratch, stream));
 }
 
 crisp_status crisp_block_masses(const crisp_shape* shape, const float* pmap, uint64_t* vmass, uint64_t* smass,
@@ -259,26 +319,28 @@ crisp_status crisp_select_pe(const crisp_shape* shape, const crisp_params* param
 
 crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t* route, const uint32_t* vbits,
                               const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits, int32_t* counts,
-                              void* ws, size_t ws_bytes, crisp_stream_t stream) {
+                              int32_t* order, void* ws, size_t ws_bytes, crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
   if (st != CRISP_OK) return st;
-  if (!route || !vbits || !sbits || !pebits || !rowbits || !counts) return CRISP_ERR_INVALID_ARG;
-  if (!aligned(vbits, 4) || !aligned(sbits, 4) || !aligned(pebits, 4) || !aligned(rowbits, 4) || !aligned(counts, 4))
+  if (!route || !vbits || !sbits || !pebits || !rowbits || !counts || !order) return CRISP_ERR_INVALID_ARG;
+  if (!aligned(vbits, 4) || !aligned(sbits, 4) || !aligned(pebits, 4) || !aligned(rowbits, 4) ||
+      !aligned(counts, 4) || !aligned(order, 4))
     return CRISP_ERR_ALIGN;
   const crisp_shape s = normalised(*shape);
   if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_build_mask(s, route, vbits, sbits, pebits, rowbits, counts, static_cast<char*>(ws), stream));
+  return from_cuda(
+      launch_build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, static_cast<char*>(ws), stream));
 }
 
 static crisp_status attention_common(const crisp_shape* shape, const void* q, const void* k, const void* v,
-                                     const uint32_t* rowbits, const int32_t* counts, void* out, void* ws,
+                                     const uint32_t* rowbits, const int32_t* order, void* out, void* ws,
                                      size_t ws_bytes, crisp_stream_t stream, bool dense) {
   crisp_status st = check_shape(shape);
   if (st != CRISP_OK) return st;
-  if (!q || !k || !v || !out || (!dense && (!rowbits || !counts))) return CRISP_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || (!dense && !rowbits)) return CRISP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
-  if (!dense && (!aligned(rowbits, 4) || !aligned(counts, 4))) return CRISP_ERR_ALIGN;
+  if (!dense && (!aligned(rowbits, 4) || !aligned(order, 4))) return CRISP_ERR_ALIGN;
   const crisp_shape s = normalised(*shape);
   if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
@@ -286,13 +348,13 @@ static crisp_status attention_common(const crisp_shape* shape, const void* q, co
   if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
   if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
   if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-  return from_cuda(launch_attention(s, maps, rowbits, counts, out, static_cast<char*>(ws), dense, stream));
+  return from_cuda(launch_attention(s, maps, rowbits, order, out, static_cast<char*>(ws), dense, stream));
 }
 
 crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v,
-                                  const uint32_t* rowbits, const int32_t* counts, void* out, void* ws,
+                                  const uint32_t* rowbits, const int32_t* order, void* out, void* ws,
                                   size_t ws_bytes, crisp_stream_t stream) {
-  return attention_common(shape, q, k, v, rowbits, counts, out, ws, ws_bytes, stream, false);
+  return attention_common(shape, q, k, v, rowbits, order, out, ws, ws_bytes, stream, false);
 }
 
 crisp_status crisp_dense_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v, void* out,
@@ -318,6 +380,7 @@ crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws, crisp_lay
   views->pebits = reinterpret_cast<uint32_t*>(b + L.pebits);
   views->rowbits = reinterpret_cast<uint32_t*>(b + L.rowbits);
   views->counts = reinterpret_cast<int32_t*>(b + L.counts);
+  views->order = reinterpret_cast<int32_t*>(b + L.order);
   return CRISP_OK;
 }
 
@@ -346,8 +409,9 @@ crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* p
       launch_select_vs(s, *params, w.vmass, w.smass, w.route, w.vbits, w.sbits, stream) != cudaSuccess ||
       launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess ||
       launch_select_pe(s, *params, w.pbar, w.route, w.pebits, stream) != cudaSuccess ||
-      launch_build_mask(s, w.route, w.vbits, w.sbits, w.pebits, w.rowbits, w.counts, wsb, stream) != cudaSuccess ||
-      launch_attention(s, maps, w.rowbits, w.counts, out, wsb, false, stream) != cudaSuccess)
+      launch_build_mask(s, w.route, w.vbits, w.sbits, w.pebits, w.rowbits, w.counts, w.order, wsb, stream) !=
+          cudaSuccess ||
+      launch_attention(s, maps, w.rowbits, w.order, out, wsb, false, stream) != cudaSuccess)
     return CRISP_ERR_CUDA;
   return CRISP_OK;
 }

@@ -120,6 +120,30 @@ CRISP_API crisp_status crisp_workspace_init(void* ws, size_t ws_bytes, crisp_str
 CRISP_API crisp_status crisp_proxy_map(const crisp_shape* shape, const void* q, const void* k, float* pmap, void* ws,
                              size_t ws_bytes, crisp_stream_t stream);
 
+/* crisp_proxy_map without a caller-provided workspace. The paper has no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory when they run this step -- for example a serving
+ * engine that hands all free device memory to its own pool at start-up, or
+ * code that must not call cudaMalloc because it synchronises the device and
+ * would stall work on other streams. Inputs and the output are as for
+ * crisp_proxy_map; q, k and pmap are still the caller's buffers.
+ *
+ * Scratch: the per-chunk softmax statistics live in one 32 MiB array in the
+ * library's static device memory, held on every GPU that loads the library
+ * until the process exits. A shape needs 256 + 8*128*hq*(2*ceil(nb/16) + 1)
+ * bytes of it, rounded up to 256-byte units (the 512k-token, 32-head layer
+ * needs about 16.8 MB); larger shapes are rejected with CRISP_ERR_WORKSPACE
+ * and nothing is launched. The first call on a device looks up the array's
+ * device address (once per device, with that device current), so make that
+ * first call before any stream capture. Every call shares the one array:
+ * calls whose kernels overlap on the GPU (other streams, other threads)
+ * race and corrupt each other's statistics; calls serialised on one stream
+ * are safe. The status word in the array is cleared by every call; a device
+ * wait that times out is recorded there but cannot be read by the caller.
+ * Allocates nothing (no cudaMalloc/cudaFree, no allocating library call). */
+CRISP_API crisp_status crisp_proxy_map_noalloc(const crisp_shape* shape, const void* q, const void* k, float* pmap,
+                                               crisp_stream_t stream);
+
 /* A3. Block masses of the proxy map ("mass at Vertical-Slash compatible
  * positions", ai-feeds page, "方法"). With q(p) the Q32 quantum:
  *   vmass[h][c] = sum over rows r and key columns j of block c of q(pmap[h][r][j])
@@ -178,22 +202,28 @@ CRISP_API crisp_status crisp_select_pe(const crisp_shape* shape, const crisp_par
  *            (a 128-wide diagonal band at offset block s crosses key blocks
  *            qb-s and qb-s-1);
  *   PE head: pebits row qb within [0, qb].
- * rowbits: uint32 [hq][nb][W]; counts: int32 [hq][nb] = blocks per row. */
+ * and the attention schedule: rows ordered by block count, largest first.
+ * rowbits: uint32 [hq][nb][W]; counts: int32 [hq][nb] = blocks per row;
+ * order: int32 [hq*nb], a permutation of the row ids h*nb + qb with
+ * non-increasing counts (the order among equal counts is unspecified). */
 CRISP_API crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t* route, const uint32_t* vbits,
-                              const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits, int32_t* counts,
-                              void* ws, size_t ws_bytes, crisp_stream_t stream);
+                                        const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits,
+                                        int32_t* counts, int32_t* order, void* ws, size_t ws_bytes,
+                                        crisp_stream_t stream);
 
 /* A8. Exact causal GQA softmax attention over the selected blocks (ai.info
  * page, "Why This Matters": exact softmax attention over the blocks it
  * selects): for token i in query block qb of head h,
  *   out_i = sum_{j in A(i)} softmax_j(scale * q_i . k_j) v_j,
  *   A(i) = { j <= i : block(j) in rowbits[h][qb] }.
- * Rows with an empty A(i) are written as zeros. q bf16 [hq][n][128]; k, v
- * bf16 [hkv][n][128]; rowbits, counts from crisp_build_mask; out bf16
- * [hq][n][128] (o strides). */
+ * Bits above the diagonal block are ignored; rows with an empty A(i) are
+ * written as zeros. q bf16 [hq][n][128]; k, v bf16 [hkv][n][128]; rowbits
+ * from crisp_build_mask; order: the schedule from crisp_build_mask, or NULL
+ * for query blocks in descending order (any permutation of the row ids gives
+ * the same result); out bf16 [hq][n][128] (o strides). */
 CRISP_API crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v,
-                                  const uint32_t* rowbits, const int32_t* counts, void* out, void* ws,
-                                  size_t ws_bytes, crisp_stream_t stream);
+                                            const uint32_t* rowbits, const int32_t* order, void* out, void* ws,
+                                            size_t ws_bytes, crisp_stream_t stream);
 
 /* A9. Dense causal attention (A(i) = [0, i]): the exact baseline the paper
  * compares against ("FlashAttention (exact dense)", ai.info page). */
@@ -208,7 +238,7 @@ typedef struct crisp_layer_views {
   uint32_t *vbits, *sbits;
   float* pbar;
   uint32_t *pebits, *rowbits;
-  int32_t* counts;
+  int32_t *counts, *order;
 } crisp_layer_views;
 
 /* Fills *views (host) with pointers into `ws` for this shape. */
