@@ -213,20 +213,19 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc_fence_after();
       const bool diag = bars.has_diag && j == count - 1;  // ascending order: qb is last
-      float x[128];
+      uint32_t sv[128];
+      tmem_ld128(s_addr, sv);
+      if (diag) {
+        // Causal edge: key jj of the diagonal block is visible to row r iff jj <= r.
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(s_addr + cc * 32, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float val = __uint_as_float(v[e]) * c_log2;
-          x[cc * 32 + e] = (diag && cc * 32 + e > r) ? -INFINITY : val;
-        }
+        for (int e = 0; e < 128; ++e)
+          if (e > r) sv[e] = 0xff800000u;  // -inf
       }
-      float mx = x[0];
+      // Row max on the raw scores (c > 0, so max(s*c) = max(s)*c exactly).
+      float mx_raw = __uint_as_float(sv[0]);
 #pragma unroll
-      for (int e = 1; e < 128; ++e) mx = fmaxf(mx, x[e]);
+      for (int e = 1; e < 128; ++e) mx_raw = fmaxf(mx_raw, __uint_as_float(sv[e]));
+      const float mx = mx_raw * c_log2;
       if (j == 0) {
         m_ref = mx;
       } else if (__any_sync(0xffffffffu, mx > m_ref + kRescaleLog2)) {
@@ -251,16 +250,19 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_st16(o_addr + cc * 32 + 16, b);
         }
       }
-      float sum = 0.f;
+      // p = 2^(s*c - m): one FFMA and one MUFU per element.
+      const float neg_m = -m_ref;
+      float sum0 = 0.f, sum1 = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
-        const float p0 = ex2_approx(x[2 * e] - m_ref);
-        const float p1 = ex2_approx(x[2 * e + 1] - m_ref);
-        sum += p0 + p1;
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), c_log2, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), c_log2, neg_m));
+        sum0 += p0;
+        sum1 += p1;
         pk[e] = pack_bf16x2(p0, p1);
       }
-      l += sum;
+      l += sum0 + sum1;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t a[16];
@@ -324,16 +326,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 }  // namespace
 
 cudaError_t launch_attention(const crisp_shape& s, const TmaMaps& maps, const uint32_t* rowbits,
-                             const int32_t* counts, void* out, char* ws, bool dense, cudaStream_t st) {
+                             const int32_t* order, void* out, char* ws, bool dense, cudaStream_t st) {
   const ScratchLayout L = scratch_layout(s);
   const int nb = num_blocks(s.seq_len);
   auto* status = reinterpret_cast<DevStatus*>(ws + L.status);
-  const int32_t* order = nullptr;
-  if (!dense) {
-    cudaError_t e = launch_row_order(s, counts, ws, st);
-    if (e != cudaSuccess) return e;
-    order = reinterpret_cast<const int32_t*>(ws + L.order);
-  }
+  if (dense) order = nullptr;
   cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int items = s.hq * nb;

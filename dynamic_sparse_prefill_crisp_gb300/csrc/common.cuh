@@ -26,9 +26,25 @@ __device__ __forceinline__ void report_error(DevStatus* st, uint32_t code, uint3
   if (atomicCAS(&st->code, 0u, code) == 0u) atomicExch(&st->detail, detail);
 }
 
-// Q32 quantum of a probability: round-half-even(p * 2^32). p * 2^32 is exact
-// in fp32 for p in [0, 1]; the conversion rounds to nearest even.
-__device__ __forceinline__ uint64_t q32(float p) { return __float2ull_rn(p * 4294967296.0f); }
+// Q32 quantum of a probability: round-half-even(p * 2^32); p * 2^32 is exact
+// in fp32. No float->64-bit conversion instruction is used (on this GPU those
+// run on the FP64 pipe): below 2^23, adding 2^23 in fp32 rounds the value to
+// the nearest even integer, whose bits minus those of 2^23 are the result;
+// from 2^23 up the product is already an integer, rebuilt from its exponent
+// and mantissa.
+constexpr float kTwo23 = 8388608.0f;
+__device__ __forceinline__ uint32_t q32_small(float x) {  // x = p * 2^32 < 2^23
+  return __float_as_uint(x + kTwo23) - 0x4B000000u;
+}
+__device__ __forceinline__ uint64_t q32_large(float x) {  // x = p * 2^32 >= 2^23
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t sh = min((b >> 23) - 150u, 40u);
+  return static_cast<uint64_t>((b & 0x7FFFFFu) | 0x800000u) << sh;
+}
+__device__ __forceinline__ uint64_t q32(float p) {
+  const float x = p * 4294967296.0f;
+  return x < kTwo23 ? static_cast<uint64_t>(q32_small(x)) : q32_large(x);
+}
 
 inline int num_blocks(int n) { return n / kB; }
 inline int bit_words(int nb) { return (nb + 31) / 32; }
@@ -44,14 +60,13 @@ struct ScratchLayout {
   size_t qbar;         // float  [hq][nb][128]
   size_t kbar;         // float  [hkv][nb][128]
   size_t srev;         // uint32 [hq][W + 2]  slash bits reversed
-  size_t order;        // int32  [hq * nb]    attention work order
   size_t bucket;       // int32  [nb + 2]     counting-sort buckets
   size_t total;
 };
 
 // Intermediates of crisp_prefill_layer, placed after the scratch.
 struct LayerLayout {
-  size_t pmap, vmass, smass, cstruct, total_mass, route, vbits, sbits, pbar, pebits, rowbits, counts;
+  size_t pmap, vmass, smass, cstruct, total_mass, route, vbits, sbits, pbar, pebits, rowbits, counts, order;
   size_t total;
 };
 
@@ -77,9 +92,8 @@ cudaError_t launch_select_pe(const crisp_shape& s, const crisp_params& p, const 
                              uint32_t* pebits, cudaStream_t st);
 cudaError_t launch_build_mask(const crisp_shape& s, const uint8_t* route, const uint32_t* vbits,
                               const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits, int32_t* counts,
-                              char* ws, cudaStream_t st);
-cudaError_t launch_row_order(const crisp_shape& s, const int32_t* counts, char* ws, cudaStream_t st);
+                              int32_t* order, char* ws, cudaStream_t st);
 cudaError_t launch_attention(const crisp_shape& s, const TmaMaps& maps, const uint32_t* rowbits,
-                             const int32_t* counts, void* out, char* ws, bool dense, cudaStream_t st);
+                             const int32_t* order, void* out, char* ws, bool dense, cudaStream_t st);
 
 }  // namespace crisp

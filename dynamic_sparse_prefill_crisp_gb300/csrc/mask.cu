@@ -72,6 +72,11 @@ __global__ void mask_kernel(const uint8_t* __restrict__ route, const uint32_t* _
 }
 
 // Counting sort of the rows by count, descending.
+__global__ void bucket_clear(int32_t* __restrict__ bucket, int len) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < len) bucket[i] = 0;
+}
+
 __global__ void count_hist(const int32_t* __restrict__ counts, int items, int nb, int32_t* __restrict__ bucket) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < items) atomicAdd(&bucket[min(max(counts[i], 0), nb)], 1);
@@ -114,24 +119,16 @@ __global__ void count_scatter(const int32_t* __restrict__ counts, int items, int
 
 cudaError_t launch_build_mask(const crisp_shape& s, const uint8_t* route, const uint32_t* vbits,
                               const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits, int32_t* counts,
-                              char* ws, cudaStream_t st) {
-  const ScratchLayout L = scratch_layout(s);
-  const int nb = num_blocks(s.seq_len);
-  auto* srev = reinterpret_cast<uint32_t*>(ws + L.srev);
-  srev_kernel<<<s.hq, 128, 0, st>>>(sbits, route, nb, srev);
-  mask_kernel<<<dim3(nb, s.hq), 128, 0, st>>>(route, vbits, srev, pebits, nb, rowbits, counts);
-  return cudaGetLastError();
-}
-
-// Used by the attention launcher: order[] = row ids sorted by count desc.
-cudaError_t launch_row_order(const crisp_shape& s, const int32_t* counts, char* ws, cudaStream_t st) {
+                              int32_t* order, char* ws, cudaStream_t st) {
   const ScratchLayout L = scratch_layout(s);
   const int nb = num_blocks(s.seq_len);
   const int items = s.hq * nb;
+  auto* srev = reinterpret_cast<uint32_t*>(ws + L.srev);
   auto* bucket = reinterpret_cast<int32_t*>(ws + L.bucket);
-  auto* order = reinterpret_cast<int32_t*>(ws + L.order);
-  cudaError_t e = cudaMemsetAsync(bucket, 0, sizeof(int32_t) * (nb + 2), st);
-  if (e != cudaSuccess) return e;
+  srev_kernel<<<s.hq, 128, 0, st>>>(sbits, route, nb, srev);
+  mask_kernel<<<dim3(nb, s.hq), 128, 0, st>>>(route, vbits, srev, pebits, nb, rowbits, counts);
+  // Schedule: row ids sorted by count, descending (counting sort).
+  bucket_clear<<<(nb + 2 + 255) / 256, 256, 0, st>>>(bucket, nb + 2);
   count_hist<<<(items + 255) / 256, 256, 0, st>>>(counts, items, nb, bucket);
   count_scan<<<1, 1024, 0, st>>>(bucket, nb);
   count_scatter<<<(items + 255) / 256, 256, 0, st>>>(counts, items, nb, bucket, order);

@@ -31,15 +31,31 @@ __global__ void __launch_bounds__(kMassThreads) mass_tiles(const float* __restri
 #pragma unroll
   for (int k = 0; k < 16; ++k)
     p[k] = __ldcs(reinterpret_cast<const float4*>(base + static_cast<size_t>(rg * 16 + k) * n));
-  uint64_t all = 0, lo = 0;
+  // Quanta below 2^23 (nearly all of them) are summed in 32 bits: 64 of them
+  // stay below 2^29. Larger ones go to 64-bit sums.
+  uint32_t all32 = 0, lo32 = 0;
+  uint64_t all64 = 0, lo64 = 0;
+  const int jj = cq * 4;
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
     const int r = rg * 16 + k;
-    const int jj = cq * 4;
-    const uint64_t a = q32(p[k].x), b = q32(p[k].y), d = q32(p[k].z), e = q32(p[k].w);
-    all += a + b + d + e;
-    lo += (r >= jj ? a : 0) + (r >= jj + 1 ? b : 0) + (r >= jj + 2 ? d : 0) + (r >= jj + 3 ? e : 0);
+    const float x[4] = {p[k].x * 4294967296.0f, p[k].y * 4294967296.0f, p[k].z * 4294967296.0f,
+                        p[k].w * 4294967296.0f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool lower = r >= jj + e;
+      if (x[e] < kTwo23) {
+        const uint32_t f = q32_small(x[e]);
+        all32 += f;
+        lo32 += lower ? f : 0u;
+      } else {
+        const uint64_t f = q32_large(x[e]);
+        all64 += f;
+        lo64 += lower ? f : 0ull;
+      }
+    }
   }
+  const uint64_t all = all64 + all32, lo = lo64 + lo32;
   uint64_t v[3] = {all, lo, all - lo};
 #pragma unroll
   for (int t = 0; t < 3; ++t) v[t] = warp_sum(v[t]);

@@ -56,21 +56,23 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
     pebits = empty((hq, nb, W), torch.int32)
     rowbits = empty((hq, nb, W), torch.int32)
     counts = empty((hq, nb), torch.int32)
+    order = empty((hq * nb,), torch.int32)
     crisp.proxy_map(s, qd, kd, pmap, ws)
     crisp.block_masses(s, pmap, vmass, smass, ws)
     crisp.route_cstruct(s, params, vmass, cstruct, total, route)
     crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws)
     crisp.pe_map(s, qd, kd, route, pbar, ws)
     crisp.select_pe(s, params, pbar, route, pebits, ws)
-    crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, ws)
-    crisp.sparse_prefill(s, qd, kd, vd, rowbits, counts, out, ws)
+    crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, ws)
+    crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws)
     torch.cuda.synchronize()
     assert_status_ok(ws)
     u64 = lambda t: t.cpu().numpy().view(np.uint64)
     u32 = lambda t: t.cpu().numpy().view(np.uint32)
     return dict(pmap=pmap.cpu().numpy(), vmass=u64(vmass), smass=u64(smass), cstruct=u64(cstruct), total=u64(total),
                 route=route.cpu().numpy(), vbits=u32(vbits), sbits=u32(sbits), pbar=pbar.cpu().numpy(),
-                pebits=u32(pebits), rowbits=u32(rowbits), counts=counts.cpu().numpy(), out=out)
+                pebits=u32(pebits), rowbits=u32(rowbits), counts=counts.cpu().numpy(), order=order.cpu().numpy(),
+                out=out)
 
 
 def attn_error(out_dev_or_np, ref):

@@ -98,6 +98,8 @@ def test_null_and_misaligned_pointers(L):
     assert L.crisp_proxy_map(ctypes.byref(s), vp(8), vp(16), vp(16), vp(256), 1 << 30, None) == 3
     assert L.crisp_sparse_prefill(ctypes.byref(s), vp(16), vp(16), vp(16), None, vp(16), vp(16), vp(256), 1 << 30,
                                   None) == 1
+    assert L.crisp_sparse_prefill(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(18), vp(16), vp(256), 1 << 30,
+                                  None) == 3
     # workspace missing / misaligned / too small
     assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), None, 1 << 30, None) == 4
     assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), vp(272), 1 << 30, None) == 3
