@@ -1,0 +1,66 @@
+"""The multi-rank logic of bench.py on CPU: two gloo ranks on 127.0.0.1.
+
+Each rank runs its own replica of the layer; the timed region is closed by a
+barrier and the reported time is the max over ranks. The reference arm runs
+on rank 0 only; other ranks exit 0 without work.
+"""
+import os
+import socket
+
+import numpy as np
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, results):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    bench.dist_init(world, "gloo")
+    t = bench.max_over_ranks(10.0 + 5.0 * rank, world)
+    bench.barrier(world)
+    results[rank] = (t,) + bench.dist_info()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_barrier_with_gloo():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    manager = ctx.Manager()
+    results = manager.dict()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, results)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert results[0] == (15.0, 0, 2, 0)
+    assert results[1] == (15.0, 1, 2, 1)
+
+
+def test_single_rank_is_identity():
+    assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.run_reference(bench.parse_args(["--impl", "reference"])) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_selected_pairs_counts_the_causal_half_of_the_diagonal():
+    nb = 3
+    rb = np.zeros((1, nb, 1), np.uint32)
+    rb[0, 0, 0] = 0b001  # diagonal only
+    rb[0, 1, 0] = 0b011  # one off-diagonal + diagonal
+    rb[0, 2, 0] = 0b001  # one off-diagonal, no diagonal
+    assert bench.selected_pairs(rb, nb) == 2 * (128 * 129 // 2) + 2 * 128 * 128
