@@ -221,11 +221,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int e = 0; e < 128; ++e)
           if (e > r) sv[e] = 0xff800000u;  // -inf
       }
-      // Row max on the raw scores (c > 0, so max(s*c) = max(s)*c exactly).
-      float mx_raw = __uint_as_float(sv[0]);
+      // Row max on the raw scores (c > 0, so max(s*c) = max(s)*c exactly):
+      // 3-input max in two independent chains.
+      float ma = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+      float mb = fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
 #pragma unroll
-      for (int e = 1; e < 128; ++e) mx_raw = fmaxf(mx_raw, __uint_as_float(sv[e]));
-      const float mx = mx_raw * c_log2;
+      for (int e = 6; e + 3 < 128; e += 4) {
+        ma = fmax3(ma, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+        mb = fmax3(mb, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+      }
+      const float mx = fmaxf(fmax3(ma, mb, __uint_as_float(sv[126])), __uint_as_float(sv[127])) * c_log2;
       if (j == 0) {
         m_ref = mx;
       } else if (__any_sync(0xffffffffu, mx > m_ref + kRescaleLog2)) {
@@ -250,19 +255,23 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_st16(o_addr + cc * 32 + 16, b);
         }
       }
-      // p = 2^(s*c - m): one FFMA and one MUFU per element.
+      // p = 2^(s*c - m): a packed FMA and a packed add per element pair, one
+      // MUFU per element; two accumulator pairs for the row sum.
       const float neg_m = -m_ref;
-      float sum0 = 0.f, sum1 = 0.f;
+      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
       uint32_t pk[64];
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), c_log2, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), c_log2, neg_m));
-        sum0 += p0;
-        sum1 += p1;
+      for (int e = 0; e < 64; e += 2) {
+        float x0, x1, x2, x3;
+        ffma2(x0, x1, __uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]), c_log2, c_log2, neg_m, neg_m);
+        ffma2(x2, x3, __uint_as_float(sv[2 * e + 2]), __uint_as_float(sv[2 * e + 3]), c_log2, c_log2, neg_m, neg_m);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+        fadd2_acc(sa0, sa1, p0, p1);
+        fadd2_acc(sb0, sb1, p2, p3);
         pk[e] = pack_bf16x2(p0, p1);
+        pk[e + 1] = pack_bf16x2(p2, p3);
       }
-      l += sum0 + sum1;
+      l += (sa0 + sa1) + (sb0 + sb1);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t a[16];
