@@ -13,8 +13,9 @@
 // a block's max exceeds m by more than 2^8, which keeps every exponent <= 2^8
 // and leaves O/l exact.
 //
-// Warp roles: 0-3 softmax + epilogue (warp w owns TMEM lanes / rows 32w..32w+31),
-// 4 TMA producer, 5 MMA issuer (and TMEM owner).
+// Warp roles: 0-7 softmax + epilogue (warp w owns TMEM lanes / rows
+// 32*(w%4)..+31 and columns 64*(w/4)..+63), 8 TMA producer, 9 MMA issuer (and
+// TMEM owner).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -25,8 +26,9 @@ using namespace ptx;
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kTmaWarp = 4, kMmaWarp = 5;
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quarter (column halves)
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kTmaWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
 constexpr uint32_t kTile = kB * kD * 2;  // 32 KB bf16 tile
 constexpr uint32_t kHalf = kTile / 2;
 constexpr uint32_t kSmemBytes = 1024 + 3 * kTile;  // Q, K, V (+ alignment slack)
@@ -39,6 +41,8 @@ struct Bars {
   int count;
   int has_diag;
   int abort;
+  float xmax[2][2][kB];  // [block parity][column half][row]: partial row maxima
+  float xsum[2][kB];     // [column half][row]: partial row sums (epilogue)
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* abort) {
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&bars.v_full, 1);
     mbar_init(&bars.v_empty, 1);
     mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_full, 4);
+    mbar_init(&bars.p_full, kSoftmaxWarps);
     mbar_init(&bars.pv_done, 1);
     mbar_init(&bars.o_full, 1);
     mbar_init(&bars.drain, 1);
@@ -199,10 +203,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!mbar_wait(&bars.drain, 0, &bars.abort)) fail(&bars.abort, status, 0x206);
     }
   } else {
-    // Softmax warps: thread owns query row r of the block.
-    const int r = threadIdx.x;
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t s_addr = tmem + lane_addr, o_addr = tmem + lane_addr + 128;
+    // Softmax warps, two per TMEM lane quarter: warp w owns query rows
+    // 32*(w%4)..+31 and score / output columns 64*(w/4)..+63. The two warps
+    // of a quarter exchange partial row maxima through shared memory (named
+    // barrier 1 + quarter); their partial row sums are added at the end.
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const int pair_bar = 1 + quarter;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_addr = tmem + lane_addr + half * 64;        // 64 S columns
+    const uint32_t p_addr = tmem + lane_addr + half * 32;        // 32 P columns (bf16 pairs)
+    const uint32_t o_addr = tmem + lane_addr + 128 + half * 64;  // 64 O columns
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < count; ++j) {
@@ -213,36 +224,72 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc_fence_after();
       const bool diag = bars.has_diag && j == count - 1;  // ascending order: qb is last
-      uint32_t sv[128];
-      tmem_ld128(s_addr, sv);
+      uint32_t sv[64];
+      tmem_ld64(s_addr, sv);
       if (diag) {
         // Causal edge: key jj of the diagonal block is visible to row r iff jj <= r.
 #pragma unroll
-        for (int e = 0; e < 128; ++e)
-          if (e > r) sv[e] = 0xff800000u;  // -inf
+        for (int e = 0; e < 64; ++e)
+          if (half * 64 + e > r) sv[e] = 0xff800000u;  // -inf
       }
-      // Row max on the raw scores (c > 0, so max(s*c) = max(s)*c exactly):
-      // 3-input max in two independent chains.
+      // Partial row max on the raw scores (c > 0, so max(s*c) = max(s)*c).
       float ma = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
       float mb = fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
 #pragma unroll
-      for (int e = 6; e + 3 < 128; e += 4) {
+      for (int e = 6; e + 3 < 64; e += 4) {
         ma = fmax3(ma, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
         mb = fmax3(mb, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
       }
-      const float mx = fmaxf(fmax3(ma, mb, __uint_as_float(sv[126])), __uint_as_float(sv[127])) * c_log2;
+      const float pm = fmaxf(fmax3(ma, mb, __uint_as_float(sv[62])), __uint_as_float(sv[63]));
+      bars.xmax[j & 1][half][r] = pm;
+      // The barrier also orders both warps' S loads before either writes P:
+      // half 1's P columns (32..63) overlap half 0's S columns.
+      tc_fence_before();
+      named_bar_sync(pair_bar, 64);
+      tc_fence_after();
+      const float mx = fmaxf(pm, bars.xmax[j & 1][half ^ 1][r]) * c_log2;
+      // Lazy max: move to the new max only when it grew by more than 2^8.
+      // Warp-uniform decision (TMEM loads/stores are warp-collective; both
+      // warps of the pair see the same maxima, so they decide alike); each
+      // row moves to its own new max, f = 1 where it did not grow.
+      bool rescale = false;
+      float f = 1.f;
       if (j == 0) {
         m_ref = mx;
       } else if (__any_sync(0xffffffffu, mx > m_ref + kRescaleLog2)) {
-        // Warp-uniform branch (TMEM loads/stores are warp-collective); each
-        // row moves to its own new max, f = 1 where it did not grow.
-        // PV_{j-1} is complete (QK_j was issued after it), so O is stable.
         const float m_new = fmaxf(m_ref, mx);
-        const float f = ex2_approx(m_ref - m_new);
+        f = ex2_approx(m_ref - m_new);
         l *= f;
         m_ref = m_new;
+        rescale = true;
+      }
+      // p = 2^(s*c - m): a packed FMA and a packed add per element pair, one
+      // MUFU per element; P goes to TMEM 32 columns at a time.
+      const float neg_m = -m_ref;
+      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const int c0 = cc * 32 + 2 * e;
+          float x0, x1, x2, x3;
+          ffma2(x0, x1, __uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1]), c_log2, c_log2, neg_m, neg_m);
+          ffma2(x2, x3, __uint_as_float(sv[c0 + 2]), __uint_as_float(sv[c0 + 3]), c_log2, c_log2, neg_m, neg_m);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          fadd2_acc(sa0, sa1, p0, p1);
+          fadd2_acc(sb0, sb1, p2, p3);
+          pk[e] = pack_bf16x2(p0, p1);
+          pk[e + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st16(p_addr + cc * 16, pk);
+      }
+      l += (sa0 + sa1) + (sb0 + sb1);
+      if (rescale) {
+        // O must carry the new max before PV_j adds to it; PV_{j-1} is
+        // complete (QK_j was issued after it), so O is stable here.
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t v[32];
           tmem_ld32(o_addr + cc * 32, v);
           uint32_t a[16], b[16];
@@ -255,47 +302,27 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_st16(o_addr + cc * 32 + 16, b);
         }
       }
-      // p = 2^(s*c - m): a packed FMA and a packed add per element pair, one
-      // MUFU per element; two accumulator pairs for the row sum.
-      const float neg_m = -m_ref;
-      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        float x0, x1, x2, x3;
-        ffma2(x0, x1, __uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]), c_log2, c_log2, neg_m, neg_m);
-        ffma2(x2, x3, __uint_as_float(sv[2 * e + 2]), __uint_as_float(sv[2 * e + 3]), c_log2, c_log2, neg_m, neg_m);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-        fadd2_acc(sa0, sa1, p0, p1);
-        fadd2_acc(sb0, sb1, p2, p3);
-        pk[e] = pack_bf16x2(p0, p1);
-        pk[e + 1] = pack_bf16x2(p2, p3);
-      }
-      l += (sa0 + sa1) + (sb0 + sb1);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t a[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) a[e] = pk[cc * 16 + e];
-        tmem_st16(s_addr + cc * 16, a);
-      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.p_full);
     }
-    // Epilogue: O / l -> bf16, staged per warp through shared memory (the
-    // K/V tiles are no longer needed) so that each store is two full rows.
+    // Epilogue: O / l -> bf16 for this warp's 64 columns, staged per warp
+    // through shared memory (the K tile is no longer needed) so that each
+    // store instruction writes four 128-byte row segments.
     bool have = ok && count > 0;
     if (have && !warp_wait(&bars.o_full, 0, &bars.abort)) {
       if (lane == 0) fail(&bars.abort, status, 0x208);
       have = false;
     }
     tc_fence_after();
-    uint4* stg = reinterpret_cast<uint4*>(sK + warp * (32 * 256));  // 32 rows x 256 B
-    const float inv_l = have && l > 0.f ? 1.0f / l : 0.f;
+    bars.xsum[half][r] = l;
+    named_bar_sync(pair_bar, 64);
+    const float l_row = l + bars.xsum[half ^ 1][r];
+    uint4* stg = reinterpret_cast<uint4*>(sK + warp * (32 * 128));  // 32 rows x 128 B
+    const float inv_l = have && l_row > 0.f ? 1.0f / l_row : 0.f;
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int cc = 0; cc < 2; ++cc) {
       uint32_t v[32];
       if (have) {
         tmem_ld32(o_addr + cc * 32, v);
@@ -310,18 +337,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         u.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * inv_l, __uint_as_float(v[q4 * 8 + 3]) * inv_l);
         u.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * inv_l, __uint_as_float(v[q4 * 8 + 5]) * inv_l);
         u.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * inv_l, __uint_as_float(v[q4 * 8 + 7]) * inv_l);
-        const int chunk = cc * 4 + q4;  // 16-byte chunk of the 256-byte row
-        stg[lane * 16 + (chunk ^ (lane & 15))] = u;
+        const int chunk = cc * 4 + q4;  // 16-byte chunk of this warp's 128-byte row part
+        stg[lane * 8 + (chunk ^ (lane & 7))] = u;
       }
     }
     __syncwarp();
-    const int chunk = lane & 15;
+    const int chunk = lane & 7;
 #pragma unroll 4
-    for (int it = 0; it < 16; ++it) {
-      const int R = it * 2 + (lane >> 4);
-      const uint4 u = stg[R * 16 + (chunk ^ (R & 15))];
-      const int tok = qb * kB + warp * 32 + R;
-      uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * o_hs + static_cast<int64_t>(tok) * o_ts);
+    for (int it = 0; it < 8; ++it) {
+      const int R = it * 4 + (lane >> 3);
+      const uint4 u = stg[R * 8 + (chunk ^ (R & 7))];
+      const int tok = qb * kB + quarter * 32 + R;
+      uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * o_hs + static_cast<int64_t>(tok) * o_ts +
+                                            half * 64);
       dst[chunk] = u;
     }
   }
