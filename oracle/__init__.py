@@ -42,8 +42,10 @@ def _load():
         lib.oracle_proxy_map.argtypes = [i, i, i, vp, vp, d, vp, i]
         lib.oracle_quantize.argtypes = [vp, i64, vp]
         lib.oracle_quantize.restype = None
-        lib.oracle_route.argtypes = [i, i, vp, u32, u32, vp, vp, vp]
-        lib.oracle_vs_masses.argtypes = [i, i, vp, vp, vp]
+        lib.oracle_proxy_rows.argtypes = [i, i, i, vp, vp, d, i64, vp, vp, vp, i]
+        lib.oracle_route.argtypes = [i, i, vp, u32, u32, vp, vp, vp, i]
+        lib.oracle_vs_masses.argtypes = [i, i, vp, vp, vp, i]
+        lib.oracle_pe_rows.argtypes = [i, i, i, vp, vp, d, i64, vp, vp, vp, i]
         lib.oracle_select_vs.argtypes = [i, i, vp, vp, vp, u32, u32, i, vp, vp]
         lib.oracle_pe_map.argtypes = [i, i, i, vp, vp, d, vp, i]
         lib.oracle_select_pe.argtypes = [i, i, vp, vp, i, u32, u32, u32, u32, i, vp, i]
@@ -85,6 +87,30 @@ def proxy_map(q, k, scale=None, nthreads=None):
     return out
 
 
+def proxy_rows(q, k, heads, rows, scale=None, nthreads=None):
+    """A1 for selected (head, row of the last block) pairs: fp64 [count][n]."""
+    q, k = _u16(q), _u16(k)
+    hq, n, _ = q.shape
+    heads = np.ascontiguousarray(heads, np.int32)
+    rows = np.ascontiguousarray(rows, np.int32)
+    out = np.empty((heads.size, n), np.float64)
+    _check(_load().oracle_proxy_rows(hq, k.shape[0], n, _p(q), _p(k), scale or default_scale(), heads.size,
+                                     _p(heads), _p(rows), _p(out), _nt(nthreads)), "proxy_rows")
+    return out
+
+
+def pe_rows(q, k, heads, blocks, scale=None, nthreads=None):
+    """A5 for selected (head, query block) pairs: fp64 [count][nb]."""
+    q, k = _u16(q), _u16(k)
+    hq, n, _ = q.shape
+    heads = np.ascontiguousarray(heads, np.int32)
+    blocks = np.ascontiguousarray(blocks, np.int32)
+    out = np.empty((heads.size, n // B), np.float64)
+    _check(_load().oracle_pe_rows(hq, k.shape[0], n, _p(q), _p(k), scale or default_scale(), heads.size,
+                                  _p(heads), _p(blocks), _p(out), _nt(nthreads)), "pe_rows")
+    return out
+
+
 def quantize(p):
     p = np.ascontiguousarray(p, dtype=np.float32)
     out = np.empty(p.shape, np.uint64)
@@ -92,22 +118,22 @@ def quantize(p):
     return out
 
 
-def route(pmap32, tau=(1, 5)):
+def route(pmap32, tau=(1, 5), nthreads=None):
     """A2: (cstruct S, total T, route) from an fp32 map [hq][128][n]."""
     pmap32 = np.ascontiguousarray(pmap32, dtype=np.float32)
     hq, _, n = pmap32.shape
     S, T, r = np.empty(hq, np.uint64), np.empty(hq, np.uint64), np.empty(hq, np.uint8)
-    _check(_load().oracle_route(hq, n, _p(pmap32), tau[0], tau[1], _p(S), _p(T), _p(r)), "route")
+    _check(_load().oracle_route(hq, n, _p(pmap32), tau[0], tau[1], _p(S), _p(T), _p(r), _nt(nthreads)), "route")
     return S, T, r
 
 
-def vs_masses(pmap32):
+def vs_masses(pmap32, nthreads=None):
     """A3: (vmass, smass) uint64 [hq][nb] from an fp32 map."""
     pmap32 = np.ascontiguousarray(pmap32, dtype=np.float32)
     hq, _, n = pmap32.shape
     nb = n // B
     vm, sm = np.empty((hq, nb), np.uint64), np.empty((hq, nb), np.uint64)
-    _check(_load().oracle_vs_masses(hq, n, _p(pmap32), _p(vm), _p(sm)), "vs_masses")
+    _check(_load().oracle_vs_masses(hq, n, _p(pmap32), _p(vm), _p(sm), _nt(nthreads)), "vs_masses")
     return vm, sm
 
 

@@ -163,6 +163,34 @@ int oracle_proxy_map(int hq, int hkv, int n, const uint16_t* q, const uint16_t* 
   return 0;
 }
 
+// A1 for selected rows only: for each requested (head, r) the row
+// pmap[h][r][0..n) of oracle_proxy_map, computed on its own (for long
+// sequences where the full map is too large to state in fp64).
+// out: double [count][n].
+int oracle_proxy_rows(int hq, int hkv, int n, const uint16_t* q, const uint16_t* k, double scale, int64_t count,
+                      const int32_t* heads, const int32_t* rows, double* out, int nthreads) {
+  if (hq <= 0 || hkv <= 0 || hq % hkv || n < kB || n % kB) return 1;
+  for (int64_t t = 0; t < count; ++t)
+    if (heads[t] < 0 || heads[t] >= hq || rows[t] < 0 || rows[t] >= kB) return 2;
+  const int G = hq / hkv;
+  parallel_for(count, nthreads, [&](int64_t t) {
+    const int h = heads[t], g = h / G, i = n - kB + rows[t];
+    double qi[kD];
+    for (int c = 0; c < kD; ++c) qi[c] = bf16_to_double(q[(static_cast<int64_t>(h) * n + i) * kD + c]);
+    std::vector<double> s(i + 1);
+    for (int j = 0; j <= i; ++j) {
+      const uint16_t* kj = k + (static_cast<int64_t>(g) * n + j) * kD;
+      double acc = 0.0;
+      for (int c = 0; c < kD; ++c) acc += qi[c] * bf16_to_double(kj[c]);
+      s[j] = scale * acc;
+    }
+    softmax_inplace(s);
+    double* row = out + t * n;
+    for (int j = 0; j < n; ++j) row[j] = j <= i ? s[j] : 0.0;
+  });
+  return 0;
+}
+
 // Q32 quanta of an fp32 array (see q32 above).
 void oracle_quantize(const float* p, int64_t count, uint64_t* out) {
   for (int64_t t = 0; t < count; ++t) out[t] = q32(p[t]);
@@ -177,9 +205,10 @@ void oracle_quantize(const float* p, int64_t count, uint64_t* out) {
 // integers as tau_den * S >= tau_num * T.
 // pmap: fp32 [hq][128][n] (the map under test); route[h] = 1 for VS, 0 for PE.
 int oracle_route(int hq, int n, const float* pmap, uint32_t tau_num, uint32_t tau_den, uint64_t* cstruct,
-                 uint64_t* total, uint8_t* route) {
+                 uint64_t* total, uint8_t* route, int nthreads) {
   if (hq <= 0 || n < 2 * kB || n % kB || tau_den == 0) return 1;
-  for (int h = 0; h < hq; ++h) {
+  parallel_for(hq, nthreads, [&](int64_t hh) {
+    const int h = static_cast<int>(hh);
     uint64_t S = 0, T = 0;
     for (int r = 0; r < kB; ++r) {
       const float* row = pmap + (static_cast<int64_t>(h) * kB + r) * n;
@@ -192,7 +221,7 @@ int oracle_route(int hq, int n, const float* pmap, uint32_t tau_num, uint32_t ta
     cstruct[h] = S;
     total[h] = T;
     route[h] = static_cast<unsigned __int128>(tau_den) * S >= static_cast<unsigned __int128>(tau_num) * T ? 1 : 0;
-  }
+  });
   return 0;
 }
 
@@ -204,10 +233,11 @@ int oracle_route(int hq, int n, const float* pmap, uint32_t tau_num, uint32_t ta
 // smass[s] sums entries with j <= i and j >= 128: sink columns are left out of
 // the slash direction (the "sink-aware" part: a sink cannot raise the
 // diagonal noise floor). Written element by element, independent of any tiling.
-int oracle_vs_masses(int hq, int n, const float* pmap, uint64_t* vmass, uint64_t* smass) {
+int oracle_vs_masses(int hq, int n, const float* pmap, uint64_t* vmass, uint64_t* smass, int nthreads) {
   if (hq <= 0 || n < 2 * kB || n % kB) return 1;
   const int nb = n / kB;
-  for (int h = 0; h < hq; ++h) {
+  parallel_for(hq, nthreads, [&](int64_t hh) {
+    const int h = static_cast<int>(hh);
     uint64_t* v = vmass + static_cast<int64_t>(h) * nb;
     uint64_t* s = smass + static_cast<int64_t>(h) * nb;
     std::fill(v, v + nb, 0ull);
@@ -221,7 +251,7 @@ int oracle_vs_masses(int hq, int n, const float* pmap, uint64_t* vmass, uint64_t
         if (j <= i && j >= 128) s[(i - j) / kB] += m;
       }
     }
-  }
+  });
   return 0;
 }
 
@@ -290,6 +320,42 @@ int oracle_pe_map(int hq, int hkv, int n, const uint16_t* q, const uint16_t* k, 
     }
     softmax_inplace(s);
     double* row = out + (h * nb + b) * nb;
+    for (int64_t c = 0; c < nb; ++c) row[c] = c <= b ? s[c] : 0.0;
+  });
+  return 0;
+}
+
+// A5 for selected rows only: row b of head h of oracle_pe_map for each
+// requested (head, b). out: double [count][nb].
+int oracle_pe_rows(int hq, int hkv, int n, const uint16_t* q, const uint16_t* k, double scale, int64_t count,
+                   const int32_t* heads, const int32_t* blocks, double* out, int nthreads) {
+  if (hq <= 0 || hkv <= 0 || hq % hkv || n < kB || n % kB) return 1;
+  const int G = hq / hkv, nb = n / kB;
+  for (int64_t t = 0; t < count; ++t)
+    if (heads[t] < 0 || heads[t] >= hq || blocks[t] < 0 || blocks[t] >= nb) return 2;
+  // Mean-pooled keys of every block of every kv head (needed by any row).
+  std::vector<double> kbar(static_cast<size_t>(hkv) * nb * kD, 0.0);
+  parallel_for(static_cast<int64_t>(hkv) * nb, nthreads, [&](int64_t t) {
+    double* dst = &kbar[t * kD];
+    const int64_t g = t / nb, c = t % nb;
+    for (int r = 0; r < kB; ++r)
+      for (int e = 0; e < kD; ++e) dst[e] += bf16_to_double(k[((g * n) + c * kB + r) * kD + e]);
+    for (int e = 0; e < kD; ++e) dst[e] /= kB;
+  });
+  parallel_for(count, nthreads, [&](int64_t t) {
+    const int64_t h = heads[t], b = blocks[t], g = h / G;
+    double qbar[kD] = {};
+    for (int r = 0; r < kB; ++r)
+      for (int e = 0; e < kD; ++e) qbar[e] += bf16_to_double(q[((h * n) + b * kB + r) * kD + e]);
+    for (int e = 0; e < kD; ++e) qbar[e] /= kB;
+    std::vector<double> s(b + 1);
+    for (int64_t c = 0; c <= b; ++c) {
+      double acc = 0.0;
+      for (int e = 0; e < kD; ++e) acc += qbar[e] * kbar[(g * nb + c) * kD + e];
+      s[c] = scale * acc;
+    }
+    softmax_inplace(s);
+    double* row = out + t * nb;
     for (int64_t c = 0; c < nb; ++c) row[c] = c <= b ? s[c] : 0.0;
   });
   return 0;

@@ -450,3 +450,34 @@ def test_empty_row_mask_gives_zero_output():
     rb = np.zeros((1, 2, 1), np.uint32)
     out = oracle.attention_rows(q, k, v, np.zeros(3, np.int32), np.array([0, 130, 255], np.int32), rowbits=rb)
     assert np.all(out == 0.0)
+
+
+# ----------------------------------------------------------------- row samplers
+def test_proxy_rows_match_torch_softmax_rows():
+    q, k, _ = rand_qkv(4, 2, 640, 22)
+    heads = np.array([0, 1, 3, 3], np.int32)
+    rows = np.array([0, 127, 5, 64], np.int32)
+    got = oracle.proxy_rows(q, k, heads, rows)
+    Q = bits_to_f64(q)
+    K = bits_to_f64(k).repeat_interleave(2, dim=0)
+    n = 640
+    for t, (h, r) in enumerate(zip(heads, rows)):
+        i = n - B + r
+        s = (K[h, : i + 1] @ Q[h, i]) / np.sqrt(128.0)
+        ref = np.zeros(n)
+        ref[: i + 1] = torch.softmax(s, dim=0).numpy()
+        assert np.max(np.abs(got[t] - ref)) < 1e-13
+
+
+def test_pe_rows_match_torch():
+    q, k, _ = rand_qkv(4, 2, 1024, 23)
+    heads = np.array([0, 2, 3], np.int32)
+    blocks = np.array([7, 0, 4], np.int32)
+    got = oracle.pe_rows(q, k, heads, blocks)
+    Qb = bits_to_f64(q).reshape(4, 8, B, 128).mean(dim=2)
+    Kb = bits_to_f64(k).reshape(2, 8, B, 128).mean(dim=2).repeat_interleave(2, dim=0)
+    for t, (h, b) in enumerate(zip(heads, blocks)):
+        z = (Kb[h, : b + 1] @ Qb[h, b]) / np.sqrt(128.0)
+        ref = np.zeros(8)
+        ref[: b + 1] = torch.softmax(z, dim=0).numpy()
+        assert np.max(np.abs(got[t] - ref)) < 1e-13
