@@ -3,9 +3,11 @@
 
 Workload (default): 32 query / 8 kv heads, head_dim 128, 524,288 tokens,
 bf16, every head sink-type with 2 slashes and 32 needle columns (seed 5).
-One step = one pass of the whole hot path over the layer: proxy map, block
-masses, C_struct routing, VS selection, pooled estimate and PE selection,
-mask + schedule, block-sparse attention. Inputs (6 GiB) are larger than L2,
+One step = one pass of the whole hot path over the layer: block masses of
+the proxy map (fused: the map is never stored), C_struct routing, VS
+selection, pooled estimate and PE selection, mask + schedule, block-sparse
+attention. The unfused map path (map write, then the mass pass) is timed
+separately after the step. Inputs (6 GiB) are larger than L2,
 so no flush between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl crisp|reference]
@@ -266,10 +268,9 @@ def run_crisp(args):
     counts, order = E((hq, nb), torch.int32), E((hq * nb,), torch.int32)
     stream = torch.cuda.current_stream()
 
-    stages = ["proxy", "masses", "route", "select_vs", "pe_map", "select_pe", "mask", "attention"]
+    stages = ["proxy_masses", "route", "select_vs", "pe_map", "select_pe", "mask", "attention"]
     calls = [
-        lambda: crisp.proxy_map(s, qd, kd, pmap, ws, stream),
-        lambda: crisp.block_masses(s, pmap, vmass, smass, ws, stream),
+        lambda: crisp.proxy_masses(s, qd, kd, vmass, smass, ws, stream),
         lambda: crisp.route_cstruct(s, params, vmass, cstruct, total, route, stream),
         lambda: crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws, stream),
         lambda: crisp.pe_map(s, qd, kd, route, pbar, ws, stream),
@@ -277,9 +278,9 @@ def run_crisp(args):
         lambda: crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, ws, stream),
         lambda: crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws, stream),
     ]
-    # our kernel launches per step: proxy 3, masses 2, route 1, select_vs 1,
-    # pe_map 3, select_pe 1, mask+schedule 6, attention 1
-    launches_per_step = 18
+    # our kernel launches per step: proxy statistics 2, fused masses 2,
+    # route 1, select_vs 1, pe_map 3, select_pe 1, mask+schedule 6, attention 1
+    launches_per_step = 17
 
     def step(events=None):
         for i, c in enumerate(calls):
@@ -330,6 +331,24 @@ def run_crisp(args):
     achieved_tf = flops / (attn_ms * 1e-3) / 1e12
     proxy_bytes = 4 * hq * B * n + 2 * (2 * hkv * n * 128) + 2 * hq * B * 128
     masses_bytes = 4 * hq * B * n
+
+    # The unfused map path on the same inputs: the proxy map written to HBM,
+    # then the mass pass reading it back (the map-reading route/select
+    # roofline); its masses must equal the fused ones.
+    vm_fused, sm_fused = vmass.clone(), smass.clone()
+    ue = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    unf = {"proxy": [], "masses": []}
+    for _ in range(3):
+        ue[0].record(stream)
+        crisp.proxy_map(s, qd, kd, pmap, ws, stream)
+        ue[1].record(stream)
+        crisp.block_masses(s, pmap, vmass, smass, ws, stream)
+        ue[2].record(stream)
+        torch.cuda.synchronize()
+        unf["proxy"].append(ue[0].elapsed_time(ue[1]))
+        unf["masses"].append(ue[1].elapsed_time(ue[2]))
+    assert torch.equal(vm_fused, vmass) and torch.equal(sm_fused, smass), "fused masses differ from the map path"
+    unf_proxy_ms, unf_masses_ms = statistics.median(unf["proxy"]), statistics.median(unf["masses"])
 
     # Dense attention over every causal block, same inputs, same run.
     dense = None
@@ -399,10 +418,13 @@ def run_crisp(args):
             "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": achieved_tf, "peak": tf_peak,
                          "unit": "TFLOP/s", "frac": achieved_tf / tf_peak, "traffic": None,
                          "peak_kind": f"bf16 dense, {peak_kind} (sustained)"},
-            "hbm": {"proxy_gbs": proxy_bytes / (stage_ms["proxy"] * 1e-3) / 1e9,
-                    "masses_gbs": masses_bytes / (stage_ms["masses"] * 1e-3) / 1e9, "peak_gbs": hbm_peak,
-                    "route_select_frac": (masses_bytes / ((stage_ms["masses"] + stage_ms["route"] +
-                                                           stage_ms["select_vs"]) * 1e-3) / 1e9) / hbm_peak},
+            "unfused_map_path": {
+                "proxy_ms": unf_proxy_ms, "masses_ms": unf_masses_ms,
+                "proxy_gbs": proxy_bytes / (unf_proxy_ms * 1e-3) / 1e9,
+                "masses_gbs": masses_bytes / (unf_masses_ms * 1e-3) / 1e9, "peak_gbs": hbm_peak,
+                "route_select_frac": (masses_bytes / ((unf_masses_ms + stage_ms["route"] + stage_ms["select_vs"])
+                                                     * 1e-3) / 1e9) / hbm_peak,
+                "fused_saving_ms": unf_proxy_ms + unf_masses_ms - stage_ms["proxy_masses"]},
             "dense": dense,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,

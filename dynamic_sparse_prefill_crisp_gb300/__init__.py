@@ -47,7 +47,7 @@ class Params(ctypes.Structure):
 
 class LayerViews(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in
-                ("pmap", "vmass", "smass", "cstruct", "total", "route", "vbits", "sbits", "pbar", "pebits",
+                ("vmass", "smass", "cstruct", "total", "route", "vbits", "sbits", "pbar", "pebits",
                  "rowbits", "counts", "order")]
 
 
@@ -68,6 +68,7 @@ def lib():
         L.crisp_proxy_map.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
         L.crisp_proxy_map_noalloc.argtypes = [P(Shape), vp, vp, vp, st]
         L.crisp_block_masses.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
+        L.crisp_proxy_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
         L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
         L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
         L.crisp_pe_map.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
@@ -82,7 +83,7 @@ def lib():
         L.crisp_status_string.restype = ctypes.c_char_p
         for name in ("crisp_workspace_size", "crisp_layer_workspace_size", "crisp_workspace_init", "crisp_proxy_map",
                      "crisp_proxy_map_noalloc",
-                     "crisp_block_masses", "crisp_route_cstruct", "crisp_select_vs", "crisp_pe_map",
+                     "crisp_block_masses", "crisp_proxy_masses", "crisp_route_cstruct", "crisp_select_vs", "crisp_pe_map",
                      "crisp_select_pe", "crisp_build_mask", "crisp_sparse_prefill", "crisp_dense_prefill",
                      "crisp_layer_views_get", "crisp_prefill_layer", "crisp_read_status"):
             getattr(L, name).restype = ctypes.c_int
@@ -169,6 +170,12 @@ def proxy_map_noalloc(shape, q, k, pmap, stream=None):
 def block_masses(shape, pmap, vmass, smass, ws, stream=None):
     _check(lib().crisp_block_masses(ctypes.byref(shape), _ptr(pmap), _ptr(vmass), _ptr(smass), _ptr(ws), _nbytes(ws),
                                     _stream(stream)), "crisp_block_masses")
+
+
+def proxy_masses(shape, q, k, vmass, smass, ws, stream=None):
+    """Block masses of the proxy map straight from q and k (the map is not stored)."""
+    _check(lib().crisp_proxy_masses(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(vmass), _ptr(smass), _ptr(ws),
+                                    _nbytes(ws), _stream(stream)), "crisp_proxy_masses")
 
 
 def route_cstruct(shape, params, vmass, cstruct, total, route, stream=None):

@@ -121,7 +121,6 @@ LayerLayout layer_layout(const crisp_shape& s) {
   const size_t hq = s.hq, n = s.seq_len, nb = num_blocks(s.seq_len), W = bit_words(static_cast<int>(nb));
   LayerLayout L{};
   size_t o = scratch_layout(s).total;
-  L.pmap = o;       o = up(o + hq * kB * n * 4);
   L.vmass = o;      o = up(o + hq * nb * 8);
   L.smass = o;      o = up(o + hq * nb * 8);
   L.cstruct = o;    o = up(o + hq * 8);
@@ -266,6 +265,22 @@ crisp_status crisp_block_masses(const crisp_shape* shape, const float* pmap, uin
   return from_cuda(launch_block_masses(s, pmap, vmass, smass, static_cast<char*>(ws), stream));
 }
 
+crisp_status crisp_proxy_masses(const crisp_shape* shape, const void* q, const void* k, uint64_t* vmass,
+                                uint64_t* smass, void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!q || !k || !vmass || !smass) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned(vmass, 8) || !aligned(smass, 8)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  TmaMaps maps;
+  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  maps.v = maps.k;
+  return from_cuda(launch_proxy_masses(s, maps, vmass, smass, static_cast<char*>(ws), stream));
+}
+
 crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
                                  uint64_t* cstruct, uint64_t* total, uint8_t* route, crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
@@ -368,7 +383,6 @@ crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws, crisp_lay
   if (!ws || !views) return CRISP_ERR_INVALID_ARG;
   const LayerLayout L = layer_layout(*shape);
   char* b = static_cast<char*>(ws);
-  views->pmap = reinterpret_cast<float*>(b + L.pmap);
   views->vmass = reinterpret_cast<uint64_t*>(b + L.vmass);
   views->smass = reinterpret_cast<uint64_t*>(b + L.smass);
   views->cstruct = reinterpret_cast<uint64_t*>(b + L.cstruct);
@@ -403,8 +417,7 @@ crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* p
   if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
   if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
   char* wsb = static_cast<char*>(ws);
-  if (launch_proxy(s, maps, w.pmap, wsb, stream) != cudaSuccess ||
-      launch_block_masses(s, w.pmap, w.vmass, w.smass, wsb, stream) != cudaSuccess ||
+  if (launch_proxy_masses(s, maps, w.vmass, w.smass, wsb, stream) != cudaSuccess ||
       launch_route(s, *params, w.vmass, w.cstruct, w.total, w.route, stream) != cudaSuccess ||
       launch_select_vs(s, *params, w.vmass, w.smass, w.route, w.vbits, w.sbits, stream) != cudaSuccess ||
       launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess ||

@@ -66,7 +66,7 @@ struct ScratchLayout {
 
 // Intermediates of crisp_prefill_layer, placed after the scratch.
 struct LayerLayout {
-  size_t pmap, vmass, smass, cstruct, total_mass, route, vbits, sbits, pbar, pebits, rowbits, counts, order;
+  size_t vmass, smass, cstruct, total_mass, route, vbits, sbits, pbar, pebits, rowbits, counts, order;
   size_t total;
 };
 
@@ -79,6 +79,10 @@ struct TmaMaps {
 
 // ---- launchers (one per translation unit); return cudaSuccess or the launch error
 cudaError_t launch_proxy(const crisp_shape& s, const TmaMaps& maps, float* pmap, char* ws, cudaStream_t st);
+cudaError_t launch_proxy_masses(const crisp_shape& s, const TmaMaps& maps, uint64_t* vmass, uint64_t* smass, char* ws,
+                                cudaStream_t st);
+cudaError_t launch_assemble_slash(const crisp_shape& s, const uint64_t* lower, const uint64_t* upper, uint64_t* smass,
+                                  cudaStream_t st);
 cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_t* vmass, uint64_t* smass, char* ws,
                                 cudaStream_t st);
 cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, uint64_t* cstruct,

@@ -177,6 +177,13 @@ cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_
   auto* lower = reinterpret_cast<uint64_t*>(ws + L.mass_lower);
   auto* upper = reinterpret_cast<uint64_t*>(ws + L.mass_upper);
   mass_tiles<<<dim3(nb, s.hq), kMassThreads, 0, st>>>(pmap, s.seq_len, vmass, lower, upper);
+  const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : launch_assemble_slash(s, lower, upper, smass, st);
+}
+
+cudaError_t launch_assemble_slash(const crisp_shape& s, const uint64_t* lower, const uint64_t* upper, uint64_t* smass,
+                                  cudaStream_t st) {
+  const int nb = num_blocks(s.seq_len);
   assemble_slash<<<dim3((nb + 255) / 256, s.hq), 256, 0, st>>>(lower, upper, nb, smass);
   return cudaGetLastError();
 }

@@ -26,14 +26,13 @@ constexpr int kTmaWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;
 constexpr uint32_t kTile = kB * kD * 2;            // one bf16 128x128 tile: 32 KB
 constexpr uint32_t kHalf = kTile / 2;              // 64-feature half (TMA box)
-constexpr int kStages = 3;                         // K ring
+constexpr int kMaxStages = 3;                      // K ring (at most)
 constexpr uint32_t kStageBytes = 32 * 32 * 4;      // per-warp transpose buffer
-constexpr uint32_t kSmemBytes = 1024 + kTile + kStages * kTile + kEpiWarps * kStageBytes;
 constexpr uint32_t kTmemCols = 256;                // two 128-column S buffers
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t k_full[kMaxStages], k_empty[kMaxStages];
   uint64_t s_full[2], s_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -50,18 +49,39 @@ __device__ __forceinline__ void fail(int* abort, DevStatus* st, uint32_t where) 
   report_error(st, CRISP_ERR_TIMEOUT, where);
 }
 
+// Pass kinds: per-chunk row statistics, the map write, and the fused block
+// masses (the same fp32 probabilities, quantised and summed per 128x128 tile
+// the way the mass pass sums the written map, so the masses are identical).
+enum : int { kStats = 0, kWriteMap = 1, kMasses = 2 };
+
+// The map write keeps a three-deep K ring and a transpose buffer (one CTA per
+// SM). The two passes that store nothing per element use a two-deep ring and
+// no buffer, so two CTAs fit on an SM (2 x 97 KB shared, 2 x 256 TMEM
+// columns) and twice the epilogue warps hide the exponential latency.
+template <int kMode>
+struct ProxyCfg {
+  static constexpr int kStages = kMode == kWriteMap ? 3 : 2;
+  static constexpr int kCtasPerSm = kMode == kWriteMap ? 1 : 2;
+  static constexpr uint32_t kSmem =
+      1024 + kTile + kStages * kTile + (kMode == kWriteMap ? kEpiWarps * kStageBytes : 0u);
+};
+
 // grid: (hq, chunks). CTA (h, chunk) covers key blocks [chunk*C, chunk*C + C).
-template <bool kWrite>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
     proxy_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk, int n, int group,
                  float c_log2, float* __restrict__ pmap, float2* __restrict__ part,
-                 const float2* __restrict__ stats, DevStatus* status) {
+                 const float2* __restrict__ stats, uint64_t* __restrict__ vmass, uint64_t* __restrict__ lower,
+                 uint64_t* __restrict__ upper, DevStatus* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
   uint8_t* sK = base + kTile;
+  constexpr int kStages = ProxyCfg<kMode>::kStages;
   float* sStage = reinterpret_cast<float*>(base + kTile + kStages * kTile);
   __shared__ Bars bars;
+  __shared__ unsigned long long tile_acc[2][2];  // [tile parity][whole, lower triangle]
+  __shared__ unsigned int tile_cnt[2];           // warps that have added to the slot
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, chunk = blockIdx.y, nchunks = gridDim.y;
@@ -72,6 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
+    tile_acc[0][0] = tile_acc[0][1] = tile_acc[1][0] = tile_acc[1][1] = 0ull;
+    tile_cnt[0] = tile_cnt[1] = 0u;
     mbar_init(&bars.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
@@ -145,11 +167,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // row of the query block
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     float m_run = -INFINITY, l_run = 0.f;
-    float M = 0.f, inv_l = 0.f;
-    if (kWrite) {
+    float M = 0.f, inv_l = 0.f, inv_l32 = 0.f;
+    if (kMode != kStats) {
       const float2 st = stats[static_cast<size_t>(h) * kB + r];
       M = st.x;
       inv_l = st.y;
+      // p * 2^32 == e * (inv_l * 2^32) exactly for every normal p; a
+      // subnormal p quantises to 0 either way.
+      inv_l32 = st.y * 4294967296.0f;
     }
     float* stg = sStage + warp * (32 * 32);
     for (int t = 0; t < T; ++t) {
@@ -161,41 +186,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int kb = kb0 + t;
       const bool diag = (kb == nb - 1);  // causal edge: keys j > n-128+r are masked
+      // Q32 quanta of this row's 64 probabilities of the tile: below 2^23 in
+      // 32 bits (64 of them stay below 2^29), larger ones in 64 bits.
+      uint32_t all32 = 0, lo32 = 0;
+      uint64_t all64 = 0, lo64 = 0;
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = half * 64 + cc * 32;
         uint32_t v[32];
         tmem_ld32(tmem + lane_addr + b * 128 + col0, v);
+        // Raw logits S; on the causal edge keys j > n-128+r are -inf.
         float x[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float val = __uint_as_float(v[e]) * c_log2;
-          x[e] = (diag && col0 + e > r) ? -INFINITY : val;
-        }
-        if (!kWrite) {
-          float mx = x[0];
+        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(v[e]);
+        if (diag) {
 #pragma unroll
-          for (int e = 1; e < 32; ++e) mx = fmaxf(mx, x[e]);
+          for (int e = 0; e < 32; ++e)
+            if (col0 + e > r) x[e] = -INFINITY;
+        }
+        if (kMode == kStats) {
+          // Running (max, sum) in base-2 units: m = c_log2 * max S, l = sum
+          // 2^(c_log2*S - m), with the exponent as one fma. Tree max and four
+          // partial sums keep the dependency chains short.
+          float t[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = fmax3(x[4 * i], x[4 * i + 1], fmaxf(x[4 * i + 2], x[4 * i + 3]));
+          const float mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7])) * c_log2;
           if (mx > m_run) {
             l_run *= ex2_approx(m_run - mx);
             m_run = mx;
           }
           if (m_run != -INFINITY) {
-            float sum = 0.f;
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sum += ex2_approx(x[e] - m_run);
-            l_run += sum;
+            for (int e = 0; e < 32; ++e) s4[e & 3] += ex2_approx(__fmaf_rn(x[e], c_log2, -m_run));
+            l_run += (s4[0] + s4[1]) + (s4[2] + s4[3]);
           }
         } else {
+          // The base-2 exponent c_log2*S - M as one fma, so the map write
+          // and the fused masses evaluate p = 2^(c_log2*S - M) / L alike.
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = __fmaf_rn(x[e], c_log2, -M);
+        }
+        if (kMode == kWriteMap) {
           // Row `lane` of this warp's 32x32 block into the transpose buffer
           // (16-byte chunks XOR-swizzled by row to spread the banks).
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
             float4 p;
-            p.x = ex2_approx(x[4 * c4 + 0] - M) * inv_l;
-            p.y = ex2_approx(x[4 * c4 + 1] - M) * inv_l;
-            p.z = ex2_approx(x[4 * c4 + 2] - M) * inv_l;
-            p.w = ex2_approx(x[4 * c4 + 3] - M) * inv_l;
+            p.x = ex2_approx(x[4 * c4 + 0]) * inv_l;
+            p.y = ex2_approx(x[4 * c4 + 1]) * inv_l;
+            p.z = ex2_approx(x[4 * c4 + 2]) * inv_l;
+            p.w = ex2_approx(x[4 * c4 + 3]) * inv_l;
             reinterpret_cast<float4*>(stg + lane * 32)[c4 ^ (lane & 7)] = p;
           }
           __syncwarp();
@@ -209,13 +251,83 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float4*>(dst) = p;
           }
           __syncwarp();
+        } else if (kMode == kMasses) {
+          // xq = p * 2^32 for the p the map write stores.
+          float xq[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) xq[e] = ex2_approx(x[e]) * inv_l32;
+          float t[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = fmax3(xq[4 * i], xq[4 * i + 1], fmaxf(xq[4 * i + 2], xq[4 * i + 3]));
+          const float mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+          // Lower triangle r >= jj of the tile: this warp's rows are
+          // 32*quarter.., its columns col0..; both multiples of 32, so the
+          // chunk is wholly below (col0 < 32*quarter), wholly above, or on
+          // the diagonal (jj = col0 + e <= r iff e <= lane).
+          const bool on_diag = col0 == quarter * 32, below = col0 < quarter * 32;
+          if (!__any_sync(0xffffffffu, mx >= kTwo23)) {
+            // Every quantum below 2^23: the bits of xq + 2^23 minus those of
+            // 2^23, with the 32 subtractions taken once at the end (mod 2^32;
+            // the true sums stay below 2^28).
+            uint32_t a4[4] = {0u, 0u, 0u, 0u}, lo = 0;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const uint32_t u = __float_as_uint(xq[e] + kTwo23);
+              a4[e & 3] += u;
+              if (on_diag) lo += e <= lane ? u : 0x4B000000u;
+            }
+            const uint32_t a = (a4[0] + a4[1]) + (a4[2] + a4[3]) - 32u * 0x4B000000u;
+            all32 += a;
+            lo32 += on_diag ? lo - 32u * 0x4B000000u : (below ? a : 0u);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const bool in_lower = r >= col0 + e;
+              if (xq[e] < kTwo23) {
+                const uint32_t f = q32_small(xq[e]);
+                all32 += f;
+                lo32 += in_lower ? f : 0u;
+              } else {
+                const uint64_t f = q32_large(xq[e]);
+                all64 += f;
+                lo64 += in_lower ? f : 0ull;
+              }
+            }
+          }
+        }
+      }
+      if (kMode == kMasses) {
+        // Tile sums: the rows of this warp by shuffles, then the eight warps
+        // by shared-memory atomics into the slot of this tile's parity; the
+        // last warp to add publishes the sums and clears the slot (before it
+        // releases S, so the slot's next use, two tiles later, sees it clear).
+        unsigned long long all = all64 + all32, lo = lo64 + lo32;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          all += __shfl_xor_sync(0xffffffffu, all, o);
+          lo += __shfl_xor_sync(0xffffffffu, lo, o);
+        }
+        if (lane == 0) {
+          atomicAdd(&tile_acc[b][0], all);
+          atomicAdd(&tile_acc[b][1], lo);
+          __threadfence_block();
+          if (atomicAdd(&tile_cnt[b], 1u) == kEpiWarps - 1) {
+            __threadfence_block();
+            const unsigned long long sa = atomicExch(&tile_acc[b][0], 0ull);
+            const unsigned long long sl = atomicExch(&tile_acc[b][1], 0ull);
+            atomicExch(&tile_cnt[b], 0u);
+            const size_t idx = static_cast<size_t>(h) * nb + kb;
+            vmass[idx] = sa;
+            lower[idx] = sl;
+            upper[idx] = sa - sl;
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.s_empty[b]);
     }
-    if (!kWrite) part[(static_cast<size_t>(h) * kB + r) * (2 * nchunks) + 2 * chunk + half] = make_float2(m_run, l_run);
+    if (kMode == kStats) part[(static_cast<size_t>(h) * kB + r) * (2 * nchunks) + 2 * chunk + half] = make_float2(m_run, l_run);
   }
 
   tc_fence_before();
@@ -240,27 +352,57 @@ __global__ void proxy_combine(const float2* __restrict__ part, float2* __restric
 
 }  // namespace
 
-cudaError_t launch_proxy(const crisp_shape& s, const TmaMaps& maps, float* pmap, char* ws, cudaStream_t st) {
+// Pass 1 (row statistics) and their combination; shared by both entry points.
+static cudaError_t proxy_stats(const crisp_shape& s, const TmaMaps& maps, char* ws, cudaStream_t st) {
   const ScratchLayout L = scratch_layout(s);
-  const int nb = num_blocks(s.seq_len);
-  const int chunks = proxy_chunks(nb);
-  const float c_log2 = s.scale * 1.4426950408889634f;  // scale * log2(e): softmax in base 2
+  const int chunks = proxy_chunks(num_blocks(s.seq_len));
   auto* part = reinterpret_cast<float2*>(ws + L.proxy_part);
   auto* stats = reinterpret_cast<float2*>(ws + L.proxy_stats);
   auto* status = reinterpret_cast<DevStatus*>(ws + L.status);
-  cudaError_t e = cudaFuncSetAttribute(proxy_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(proxy_kernel<kStats>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           ProxyCfg<kStats>::kSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(proxy_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  const dim3 grid(s.hq, chunks);
-  const int group = s.hq / s.hkv;
-  proxy_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(maps.q, maps.k, s.seq_len, group, c_log2, pmap, part,
-                                                          stats, status);
+  proxy_kernel<kStats><<<dim3(s.hq, chunks), kThreads, ProxyCfg<kStats>::kSmem, st>>>(
+      maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, nullptr, part, stats, nullptr, nullptr,
+      nullptr, status);
   const int rows = s.hq * kB;
   proxy_combine<<<(rows + 127) / 128, 128, 0, st>>>(part, stats, rows, 2 * chunks);
-  proxy_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(maps.q, maps.k, s.seq_len, group, c_log2, pmap, part,
-                                                         stats, status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_proxy(const crisp_shape& s, const TmaMaps& maps, float* pmap, char* ws, cudaStream_t st) {
+  cudaError_t e = proxy_stats(s, maps, ws, st);
+  if (e != cudaSuccess) return e;
+  const ScratchLayout L = scratch_layout(s);
+  const int chunks = proxy_chunks(num_blocks(s.seq_len));
+  e = cudaFuncSetAttribute(proxy_kernel<kWriteMap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           ProxyCfg<kWriteMap>::kSmem);
+  if (e != cudaSuccess) return e;
+  proxy_kernel<kWriteMap><<<dim3(s.hq, chunks), kThreads, ProxyCfg<kWriteMap>::kSmem, st>>>(
+      maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, pmap,
+      reinterpret_cast<float2*>(ws + L.proxy_part), reinterpret_cast<const float2*>(ws + L.proxy_stats), nullptr,
+      nullptr, nullptr, reinterpret_cast<DevStatus*>(ws + L.status));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_proxy_masses(const crisp_shape& s, const TmaMaps& maps, uint64_t* vmass, uint64_t* smass, char* ws,
+                                cudaStream_t st) {
+  cudaError_t e = proxy_stats(s, maps, ws, st);
+  if (e != cudaSuccess) return e;
+  const ScratchLayout L = scratch_layout(s);
+  const int chunks = proxy_chunks(num_blocks(s.seq_len));
+  auto* lower = reinterpret_cast<uint64_t*>(ws + L.mass_lower);
+  auto* upper = reinterpret_cast<uint64_t*>(ws + L.mass_upper);
+  e = cudaFuncSetAttribute(proxy_kernel<kMasses>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           ProxyCfg<kMasses>::kSmem);
+  if (e != cudaSuccess) return e;
+  proxy_kernel<kMasses><<<dim3(s.hq, chunks), kThreads, ProxyCfg<kMasses>::kSmem, st>>>(
+      maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, nullptr,
+      reinterpret_cast<float2*>(ws + L.proxy_part), reinterpret_cast<const float2*>(ws + L.proxy_stats), vmass, lower,
+      upper, reinterpret_cast<DevStatus*>(ws + L.status));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_assemble_slash(s, lower, upper, smass, st);
 }
 
 }  // namespace crisp

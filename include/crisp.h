@@ -8,6 +8,7 @@
  *
  *   A1 crisp_proxy_map       proxy attention map of the last query block
  *   A3 crisp_block_masses    vertical / slash block masses of that map
+ *   A1+A3 crisp_proxy_masses the same masses straight from q and k (map not stored)
  *   A2 crisp_route_cstruct   C_struct routing: Vertical-Slash or Pooled-Estimation
  *   A4 crisp_select_vs       sink-aware noise-floor selection (VS heads)
  *   A5 crisp_pe_map          pooled attention estimate (PE heads)
@@ -155,6 +156,17 @@ CRISP_API crisp_status crisp_proxy_map_noalloc(const crisp_shape* shape, const v
 CRISP_API crisp_status crisp_block_masses(const crisp_shape* shape, const float* pmap, uint64_t* vmass, uint64_t* smass,
                                 void* ws, size_t ws_bytes, crisp_stream_t stream);
 
+/* A1 and A3 in one pass: the block masses of the proxy map, computed from q
+ * and k without storing the map (routing and Vertical-Slash selection read
+ * only these masses; ai.info page, "Key Contributions" 2; ai-feeds page,
+ * "方法"). Each fp32 probability is formed exactly as crisp_proxy_map stores
+ * it and quantised exactly as crisp_block_masses reads it, so vmass and
+ * smass are bit-identical to crisp_block_masses(crisp_proxy_map(q, k)).
+ * q, k as for crisp_proxy_map; vmass, smass uint64 [hq][nb], 8-byte aligned.
+ * Saves the 4*hq*128*n-byte map write and its re-read. */
+CRISP_API crisp_status crisp_proxy_masses(const crisp_shape* shape, const void* q, const void* k, uint64_t* vmass,
+                                          uint64_t* smass, void* ws, size_t ws_bytes, crisp_stream_t stream);
+
 /* A2. C_struct routing (ai.info page, "Key Contributions" 2: mass at the
  * first 128 and the last 128 tokens of the proxy map; tau_proxy = 0.2). With
  * B = 128 those slices are key blocks 0 and nb-1, so
@@ -232,7 +244,6 @@ CRISP_API crisp_status crisp_dense_prefill(const crisp_shape* shape, const void*
 
 /* Device views of the intermediates crisp_prefill_layer leaves in `ws`. */
 typedef struct crisp_layer_views {
-  float* pmap;
   uint64_t *vmass, *smass, *cstruct, *total;
   uint8_t* route;
   uint32_t *vbits, *sbits;
@@ -244,8 +255,9 @@ typedef struct crisp_layer_views {
 /* Fills *views (host) with pointers into `ws` for this shape. */
 CRISP_API crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws, crisp_layer_views* views /* host */);
 
-/* A1..A8 for one layer: proxy map, masses, routing, VS and PE selection,
- * mask, sparse attention. ws must hold crisp_layer_workspace_size bytes. */
+/* A1..A8 for one layer: block masses of the proxy map (crisp_proxy_masses;
+ * the map itself is never stored), routing, VS and PE selection, mask,
+ * sparse attention. ws must hold crisp_layer_workspace_size bytes. */
 CRISP_API crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* params, const void* q, const void* k,
                                  const void* v, void* out, void* ws, size_t ws_bytes, crisp_stream_t stream);
 

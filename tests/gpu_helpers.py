@@ -33,7 +33,9 @@ def assert_status_ok(ws):
 
 
 def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_only=True):
-    """Runs A1..A8 through the step entry points; returns numpy copies."""
+    """Runs A1..A8 through the step entry points; returns numpy copies. Also
+    runs the fused A1+A3 pass (vmass_fused, smass_fused), whose outputs start
+    as all-ones words so that an entry it fails to write shows."""
     hq, n, _ = q.shape
     hkv = k.shape[0]
     nb = n // B
@@ -57,6 +59,9 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
     rowbits = empty((hq, nb, W), torch.int32)
     counts = empty((hq, nb), torch.int32)
     order = empty((hq * nb,), torch.int32)
+    vmass_f = torch.full((hq, nb), -1, dtype=torch.int64, device="cuda")
+    smass_f = torch.full((hq, nb), -1, dtype=torch.int64, device="cuda")
+    crisp.proxy_masses(s, qd, kd, vmass_f, smass_f, ws)
     crisp.proxy_map(s, qd, kd, pmap, ws)
     crisp.block_masses(s, pmap, vmass, smass, ws)
     crisp.route_cstruct(s, params, vmass, cstruct, total, route)
@@ -69,7 +74,8 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
     assert_status_ok(ws)
     u64 = lambda t: t.cpu().numpy().view(np.uint64)
     u32 = lambda t: t.cpu().numpy().view(np.uint32)
-    return dict(pmap=pmap.cpu().numpy(), vmass=u64(vmass), smass=u64(smass), cstruct=u64(cstruct), total=u64(total),
+    return dict(pmap=pmap.cpu().numpy(), vmass=u64(vmass), smass=u64(smass), vmass_fused=u64(vmass_f),
+                smass_fused=u64(smass_f), cstruct=u64(cstruct), total=u64(total),
                 route=route.cpu().numpy(), vbits=u32(vbits), sbits=u32(sbits), pbar=pbar.cpu().numpy(),
                 pebits=u32(pebits), rowbits=u32(rowbits), counts=counts.cpu().numpy(), order=order.cpu().numpy(),
                 out=out)

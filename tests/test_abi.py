@@ -28,7 +28,8 @@ def test_header_declares_the_steps():
     names = declared_functions()
     for want in ("crisp_proxy_map", "crisp_route_cstruct", "crisp_select_vs", "crisp_select_pe",
                  "crisp_sparse_prefill", "crisp_dense_prefill", "crisp_block_masses", "crisp_pe_map",
-                 "crisp_build_mask", "crisp_prefill_layer", "crisp_read_status", "crisp_status_string"):
+                 "crisp_build_mask", "crisp_prefill_layer", "crisp_proxy_masses", "crisp_read_status",
+                 "crisp_status_string"):
         assert want in names
 
 
@@ -60,8 +61,10 @@ def test_workspace_sizes(L):
     small = crisp.workspace_size(s)
     layer = crisp.layer_workspace_size(s)
     assert 0 < small < layer
-    # the layer workspace holds the fp32 proxy map of the last block
-    assert layer > 4 * 32 * 128 * 524288
+    # the layer workspace holds the fp32 pooled map (nb x nb per head) but not
+    # the proxy map of the last block, which the fused mass pass never stores
+    nb = 524288 // 128
+    assert 4 * 32 * nb * nb < layer < 4 * 32 * 128 * 524288
 
 
 @pytest.mark.parametrize("field,value,code", [
@@ -100,6 +103,9 @@ def test_null_and_misaligned_pointers(L):
                                   None) == 1
     assert L.crisp_sparse_prefill(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(18), vp(16), vp(256), 1 << 30,
                                   None) == 3
+    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), None, vp(16), vp(256), 1 << 30, None) == 1
+    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(20), vp(256), 1 << 30, None) == 3
+    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(256), 64, None) == 4
     # workspace missing / misaligned / too small
     assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), None, 1 << 30, None) == 4
     assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), vp(272), 1 << 30, None) == 3

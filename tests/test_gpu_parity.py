@@ -33,6 +33,9 @@ def check_index_sets(r, params):
     vm, sm = oracle.vs_masses(r["pmap"])
     assert np.array_equal(vm, r["vmass"])
     assert np.array_equal(sm, r["smass"])
+    # the fused pass that never stores the map gives the same integers
+    assert np.array_equal(vm, r["vmass_fused"])
+    assert np.array_equal(sm, r["smass_fused"])
     S, T, route = oracle.route(r["pmap"], tau=(params.tau_num, params.tau_den))
     assert np.array_equal(S, r["cstruct"]) and np.array_equal(T, r["total"])
     assert np.array_equal(route, r["route"])
@@ -218,7 +221,8 @@ def test_prefill_layer_matches_steps():
             t.view(torch.uint8).view(-1).copy_(ws[off:off + nbytes])
             return t.cpu().numpy()
 
-        assert np.array_equal(grab("pmap", (hq, B, n), torch.float32), steps["pmap"])
+        assert np.array_equal(grab("vmass", (hq, nb), torch.int64).view(np.uint64), steps["vmass"])
+        assert np.array_equal(grab("smass", (hq, nb), torch.int64).view(np.uint64), steps["smass"])
         assert np.array_equal(grab("route", (hq,), torch.uint8), steps["route"])
         assert np.array_equal(grab("rowbits", (hq, nb, W), torch.int32).view(np.uint32), steps["rowbits"])
         assert torch.equal(out, steps["out"])
