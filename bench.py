@@ -279,8 +279,8 @@ def run_crisp(args):
         lambda: crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws, stream),
     ]
     # our kernel launches per step: proxy statistics 2, fused masses 2,
-    # route 1, select_vs 1, pe_map 3, select_pe 1, mask+schedule 6, attention 1
-    launches_per_step = 17
+    # route 1, select_vs 1, pe_map 3, select_pe 1, mask+schedule 2, attention 1
+    launches_per_step = 13
 
     def step(events=None):
         for i, c in enumerate(calls):

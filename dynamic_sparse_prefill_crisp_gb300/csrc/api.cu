@@ -112,13 +112,12 @@ ScratchLayout scratch_layout(const crisp_shape& s) {
   L.qbar = o;        o = up(o + hq * nb * kD * 4);
   L.kbar = o;        o = up(o + hkv * nb * kD * 4);
   L.srev = o;        o = up(o + hq * (W + 2) * 4);
-  L.bucket = o;      o = up(o + (nb + 2) * 4);
   L.total = o;
   return L;
 }
 
 LayerLayout layer_layout(const crisp_shape& s) {
-  const size_t hq = s.hq, n = s.seq_len, nb = num_blocks(s.seq_len), W = bit_words(static_cast<int>(nb));
+  const size_t hq = s.hq, nb = num_blocks(s.seq_len), W = bit_words(static_cast<int>(nb));
   LayerLayout L{};
   size_t o = scratch_layout(s).total;
   L.vmass = o;      o = up(o + hq * nb * 8);

@@ -9,9 +9,10 @@
 //   P  = 2^(S*c - m)     softmax warps: TMEM -> registers -> bf16 -> TMEM (over S)
 //   O += P V_kb          tcgen05.mma, A = P (TMEM), B = V (smem, MN-major), D = O (TMEM)
 // K and V tiles arrive by TMA at row coordinate kb*128 (gather by block index).
-// The running max m is raised lazily: O and the row sum are rescaled only when
-// a block's max exceeds m by more than 2^8, which keeps every exponent <= 2^8
-// and leaves O/l exact.
+// The reference max m is raised lazily: each block is first exponentiated at
+// the current m; only if some row's block sum exceeds 2^8 (so possibly one p
+// > 2^8) do the warps take the exact row max, move m, rescale O and the row
+// sum, and recompute the block. Every p stays <= 2^8 and O/l is exact.
 //
 // Warp roles: 0-7 softmax + epilogue (warp w owns TMEM lanes / rows
 // 32*(w%4)..+31 and columns 64*(w/4)..+63), 8 TMA producer, 9 MMA issuer (and
@@ -33,7 +34,7 @@ constexpr uint32_t kTile = kB * kD * 2;  // 32 KB bf16 tile
 constexpr uint32_t kHalf = kTile / 2;
 constexpr uint32_t kSmemBytes = 1024 + 3 * kTile;  // Q, K, V (+ alignment slack)
 constexpr uint32_t kTmemCols = 256;                // S/P [0,128), O [128,256)
-constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleSum = 256.0f;  // 2^8: the largest block row sum kept at the current reference
 
 struct Bars {
   uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, o_full, drain;
@@ -42,6 +43,7 @@ struct Bars {
   int has_diag;
   int abort;
   float xmax[2][2][kB];  // [block parity][column half][row]: partial row maxima
+  int flag[2][4][2];     // [block parity][lane quarter][column half]: needs the exact max
   float xsum[2][kB];     // [column half][row]: partial row sums (epilogue)
 };
 
@@ -53,6 +55,36 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* a
 __device__ __forceinline__ void fail(int* abort, DevStatus* st, uint32_t where) {
   *reinterpret_cast<volatile int*>(abort) = 1;
   report_error(st, CRISP_ERR_TIMEOUT, where);
+}
+
+// p = 2^(s*c - m) for 32 scores of this thread's row: a packed FMA and a
+// packed add per element pair, one MUFU per element. pk: bf16 pairs (even key
+// low); sum += the fp32 sum of the 32 values.
+__device__ __forceinline__ void p_exp32(const uint32_t (&sv)[32], float c, float neg_m, uint32_t* pk, float& sum) {
+  float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    float x0, x1, x2, x3;
+    ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), c, c, neg_m, neg_m);
+    ffma2(x2, x3, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]), c, c, neg_m, neg_m);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+    fadd2_acc(sa0, sa1, p0, p1);
+    fadd2_acc(sb0, sb1, p2, p3);
+    pk[e / 2] = pack_bf16x2(p0, p1);
+    pk[e / 2 + 1] = pack_bf16x2(p2, p3);
+  }
+  sum += (sa0 + sa1) + (sb0 + sb1);
+}
+
+// 32 S columns of this thread's row from TMEM; on the diagonal block the keys
+// above the row (column index col0 + e > r) are set to -inf.
+__device__ __forceinline__ void load_s32(uint32_t taddr, bool diag, int col0, int r, uint32_t (&sv)[32]) {
+  tmem_ld32(taddr, sv);
+  if (diag) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (col0 + e > r) sv[e] = 0xff800000u;  // -inf
+  }
 }
 
 // Bits of row word w restricted to key blocks <= qb.
@@ -76,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = n / kB, W = (nb + 31) / 32;
-  // Work item: rows in order[] (longest first) or, dense, qb descending.
+  // Work item: the schedule order[] or, without one, query blocks descending.
   int item;
   if (order != nullptr) {
     item = order[blockIdx.x];
@@ -224,69 +256,76 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc_fence_after();
       const bool diag = bars.has_diag && j == count - 1;  // ascending order: qb is last
-      uint32_t sv[64];
-      tmem_ld64(s_addr, sv);
-      if (diag) {
-        // Causal edge: key jj of the diagonal block is visible to row r iff jj <= r.
+      // Optimistic pass: P at the current reference m (every block after the
+      // first). The reference must move only when some p would exceed 2^8;
+      // a row's block sum above 2^8 (or not finite) covers every such case,
+      // so that sum is the test and no row max is needed on this path. The
+      // two warps of a quarter hold the two column halves of the same rows,
+      // so they agree through shared memory before either stores P (the
+      // barrier also orders both S loads before P overwrites S: half 1's P
+      // columns 32..63 overlap half 0's S columns).
+      uint32_t pk[32];
+      float bsum = 0.f;
+      bool need = (j == 0);
+      if (!need) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
-          if (half * 64 + e > r) sv[e] = 0xff800000u;  // -inf
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t sv[32];
+          load_s32(s_addr + cc * 32, diag, half * 64 + cc * 32, r, sv);
+          p_exp32(sv, c_log2, -m_ref, pk + cc * 16, bsum);
+        }
+        need = __any_sync(0xffffffffu, !(bsum <= kRescaleSum));
       }
-      // Partial row max on the raw scores (c > 0, so max(s*c) = max(s)*c).
-      float ma = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
-      float mb = fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
-#pragma unroll
-      for (int e = 6; e + 3 < 64; e += 4) {
-        ma = fmax3(ma, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-        mb = fmax3(mb, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
-      }
-      const float pm = fmaxf(fmax3(ma, mb, __uint_as_float(sv[62])), __uint_as_float(sv[63]));
-      bars.xmax[j & 1][half][r] = pm;
-      // The barrier also orders both warps' S loads before either writes P:
-      // half 1's P columns (32..63) overlap half 0's S columns.
+      if (lane == 0) bars.flag[j & 1][quarter][half] = need ? 1 : 0;
       tc_fence_before();
       named_bar_sync(pair_bar, 64);
       tc_fence_after();
-      const float mx = fmaxf(pm, bars.xmax[j & 1][half ^ 1][r]) * c_log2;
-      // Lazy max: move to the new max only when it grew by more than 2^8.
-      // Warp-uniform decision (TMEM loads/stores are warp-collective; both
-      // warps of the pair see the same maxima, so they decide alike); each
-      // row moves to its own new max, f = 1 where it did not grow.
+      need = need || bars.flag[j & 1][quarter][half ^ 1] != 0;  // warp-uniform; alike in both warps
       bool rescale = false;
       float f = 1.f;
-      if (j == 0) {
-        m_ref = mx;
-      } else if (__any_sync(0xffffffffu, mx > m_ref + kRescaleLog2)) {
-        const float m_new = fmaxf(m_ref, mx);
-        f = ex2_approx(m_ref - m_new);
-        l *= f;
-        m_ref = m_new;
-        rescale = true;
-      }
-      // p = 2^(s*c - m): a packed FMA and a packed add per element pair, one
-      // MUFU per element; P goes to TMEM 32 columns at a time.
-      const float neg_m = -m_ref;
-      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+      if (need) {
+        // Exact path: both warps reload S (nothing has been stored over it),
+        // exchange partial row maxima and move each row's reference to its
+        // max (first block: set it), then recompute P. Row max on the raw
+        // scores (c > 0, so max(s*c) = max(s)*c).
+        float pm = -INFINITY;
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t sv[32];
+          load_s32(s_addr + cc * 32, diag, half * 64 + cc * 32, r, sv);
+          float ma = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+          float mb = fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          const int c0 = cc * 32 + 2 * e;
-          float x0, x1, x2, x3;
-          ffma2(x0, x1, __uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1]), c_log2, c_log2, neg_m, neg_m);
-          ffma2(x2, x3, __uint_as_float(sv[c0 + 2]), __uint_as_float(sv[c0 + 3]), c_log2, c_log2, neg_m, neg_m);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          fadd2_acc(sa0, sa1, p0, p1);
-          fadd2_acc(sb0, sb1, p2, p3);
-          pk[e] = pack_bf16x2(p0, p1);
-          pk[e + 1] = pack_bf16x2(p2, p3);
+          for (int e = 6; e + 3 < 32; e += 4) {
+            ma = fmax3(ma, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+            mb = fmax3(mb, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+          }
+          pm = fmax3(pm, fmax3(ma, mb, __uint_as_float(sv[30])), __uint_as_float(sv[31]));
         }
-        tmem_st16(p_addr + cc * 16, pk);
+        bars.xmax[j & 1][half][r] = pm;
+        named_bar_sync(pair_bar, 64);
+        const float mx = fmaxf(pm, bars.xmax[j & 1][half ^ 1][r]) * c_log2;
+        if (j == 0) {
+          m_ref = mx;
+        } else {
+          const float m_new = fmaxf(m_ref, mx);  // unchanged rows keep f = 1
+          f = ex2_approx(m_ref - m_new);
+          l *= f;
+          m_ref = m_new;
+          rescale = true;
+        }
+        bsum = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t sv[32];
+          load_s32(s_addr + cc * 32, diag, half * 64 + cc * 32, r, sv);
+          p_exp32(sv, c_log2, -m_ref, pk + cc * 16, bsum);
+        }
       }
-      l += (sa0 + sa1) + (sb0 + sb1);
+      tmem_st32(p_addr, pk);
+      l += bsum;
       if (rescale) {
-        // O must carry the new max before PV_j adds to it; PV_{j-1} is
+        // O must carry the new reference before PV_j adds to it; PV_{j-1} is
         // complete (QK_j was issued after it), so O is stable here.
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {

@@ -60,7 +60,6 @@ struct ScratchLayout {
   size_t qbar;         // float  [hq][nb][128]
   size_t kbar;         // float  [hkv][nb][128]
   size_t srev;         // uint32 [hq][W + 2]  slash bits reversed
-  size_t bucket;       // int32  [nb + 2]     counting-sort buckets
   size_t total;
 };
 

@@ -2,8 +2,12 @@
 // is a per-head sparse attention mask), one bitset row per query block:
 //   VS head: {kb <= qb : kb in V} U {qb - s, qb - s - 1 : s in S}
 //   PE head: the pebits row qb
-// and the attention work order: rows sorted by block count, largest first
-// (longest-processing-time order for the attention grid).
+// and the attention work order: query blocks descending, the heads of one
+// query block consecutive. A causal row's block count grows with qb, so this
+// runs the longest rows first (the short rows of the first query blocks fill
+// the tail), and consecutive CTAs gather the same kv-group blocks while they
+// are in L2. A strict sort by count was measured slower: it scatters the heads
+// of a query block over the grid.
 //
 // The slash part is built a word at a time: with Srev the slash set reversed
 // (bit x of Srev = bit nb-1-x of S), bit b of word w of {qb - s} is Srev bit
@@ -43,7 +47,8 @@ __device__ __forceinline__ uint32_t window32(const uint32_t* v, int p) {
 // grid (nb, hq); one thread per bitset word.
 __global__ void mask_kernel(const uint8_t* __restrict__ route, const uint32_t* __restrict__ vbits,
                             const uint32_t* __restrict__ srev, const uint32_t* __restrict__ pebits, int nb,
-                            uint32_t* __restrict__ rowbits, int32_t* __restrict__ counts) {
+                            uint32_t* __restrict__ rowbits, int32_t* __restrict__ counts,
+                            int32_t* __restrict__ order) {
   __shared__ int scratch[32];
   const int qb = blockIdx.x, h = blockIdx.y;
   const int W = (nb + 31) / 32, wq = qb >> 5;
@@ -68,51 +73,10 @@ __global__ void mask_kernel(const uint8_t* __restrict__ route, const uint32_t* _
     cnt += __popc(word);
   }
   const int total = block_sum(cnt, scratch);
-  if (threadIdx.x == 0) counts[static_cast<size_t>(h) * nb + qb] = total;
-}
-
-// Counting sort of the rows by count, descending.
-__global__ void bucket_clear(int32_t* __restrict__ bucket, int len) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < len) bucket[i] = 0;
-}
-
-__global__ void count_hist(const int32_t* __restrict__ counts, int items, int nb, int32_t* __restrict__ bucket) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < items) atomicAdd(&bucket[min(max(counts[i], 0), nb)], 1);
-}
-
-// bucket[c] <- number of items with count > c (exclusive scan from the top).
-__global__ void count_scan(int32_t* __restrict__ bucket, int nb) {
-  __shared__ int32_t part[1024];
-  const int per = (nb + 1 + blockDim.x - 1) / blockDim.x;
-  // thread t owns counts [nb - (t+1)*per + 1, nb - t*per] (descending order)
-  const int hi = nb - threadIdx.x * per;
-  int32_t s = 0;
-  for (int c = hi; c > hi - per && c >= 0; --c) s += bucket[c];
-  part[threadIdx.x] = s;
-  __syncthreads();
   if (threadIdx.x == 0) {
-    int32_t run = 0;
-    for (int t = 0; t < static_cast<int>(blockDim.x); ++t) {
-      const int32_t v = part[t];
-      part[t] = run;
-      run += v;
-    }
+    counts[static_cast<size_t>(h) * nb + qb] = total;
+    order[static_cast<size_t>(nb - 1 - qb) * gridDim.y + h] = h * nb + qb;
   }
-  __syncthreads();
-  int32_t run = part[threadIdx.x];
-  for (int c = hi; c > hi - per && c >= 0; --c) {
-    const int32_t v = bucket[c];
-    bucket[c] = run;
-    run += v;
-  }
-}
-
-__global__ void count_scatter(const int32_t* __restrict__ counts, int items, int nb, int32_t* __restrict__ bucket,
-                              int32_t* __restrict__ order) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < items) order[atomicAdd(&bucket[min(max(counts[i], 0), nb)], 1)] = i;
 }
 
 }  // namespace
@@ -122,16 +86,9 @@ cudaError_t launch_build_mask(const crisp_shape& s, const uint8_t* route, const 
                               int32_t* order, char* ws, cudaStream_t st) {
   const ScratchLayout L = scratch_layout(s);
   const int nb = num_blocks(s.seq_len);
-  const int items = s.hq * nb;
   auto* srev = reinterpret_cast<uint32_t*>(ws + L.srev);
-  auto* bucket = reinterpret_cast<int32_t*>(ws + L.bucket);
   srev_kernel<<<s.hq, 128, 0, st>>>(sbits, route, nb, srev);
-  mask_kernel<<<dim3(nb, s.hq), 128, 0, st>>>(route, vbits, srev, pebits, nb, rowbits, counts);
-  // Schedule: row ids sorted by count, descending (counting sort).
-  bucket_clear<<<(nb + 2 + 255) / 256, 256, 0, st>>>(bucket, nb + 2);
-  count_hist<<<(items + 255) / 256, 256, 0, st>>>(counts, items, nb, bucket);
-  count_scan<<<1, 1024, 0, st>>>(bucket, nb);
-  count_scatter<<<(items + 255) / 256, 256, 0, st>>>(counts, items, nb, bucket, order);
+  mask_kernel<<<dim3(nb, s.hq), 128, 0, st>>>(route, vbits, srev, pebits, nb, rowbits, counts, order);
   return cudaGetLastError();
 }
 

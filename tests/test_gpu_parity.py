@@ -51,10 +51,10 @@ def check_index_sets(r, params):
     assert np.array_equal(rb, r["rowbits"])
     pop = np.unpackbits(rb.view(np.uint8), axis=-1).sum(-1).astype(np.int64)
     assert np.array_equal(pop, r["counts"])
-    # schedule: a permutation of the rows with non-increasing counts
-    order = r["order"]
-    assert np.array_equal(np.sort(order), np.arange(order.size))
-    assert np.all(np.diff(pop.reshape(-1)[order]) <= 0)
+    # schedule: query blocks descending, heads ascending within a query block
+    hq, nb = pop.shape
+    t = np.arange(hq * nb)
+    assert np.array_equal(r["order"], (t % hq) * nb + (nb - 1 - t // hq))
     return rb, route
 
 
