@@ -363,8 +363,10 @@ def run_crisp(args):
                  "attention_speedup": d_ms / attn_ms, "layer_speedup": d_ms / ms_per_step}
         crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws, stream)
 
-    # End to end through the public API: pinned host -> device, the whole
-    # layer (crisp_prefill_layer), device -> pinned host of the output.
+    # End to end through the public API with HOST buffers: one call of
+    # crisp_prefill_layer_host per step, which uploads q, k, v from pinned
+    # host memory, runs the whole layer and downloads the output, one kv
+    # group at a time with the copies overlapped with the compute.
     e2e = None
     if not args.no_e2e:
         lws = torch.empty(crisp.layer_workspace_size(s), dtype=torch.uint8, device=dev)
@@ -372,13 +374,10 @@ def run_crisp(args):
         oh = torch.empty((hq, n, 128), dtype=torch.int16, pin_memory=True)
         qx, kx, vx = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
         ox = torch.empty_like(out)
+        pipe = crisp.HostPipeline()
 
         def e2e_step():
-            qx.view(torch.int16).copy_(qh, non_blocking=True)
-            kx.view(torch.int16).copy_(kh, non_blocking=True)
-            vx.view(torch.int16).copy_(vh, non_blocking=True)
-            crisp.prefill_layer(s, params, qx, kx, vx, ox, lws, stream)
-            oh.copy_(ox.view(torch.int16), non_blocking=True)
+            crisp.prefill_layer_host(pipe, s, params, qh, kh, vh, oh, qx, kx, vx, ox, lws, stream)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -394,7 +393,19 @@ def run_crisp(args):
             raise RuntimeError("device status after e2e")
         assert torch.equal(oh.view(torch.bfloat16).to(dev), out), "e2e output differs from the device-resident run"
         h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
-        e2e = {"value": e2e_ms / world, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": oh.numel() * 2}
+        e2e = {"value": e2e_ms / world, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": oh.numel() * 2,
+               "api": "crisp_prefill_layer_host"}
+        # Raw copy rates on this machine, for context: one 4 GiB upload, one download.
+        c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        c0.record(stream)
+        qx.view(torch.int16).copy_(qh, non_blocking=True)
+        c1.record(stream)
+        oh.copy_(ox.view(torch.int16), non_blocking=True)
+        c2.record(stream)
+        torch.cuda.synchronize()
+        e2e["copy_gbs"] = {"h2d": qh.numel() * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9,
+                           "d2h": oh.numel() * 2 / (c1.elapsed_time(c2) * 1e-3) / 1e9}
+        pipe.close()
         del lws, qx, kx, vx, ox
 
     cpu = None

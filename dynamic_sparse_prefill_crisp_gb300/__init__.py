@@ -69,6 +69,9 @@ def lib():
         L.crisp_proxy_map_noalloc.argtypes = [P(Shape), vp, vp, vp, st]
         L.crisp_block_masses.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
         L.crisp_proxy_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
+        L.crisp_host_pipeline_create.argtypes = [P(vp)]
+        L.crisp_host_pipeline_destroy.argtypes = [vp]
+        L.crisp_prefill_layer_host.argtypes = [vp, P(Shape), P(Params)] + [vp] * 9 + [sz, st]
         L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
         L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
         L.crisp_pe_map.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
@@ -85,7 +88,8 @@ def lib():
                      "crisp_proxy_map_noalloc",
                      "crisp_block_masses", "crisp_proxy_masses", "crisp_route_cstruct", "crisp_select_vs", "crisp_pe_map",
                      "crisp_select_pe", "crisp_build_mask", "crisp_sparse_prefill", "crisp_dense_prefill",
-                     "crisp_layer_views_get", "crisp_prefill_layer", "crisp_read_status"):
+                     "crisp_layer_views_get", "crisp_prefill_layer", "crisp_read_status",
+                     "crisp_host_pipeline_create", "crisp_host_pipeline_destroy", "crisp_prefill_layer_host"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -224,6 +228,38 @@ def layer_views(shape, ws) -> dict:
 def prefill_layer(shape, params, q, k, v, out, ws, stream=None):
     _check(lib().crisp_prefill_layer(ctypes.byref(shape), ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
                                      _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_prefill_layer")
+
+
+class HostPipeline:
+    """Streams and events of crisp_prefill_layer_host (on the current device)."""
+
+    def __init__(self):
+        self._h = ctypes.c_void_p()
+        _check(lib().crisp_host_pipeline_create(ctypes.byref(self._h)), "crisp_host_pipeline_create")
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h:
+            _check(lib().crisp_host_pipeline_destroy(self._h), "crisp_host_pipeline_destroy")
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def prefill_layer_host(pipeline, shape, params, q_host, k_host, v_host, out_host, q, k, v, out, ws, stream=None):
+    """crisp_prefill_layer from host buffers (pinned torch CPU tensors), copies
+    overlapped with compute; q, k, v, out are the device staging buffers."""
+    _check(lib().crisp_prefill_layer_host(pipeline.handle, ctypes.byref(shape), ctypes.byref(params), _ptr(q_host),
+                                          _ptr(k_host), _ptr(v_host), _ptr(out_host), _ptr(q), _ptr(k), _ptr(v),
+                                          _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "crisp_prefill_layer_host")
 
 
 def read_status(ws, stream=None) -> int:

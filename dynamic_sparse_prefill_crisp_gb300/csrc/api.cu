@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "common.cuh"
 
@@ -397,6 +398,55 @@ crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws, crisp_lay
   return CRISP_OK;
 }
 
+}  // extern "C"
+
+namespace crisp {
+namespace {
+
+// A1..A8 for one (normalised, validated) shape; intermediates in ws.
+crisp_status run_layer(const crisp_shape& s, const crisp_params& p, const void* q, const void* k, const void* v,
+                       void* out, void* ws, cudaStream_t stream) {
+  crisp_layer_views w;
+  crisp_layer_views_get(&s, ws, &w);
+  TmaMaps maps;
+  crisp_status st;
+  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  char* wsb = static_cast<char*>(ws);
+  if (launch_proxy_masses(s, maps, w.vmass, w.smass, wsb, stream) != cudaSuccess ||
+      launch_route(s, p, w.vmass, w.cstruct, w.total, w.route, stream) != cudaSuccess ||
+      launch_select_vs(s, p, w.vmass, w.smass, w.route, w.vbits, w.sbits, stream) != cudaSuccess ||
+      launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess ||
+      launch_select_pe(s, p, w.pbar, w.route, w.pebits, stream) != cudaSuccess ||
+      launch_build_mask(s, w.route, w.vbits, w.sbits, w.pebits, w.rowbits, w.counts, w.order, wsb, stream) !=
+          cudaSuccess ||
+      launch_attention(s, maps, w.rowbits, w.order, out, wsb, false, stream) != cudaSuccess)
+    return CRISP_ERR_CUDA;
+  return CRISP_OK;
+}
+
+bool contiguous(const crisp_shape& s) {
+  const int64_t plane = static_cast<int64_t>(s.seq_len) * kD;
+  return s.q_tok_stride == kD && s.kv_tok_stride == kD && s.o_tok_stride == kD && s.q_head_stride == plane &&
+         s.kv_head_stride == plane && s.o_head_stride == plane;
+}
+
+}  // namespace
+}  // namespace crisp
+
+// Streams and events of the host-buffer path (created by
+// crisp_host_pipeline_create on the current device).
+struct crisp_host_pipeline {
+  static constexpr int kRing = 4;  // events are reused round-robin across kv groups
+  int device;
+  cudaStream_t in, out;
+  cudaEvent_t start, done;
+  cudaEvent_t ev_in[kRing], ev_comp[kRing];
+};
+
+extern "C" {
+
 crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* params, const void* q, const void* k,
                                  const void* v, void* out, void* ws, size_t ws_bytes, crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
@@ -409,21 +459,100 @@ crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* p
   if (!aligned(ws, kAlign)) return CRISP_ERR_ALIGN;
   if (ws_bytes < layer_layout(s).total) return CRISP_ERR_WORKSPACE;
   if ((st = check_device()) != CRISP_OK) return st;
-  crisp_layer_views w;
-  crisp_layer_views_get(&s, ws, &w);
-  TmaMaps maps;
-  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
-  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-  if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-  char* wsb = static_cast<char*>(ws);
-  if (launch_proxy_masses(s, maps, w.vmass, w.smass, wsb, stream) != cudaSuccess ||
-      launch_route(s, *params, w.vmass, w.cstruct, w.total, w.route, stream) != cudaSuccess ||
-      launch_select_vs(s, *params, w.vmass, w.smass, w.route, w.vbits, w.sbits, stream) != cudaSuccess ||
-      launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess ||
-      launch_select_pe(s, *params, w.pbar, w.route, w.pebits, stream) != cudaSuccess ||
-      launch_build_mask(s, w.route, w.vbits, w.sbits, w.pebits, w.rowbits, w.counts, w.order, wsb, stream) !=
-          cudaSuccess ||
-      launch_attention(s, maps, w.rowbits, w.order, out, wsb, false, stream) != cudaSuccess)
+  return run_layer(s, *params, q, k, v, out, ws, stream);
+}
+
+crisp_status crisp_host_pipeline_create(crisp_host_pipeline** pipeline) {
+  if (!pipeline) return CRISP_ERR_INVALID_ARG;
+  *pipeline = nullptr;
+  crisp_status st = check_device();
+  if (st != CRISP_OK) return st;
+  auto* p = new (std::nothrow) crisp_host_pipeline();
+  if (!p) return CRISP_ERR_CUDA;
+  bool ok = cudaGetDevice(&p->device) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&p->start, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < crisp_host_pipeline::kRing; ++i)
+    ok = cudaEventCreateWithFlags(&p->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    crisp_host_pipeline_destroy(p);
+    return CRISP_ERR_CUDA;
+  }
+  *pipeline = p;
+  return CRISP_OK;
+}
+
+crisp_status crisp_host_pipeline_destroy(crisp_host_pipeline* p) {
+  if (!p) return CRISP_OK;
+  // Objects never created are null handles; destroying those is skipped.
+  if (p->in) cudaStreamSynchronize(p->in);
+  if (p->out) cudaStreamSynchronize(p->out);
+  for (int i = 0; i < crisp_host_pipeline::kRing; ++i) {
+    if (p->ev_in[i]) cudaEventDestroy(p->ev_in[i]);
+    if (p->ev_comp[i]) cudaEventDestroy(p->ev_comp[i]);
+  }
+  if (p->start) cudaEventDestroy(p->start);
+  if (p->done) cudaEventDestroy(p->done);
+  if (p->in) cudaStreamDestroy(p->in);
+  if (p->out) cudaStreamDestroy(p->out);
+  delete p;
+  return CRISP_OK;
+}
+
+crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp_shape* shape,
+                                      const crisp_params* params, const void* q_host, const void* k_host,
+                                      const void* v_host, void* out_host, void* q, void* k, void* v, void* out,
+                                      void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  if (!pipeline) return CRISP_ERR_INVALID_ARG;
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if ((st = check_params(params)) != CRISP_OK) return st;
+  if (!q_host || !k_host || !v_host || !out_host || !q || !k || !v || !out) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if (!contiguous(s)) return CRISP_ERR_SHAPE;
+  if (!ws) return CRISP_ERR_WORKSPACE;
+  if (!aligned(ws, kAlign)) return CRISP_ERR_ALIGN;
+  if (ws_bytes < layer_layout(s).total) return CRISP_ERR_WORKSPACE;
+  if ((st = check_device()) != CRISP_OK) return st;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != pipeline->device) return CRISP_ERR_DEVICE;
+
+  // One kv group (its G query heads, its K and V) at a time: the upload of
+  // group g+1 and the download of group g-1 overlap the compute of group g.
+  const int G = s.hq / s.hkv;
+  const size_t plane = static_cast<size_t>(s.seq_len) * kD * 2;  // bytes of one head
+  crisp_shape sub = s;
+  sub.hq = G;
+  sub.hkv = 1;
+  auto* p = pipeline;
+  cudaStream_t cs = stream;
+  auto cb = [](const void* b, size_t off) { return static_cast<const char*>(b) + off; };
+  auto mb = [](void* b, size_t off) { return static_cast<char*>(b) + off; };
+  // Work already on `stream` (earlier users of these buffers) comes first.
+  if (cudaEventRecord(p->start, cs) != cudaSuccess || cudaStreamWaitEvent(p->in, p->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->out, p->start, 0) != cudaSuccess)
+    return CRISP_ERR_CUDA;
+  for (int g = 0; g < s.hkv; ++g) {
+    const int e = g % crisp_host_pipeline::kRing;
+    const size_t kv_off = static_cast<size_t>(g) * plane, q_off = static_cast<size_t>(g) * G * plane;
+    if (cudaMemcpyAsync(mb(k, kv_off), cb(k_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+        cudaMemcpyAsync(mb(v, kv_off), cb(v_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+        cudaMemcpyAsync(mb(q, q_off), cb(q_host, q_off), G * plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+        cudaEventRecord(p->ev_in[e], p->in) != cudaSuccess || cudaStreamWaitEvent(cs, p->ev_in[e], 0) != cudaSuccess)
+      return CRISP_ERR_CUDA;
+    if ((st = run_layer(sub, *params, mb(q, q_off), mb(k, kv_off), mb(v, kv_off), mb(out, q_off), ws, cs)) !=
+        CRISP_OK)
+      return st;
+    if (cudaEventRecord(p->ev_comp[e], cs) != cudaSuccess || cudaStreamWaitEvent(p->out, p->ev_comp[e], 0) != cudaSuccess ||
+        cudaMemcpyAsync(mb(out_host, q_off), cb(out, q_off), G * plane, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
+      return CRISP_ERR_CUDA;
+  }
+  // `stream` completes after the last download.
+  if (cudaEventRecord(p->done, p->out) != cudaSuccess || cudaStreamWaitEvent(cs, p->done, 0) != cudaSuccess)
     return CRISP_ERR_CUDA;
   return CRISP_OK;
 }

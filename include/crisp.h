@@ -17,6 +17,7 @@
  *   A8 crisp_sparse_prefill  causal GQA block-sparse attention
  *   A9 crisp_dense_prefill   the same kernel over every causal block
  *   crisp_prefill_layer      A1..A8 in order, intermediates in the workspace
+ *   crisp_prefill_layer_host the same from host buffers, copies overlapped with compute
  *
  * Conventions (every function):
  *  - Pointers are DEVICE pointers unless marked "host". The caller owns and
@@ -262,6 +263,33 @@ CRISP_API crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws,
  * sparse attention. ws must hold crisp_layer_workspace_size bytes. */
 CRISP_API crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* params, const void* q, const void* k,
                                  const void* v, void* out, void* ws, size_t ws_bytes, crisp_stream_t stream);
+
+/* Prefill from HOST buffers: the streams and events the host-buffer path
+ * uses, created on the current device (the one call of this library that
+ * creates CUDA objects; destroy it with crisp_host_pipeline_destroy). */
+typedef struct crisp_host_pipeline crisp_host_pipeline;
+CRISP_API crisp_status crisp_host_pipeline_create(crisp_host_pipeline** pipeline /* host out */);
+/* Waits for the pipeline's streams and destroys them; NULL is a no-op. */
+CRISP_API crisp_status crisp_host_pipeline_destroy(crisp_host_pipeline* pipeline);
+
+/* crisp_prefill_layer with q, k, v read from host memory and out written to
+ * host memory. The layer is processed one kv group at a time (its G query
+ * heads, its K and V; every step of the method is per head): the upload of
+ * group g+1 and the download of group g-1 run on the pipeline's two streams
+ * while group g computes on `stream`, so the copies overlap the compute.
+ * Results are bit-identical to crisp_prefill_layer.
+ * q_host, k_host, v_host, out_host: host, contiguous [heads][n][128] bf16,
+ * page-locked for the copies to be asynchronous. q, k, v, out: device
+ * buffers of the same sizes (staging; afterwards they hold the inputs and
+ * the output). shape: contiguous strides only (else CRISP_ERR_SHAPE). ws:
+ * crisp_layer_workspace_size bytes. Ordered after earlier work on `stream`;
+ * `stream` completes after the last download. The pipeline must belong to
+ * the current device (else CRISP_ERR_DEVICE) and serves one call at a time
+ * per stream order. */
+CRISP_API crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp_shape* shape,
+                                                const crisp_params* params, const void* q_host, const void* k_host,
+                                                const void* v_host, void* out_host, void* q, void* k, void* v,
+                                                void* out, void* ws, size_t ws_bytes, crisp_stream_t stream);
 
 /* Synchronises `stream` and copies the workspace status word to *status
  * (host). Returns CRISP_ERR_CUDA if the stream or the copy failed. */

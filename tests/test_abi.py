@@ -106,6 +106,11 @@ def test_null_and_misaligned_pointers(L):
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), None, vp(16), vp(256), 1 << 30, None) == 1
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(20), vp(256), 1 << 30, None) == 3
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(256), 64, None) == 4
+    # host-buffer path: argument errors before any CUDA call
+    assert L.crisp_host_pipeline_create(None) == 1
+    assert L.crisp_host_pipeline_destroy(None) == 0
+    assert L.crisp_prefill_layer_host(None, ctypes.byref(s), ctypes.byref(crisp.params_default()),
+                                      *([vp(256)] * 9), 1 << 30, None) == 1
     # workspace missing / misaligned / too small
     assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), None, 1 << 30, None) == 4
     assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), vp(272), 1 << 30, None) == 3

@@ -228,6 +228,34 @@ def test_prefill_layer_matches_steps():
         assert torch.equal(out, steps["out"])
 
 
+def test_prefill_layer_host_matches_device_layer():
+    # Host buffers in, host buffer out, one kv group at a time with the copies
+    # overlapped: bit-identical to the device-resident layer.
+    pipe = crisp.HostPipeline()
+    for hq, hkv, n, seed in ((8, 2, 2048, 71), (7, 1, 1152, 72), (4, 4, 640, 73)):
+        w = synth.small("host", hq, hkv, n, seed)
+        q, k, v = w.generate()
+        params = crisp.params_default()
+        qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+        ref = empty((hq, n, 128), torch.bfloat16)
+        s = crisp.make_shape(hq, hkv, n, qd, kd, ref)
+        ws = new_workspace(s, layer=True)
+        crisp.prefill_layer(s, params, qd, kd, vd, ref, ws)
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+        qh, kh, vh = pin(q), pin(k), pin(v)
+        oh = torch.zeros((hq, n, 128), dtype=torch.int16).pin_memory()
+        qs, ks, vs = (torch.empty_like(t) for t in (qd, kd, vd))
+        os_ = empty((hq, n, 128), torch.bfloat16)
+        ws2 = new_workspace(s, layer=True)
+        crisp.prefill_layer_host(pipe, s, params, qh, kh, vh, oh, qs, ks, vs, os_, ws2)
+        torch.cuda.synchronize()
+        assert_status_ok(ws2)
+        assert torch.equal(qs, qd) and torch.equal(ks, kd) and torch.equal(vs, vd)
+        assert torch.equal(os_, ref)
+        assert torch.equal(oh.view(torch.bfloat16).cuda(), ref)
+    pipe.close()
+
+
 def test_cfg1_full_layer():
     w = synth.WORKLOADS["cfg1"]
     q, k, v = w.generate()
