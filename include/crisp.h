@@ -22,7 +22,8 @@
  * Conventions (every function):
  *  - Pointers are DEVICE pointers unless marked "host". The caller owns and
  *    allocates every buffer, including the workspace; the library allocates
- *    and frees nothing and keeps no mutable global state.
+ *    and frees no memory, and creates CUDA objects only in
+ *    crisp_host_pipeline_create (two streams and their events).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream); calls return without synchronising, except crisp_read_status.
  *  - Argument errors are detected on the host, returned synchronously, and
