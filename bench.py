@@ -144,6 +144,24 @@ def selected_pairs(rowbits: np.ndarray, nb: int) -> int:
     return (total - diag) * B * B + diag * B * (B + 1) // 2
 
 
+def profiled_traffic(kernel_src: str, profile: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source has changed since the counters were taken."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, profile)).read()
+        src = open(os.path.join(ROOT, kernel_src), "rb").read()
+    except OSError:
+        return None
+    fields = dict(line.split(": ", 1) for line in text.splitlines() if ": " in line and " " not in line.split(": ")[0])
+    if fields.get("source_sha256", "").strip() != hashlib.sha256(src).hexdigest():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -327,6 +345,8 @@ def run_crisp(args):
     dense_pairs = hq * n * (n + 1) // 2
     routes = route.cpu().numpy()
     hbm_peak, tf_peak, peak_kind = measured_peaks()
+    traffic = profiled_traffic("dynamic_sparse_prefill_crisp_gb300/csrc/attention.cu",
+                               "profiles/attention_cfg5_512k_traffic.md")
     attn_ms = stage_ms["attention"]
     achieved_tf = flops / (attn_ms * 1e-3) / 1e12
     proxy_bytes = 4 * hq * B * n + 2 * (2 * hkv * n * 128) + 2 * hq * B * 128
@@ -427,7 +447,9 @@ def run_crisp(args):
             "density": pairs / dense_pairs,
             "eff_tflops": achieved_tf,
             "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": achieved_tf, "peak": tf_peak,
-                         "unit": "TFLOP/s", "frac": achieved_tf / tf_peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved_tf / tf_peak,
+                         "traffic": traffic if w.name == "cfg5-512k-llama8b" else None,
+                         "traffic_source": "profiles/attention_cfg5_512k_traffic.md",
                          "peak_kind": f"bf16 dense, {peak_kind} (sustained)"},
             "unfused_map_path": {
                 "proxy_ms": unf_proxy_ms, "masses_ms": unf_masses_ms,
