@@ -48,6 +48,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention baseline launch")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--sweep", choices=["lengths", "alpha", "pe", "flex"], default=None,
+                    help="instead of the step: sparse layer vs dense attention over sequence lengths (cfg2 "
+                         "recipe, 2k-128k), over alpha (cfg5), PE gamma vs noise-floor rule (cfg2), or CRISP "
+                         "vs the FlexPrefill rules it replaces (cfg5 and cfg2)")
     return ap.parse_args(argv)
 
 
@@ -473,10 +477,118 @@ def run_crisp(args):
     return 0
 
 
+# ------------------------------------------------------------------- sweeps
+def time_layer(w, params, reps, dense=True):
+    """One layer through crisp_prefill_layer (device-resident inputs; the
+    routing and selection rules follow params) and dense attention on the
+    same inputs; CUDA events, median of reps after one warm-up."""
+    import torch
+    import dynamic_sparse_prefill_crisp_gb300 as crisp
+    q, k, v = w.generate()
+    dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+    qd, kd, vd = dev(q), dev(k), dev(v)
+    hq, hkv, n = w.hq, w.hkv, w.n
+    nb, W = n // B, (n // B + 31) // 32
+    out = torch.empty((hq, n, 128), dtype=torch.bfloat16, device="cuda")
+    s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+    ws = torch.empty(crisp.layer_workspace_size(s), dtype=torch.uint8, device="cuda")
+    crisp.workspace_init(ws)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    layer_ms = timed(lambda: crisp.prefill_layer(s, params, qd, kd, vd, out, ws))
+    if crisp.read_status(ws) != 0:
+        raise RuntimeError("device status after the sweep layer")
+    views = crisp.layer_views(s, ws)
+
+    def grab(name, shape, dtype):
+        t = torch.empty(shape, dtype=dtype, device="cuda")
+        off = views[name] - ws.data_ptr()
+        t.view(torch.uint8).view(-1).copy_(ws[off:off + t.numel() * t.element_size()])
+        return t.cpu().numpy()
+
+    rb = grab("rowbits", (hq, nb, W), torch.int32).view(np.uint32)
+    route = grab("route", (hq,), torch.uint8)
+    counts = grab("counts", (hq, nb), torch.int32)
+    pairs = selected_pairs(rb, nb)
+    dense_pairs = hq * n * (n + 1) // 2
+    r = {"seq_len": n, "layer_ms": layer_ms, "density": pairs / dense_pairs, "routes_vs": int(route.sum()),
+         "blocks_per_row": float(counts.mean())}
+    if dense:
+        r["dense_ms"] = timed(lambda: crisp.dense_prefill(s, qd, kd, vd, out, ws))
+        r["speedup_vs_dense"] = r["dense_ms"] / layer_ms
+    return r
+
+
+def run_sweep(args):
+    import torch
+    import dynamic_sparse_prefill_crisp_gb300 as crisp
+    import synth
+    from dynamic_sparse_prefill_crisp_gb300 import build as crisp_build
+    crisp_build.build()
+    torch.cuda.set_device(0)
+    rows = []
+    if args.sweep == "lengths":
+        base = synth.WORKLOADS["cfg2"]
+        for n in (2048, 4096, 8192, 16384, 32768, 65536, 131072):
+            w = synth.Workload(**{**base.__dict__, "name": f"cfg2-recipe-{n}", "n": n})
+            rows.append(time_layer(w, crisp.params_default(), reps=5))
+        workload = "cfg2 recipe (32 q / 8 kv heads, half sink-type, half diffuse) at 2k-128k tokens"
+    elif args.sweep == "alpha":
+        w = synth.WORKLOADS["cfg5"]
+        for i, a in enumerate(((1, 1), (5, 4), (3, 2))):
+            r = time_layer(w, crisp.params_default(alpha=a), reps=3, dense=(i == 0))
+            r["alpha"] = f"{a[0]}/{a[1]}"
+            rows.append(r)
+        d = rows[0]["dense_ms"]
+        for r in rows:
+            r["speedup_vs_dense"] = d / r["layer_ms"]
+        workload = "cfg5 (512k tokens, 32 q / 8 kv heads)"
+    elif args.sweep == "flex":
+        variants = [("CRISP (C_struct, noise floor alpha 1)", crisp.params_default()),
+                    ("CRISP alpha 5/4", crisp.params_default(alpha=(5, 4))),
+                    ("FlexPrefill rules gamma 0.95 (JSD routing, coverage on VS heads)",
+                     crisp.params_default(route_mode=crisp.ROUTE_JSD, vs_mode=crisp.VS_GAMMA, vs_gamma=(95, 100))),
+                    ("FlexPrefill rules gamma 0.97",
+                     crisp.params_default(route_mode=crisp.ROUTE_JSD, vs_mode=crisp.VS_GAMMA, vs_gamma=(97, 100)))]
+        for cfg in ("cfg5", "cfg2"):
+            w = synth.WORKLOADS[cfg]
+            for i, (label, p) in enumerate(variants):
+                r = time_layer(w, p, reps=3, dense=(i == 0))
+                r.update(workload=cfg, rules=label)
+                rows.append(r)
+            d = rows[-len(variants)]["dense_ms"]
+            for r in rows[-len(variants):]:
+                r["speedup_vs_dense"] = d / r["layer_ms"]
+        workload = "cfg5 (512k, all heads sink-type) and cfg2 (32k, half diffuse); same kernels, rules differ"
+    else:
+        w = synth.WORKLOADS["cfg2"]
+        for mode in (crisp.PE_GAMMA, crisp.PE_NOISE):
+            r = time_layer(w, crisp.params_default(pe_mode=mode), reps=5, dense=(mode == crisp.PE_GAMMA))
+            r["pe_mode"] = "gamma 19/20" if mode == crisp.PE_GAMMA else "noise floor (alpha 1)"
+            rows.append(r)
+        workload = "cfg2 (32k tokens, 16 sink-type + 16 diffuse heads)"
+    print(json.dumps({"sweep": args.sweep, "workload": workload, "unit": "ms", "rows": rows}), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_crisp(args)
 
 

@@ -21,6 +21,8 @@ D = 128
 STATUS_NAMES = {0: "CRISP_OK", 1: "CRISP_ERR_INVALID_ARG", 2: "CRISP_ERR_SHAPE", 3: "CRISP_ERR_ALIGN",
                 4: "CRISP_ERR_WORKSPACE", 5: "CRISP_ERR_CUDA", 6: "CRISP_ERR_TIMEOUT", 7: "CRISP_ERR_DEVICE"}
 PE_GAMMA, PE_NOISE = 0, 1
+ROUTE_CSTRUCT, ROUTE_JSD = 0, 1
+VS_NOISE, VS_GAMMA = 0, 1
 
 
 class CrispError(RuntimeError):
@@ -42,7 +44,10 @@ class Params(ctypes.Structure):
     _fields_ = [("tau_num", ctypes.c_uint32), ("tau_den", ctypes.c_uint32),
                 ("alpha_num", ctypes.c_uint32), ("alpha_den", ctypes.c_uint32),
                 ("gamma_num", ctypes.c_uint32), ("gamma_den", ctypes.c_uint32),
-                ("kmin_blocks", ctypes.c_int32), ("pe_mode", ctypes.c_int32)]
+                ("kmin_blocks", ctypes.c_int32), ("pe_mode", ctypes.c_int32),
+                ("route_mode", ctypes.c_int32), ("vs_mode", ctypes.c_int32),
+                ("vs_gamma_num", ctypes.c_uint32), ("vs_gamma_den", ctypes.c_uint32),
+                ("jsd_tau", ctypes.c_float), ("dense_below", ctypes.c_int32)]
 
 
 class LayerViews(ctypes.Structure):
@@ -73,6 +78,7 @@ def lib():
         L.crisp_host_pipeline_destroy.argtypes = [vp]
         L.crisp_prefill_layer_host.argtypes = [vp, P(Shape), P(Params)] + [vp] * 9 + [sz, st]
         L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
+        L.crisp_route_jsd.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
         L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
         L.crisp_pe_map.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
         L.crisp_select_pe.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, sz, st]
@@ -86,7 +92,7 @@ def lib():
         L.crisp_status_string.restype = ctypes.c_char_p
         for name in ("crisp_workspace_size", "crisp_layer_workspace_size", "crisp_workspace_init", "crisp_proxy_map",
                      "crisp_proxy_map_noalloc",
-                     "crisp_block_masses", "crisp_proxy_masses", "crisp_route_cstruct", "crisp_select_vs", "crisp_pe_map",
+                     "crisp_block_masses", "crisp_proxy_masses", "crisp_route_cstruct", "crisp_route_jsd", "crisp_select_vs", "crisp_pe_map",
                      "crisp_select_pe", "crisp_build_mask", "crisp_sparse_prefill", "crisp_dense_prefill",
                      "crisp_layer_views_get", "crisp_prefill_layer", "crisp_read_status",
                      "crisp_host_pipeline_create", "crisp_host_pipeline_destroy", "crisp_prefill_layer_host"):
@@ -135,7 +141,7 @@ def params_default(**overrides) -> Params:
     p = Params()
     lib().crisp_params_default(ctypes.byref(p))
     for key, val in overrides.items():
-        if key in ("alpha", "tau", "gamma"):
+        if key in ("alpha", "tau", "gamma", "vs_gamma"):
             setattr(p, f"{key}_num", val[0])
             setattr(p, f"{key}_den", val[1])
         else:
@@ -185,6 +191,12 @@ def proxy_masses(shape, q, k, vmass, smass, ws, stream=None):
 def route_cstruct(shape, params, vmass, cstruct, total, route, stream=None):
     _check(lib().crisp_route_cstruct(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(cstruct),
                                      _ptr(total), _ptr(route), _stream(stream)), "crisp_route_cstruct")
+
+
+def route_jsd(shape, params, vmass, pbar, jsd, route, stream=None):
+    """FlexPrefill's divergence routing (comparator); pbar must hold row nb-1 of every head."""
+    _check(lib().crisp_route_jsd(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(pbar), _ptr(jsd),
+                                 _ptr(route), _stream(stream)), "crisp_route_jsd")
 
 
 def select_vs(shape, params, vmass, smass, route, vbits, sbits, ws, stream=None):

@@ -39,6 +39,11 @@ crisp_status check_params(const crisp_params* p) {
   if (p->gamma_den == 0 || p->gamma_num > p->gamma_den) return CRISP_ERR_INVALID_ARG;
   if (p->kmin_blocks < 0 || p->kmin_blocks > kMaxBlocks) return CRISP_ERR_INVALID_ARG;
   if (p->pe_mode != CRISP_PE_GAMMA && p->pe_mode != CRISP_PE_NOISE) return CRISP_ERR_INVALID_ARG;
+  if (p->route_mode != CRISP_ROUTE_CSTRUCT && p->route_mode != CRISP_ROUTE_JSD) return CRISP_ERR_INVALID_ARG;
+  if (p->vs_mode != CRISP_VS_NOISE && p->vs_mode != CRISP_VS_GAMMA) return CRISP_ERR_INVALID_ARG;
+  if (p->vs_gamma_den == 0 || p->vs_gamma_num > p->vs_gamma_den) return CRISP_ERR_INVALID_ARG;
+  if (!(p->jsd_tau >= 0.f && p->jsd_tau <= 1.f)) return CRISP_ERR_INVALID_ARG;
+  if (p->dense_below < 0) return CRISP_ERR_INVALID_ARG;
   return CRISP_OK;
 }
 
@@ -153,6 +158,12 @@ void crisp_params_default(crisp_params* p) {
   p->gamma_den = 20;
   p->kmin_blocks = 8;
   p->pe_mode = CRISP_PE_GAMMA;
+  p->route_mode = CRISP_ROUTE_CSTRUCT;
+  p->vs_mode = CRISP_VS_NOISE;
+  p->vs_gamma_num = 95;
+  p->vs_gamma_den = 100;
+  p->jsd_tau = 0.1f;
+  p->dense_below = 0;
 }
 
 crisp_status crisp_workspace_size(const crisp_shape* shape, size_t* bytes) {
@@ -292,6 +303,17 @@ crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* p
   return from_cuda(launch_route(normalised(*shape), *params, vmass, cstruct, total, route, stream));
 }
 
+crisp_status crisp_route_jsd(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
+                             const float* pbar, double* jsd, uint8_t* route, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if ((st = check_params(params)) != CRISP_OK) return st;
+  if (!vmass || !pbar || !route) return CRISP_ERR_INVALID_ARG;
+  if (!aligned(vmass, 8) || !aligned(pbar, 4) || (jsd && !aligned(jsd, 8))) return CRISP_ERR_ALIGN;
+  if ((st = check_device()) != CRISP_OK) return st;
+  return from_cuda(launch_route_jsd(normalised(*shape), *params, vmass, pbar, jsd, route, stream));
+}
+
 crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
                              const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
                              void* ws, size_t ws_bytes, crisp_stream_t stream) {
@@ -414,10 +436,22 @@ crisp_status run_layer(const crisp_shape& s, const crisp_params& p, const void* 
   if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
   if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
   char* wsb = static_cast<char*>(ws);
-  if (launch_proxy_masses(s, maps, w.vmass, w.smass, wsb, stream) != cudaSuccess ||
-      launch_route(s, p, w.vmass, w.cstruct, w.total, w.route, stream) != cudaSuccess ||
-      launch_select_vs(s, p, w.vmass, w.smass, w.route, w.vbits, w.sbits, stream) != cudaSuccess ||
-      launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess ||
+  // Length gate: below it the layer is plain dense attention.
+  if (s.seq_len < p.dense_below)
+    return from_cuda(launch_attention(s, maps, nullptr, nullptr, out, wsb, true, stream));
+  if (launch_proxy_masses(s, maps, w.vmass, w.smass, wsb, stream) != cudaSuccess) return CRISP_ERR_CUDA;
+  if (p.route_mode == CRISP_ROUTE_JSD) {
+    // The comparator needs the pooled estimate of every head before routing
+    // (a zero route array selects all heads), then routes by divergence.
+    if (cudaMemsetAsync(w.route, 0, static_cast<size_t>(s.hq), stream) != cudaSuccess ||
+        launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess ||
+        launch_route_jsd(s, p, w.vmass, w.pbar, nullptr, w.route, stream) != cudaSuccess)
+      return CRISP_ERR_CUDA;
+  } else if (launch_route(s, p, w.vmass, w.cstruct, w.total, w.route, stream) != cudaSuccess ||
+             launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess) {
+    return CRISP_ERR_CUDA;
+  }
+  if (launch_select_vs(s, p, w.vmass, w.smass, w.route, w.vbits, w.sbits, stream) != cudaSuccess ||
       launch_select_pe(s, p, w.pbar, w.route, w.pebits, stream) != cudaSuccess ||
       launch_build_mask(s, w.route, w.vbits, w.sbits, w.pebits, w.rowbits, w.counts, w.order, wsb, stream) !=
           cudaSuccess ||

@@ -86,6 +86,8 @@ cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_
                                 cudaStream_t st);
 cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, uint64_t* cstruct,
                          uint64_t* total, uint8_t* route, cudaStream_t st);
+cudaError_t launch_route_jsd(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const float* pbar,
+                             double* jsd, uint8_t* route, cudaStream_t st);
 cudaError_t launch_select_vs(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass,
                              const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
                              cudaStream_t st);

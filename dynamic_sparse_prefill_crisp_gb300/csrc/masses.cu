@@ -103,12 +103,16 @@ __global__ void route_kernel(const uint64_t* __restrict__ vmass, int nb, uint32_
 }
 
 // A4 for one (head, direction): direction 0 = vertical (always keeps {0,
-// nb-1}), 1 = slash (always keeps {0}); candidates [1, nb-2].
+// nb-1}), 1 = slash (always keeps {0}). Noise floor (CRISP): candidates
+// [1, nb-2] above alpha times their mean. Cumulative coverage (FlexPrefill,
+// the comparator): candidates [0, nb-1], the shortest (mass desc, index asc)
+// prefix reaching gamma of their total. Both then fill to k_min.
 constexpr int kSelThreads = 512;
 __global__ void __launch_bounds__(kSelThreads) select_vs_kernel(const uint64_t* __restrict__ vmass,
                                                                 const uint64_t* __restrict__ smass,
                                                                 const uint8_t* __restrict__ route, int nb,
                                                                 uint32_t alpha_num, uint32_t alpha_den, int kmin,
+                                                                int vs_mode, uint32_t gamma_num, uint32_t gamma_den,
                                                                 uint32_t* __restrict__ vbits,
                                                                 uint32_t* __restrict__ sbits) {
   __shared__ uint32_t chosen[kMaxBlocks / 32];
@@ -124,7 +128,8 @@ __global__ void __launch_bounds__(kSelThreads) select_vs_kernel(const uint64_t* 
     return;
   }
   const uint64_t* m = (dir == 0 ? vmass : smass) + static_cast<size_t>(h) * nb;
-  const int c_lo = 1, c_hi = nb - 2;  // candidates [c_lo, c_hi]
+  const bool coverage = vs_mode == CRISP_VS_GAMMA;
+  const int c_lo = coverage ? 0 : 1, c_hi = coverage ? nb - 1 : nb - 2;  // candidates [c_lo, c_hi]
   const int N = max(0, c_hi - c_lo + 1);
   const int nforced = (dir == 0 && nb >= 2) ? 2 : 1;
   if (threadIdx.x == 0) {
@@ -134,20 +139,33 @@ __global__ void __launch_bounds__(kSelThreads) select_vs_kernel(const uint64_t* 
   uint64_t part = 0;
   for (int c = c_lo + threadIdx.x; c <= c_hi; c += blockDim.x) part += m[c];
   const uint64_t sum = block_sum(part, scratch64);
-  int mine = 0;
-  if (N > 0) {
+  if (coverage) {
+    // Largest key x whose suffix mass reaches gamma of the total: the last
+    // member of the shortest (mass desc, index asc) prefix.
+    const unsigned __int128 goal = static_cast<unsigned __int128>(gamma_num) * sum;
+    uint64_t x = 0;
+    for (int bit = kKeyBits - 1; bit >= 0; --bit) {
+      const uint64_t cand = x | (1ull << bit);
+      uint64_t f = 0;
+      for (int c = c_lo + threadIdx.x; c <= c_hi; c += blockDim.x)
+        if (sel_key(m[c], c) >= cand) f += m[c];
+      if (static_cast<unsigned __int128>(gamma_den) * block_sum(f, scratch64) >= goal) x = cand;
+    }
+    for (int c = c_lo + threadIdx.x; c <= c_hi; c += blockDim.x)
+      if (sel_key(m[c], c) >= x) atomicOr(&chosen[c >> 5], 1u << (c & 31));
+  } else if (N > 0) {
     const unsigned __int128 rhs = static_cast<unsigned __int128>(alpha_num) * sum;
     for (int c = c_lo + threadIdx.x; c <= c_hi; c += blockDim.x) {
       const unsigned __int128 lhs = static_cast<unsigned __int128>(m[c]) * static_cast<unsigned>(N) * alpha_den;
-      if (lhs > rhs) {
-        atomicOr(&chosen[c >> 5], 1u << (c & 31));
-        ++mine;
-      }
+      if (lhs > rhs) atomicOr(&chosen[c >> 5], 1u << (c & 31));
     }
   }
-  const int count = nforced + block_sum(mine, scratch32);
-  const int target = min(kmin, nforced + N);
-  int need = target - count;
+  __syncthreads();
+  int pc = 0;
+  for (int w = threadIdx.x; w < W; w += blockDim.x) pc += __popc(chosen[w]);
+  const int count = block_sum(pc, scratch32);
+  const int target = min(kmin, coverage ? nb : nforced + N);
+  const int need = target - count;
   if (need > 0) {
     // Largest key x with #{unchosen candidates: key >= x} >= need; keys are
     // unique, so exactly `need` candidates reach it: the (mass desc, index
@@ -166,6 +184,34 @@ __global__ void __launch_bounds__(kSelThreads) select_vs_kernel(const uint64_t* 
   }
   __syncthreads();
   for (int w = threadIdx.x; w < W; w += blockDim.x) out[w] = chosen[w];
+}
+
+// FlexPrefill's routing rule (the comparator): Jensen-Shannon divergence
+// between the last query block's block-pooled attention a (from the block
+// masses) and its pooled estimate e (row nb-1 of the pooled map), in fp64.
+__global__ void jsd_route_kernel(const uint64_t* __restrict__ vmass, const float* __restrict__ pbar, int nb,
+                                 float tau, double* __restrict__ jsd, uint8_t* __restrict__ route) {
+  __shared__ uint64_t scratch64[32];
+  __shared__ double scratchd[32];
+  const int h = blockIdx.x;
+  const uint64_t* v = vmass + static_cast<size_t>(h) * nb;
+  const float* e = pbar + (static_cast<size_t>(h) * nb + (nb - 1)) * nb;
+  uint64_t part = 0;
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) part += v[c];
+  const double T = static_cast<double>(block_sum(part, scratch64));
+  double acc = 0.0;
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+    const double a = T > 0.0 ? static_cast<double>(v[c]) / T : 0.0;
+    const double b = static_cast<double>(e[c]);
+    const double mid = 0.5 * (a + b);
+    if (a > 0.0) acc += a * log(a / mid);
+    if (b > 0.0) acc += b * log(b / mid);
+  }
+  const double D = 0.5 * block_sum(acc, scratchd);
+  if (threadIdx.x == 0) {
+    if (jsd) jsd[h] = D;
+    route[h] = sqrt(fmax(D, 0.0)) >= static_cast<double>(tau) ? 1 : 0;
+  }
 }
 
 }  // namespace
@@ -198,7 +244,14 @@ cudaError_t launch_select_vs(const crisp_shape& s, const crisp_params& p, const 
                              const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
                              cudaStream_t st) {
   select_vs_kernel<<<dim3(s.hq, 2), kSelThreads, 0, st>>>(vmass, smass, route, num_blocks(s.seq_len), p.alpha_num,
-                                                          p.alpha_den, p.kmin_blocks, vbits, sbits);
+                                                          p.alpha_den, p.kmin_blocks, p.vs_mode, p.vs_gamma_num,
+                                                          p.vs_gamma_den, vbits, sbits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_jsd(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const float* pbar,
+                             double* jsd, uint8_t* route, cudaStream_t st) {
+  jsd_route_kernel<<<s.hq, 256, 0, st>>>(vmass, pbar, num_blocks(s.seq_len), p.jsd_tau, jsd, route);
   return cudaGetLastError();
 }
 

@@ -76,6 +76,20 @@ typedef enum crisp_pe_mode {
   CRISP_PE_NOISE = 1  /* the noise-floor rule applied to each pooled row */
 } crisp_pe_mode;
 
+/* Head routing: CRISP's structural mass (default) or the Jensen-Shannon
+ * divergence rule of FlexPrefill that CRISP replaces (a comparator). */
+typedef enum crisp_route_mode {
+  CRISP_ROUTE_CSTRUCT = 0,
+  CRISP_ROUTE_JSD = 1
+} crisp_route_mode;
+
+/* Vertical-Slash block selection: CRISP's sink-aware noise floor (default)
+ * or FlexPrefill's cumulative coverage (a comparator). */
+typedef enum crisp_vs_mode {
+  CRISP_VS_NOISE = 0,
+  CRISP_VS_GAMMA = 1
+} crisp_vs_mode;
+
 /* Problem shape. Strides are in elements. scale = 0 selects 1/sqrt(128). */
 typedef struct crisp_shape {
   int32_t hq;       /* query heads */
@@ -91,13 +105,21 @@ typedef struct crisp_shape {
 
 /* Method parameters; crisp_params_default gives the paper's universal
  * configuration: tau_proxy = 1/5, alpha = 1, gamma = 19/20 (PE only),
- * k_min = 8 blocks (1024 tokens) per direction, pe_mode = CRISP_PE_GAMMA. */
+ * k_min = 8 blocks (1024 tokens) per direction, pe_mode = CRISP_PE_GAMMA,
+ * route_mode = CRISP_ROUTE_CSTRUCT, vs_mode = CRISP_VS_NOISE (the comparator
+ * fields default to FlexPrefill's settings as we read them: vs_gamma =
+ * 95/100, jsd_tau = 0.1), dense_below = 0 (no length gate). */
 typedef struct crisp_params {
   uint32_t tau_num, tau_den;     /* 0 <= tau <= 1, tau_den > 0 */
   uint32_t alpha_num, alpha_den; /* alpha_num, alpha_den <= 65535, alpha_den > 0 */
   uint32_t gamma_num, gamma_den; /* 0 <= gamma <= 1, gamma_den > 0 */
   int32_t kmin_blocks;           /* 0 <= kmin_blocks <= 8192 */
   int32_t pe_mode;               /* crisp_pe_mode */
+  int32_t route_mode;            /* crisp_route_mode */
+  int32_t vs_mode;               /* crisp_vs_mode */
+  uint32_t vs_gamma_num, vs_gamma_den; /* coverage of CRISP_VS_GAMMA, 0 <= gamma <= 1 */
+  float jsd_tau;                 /* CRISP_ROUTE_JSD: VS iff sqrt(JSD) >= jsd_tau; 0 <= jsd_tau <= 1 */
+  int32_t dense_below;           /* crisp_prefill_layer*: n < dense_below runs dense attention only */
 } crisp_params;
 
 /* Fills *p (host) with the defaults above. */
@@ -179,6 +201,19 @@ CRISP_API crisp_status crisp_proxy_masses(const crisp_shape* shape, const void* 
 CRISP_API crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
                                  uint64_t* cstruct, uint64_t* total, uint8_t* route, crisp_stream_t stream);
 
+/* A2 comparator: FlexPrefill's routing, which CRISP replaces (ai.info page,
+ * "Methodology in Plain English": a pooled attention estimate compared with
+ * the per-query attention by Jensen-Shannon divergence). For head h, with
+ *   a[c] = vmass[h][c] / sum_c vmass[h][c]   (the last query block's true
+ *          attention pooled into key blocks, from the proxy map),
+ *   e[c] = pbar[h][nb-1][c]                  (the pooled estimate of that block),
+ *   D    = (KL(a || m) + KL(e || m)) / 2,  m = (a + e) / 2, natural log, in fp64,
+ *   route[h] = 1 (Vertical-Slash) iff sqrt(D) >= jsd_tau, else 0.
+ * pbar: fp32 [hq][nb][nb] holding row nb-1 of EVERY head (crisp_pe_map with a
+ * route array of zeros computes it); jsd: double [hq] (D), or NULL. */
+CRISP_API crisp_status crisp_route_jsd(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
+                                       const float* pbar, double* jsd, uint8_t* route, crisp_stream_t stream);
+
 /* A4. Sink-aware noise-floor selection for VS heads (ai.info page,
  * "Methodology in Plain English": keep each block whose mass exceeds alpha
  * times the expected background mass of the blocks that are not always
@@ -186,6 +221,11 @@ CRISP_API crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp
  * always-retained vertical {0, nb-1}, slash {0}; candidates [1, nb-2], N of
  * them, mass sum M; keep c iff m[c]*N*alpha_den > alpha_num*M; then fill to
  * min(kmin, available) by (mass desc, index asc). PE heads get empty rows.
+ * vs_mode = CRISP_VS_GAMMA (FlexPrefill's cumulative coverage, the rule CRISP
+ * replaces): per direction, every block [0, nb-1] is a candidate; keep the
+ * shortest (mass desc, index asc) prefix whose mass reaches vs_gamma of the
+ * direction's total (vs_gamma_den * prefix >= vs_gamma_num * total), add the
+ * always-retained blocks and fill to min(kmin, nb) the same way.
  * vbits, sbits: uint32 [hq][W]. */
 CRISP_API crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
                              const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
@@ -261,7 +301,10 @@ CRISP_API crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws,
 
 /* A1..A8 for one layer: block masses of the proxy map (crisp_proxy_masses;
  * the map itself is never stored), routing, VS and PE selection, mask,
- * sparse attention. ws must hold crisp_layer_workspace_size bytes. */
+ * sparse attention. ws must hold crisp_layer_workspace_size bytes. With
+ * route_mode = CRISP_ROUTE_JSD the pooled map is computed for every head and
+ * routing is crisp_route_jsd. If seq_len < params->dense_below the layer is
+ * dense attention only and the workspace intermediates are not written. */
 CRISP_API crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* params, const void* q, const void* k,
                                  const void* v, void* out, void* ws, size_t ws_bytes, crisp_stream_t stream);
 

@@ -47,6 +47,8 @@ def _load():
         lib.oracle_vs_masses.argtypes = [i, i, vp, vp, vp, i]
         lib.oracle_pe_rows.argtypes = [i, i, i, vp, vp, d, i64, vp, vp, vp, i]
         lib.oracle_select_vs.argtypes = [i, i, vp, vp, vp, u32, u32, i, vp, vp]
+        lib.oracle_select_vs_gamma.argtypes = [i, i, vp, vp, vp, u32, u32, i, vp, vp]
+        lib.oracle_route_jsd.argtypes = [i, i, vp, vp, d, vp, vp]
         lib.oracle_pe_map.argtypes = [i, i, i, vp, vp, d, vp, i]
         lib.oracle_select_pe.argtypes = [i, i, vp, vp, i, u32, u32, u32, u32, i, vp, i]
         lib.oracle_build_mask.argtypes = [i, i, vp, vp, vp, vp, vp]
@@ -148,6 +150,30 @@ def select_vs(vmass, smass, route_, alpha=(1, 1), kmin=8):
     _check(_load().oracle_select_vs(hq, nb, _p(vmass), _p(smass), _p(route_), alpha[0], alpha[1], kmin, _p(vb),
                                     _p(sb)), "select_vs")
     return vb, sb
+
+
+def select_vs_gamma(vmass, smass, route_, gamma=(95, 100), kmin=8):
+    """A4 comparator (FlexPrefill's cumulative coverage): (vbits, sbits)."""
+    vmass = np.ascontiguousarray(vmass, np.uint64)
+    smass = np.ascontiguousarray(smass, np.uint64)
+    route_ = np.ascontiguousarray(route_, np.uint8)
+    hq, nb = vmass.shape
+    W = (nb + 31) // 32
+    vb, sb = np.empty((hq, W), np.uint32), np.empty((hq, W), np.uint32)
+    _check(_load().oracle_select_vs_gamma(hq, nb, _p(vmass), _p(smass), _p(route_), gamma[0], gamma[1], kmin,
+                                          _p(vb), _p(sb)), "select_vs_gamma")
+    return vb, sb
+
+
+def route_jsd(vmass, pbar_last32, tau=0.1):
+    """A2 comparator (FlexPrefill's divergence routing): (jsd D, route) from
+    the block masses [hq][nb] and the pooled map's last rows [hq][nb] (fp32)."""
+    vmass = np.ascontiguousarray(vmass, np.uint64)
+    pl = np.ascontiguousarray(pbar_last32, np.float32)
+    hq, nb = vmass.shape
+    D, r = np.empty(hq, np.float64), np.empty(hq, np.uint8)
+    _check(_load().oracle_route_jsd(hq, nb, _p(vmass), _p(pl), float(tau), _p(D), _p(r)), "route_jsd")
+    return D, r
 
 
 def pe_map(q, k, scale=None, nthreads=None):

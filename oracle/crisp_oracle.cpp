@@ -286,6 +286,89 @@ int oracle_select_vs(int hq, int nb, const uint64_t* vmass, const uint64_t* smas
 }
 
 // ---------------------------------------------------------------------------
+// A4 comparator: FlexPrefill's cumulative coverage on Vertical-Slash heads,
+// the rule CRISP replaces (ai.info, Key Findings: at gamma = 0.95 a large
+// sink mass ends the selection inside the sink, "sink-only collapse").
+// Reading: per direction every block [0, nb-1] is a candidate (the sink block
+// included, which is what lets the sink fill the coverage); keep the shortest
+// prefix in (mass desc, index asc) order whose mass reaches gamma of the
+// direction total (gamma_den * prefix >= gamma_num * total); add the
+// always-retained blocks of A4; fill to min(kmin, nb) in the same order.
+int oracle_select_vs_gamma(int hq, int nb, const uint64_t* vmass, const uint64_t* smass, const uint8_t* route,
+                           uint32_t gamma_num, uint32_t gamma_den, int kmin, uint32_t* vbits, uint32_t* sbits) {
+  if (hq <= 0 || nb < 2 || gamma_den == 0 || gamma_num > gamma_den) return 1;
+  const int W = (nb + 31) / 32;
+  std::vector<int> all;
+  for (int c = 0; c < nb; ++c) all.push_back(c);
+  for (int h = 0; h < hq; ++h) {
+    uint32_t* bits[2] = {vbits + static_cast<int64_t>(h) * W, sbits + static_cast<int64_t>(h) * W};
+    std::fill(bits[0], bits[0] + W, 0u);
+    std::fill(bits[1], bits[1] + W, 0u);
+    if (!route[h]) continue;
+    for (int dir = 0; dir < 2; ++dir) {
+      const uint64_t* src = (dir == 0 ? vmass : smass) + static_cast<int64_t>(h) * nb;
+      std::vector<uint64_t> m(src, src + nb);
+      std::vector<int> order = all;
+      std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        if (m[a] != m[b]) return m[a] > m[b];
+        return a < b;
+      });
+      unsigned __int128 T = 0, cum = 0;
+      for (uint64_t x : m) T += x;
+      std::vector<char> chosen(nb, 0);
+      for (int c : order) {
+        if (static_cast<unsigned __int128>(gamma_den) * cum >= static_cast<unsigned __int128>(gamma_num) * T) break;
+        chosen[c] = 1;
+        cum += m[c];
+      }
+      chosen[0] = 1;
+      if (dir == 0) chosen[nb - 1] = 1;
+      int count = 0;
+      for (char x : chosen) count += x;
+      fill_to(chosen, count, std::min(kmin, nb), all, m);
+      for (int c = 0; c < nb; ++c)
+        if (chosen[c]) set_bit(bits[dir], c);
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// A2 comparator: FlexPrefill's routing, which CRISP replaces (ai.info,
+// Methodology in Plain English: FlexPrefill builds a pooled attention
+// estimate and takes its Jensen-Shannon divergence from the per-query
+// attention to decide whether a head is concentrated). Reading: the true
+// distribution is the last query block's attention pooled into key blocks,
+// a[c] = vmass[c] / sum(vmass) (the A3 masses); the estimate is row nb-1 of
+// the A5 pooled map, e[c]; D = (KL(a||m) + KL(e||m)) / 2 with m = (a+e)/2
+// and natural logarithms (0 log 0 = 0); the head is Vertical-Slash iff
+// sqrt(D) >= tau (the block average misses the head's structure). The
+// threshold value is not on the pages; 0.1 is our default.
+// pbar_last: fp32 [hq][nb] (row nb-1 of each head); jsd: double [hq].
+int oracle_route_jsd(int hq, int nb, const uint64_t* vmass, const float* pbar_last, double tau, double* jsd,
+                     uint8_t* route) {
+  if (hq <= 0 || nb < 1) return 1;
+  for (int h = 0; h < hq; ++h) {
+    const uint64_t* v = vmass + static_cast<int64_t>(h) * nb;
+    const float* e = pbar_last + static_cast<int64_t>(h) * nb;
+    long double T = 0.0L;
+    for (int c = 0; c < nb; ++c) T += static_cast<long double>(v[c]);
+    double kl_a = 0.0, kl_e = 0.0;
+    for (int c = 0; c < nb; ++c) {
+      const double a = static_cast<double>(static_cast<long double>(v[c]) / T);
+      const double b = static_cast<double>(e[c]);
+      const double m = 0.5 * (a + b);
+      if (a > 0.0) kl_a += a * std::log(a / m);
+      if (b > 0.0) kl_e += b * std::log(b / m);
+    }
+    const double D = 0.5 * (kl_a + kl_e);
+    jsd[h] = D;
+    route[h] = std::sqrt(std::max(D, 0.0)) >= tau ? 1 : 0;
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
 // A5. Pooled-Estimation map (the PE route CRISP keeps from FlexPrefill;
 // ai.info, Overview/Methodology). Reading: mean-pool queries and keys over
 // each B-token block, logits scale * Qbar[b] . Kbar[c] for c <= b, softmax

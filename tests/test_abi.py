@@ -48,6 +48,10 @@ def test_params_default_is_the_universal_configuration(L):
     assert (p.alpha_num, p.alpha_den) == (1, 1)
     assert (p.gamma_num, p.gamma_den) == (19, 20)
     assert p.kmin_blocks == 8 and p.pe_mode == crisp.PE_GAMMA
+    # CRISP's own rules by default; the comparators' settings as we read FlexPrefill's
+    assert p.route_mode == crisp.ROUTE_CSTRUCT and p.vs_mode == crisp.VS_NOISE
+    assert (p.vs_gamma_num, p.vs_gamma_den) == (95, 100) and abs(p.jsd_tau - 0.1) < 1e-7
+    assert p.dense_below == 0
 
 
 def test_status_strings(L):
@@ -84,7 +88,9 @@ def test_shape_validation(L, field, value, code):
 
 @pytest.mark.parametrize("field,value", [("tau_den", 0), ("tau_num", 6), ("alpha_den", 0), ("alpha_num", 70000),
                                          ("gamma_num", 21), ("kmin_blocks", -1), ("kmin_blocks", 9000),
-                                         ("pe_mode", 2)])
+                                         ("pe_mode", 2), ("route_mode", 2), ("vs_mode", -1), ("vs_gamma_den", 0),
+                                         ("vs_gamma_num", 101), ("jsd_tau", -0.1), ("jsd_tau", 1.5),
+                                         ("jsd_tau", float("nan")), ("dense_below", -1)])
 def test_params_validation(L, field, value):
     s = crisp.make_shape(8, 4, 1024)
     p = crisp.params_default()

@@ -276,3 +276,110 @@ def test_repeat_calls_are_deterministic():
     for key in ("pmap", "vmass", "smass", "rowbits", "pbar"):
         assert np.array_equal(a[key], b[key]), key
     assert torch.equal(a["out"], b["out"])
+
+
+# --------------------------------------------------------------------------
+# FlexPrefill comparators (divergence routing, cumulative coverage on VS
+# heads) and the length gate.
+
+def run_comparator_steps(q, k, v, params):
+    """A1+A3 fused, the pooled map of every head, divergence routing, then
+    A4..A8 as in the layer; returns numpy copies and the output."""
+    hq, n, _ = q.shape
+    hkv = k.shape[0]
+    nb, W = n // B, (n // B + 31) // 32
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    out = empty((hq, n, 128), torch.bfloat16)
+    s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+    ws = new_workspace(s)
+    vmass, smass = empty((hq, nb), torch.int64), empty((hq, nb), torch.int64)
+    route = torch.zeros((hq,), dtype=torch.uint8, device="cuda")
+    jsd = empty((hq,), torch.float64)
+    vbits, sbits = empty((hq, W), torch.int32), empty((hq, W), torch.int32)
+    pbar = torch.zeros((hq, nb, nb), dtype=torch.float32, device="cuda")
+    pebits, rowbits = empty((hq, nb, W), torch.int32), empty((hq, nb, W), torch.int32)
+    counts, order = empty((hq, nb), torch.int32), empty((hq * nb,), torch.int32)
+    crisp.proxy_masses(s, qd, kd, vmass, smass, ws)
+    crisp.pe_map(s, qd, kd, route, pbar, ws)  # route all zeros: every head's pooled map
+    crisp.route_jsd(s, params, vmass, pbar, jsd, route)
+    crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws)
+    crisp.select_pe(s, params, pbar, route, pebits, ws)
+    crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, ws)
+    crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws)
+    torch.cuda.synchronize()
+    assert_status_ok(ws)
+    u64 = lambda t: t.cpu().numpy().view(np.uint64)
+    u32 = lambda t: t.cpu().numpy().view(np.uint32)
+    return dict(vmass=u64(vmass), smass=u64(smass), route=route.cpu().numpy(), jsd=jsd.cpu().numpy(),
+                vbits=u32(vbits), sbits=u32(sbits), pbar=pbar.cpu().numpy(), pebits=u32(pebits),
+                rowbits=u32(rowbits), out=out)
+
+
+COMPARATOR_CASES = [
+    # name, hq, hkv, n, seed, jsd_tau, vs_gamma
+    ("mixed-2k-t02", 8, 2, 2048, 2, 0.2, (95, 100)),
+    ("gqa4-4k-t01", 4, 1, 4096, 9, 0.1, (95, 100)),
+    ("gqa7-1152-t02", 7, 1, 1152, 6, 0.2, (97, 100)),
+    ("nb33-4224-t03", 4, 2, 4224, 7, 0.3, (9, 10)),
+]
+
+
+@pytest.mark.parametrize("name,hq,hkv,n,seed,tau,vg", COMPARATOR_CASES, ids=[c[0] for c in COMPARATOR_CASES])
+def test_flexprefill_comparators_match_oracle(name, hq, hkv, n, seed, tau, vg):
+    w = synth.small(name, hq, hkv, n, seed)
+    q, k, v = w.generate()
+    params = crisp.params_default(route_mode=crisp.ROUTE_JSD, vs_mode=crisp.VS_GAMMA, jsd_tau=tau, vs_gamma=vg)
+    r = run_comparator_steps(q, k, v, params)
+    nb = n // B
+    # masses as in the CRISP path (the fused pass is checked elsewhere)
+    ref_map = run_steps(q, k, v, crisp.params_default())
+    assert np.array_equal(r["vmass"], ref_map["vmass"]) and np.array_equal(r["smass"], ref_map["smass"])
+    # divergence in fp64 on both sides, from the GPU's own masses and pooled rows
+    D, route = oracle.route_jsd(r["vmass"], r["pbar"][:, nb - 1, :], tau=params.jsd_tau)
+    assert np.allclose(r["jsd"], D, rtol=1e-12, atol=1e-15)
+    near = np.abs(np.sqrt(np.maximum(D, 0)) - params.jsd_tau) < 1e-9  # either decision is correct there
+    assert np.array_equal(r["route"][~near], route[~near])
+    route = r["route"]
+    vb, sb = oracle.select_vs_gamma(r["vmass"], r["smass"], route, gamma=vg, kmin=params.kmin_blocks)
+    assert np.array_equal(vb, r["vbits"]) and np.array_equal(sb, r["sbits"])
+    pbar = r["pbar"].copy()
+    pe = oracle.select_pe(pbar, route, pe_mode=params.pe_mode, gamma=(params.gamma_num, params.gamma_den),
+                          alpha=(params.alpha_num, params.alpha_den), kmin=params.kmin_blocks)
+    assert np.array_equal(pe, r["pebits"])
+    rb = oracle.build_mask(route, vb, sb, pe)
+    assert np.array_equal(rb, r["rowbits"])
+    check_attention(q, k, v, r["out"], rb, rows=sample_rows(hq, n, 24, seed))
+
+
+def test_prefill_layer_comparator_mode_matches_steps():
+    w = synth.small("layer-flex", 8, 2, 2048, 91)
+    q, k, v = w.generate()
+    params = crisp.params_default(route_mode=crisp.ROUTE_JSD, vs_mode=crisp.VS_GAMMA, jsd_tau=0.2)
+    steps = run_comparator_steps(q, k, v, params)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    out = empty((8, 2048, 128), torch.bfloat16)
+    s = crisp.make_shape(8, 2, 2048, qd, kd, out)
+    ws = new_workspace(s, layer=True)
+    crisp.prefill_layer(s, params, qd, kd, vd, out, ws)
+    torch.cuda.synchronize()
+    assert_status_ok(ws)
+    assert torch.equal(out, steps["out"])
+    assert 0 < steps["route"].sum() < 8  # both routes exercised
+
+
+def test_length_gate_runs_dense():
+    n = 4096  # 32 blocks: the sparse selection keeps fewer than all of them
+    w = synth.small("gate", 4, 1, n, 92)
+    q, k, v = w.generate()
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    out, ref = empty((4, n, 128), torch.bfloat16), empty((4, n, 128), torch.bfloat16)
+    s = crisp.make_shape(4, 1, n, qd, kd, out)
+    ws = new_workspace(s, layer=True)
+    crisp.dense_prefill(s, qd, kd, vd, ref, ws)
+    crisp.prefill_layer(s, crisp.params_default(dense_below=n + 1), qd, kd, vd, out, ws)
+    torch.cuda.synchronize()
+    assert_status_ok(ws)
+    assert torch.equal(out, ref)
+    crisp.prefill_layer(s, crisp.params_default(dense_below=n), qd, kd, vd, out, ws)  # not below: sparse
+    torch.cuda.synchronize()
+    assert not torch.equal(out, ref)

@@ -481,3 +481,118 @@ def test_pe_rows_match_torch():
         ref = np.zeros(8)
         ref[: b + 1] = torch.softmax(z, dim=0).numpy()
         assert np.max(np.abs(got[t] - ref)) < 1e-13
+
+
+# --------------------------------------------------------------------------
+# FlexPrefill comparators: divergence routing and cumulative coverage on
+# Vertical-Slash heads (the two rules CRISP replaces).
+
+def _bits(row, nb):
+    return {c for c in range(nb) if (int(row[c >> 5]) >> (c & 31)) & 1}
+
+
+def test_route_jsd_matches_scipy_jensenshannon():
+    scipy_distance = pytest.importorskip("scipy.spatial.distance")
+    rng = np.random.default_rng(81)
+    hq, nb = 6, 40
+    vm = rng.integers(1, 2**36, size=(hq, nb)).astype(np.uint64)
+    vm[1, 5:] = 0  # zero-mass blocks (0 log 0 = 0)
+    e = rng.random((hq, nb)) ** 3
+    e[2, :20] = 0.0
+    e = (e / e.sum(1, keepdims=True)).astype(np.float32)
+    D, _ = oracle.route_jsd(vm, e, tau=0.1)
+    for h in range(hq):
+        a = vm[h].astype(np.float64) / vm[h].astype(np.float64).sum()
+        # scipy renormalises e in double; ours takes the fp32 row as given
+        ref = scipy_distance.jensenshannon(a, e[h].astype(np.float64)) ** 2
+        assert D[h] == pytest.approx(ref, rel=1e-5, abs=1e-12)
+
+
+def test_route_jsd_closed_forms_and_threshold_direction():
+    nb = 4
+    # identical distributions: D = 0 -> the pooled estimate is faithful -> PE
+    vm = np.array([[1, 1, 2, 4]], np.uint64)
+    e = np.array([[0.125, 0.125, 0.25, 0.5]], np.float32)
+    D, r = oracle.route_jsd(vm, e, tau=0.1)
+    assert D[0] == 0.0 and r[0] == 0
+    # disjoint supports: D = ln 2 -> VS for any tau <= sqrt(ln 2)
+    vm = np.array([[5, 0, 0, 0]], np.uint64)
+    e = np.array([[0.0, 0.5, 0.5, 0.0]], np.float32)
+    D, r = oracle.route_jsd(vm, e, tau=0.8)
+    assert D[0] == pytest.approx(np.log(2.0), rel=1e-15) and r[0] == 1
+    # a = (1, 0), e = (1/2, 1/2): m = (3/4, 1/4),
+    # D = [ln(4/3) + (1/2) ln(2/3) + (1/2) ln 2] / 2
+    vm = np.array([[7, 0]], np.uint64)
+    e = np.array([[0.5, 0.5]], np.float32)
+    D, _ = oracle.route_jsd(vm, e, tau=0.1)
+    want = 0.5 * (np.log(4.0 / 3.0) + 0.5 * np.log(2.0 / 3.0) + 0.5 * np.log(2.0))
+    assert D[0] == pytest.approx(want, rel=1e-14)
+    # threshold is inclusive: sqrt(D) == tau routes to VS
+    _, r = oracle.route_jsd(vm, e, tau=float(np.sqrt(want)))
+    assert r[0] == 1
+    _, r = oracle.route_jsd(vm, e, tau=float(np.nextafter(np.sqrt(want), 1.0)))
+    assert r[0] == 0
+    del nb
+
+
+def test_select_vs_gamma_sink_only_collapse():
+    # The pages' failure mode: a sink block holding >= gamma of the vertical
+    # mass ends the coverage inside the sink; only the always-retained blocks
+    # and the k_min fill remain, however strong the other columns are.
+    nb = 64
+    vm = np.full((1, nb), 10, np.uint64)
+    vm[0, 0] = 10**9          # sink block
+    vm[0, [17, 33, 41]] = 10**6  # strong needles, far below the sink
+    sm = np.full((1, nb), 3, np.uint64)
+    vb, _ = oracle.select_vs_gamma(vm, sm, np.array([1], np.uint8), gamma=(95, 100), kmin=0)
+    assert _bits(vb[0], nb) == {0, nb - 1}
+    vb, _ = oracle.select_vs_gamma(vm, sm, np.array([1], np.uint8), gamma=(95, 100), kmin=5)
+    assert _bits(vb[0], nb) == {0, nb - 1, 17, 33, 41}
+    # the noise floor keeps the needles without any k_min help
+    vb, _ = oracle.select_vs(vm, sm, np.array([1], np.uint8), alpha=(1, 1), kmin=0)
+    assert {17, 33, 41} <= _bits(vb[0], nb)
+
+
+def test_select_vs_gamma_one_keeps_all_nonzero_and_zero_keeps_forced():
+    rng = np.random.default_rng(82)
+    nb = 50
+    vm = rng.integers(0, 1000, size=(2, nb)).astype(np.uint64)
+    vm[:, ::7] = 0
+    sm = rng.integers(0, 1000, size=(2, nb)).astype(np.uint64)
+    route = np.array([1, 1], np.uint8)
+    vb, sb = oracle.select_vs_gamma(vm, sm, route, gamma=(1, 1), kmin=0)
+    for h in range(2):
+        assert _bits(vb[h], nb) == set(np.nonzero(vm[h])[0].tolist()) | {0, nb - 1}
+        assert _bits(sb[h], nb) == set(np.nonzero(sm[h])[0].tolist()) | {0}
+    vb, sb = oracle.select_vs_gamma(vm, sm, route, gamma=(0, 1), kmin=0)
+    assert _bits(vb[0], nb) == {0, nb - 1} and _bits(sb[0], nb) == {0}
+
+
+def test_select_vs_gamma_prefix_properties():
+    # Characterisation of the coverage prefix (kmin = 0, forced blocks given
+    # the smallest masses so that they stay outside it): the chosen non-forced
+    # blocks outrank every other block, cover gamma of the total, and stop
+    # covering it once their lowest-ranked member is dropped.
+    rng = np.random.default_rng(83)
+    nb = 96
+    for trial in range(20):
+        g = (int(rng.integers(1, 100)), 100)
+        m = rng.integers(10, 10**6, size=nb).astype(np.uint64)
+        m[rng.integers(0, nb, 5)] = m[rng.integers(0, nb, 5)]  # some ties
+        m[0], m[nb - 1] = 0, 0
+        vb, _ = oracle.select_vs_gamma(m[None], m[None], np.array([1], np.uint8), gamma=g, kmin=0)
+        chosen = _bits(vb[0], nb) - {0, nb - 1}
+        key = lambda c: (int(m[c]), -c)
+        rest = set(range(1, nb - 1)) - chosen
+        assert chosen and all(key(a) > key(b) for a in chosen for b in rest)
+        T = int(m.sum())
+        mass = sum(int(m[c]) for c in chosen)
+        assert g[1] * mass >= g[0] * T
+        last = min(chosen, key=key)
+        assert g[1] * (mass - int(m[last])) < g[0] * T
+
+
+def test_select_vs_gamma_route_pe_gives_empty():
+    vm = np.ones((2, 8), np.uint64)
+    vb, sb = oracle.select_vs_gamma(vm, vm, np.array([0, 1], np.uint8), gamma=(95, 100), kmin=8)
+    assert not vb[0].any() and not sb[0].any() and vb[1].any()
