@@ -79,6 +79,7 @@ def lib():
         L.crisp_prefill_layer_host.argtypes = [vp, P(Shape), P(Params)] + [vp] * 9 + [sz, st]
         L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
         L.crisp_route_jsd.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
+        L.crisp_wait_selftest.argtypes = [vp, sz, ctypes.c_int64, st]
         L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
         L.crisp_pe_map.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
         L.crisp_select_pe.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, sz, st]
@@ -95,7 +96,8 @@ def lib():
                      "crisp_block_masses", "crisp_proxy_masses", "crisp_route_cstruct", "crisp_route_jsd", "crisp_select_vs", "crisp_pe_map",
                      "crisp_select_pe", "crisp_build_mask", "crisp_sparse_prefill", "crisp_dense_prefill",
                      "crisp_layer_views_get", "crisp_prefill_layer", "crisp_read_status",
-                     "crisp_host_pipeline_create", "crisp_host_pipeline_destroy", "crisp_prefill_layer_host"):
+                     "crisp_host_pipeline_create", "crisp_host_pipeline_destroy", "crisp_prefill_layer_host",
+                     "crisp_wait_selftest"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -272,6 +274,11 @@ def prefill_layer_host(pipeline, shape, params, q_host, k_host, v_host, out_host
                                           _ptr(k_host), _ptr(v_host), _ptr(out_host), _ptr(q), _ptr(k), _ptr(v),
                                           _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)),
            "crisp_prefill_layer_host")
+
+
+def wait_selftest(ws, limit_ns, stream=None):
+    """Launches the bounded-wait self-test (a wait that nothing ends)."""
+    _check(lib().crisp_wait_selftest(_ptr(ws), _nbytes(ws), int(limit_ns), _stream(stream)), "crisp_wait_selftest")
 
 
 def read_status(ws, stream=None) -> int:

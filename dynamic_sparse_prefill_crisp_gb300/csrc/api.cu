@@ -6,6 +6,7 @@
 #include <new>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace crisp {
 
@@ -589,6 +590,40 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
   if (cudaEventRecord(p->done, p->out) != cudaSuccess || cudaStreamWaitEvent(cs, p->done, 0) != cudaSuccess)
     return CRISP_ERR_CUDA;
   return CRISP_OK;
+}
+
+}  // extern "C"
+
+namespace crisp {
+namespace {
+
+// One thread waits on an mbarrier that nothing arrives at, through the same
+// bounded wait the pipeline kernels use; the wait must give up and record
+// CRISP_ERR_TIMEOUT in the status word, and the kernel must return.
+__global__ void wait_selftest_kernel(DevStatus* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+    abort = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0, &abort, limit_ns)) report_error(status, CRISP_ERR_TIMEOUT, 0xF01);
+}
+
+}  // namespace
+}  // namespace crisp
+
+extern "C" {
+
+crisp_status crisp_wait_selftest(void* ws, size_t ws_bytes, int64_t limit_ns, crisp_stream_t stream) {
+  if (!ws || ws_bytes < sizeof(DevStatus)) return CRISP_ERR_WORKSPACE;
+  if (limit_ns <= 0 || limit_ns > 10000000000ll) return CRISP_ERR_INVALID_ARG;
+  crisp_status st = check_device();
+  if (st != CRISP_OK) return st;
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<DevStatus*>(ws), static_cast<unsigned long long>(limit_ns));
+  return from_cuda(cudaGetLastError());
 }
 
 crisp_status crisp_read_status(const void* ws, crisp_stream_t stream, crisp_status* status) {

@@ -339,6 +339,14 @@ CRISP_API crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, c
  * (host). Returns CRISP_ERR_CUDA if the stream or the copy failed. */
 CRISP_API crisp_status crisp_read_status(const void* ws, crisp_stream_t stream, crisp_status* status /* host */);
 
+/* Failure-detection self-test: launches one kernel that waits, through the
+ * same bounded mbarrier wait every pipeline kernel uses, on a barrier that
+ * nothing arrives at, for limit_ns (0 < limit_ns <= 10 s). The wait gives up,
+ * the kernel records CRISP_ERR_TIMEOUT in the status word of ws and returns,
+ * and the context stays usable (crisp_read_status then reports the timeout;
+ * crisp_workspace_init clears it). */
+CRISP_API crisp_status crisp_wait_selftest(void* ws, size_t ws_bytes, int64_t limit_ns, crisp_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 CRISP_API const char* crisp_status_string(crisp_status status);
 

@@ -112,6 +112,10 @@ def test_null_and_misaligned_pointers(L):
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), None, vp(16), vp(256), 1 << 30, None) == 1
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(20), vp(256), 1 << 30, None) == 3
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(256), 64, None) == 4
+    # failure-detection self-test: argument errors before any CUDA call
+    assert L.crisp_wait_selftest(None, 1 << 20, 1000000, None) == 4
+    assert L.crisp_wait_selftest(vp(256), 1 << 20, 0, None) == 1
+    assert L.crisp_wait_selftest(vp(256), 1 << 20, 20 * 10**9, None) == 1
     # host-buffer path: argument errors before any CUDA call
     assert L.crisp_host_pipeline_create(None) == 1
     assert L.crisp_host_pipeline_destroy(None) == 0

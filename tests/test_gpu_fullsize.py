@@ -88,6 +88,14 @@ def test_cfg5_512k_llama_shape():
     assert route.all()
 
 
+def test_max_length_one_million_tokens():
+    # The largest supported sequence, 2^20 tokens (8192 blocks; bitset rows
+    # of 256 words), on 4 q / 1 kv heads so that the fp64 checks stay quick.
+    w = synth.small("max-1m", 4, 1, 1 << 20, 77, d_sink=12.0)  # sink strong enough to dominate 1M keys
+    route = _check_layer(w, 77)
+    assert route.tolist() == [1, 0, 1, 0]
+
+
 def test_cfg5_512k_dense_sampled_rows():
     w = synth.WORKLOADS["cfg5"]
     q, k, v = w.generate()
