@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_arrive_expect_tx(&bars.q_full, kTile);
       tma_load_3d(sQ, &tq, &bars.q_full, 0, qb * kB, h);
       tma_load_3d(sQ + kHalf, &tq, &bars.q_full, 64, qb * kB, h);
-      int j = 0;
+      int j = 0, nk = 0, nv = 0;  // blocks started, K and V loads issued
       bool ok = true;
       for (int w = 0; ok && w <= (qb >> 5); ++w) {
         uint32_t bits = row_word(row, is_dense, w, qb);
@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
           }
           mbar_arrive_expect_tx(&bars.k_full, kTile);
+          ++nk;
           tma_load_3d(sK, &tk, &bars.k_full, 0, kb * kB, g);
           tma_load_3d(sK + kHalf, &tk, &bars.k_full, 64, kb * kB, g);
           if (!mbar_wait(&bars.v_empty, par, &bars.abort)) {
@@ -185,11 +186,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
           }
           mbar_arrive_expect_tx(&bars.v_full, kTile);
+          ++nv;
           tma_load_3d(sV, &tv, &bars.v_full, 0, kb * kB, g);
           tma_load_3d(sV + kHalf, &tv, &bars.v_full, 64, kb * kB, g);
           ++j;
         }
       }
+      // Every copy issued has landed before the CTA may exit: on the normal
+      // path the consumers already waited for them; after a timeout they may
+      // not have. Bounded waits that ignore the abort flag.
+      const int never = 0;
+      mbar_wait(&bars.q_full, 0, &never);
+      if (nk > 0) mbar_wait(&bars.k_full, static_cast<uint32_t>(nk - 1) & 1u, &never);
+      if (nv > 0) mbar_wait(&bars.v_full, static_cast<uint32_t>(nv - 1) & 1u, &never);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && count > 0) {

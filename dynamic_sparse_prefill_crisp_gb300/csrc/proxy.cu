@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
       mbar_arrive_expect_tx(&bars.q_full, kTile);
       tma_load_3d(sQ, &tq, &bars.q_full, 0, n - kB, h);
       tma_load_3d(sQ + kHalf, &tq, &bars.q_full, 64, n - kB, h);
+      int issued = 0;  // K tiles whose copies were started
       for (int t = 0; t < T; ++t) {
         const int s = t % kStages;
         const uint32_t use = t / kStages;
@@ -130,9 +131,18 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
           break;
         }
         mbar_arrive_expect_tx(&bars.k_full[s], kTile);
+        ++issued;
         uint8_t* dst = sK + s * kTile;
         tma_load_3d(dst, &tk, &bars.k_full[s], 0, (kb0 + t) * kB, g);
         tma_load_3d(dst + kHalf, &tk, &bars.k_full[s], 64, (kb0 + t) * kB, g);
+      }
+      // Every copy issued has landed before the CTA may exit (after a timeout
+      // the consumers may not have waited for it): the last use of each slot.
+      const int never = 0;
+      mbar_wait(&bars.q_full, 0, &never);
+      for (int s = 0; s < kStages && s < issued; ++s) {
+        const int last_use = (issued - 1 - s) / kStages;  // uses of slot s: t = s, s + kStages, ...
+        mbar_wait(&bars.k_full[s], static_cast<uint32_t>(last_use) & 1u, &never);
       }
     }
   } else if (warp == kMmaWarp) {
