@@ -330,6 +330,11 @@ __global__ void __launch_bounds__(kThreads, 2)
           load_s32(s_addr + cc * 32, diag, half * 64 + cc * 32, r, sv);
           p_exp32(sv, c_log2, -m_ref, pk + cc * 16, bsum);
         }
+        // Both warps have re-read their S before either stores P over it
+        // (half 1's P columns 32..63 are half 0's S columns).
+        tc_fence_before();
+        named_bar_sync(pair_bar, 64);
+        tc_fence_after();
       }
       tmem_st32(p_addr, pk);
       l += bsum;
