@@ -56,6 +56,13 @@ def parse_args(argv=None):
     return ap.parse_args(argv)
 
 
+def workload_config(w, args, world):
+    """The config keys both arms report for a workload."""
+    return {"workload": w.name, "hq": w.hq, "hkv": w.hkv, "seq_len": w.n, "head_dim": 128, "block": B,
+            "alpha": args.alpha, "tau": "1/5", "gamma": "19/20", "kmin_blocks": 8,
+            "parallelism": f"replicas x{world}"}
+
+
 def workload(synth, name):
     """A named workload; cfg4-L0..cfg4-L3 are the layers of the 4-layer stack."""
     if name.startswith("cfg4-L"):
@@ -246,8 +253,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": ms, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "hq": w.hq, "hkv": w.hkv, "seq_len": w.n, "head_dim": 128,
-                       "alpha": args.alpha},
+            "config": {**workload_config(w, args, 1), "host": "fp64 oracle on the host cores"},
             "cpu_baseline": {"value": ms, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": ms, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -466,9 +472,7 @@ def run_crisp(args):
             "metric": METRIC, "value": ms_per_step / world, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, planted sink/slash/needle structure)",
-            "config": {"workload": w.name, "hq": hq, "hkv": hkv, "seq_len": n, "head_dim": 128, "block": B,
-                       "alpha": args.alpha, "tau": "1/5", "gamma": "19/20", "kmin_blocks": 8,
-                       "l2": l2_note, "parallelism": f"replicas x{world}"},
+            "config": {**workload_config(w, args, world), "l2": l2_note},
             "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
             "routes": {"vs": int(routes.sum()), "pe": int((routes == 0).sum())},
             "density": pairs / dense_pairs,
