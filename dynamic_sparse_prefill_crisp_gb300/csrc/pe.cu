@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kPeThreads) select_pe_kernel(const float* __re
   __shared__ uint32_t chosen[kMaxBlocks / 32];
   __shared__ uint64_t scratch64[32];
   __shared__ int scratch32[32];
+  __shared__ unsigned long long hist[256], bcast[2];
   const int b = blockIdx.x, h = blockIdx.y;
   const int W = (nb + 31) / 32;
   uint32_t* out = pebits + (static_cast<size_t>(h) * nb + b) * W;
@@ -160,18 +161,12 @@ __global__ void __launch_bounds__(kPeThreads) select_pe_kernel(const float* __re
     const uint64_t T = block_sum(part, scratch64);
     const unsigned __int128 goal = static_cast<unsigned __int128>(gamma_num) * T;
     // Largest key x whose suffix mass reaches gamma of the row: the last
-    // member of the shortest (mass desc, index asc) prefix.
-    uint64_t x = 0;
-    for (int bit = kKeyBits - 1; bit >= 0; --bit) {
-      const uint64_t cand = x | (1ull << bit);
-      uint64_t f = 0;
-      for (int c = threadIdx.x; c <= b; c += blockDim.x) {
-        const uint64_t m = q32(z[c]);
-        if (sel_key(m, c) >= cand) f += m;
-      }
-      const uint64_t F = block_sum(f, scratch64);
-      if (static_cast<unsigned __int128>(gamma_den) * F >= goal) x = cand;
-    }
+    // member of the shortest (mass desc, index asc) prefix. Pooled quanta
+    // are <= 2^33, so the keys fit in 48 bits.
+    const uint64_t x = radix_max_key(
+        b + 1, [&](int c) { return sel_key(q32(z[c]), c); },
+        [&](int c) { return static_cast<unsigned long long>(q32(z[c])); }, [](int) { return true; },
+        [&](unsigned long long f) { return static_cast<unsigned __int128>(gamma_den) * f >= goal; }, hist, bcast);
     for (int c = threadIdx.x; c <= b; c += blockDim.x)
       if (sel_key(q32(z[c]), c) >= x) atomicOr(&chosen[c >> 5], 1u << (c & 31));
     __syncthreads();
@@ -201,14 +196,11 @@ __global__ void __launch_bounds__(kPeThreads) select_pe_kernel(const float* __re
   const int count = block_sum(pc, scratch32);
   const int need = min(kmin, b + 1) - count;
   if (need > 0) {
-    uint64_t x = 0;
-    for (int bit = kKeyBits - 1; bit >= 0; --bit) {
-      const uint64_t cand = x | (1ull << bit);
-      int cnt = 0;
-      for (int c = threadIdx.x; c <= b; c += blockDim.x)
-        if (!((chosen[c >> 5] >> (c & 31)) & 1u) && sel_key(q32(z[c]), c) >= cand) ++cnt;
-      if (block_sum(cnt, scratch32) >= need) x = cand;
-    }
+    // k_min fill: the `need` unchosen blocks with the largest keys.
+    auto unchosen = [&](int c) { return !((chosen[c >> 5] >> (c & 31)) & 1u); };
+    const uint64_t x = radix_max_key(
+        b + 1, [&](int c) { return sel_key(q32(z[c]), c); }, [](int) { return 1ull; }, unchosen,
+        [&](unsigned long long cnt) { return cnt >= static_cast<unsigned long long>(need); }, hist, bcast);
     __syncthreads();
     for (int c = threadIdx.x; c <= b; c += blockDim.x)
       if (!((chosen[c >> 5] >> (c & 31)) & 1u) && sel_key(q32(z[c]), c) >= x)

@@ -1,4 +1,4 @@
-// Block-wide reductions and the exact top-k threshold search shared by the
+// Block-wide reductions and the exact top-k threshold searches shared by the
 // selection kernels.
 #pragma once
 
@@ -34,6 +34,84 @@ constexpr int kKeyBits = 56;
 __device__ __forceinline__ uint64_t sel_key(uint64_t m, int c) {
   const uint64_t cap = (1ull << 43) - 1;
   return ((m < cap ? m : cap) << 13) | static_cast<uint64_t>(8191 - c);
+}
+
+// The largest 48-bit value x such that reach(W(x)) holds, where W(x) is the
+// weight of the eligible elements c in [0, len) whose key(c) >= x. With
+// unique keys and a reach that grows with W, this x is the key of the last
+// member of the (key descending) prefix that first reaches the goal: the
+// same answer as a bit-by-bit search from the top, found one 8-bit digit
+// per pass (six passes) from a shared-memory histogram of weights. Digit 0,
+// where most small masses fall in the first passes, is summed per warp
+// before its one shared atomic. Keys must be < 2^48; reach(total eligible
+// weight) must hold (then every pass finds a digit). If reach(0) holds the
+// result is 2^48 - 1 (no key reaches it). All threads of the block call it.
+// hist: 256 entries; bcast: 2 entries (shared memory).
+template <typename KeyFn, typename WeightFn, typename EligFn, typename ReachFn>
+__device__ __forceinline__ uint64_t radix_max_key(int len, KeyFn key_of, WeightFn weight_of, EligFn eligible,
+                                                  ReachFn reach, unsigned long long* hist,
+                                                  unsigned long long* bcast) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t prefix = 0;            // digits decided so far
+  unsigned long long above = 0;   // weight of eligible keys above the current bucket
+  for (int shift = 40; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0ull;
+    __syncthreads();
+    unsigned long long w0 = 0;
+    for (int c = threadIdx.x; c < len; c += blockDim.x) {
+      if (!eligible(c)) continue;
+      const uint64_t key = key_of(c);
+      if ((key >> (shift + 8)) != prefix) continue;
+      const int d = static_cast<int>((key >> shift) & 255u);
+      const unsigned long long w = weight_of(c);
+      if (d == 0)
+        w0 += w;
+      else
+        atomicAdd(&hist[d], w);
+    }
+    w0 = warp_sum(w0);
+    if (lane == 0 && w0 != 0ull) atomicAdd(&hist[0], w0);
+    __syncthreads();
+    if (warp == 0) {
+      // Lane l holds bins 255-8l .. 248-8l (descending); cumulative weights
+      // from the top find the largest digit whose suffix reaches the goal.
+      unsigned long long v[8], mine = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        v[k] = hist[255 - 8 * lane - k];
+        mine += v[k];
+      }
+      unsigned long long before = mine;  // inclusive scan over lanes, then exclusive
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, before, o);
+        if (lane >= o) before += t;
+      }
+      before -= mine;
+      unsigned long long run = above + before;
+      int found = -1;
+      unsigned long long run_above = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (found < 0 && reach(run + v[k])) {
+          found = 255 - 8 * lane - k;
+          run_above = run;
+        }
+        run += v[k];
+      }
+      const unsigned int hits = __ballot_sync(0xffffffffu, found >= 0);
+      const int first = hits ? __ffs(hits) - 1 : 31;
+      if (lane == first) {
+        bcast[0] = static_cast<unsigned long long>(found >= 0 ? found : 0);
+        bcast[1] = found >= 0 ? run_above : above;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << 8) | bcast[0];
+    above = bcast[1];
+    __syncthreads();
+  }
+  return prefix;
 }
 
 }  // namespace crisp
