@@ -134,13 +134,16 @@ __global__ void pooled_softmax(const uint8_t* __restrict__ route, int hq, int nb
   for (int c = lane; c <= b; c += 32) z[c] = ptx::ex2_approx(z[c] - mx) * inv;
 }
 
-// A6: one CTA per (head, query block b).
+// A6: one CTA per (head, query block b). The row's selection keys
+// (quantum << 13 | 8191 - c) are formed once into shared memory (nb x 8
+// bytes, dynamic); every search pass then reads them from there.
 constexpr int kPeThreads = 256;
 __global__ void __launch_bounds__(kPeThreads) select_pe_kernel(const float* __restrict__ pbar,
                                                                const uint8_t* __restrict__ route, int nb,
                                                                int pe_mode, uint32_t gamma_num, uint32_t gamma_den,
                                                                uint32_t alpha_num, uint32_t alpha_den, int kmin,
                                                                uint32_t* __restrict__ pebits) {
+  extern __shared__ unsigned long long keys[];  // [b + 1]
   __shared__ uint32_t chosen[kMaxBlocks / 32];
   __shared__ uint64_t scratch64[32];
   __shared__ int scratch32[32];
@@ -154,34 +157,35 @@ __global__ void __launch_bounds__(kPeThreads) select_pe_kernel(const float* __re
     return;
   }
   const float* z = pbar + (static_cast<size_t>(h) * nb + b) * nb;
-  __syncthreads();
+  // Pooled quanta are <= 2^33, so the keys fit in 48 bits and key >> 13 is
+  // the quantum.
+  uint64_t part = 0;
+  for (int c = threadIdx.x; c <= b; c += blockDim.x) {
+    const uint64_t m = q32(z[c]);
+    keys[c] = sel_key(m, c);
+    if (pe_mode == CRISP_PE_GAMMA || (c >= 1 && c <= b - 1)) part += m;
+  }
+  const uint64_t T = block_sum(part, scratch64);  // also orders the key writes before the reads below
+  auto key_of = [&](int c) { return static_cast<uint64_t>(keys[c]); };
   if (pe_mode == CRISP_PE_GAMMA) {
-    uint64_t part = 0;
-    for (int c = threadIdx.x; c <= b; c += blockDim.x) part += q32(z[c]);
-    const uint64_t T = block_sum(part, scratch64);
     const unsigned __int128 goal = static_cast<unsigned __int128>(gamma_num) * T;
     // Largest key x whose suffix mass reaches gamma of the row: the last
-    // member of the shortest (mass desc, index asc) prefix. Pooled quanta
-    // are <= 2^33, so the keys fit in 48 bits.
+    // member of the shortest (mass desc, index asc) prefix.
     const uint64_t x = radix_max_key(
-        b + 1, [&](int c) { return sel_key(q32(z[c]), c); },
-        [&](int c) { return static_cast<unsigned long long>(q32(z[c])); }, [](int) { return true; },
+        b + 1, key_of, [&](int c) { return keys[c] >> 13; }, [](int) { return true; },
         [&](unsigned long long f) { return static_cast<unsigned __int128>(gamma_den) * f >= goal; }, hist, bcast);
     for (int c = threadIdx.x; c <= b; c += blockDim.x)
-      if (sel_key(q32(z[c]), c) >= x) atomicOr(&chosen[c >> 5], 1u << (c & 31));
+      if (keys[c] >= x) atomicOr(&chosen[c >> 5], 1u << (c & 31));
     __syncthreads();
     if (threadIdx.x == 0) {
       chosen[0] |= 1u;
       chosen[b >> 5] |= 1u << (b & 31);
     }
   } else {
-    const int N = max(0, b - 1);  // candidates [1, b-1]
-    uint64_t part = 0;
-    for (int c = 1 + threadIdx.x; c <= b - 1; c += blockDim.x) part += q32(z[c]);
-    const uint64_t sum = block_sum(part, scratch64);
-    const unsigned __int128 rhs = static_cast<unsigned __int128>(alpha_num) * sum;
+    const int N = max(0, b - 1);  // candidates [1, b-1]; T is their mass
+    const unsigned __int128 rhs = static_cast<unsigned __int128>(alpha_num) * T;
     for (int c = 1 + threadIdx.x; c <= b - 1; c += blockDim.x) {
-      const unsigned __int128 lhs = static_cast<unsigned __int128>(q32(z[c])) * static_cast<unsigned>(N) * alpha_den;
+      const unsigned __int128 lhs = static_cast<unsigned __int128>(keys[c] >> 13) * static_cast<unsigned>(N) * alpha_den;
       if (lhs > rhs) atomicOr(&chosen[c >> 5], 1u << (c & 31));
     }
     __syncthreads();
@@ -199,12 +203,11 @@ __global__ void __launch_bounds__(kPeThreads) select_pe_kernel(const float* __re
     // k_min fill: the `need` unchosen blocks with the largest keys.
     auto unchosen = [&](int c) { return !((chosen[c >> 5] >> (c & 31)) & 1u); };
     const uint64_t x = radix_max_key(
-        b + 1, [&](int c) { return sel_key(q32(z[c]), c); }, [](int) { return 1ull; }, unchosen,
+        b + 1, key_of, [](int) { return 1ull; }, unchosen,
         [&](unsigned long long cnt) { return cnt >= static_cast<unsigned long long>(need); }, hist, bcast);
     __syncthreads();
     for (int c = threadIdx.x; c <= b; c += blockDim.x)
-      if (!((chosen[c >> 5] >> (c & 31)) & 1u) && sel_key(q32(z[c]), c) >= x)
-        atomicOr(&chosen[c >> 5], 1u << (c & 31));
+      if (unchosen(c) && keys[c] >= x) atomicOr(&chosen[c >> 5], 1u << (c & 31));
   }
   __syncthreads();
   for (int w = threadIdx.x; w < W; w += blockDim.x) out[w] = chosen[w];
@@ -233,8 +236,13 @@ cudaError_t launch_pe_map(const crisp_shape& s, const void* q, const void* k, co
 cudaError_t launch_select_pe(const crisp_shape& s, const crisp_params& p, const float* pbar, const uint8_t* route,
                              uint32_t* pebits, cudaStream_t st) {
   const int nb = num_blocks(s.seq_len);
-  select_pe_kernel<<<dim3(nb, s.hq), kPeThreads, 0, st>>>(pbar, route, nb, p.pe_mode, p.gamma_num, p.gamma_den,
-                                                          p.alpha_num, p.alpha_den, p.kmin_blocks, pebits);
+  const size_t key_bytes = static_cast<size_t>(nb) * sizeof(unsigned long long);  // <= 64 KB (nb <= 8192)
+  cudaError_t e = cudaFuncSetAttribute(select_pe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(key_bytes));
+  if (e != cudaSuccess) return e;
+  select_pe_kernel<<<dim3(nb, s.hq), kPeThreads, key_bytes, st>>>(pbar, route, nb, p.pe_mode, p.gamma_num,
+                                                                  p.gamma_den, p.alpha_num, p.alpha_den,
+                                                                  p.kmin_blocks, pebits);
   return cudaGetLastError();
 }
 
