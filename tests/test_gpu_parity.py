@@ -412,3 +412,33 @@ def test_attention_is_deterministic_under_load():
     got = r["out"].float().cpu().numpy()[heads, toks]
     mx, mean = attn_error(got, ref)
     assert mx <= ATT_MAX and mean <= ATT_MEAN, (mx, mean)
+
+
+def test_prefill_layer_replays_from_a_cuda_graph():
+    # Every call enqueues on the caller's stream and allocates nothing, so a
+    # whole layer can be captured once and replayed (the short-sequence case
+    # is launch-bound: 13 launches for a 2k-token layer).
+    w = synth.small("graph", 8, 2, 2048, 121)
+    q, k, v = w.generate()
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    out, ref = empty((8, 2048, 128), torch.bfloat16), empty((8, 2048, 128), torch.bfloat16)
+    s = crisp.make_shape(8, 2, 2048, qd, kd, out)
+    params = crisp.params_default()
+    ws = new_workspace(s, layer=True)
+    crisp.prefill_layer(s, params, qd, kd, vd, ref, ws)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up on a side stream before capture
+        crisp.prefill_layer(s, params, qd, kd, vd, out, ws, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        crisp.prefill_layer(s, params, qd, kd, vd, out, ws, stream=torch.cuda.current_stream())
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert_status_ok(ws)
+    assert torch.equal(out, ref)
