@@ -10,6 +10,7 @@
  *   A3 crisp_block_masses    vertical / slash block masses of that map
  *   A1+A3 crisp_proxy_masses the same masses straight from q and k (map not stored)
  *   A2 crisp_route_cstruct   C_struct routing: Vertical-Slash or Pooled-Estimation
+ *      crisp_route_jsd       FlexPrefill's divergence routing (the rule CRISP replaces)
  *   A4 crisp_select_vs       sink-aware noise-floor selection (VS heads)
  *   A5 crisp_pe_map          pooled attention estimate (PE heads)
  *   A6 crisp_select_pe       PE block selection (gamma coverage or noise floor)
@@ -18,6 +19,8 @@
  *   A9 crisp_dense_prefill   the same kernel over every causal block
  *   crisp_prefill_layer      A1..A8 in order, intermediates in the workspace
  *   crisp_prefill_layer_host the same from host buffers, copies overlapped with compute
+ *   crisp_proxy_map_noalloc  A1 without a caller workspace (static scratch)
+ *   crisp_wait_selftest      failure detection: a bounded wait that must time out
  *
  * Conventions (every function):
  *  - Pointers are DEVICE pointers unless marked "host". The caller owns and
