@@ -233,6 +233,24 @@ def cpu_sample(w, q, k, v, params_alpha, nthreads=None):
     }
 
 
+def cpu_full_layer(w, q, k, v, params_alpha):
+    """The whole layer through the fp64 oracle on one core (small layers)."""
+    import oracle
+    nb = w.n // B
+    t0 = time.perf_counter()
+    P = oracle.proxy_map(q, k, nthreads=1).astype(np.float32)
+    vm, sm = oracle.vs_masses(P, nthreads=1)
+    _, _, route = oracle.route(P, nthreads=1)
+    vb, sb = oracle.select_vs(vm, sm, route, alpha=params_alpha)
+    pbar = oracle.pe_map(q, k, nthreads=1).astype(np.float32)
+    pe = oracle.select_pe(pbar, route, nthreads=1)
+    rb = oracle.build_mask(route, vb, sb, pe)
+    hh, tt = np.meshgrid(np.arange(w.hq), np.arange(w.n), indexing="ij")
+    oracle.attention_rows(q, k, v, hh.ravel().astype(np.int32), tt.ravel().astype(np.int32), rowbits=rb, nthreads=1)
+    del nb
+    return (time.perf_counter() - t0) * 1e3
+
+
 def run_reference(args):
     rank, world, _ = dist_info()
     if rank != 0:
@@ -466,6 +484,9 @@ def run_crisp(args):
         r = cpu_sample(w, qh.numpy().view(np.uint16), kh.numpy().view(np.uint16), vh.numpy().view(np.uint16), alpha,
                        nthreads=os.cpu_count())
         cpu = {"value": r["layer_ms"], "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": r["sample"]}
+        if n <= 8192:  # small layers: also the whole layer through the oracle on one core, no sampling
+            cpu["full_layer_1core_ms"] = cpu_full_layer(w, qh.numpy().view(np.uint16), kh.numpy().view(np.uint16),
+                                                        vh.numpy().view(np.uint16), alpha)
 
     if rank == 0:
         line = {
