@@ -556,12 +556,16 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != pipeline->device) return CRISP_ERR_DEVICE;
 
-  // One kv group (its G query heads, its K and V) at a time: the upload of
-  // group g+1 and the download of group g-1 overlap the compute of group g.
+  // The layer in chunks of query heads within a kv group (half of the
+  // group's G heads when G is even, else all of them), the group's K and V
+  // uploaded with its first chunk: the upload of chunk c+1 and the download
+  // of chunk c-1 overlap the compute of chunk c, and the pipeline fills and
+  // drains with one chunk rather than a whole group.
   const int G = s.hq / s.hkv;
+  const int hc = (G % 2 == 0) ? G / 2 : G;  // query heads per chunk
   const size_t plane = static_cast<size_t>(s.seq_len) * kD * 2;  // bytes of one head
   crisp_shape sub = s;
-  sub.hq = G;
+  sub.hq = hc;
   sub.hkv = 1;
   auto* p = pipeline;
   cudaStream_t cs = stream;
@@ -571,19 +575,23 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
   if (cudaEventRecord(p->start, cs) != cudaSuccess || cudaStreamWaitEvent(p->in, p->start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(p->out, p->start, 0) != cudaSuccess)
     return CRISP_ERR_CUDA;
-  for (int g = 0; g < s.hkv; ++g) {
-    const int e = g % crisp_host_pipeline::kRing;
-    const size_t kv_off = static_cast<size_t>(g) * plane, q_off = static_cast<size_t>(g) * G * plane;
-    if (cudaMemcpyAsync(mb(k, kv_off), cb(k_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
-        cudaMemcpyAsync(mb(v, kv_off), cb(v_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
-        cudaMemcpyAsync(mb(q, q_off), cb(q_host, q_off), G * plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+  const int chunks = s.hq / hc;
+  for (int c = 0; c < chunks; ++c) {
+    const int e = c % crisp_host_pipeline::kRing;
+    const int g = (c * hc) / G;  // the chunk's kv group
+    const size_t kv_off = static_cast<size_t>(g) * plane, q_off = static_cast<size_t>(c) * hc * plane;
+    if (c * hc % G == 0 &&
+        (cudaMemcpyAsync(mb(k, kv_off), cb(k_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+         cudaMemcpyAsync(mb(v, kv_off), cb(v_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess))
+      return CRISP_ERR_CUDA;
+    if (cudaMemcpyAsync(mb(q, q_off), cb(q_host, q_off), hc * plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
         cudaEventRecord(p->ev_in[e], p->in) != cudaSuccess || cudaStreamWaitEvent(cs, p->ev_in[e], 0) != cudaSuccess)
       return CRISP_ERR_CUDA;
     if ((st = run_layer(sub, *params, mb(q, q_off), mb(k, kv_off), mb(v, kv_off), mb(out, q_off), ws, cs)) !=
         CRISP_OK)
       return st;
     if (cudaEventRecord(p->ev_comp[e], cs) != cudaSuccess || cudaStreamWaitEvent(p->out, p->ev_comp[e], 0) != cudaSuccess ||
-        cudaMemcpyAsync(mb(out_host, q_off), cb(out, q_off), G * plane, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
+        cudaMemcpyAsync(mb(out_host, q_off), cb(out, q_off), hc * plane, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
       return CRISP_ERR_CUDA;
   }
   // `stream` completes after the last download.

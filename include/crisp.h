@@ -320,10 +320,12 @@ CRISP_API crisp_status crisp_host_pipeline_create(crisp_host_pipeline** pipeline
 CRISP_API crisp_status crisp_host_pipeline_destroy(crisp_host_pipeline* pipeline);
 
 /* crisp_prefill_layer with q, k, v read from host memory and out written to
- * host memory. The layer is processed one kv group at a time (its G query
- * heads, its K and V; every step of the method is per head): the upload of
- * group g+1 and the download of group g-1 run on the pipeline's two streams
- * while group g computes on `stream`, so the copies overlap the compute.
+ * host memory. The layer is processed in chunks of the query heads of one
+ * kv group (half of its G heads when G is even, else all G; every step of
+ * the method is per head), the group's K and V uploaded with its first
+ * chunk: the upload of chunk c+1 and the download of chunk c-1 run on the
+ * pipeline's two streams while chunk c computes on `stream`, so the copies
+ * overlap the compute.
  * Results are bit-identical to crisp_prefill_layer.
  * q_host, k_host, v_host, out_host: host, contiguous [heads][n][128] bf16,
  * page-locked for the copies to be asynchronous. q, k, v, out: device
