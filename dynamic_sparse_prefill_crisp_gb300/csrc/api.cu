@@ -470,6 +470,10 @@ bool contiguous(const crisp_shape& s) {
 }  // namespace
 }  // namespace crisp
 
+// Sequence length from which the host-buffer path uploads half a kv group
+// per chunk (measured: 256k and 512k layers gain 1-4 ms, a 32k layer loses 1).
+constexpr int kHalfGroupChunkLen = 131072;
+
 // Streams and events of the host-buffer path (created by
 // crisp_host_pipeline_create on the current device).
 struct crisp_host_pipeline {
@@ -556,13 +560,14 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != pipeline->device) return CRISP_ERR_DEVICE;
 
-  // The layer in chunks of query heads within a kv group (half of the
-  // group's G heads when G is even, else all of them), the group's K and V
-  // uploaded with its first chunk: the upload of chunk c+1 and the download
-  // of chunk c-1 overlap the compute of chunk c, and the pipeline fills and
-  // drains with one chunk rather than a whole group.
+  // The layer in chunks of query heads within a kv group, the group's K and
+  // V uploaded with its first chunk: the upload of chunk c+1 and the
+  // download of chunk c-1 overlap the compute of chunk c. Long sequences use
+  // half a group per chunk (when G is even), so that the pipeline fills and
+  // drains with half a group; shorter ones a whole group, where the extra
+  // launches and copies would cost more than the shorter fill.
   const int G = s.hq / s.hkv;
-  const int hc = (G % 2 == 0) ? G / 2 : G;  // query heads per chunk
+  const int hc = (G % 2 == 0 && s.seq_len >= kHalfGroupChunkLen) ? G / 2 : G;  // query heads per chunk
   const size_t plane = static_cast<size_t>(s.seq_len) * kD * 2;  // bytes of one head
   crisp_shape sub = s;
   sub.hq = hc;

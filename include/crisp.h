@@ -321,8 +321,8 @@ CRISP_API crisp_status crisp_host_pipeline_destroy(crisp_host_pipeline* pipeline
 
 /* crisp_prefill_layer with q, k, v read from host memory and out written to
  * host memory. The layer is processed in chunks of the query heads of one
- * kv group (half of its G heads when G is even, else all G; every step of
- * the method is per head), the group's K and V uploaded with its first
+ * kv group (half of its G heads when G is even and n >= 131072, else all G;
+ * every step of the method is per head), the group's K and V uploaded with its first
  * chunk: the upload of chunk c+1 and the download of chunk c-1 run on the
  * pipeline's two streams while chunk c computes on `stream`, so the copies
  * overlap the compute.
