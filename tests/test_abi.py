@@ -112,6 +112,13 @@ def test_null_and_misaligned_pointers(L):
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), None, vp(16), vp(256), 1 << 30, None) == 1
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(20), vp(256), 1 << 30, None) == 3
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(256), 64, None) == 4
+    # divergence routing and fused masses: argument errors before any CUDA call
+    pd = ctypes.byref(crisp.params_default())
+    assert L.crisp_route_jsd(ctypes.byref(s), pd, None, vp(256), None, vp(256), None) == 1
+    assert L.crisp_route_jsd(ctypes.byref(s), pd, vp(260), vp(256), None, vp(256), None) == 3
+    assert L.crisp_route_jsd(ctypes.byref(s), pd, vp(256), vp(256), vp(260), vp(256), None) == 3
+    bad = crisp.params_default(route_mode=7)
+    assert L.crisp_route_jsd(ctypes.byref(s), ctypes.byref(bad), vp(256), vp(256), None, vp(256), None) == 1
     # failure-detection self-test: argument errors before any CUDA call
     assert L.crisp_wait_selftest(None, 1 << 20, 1000000, None) == 4
     assert L.crisp_wait_selftest(vp(256), 1 << 20, 0, None) == 1
