@@ -6,7 +6,8 @@
 // One CTA per (head h, query block qb), two CTAs per SM so that one CTA's
 // softmax overlaps the other's matrix products. Per selected key block kb:
 //   S  = Q K_kb^T        tcgen05.mma, A = Q (smem), B = K (smem), D = S (TMEM)
-//   P  = 2^(S*c - m)     softmax warps: TMEM -> registers -> bf16 -> TMEM (over S)
+//   P  = 2^(S*c - m)     softmax warps: TMEM -> registers -> bf16 -> TMEM (each warp
+//                        over its own S columns)
 //   O += P V_kb          tcgen05.mma, A = P (TMEM), B = V (smem, MN-major), D = O (TMEM)
 // K and V tiles arrive by TMA at row coordinate kb*128 (gather by block index).
 // The reference max m is raised lazily: each block is first exponentiated at
@@ -230,10 +231,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          // A = P rows in TMEM (bf16 pairs, 8 columns per 16 keys);
+          // A = P rows in TMEM (bf16 pairs, 8 columns per 16 keys; keys
+          // 0..63 at columns 0..31, keys 64..127 at columns 64..95);
           // B = V, 16 keys x 128 features, MN-major: 16 rows of 128 B per
           // step, the second 64-feature half kHalf bytes further.
-          umma_ts(tmem + 128, tmem + kk * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), idesc_pv,
+          umma_ts(tmem + 128, tmem + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), idesc_pv,
                   (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bars.v_empty);
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int pair_bar = 1 + quarter;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + half * 64;        // 64 S columns
-    const uint32_t p_addr = tmem + lane_addr + half * 32;        // 32 P columns (bf16 pairs)
+    const uint32_t p_addr = tmem + lane_addr + half * 64;        // 32 P columns (bf16 pairs), over own S
     const uint32_t o_addr = tmem + lane_addr + 128 + half * 64;  // 64 O columns
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
@@ -270,9 +272,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       // a row's block sum above 2^8 (or not finite) covers every such case,
       // so that sum is the test and no row max is needed on this path. The
       // two warps of a quarter hold the two column halves of the same rows,
-      // so they agree through shared memory before either stores P (the
-      // barrier also orders both S loads before P overwrites S: half 1's P
-      // columns 32..63 overlap half 0's S columns).
+      // so they agree through shared memory before either stores P. Each
+      // warp stores P only over its own S columns, so neither store can
+      // overwrite scores the other warp has still to read.
       uint32_t pk[32];
       float bsum = 0.f;
       bool need = (j == 0);
@@ -330,11 +332,6 @@ __global__ void __launch_bounds__(kThreads, 2)
           load_s32(s_addr + cc * 32, diag, half * 64 + cc * 32, r, sv);
           p_exp32(sv, c_log2, -m_ref, pk + cc * 16, bsum);
         }
-        // Both warps have re-read their S before either stores P over it
-        // (half 1's P columns 32..63 are half 0's S columns).
-        tc_fence_before();
-        named_bar_sync(pair_bar, 64);
-        tc_fence_after();
       }
       tmem_st32(p_addr, pk);
       l += bsum;
