@@ -74,6 +74,11 @@ def _u16(a):
     return a
 
 
+def num_blocks(n):
+    """Blocks of n tokens: ceil(n / 128) (a short last block when 128 does not divide n)."""
+    return (n + B - 1) // B
+
+
 def default_scale():
     return 1.0 / np.sqrt(D)
 
@@ -107,7 +112,7 @@ def pe_rows(q, k, heads, blocks, scale=None, nthreads=None):
     hq, n, _ = q.shape
     heads = np.ascontiguousarray(heads, np.int32)
     blocks = np.ascontiguousarray(blocks, np.int32)
-    out = np.empty((heads.size, n // B), np.float64)
+    out = np.empty((heads.size, num_blocks(n)), np.float64)
     _check(_load().oracle_pe_rows(hq, k.shape[0], n, _p(q), _p(k), scale or default_scale(), heads.size,
                                   _p(heads), _p(blocks), _p(out), _nt(nthreads)), "pe_rows")
     return out
@@ -133,7 +138,7 @@ def vs_masses(pmap32, nthreads=None):
     """A3: (vmass, smass) uint64 [hq][nb] from an fp32 map."""
     pmap32 = np.ascontiguousarray(pmap32, dtype=np.float32)
     hq, _, n = pmap32.shape
-    nb = n // B
+    nb = num_blocks(n)
     vm, sm = np.empty((hq, nb), np.uint64), np.empty((hq, nb), np.uint64)
     _check(_load().oracle_vs_masses(hq, n, _p(pmap32), _p(vm), _p(sm), _nt(nthreads)), "vs_masses")
     return vm, sm
@@ -180,7 +185,7 @@ def pe_map(q, k, scale=None, nthreads=None):
     """A5: fp64 pooled map [hq][nb][nb]."""
     q, k = _u16(q), _u16(k)
     hq, n, _ = q.shape
-    nb = n // B
+    nb = num_blocks(n)
     out = np.empty((hq, nb, nb), np.float64)
     _check(_load().oracle_pe_map(hq, k.shape[0], n, _p(q), _p(k), scale or default_scale(), _p(out),
                                  _nt(nthreads)), "pe_map")
@@ -227,10 +232,13 @@ def attention_rows(q, k, v, heads, tokens, rowbits=None, scale=None, nthreads=No
     return out
 
 
-def selected_pairs(rowbits):
+def selected_pairs(rowbits, n):
+    """Causal (row, key) pairs over the selected blocks of an n-token layer."""
     rowbits = np.ascontiguousarray(rowbits, np.uint32)
     hq, nb, _ = rowbits.shape
-    return int(_load().oracle_selected_pairs(hq, nb, _p(rowbits)))
+    if nb != num_blocks(n):
+        raise ValueError("selected_pairs: rowbits has the wrong block count for n")
+    return int(_load().oracle_selected_pairs(hq, n, _p(rowbits)))
 
 
 def bits_to_sets(bits, nb):

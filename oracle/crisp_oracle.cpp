@@ -11,8 +11,10 @@
 // used.
 //
 // Notation: Hq query heads, Hkv kv heads, G = Hq/Hkv, d = 128, B = 128,
-// n tokens, nb = n/B blocks, W = ceil(nb/32) bitset words. Query row r of the
-// last block is token i = n - B + r. All bf16 inputs are widened exactly to
+// n tokens, nb = ceil(n/B) blocks (block b holds tokens [bB, min(n, bB+B));
+// only the last can be short), W = ceil(nb/32) bitset words. Query row r of
+// the proxy block is token i = n - B + r: the last B tokens, which straddle
+// two blocks when B does not divide n. All bf16 inputs are widened exactly to
 // double. Bitsets: bit c of a row is word[c >> 5] >> (c & 31) & 1.
 //
 // Parity status: every function below is pinned by tests/test_oracle_*.py
@@ -30,6 +32,10 @@ namespace {
 
 constexpr int kB = 128;  // block size, "block size B=128" (ai.info, Methodology)
 constexpr int kD = 128;  // head dimension of the evaluated models
+
+int num_blocks(int n) { return (n + kB - 1) / kB; }
+// Tokens of block b: B, except a short last block.
+int block_len(int n, int b) { return std::min(kB, n - b * kB); }
 
 double bf16_to_double(uint16_t b) {
   uint32_t u = static_cast<uint32_t>(b) << 16;
@@ -141,7 +147,7 @@ extern "C" {
 // q: bf16 [hq][n][128], k: bf16 [hkv][n][128]; out: double [hq][128][n].
 int oracle_proxy_map(int hq, int hkv, int n, const uint16_t* q, const uint16_t* k, double scale, double* out,
                      int nthreads) {
-  if (hq <= 0 || hkv <= 0 || hq % hkv || n < kB || n % kB) return 1;
+  if (hq <= 0 || hkv <= 0 || hq % hkv || n < kB) return 1;
   const int G = hq / hkv;
   parallel_for(static_cast<int64_t>(hq) * kB, nthreads, [&](int64_t t) {
     const int h = static_cast<int>(t / kB), r = static_cast<int>(t % kB);
@@ -169,7 +175,7 @@ int oracle_proxy_map(int hq, int hkv, int n, const uint16_t* q, const uint16_t* 
 // out: double [count][n].
 int oracle_proxy_rows(int hq, int hkv, int n, const uint16_t* q, const uint16_t* k, double scale, int64_t count,
                       const int32_t* heads, const int32_t* rows, double* out, int nthreads) {
-  if (hq <= 0 || hkv <= 0 || hq % hkv || n < kB || n % kB) return 1;
+  if (hq <= 0 || hkv <= 0 || hq % hkv || n < kB) return 1;
   for (int64_t t = 0; t < count; ++t)
     if (heads[t] < 0 || heads[t] >= hq || rows[t] < 0 || rows[t] >= kB) return 2;
   const int G = hq / hkv;
@@ -206,7 +212,7 @@ void oracle_quantize(const float* p, int64_t count, uint64_t* out) {
 // pmap: fp32 [hq][128][n] (the map under test); route[h] = 1 for VS, 0 for PE.
 int oracle_route(int hq, int n, const float* pmap, uint32_t tau_num, uint32_t tau_den, uint64_t* cstruct,
                  uint64_t* total, uint8_t* route, int nthreads) {
-  if (hq <= 0 || n < 2 * kB || n % kB || tau_den == 0) return 1;
+  if (hq <= 0 || n < 2 * kB || tau_den == 0) return 1;
   parallel_for(hq, nthreads, [&](int64_t hh) {
     const int h = static_cast<int>(hh);
     uint64_t S = 0, T = 0;
@@ -234,8 +240,8 @@ int oracle_route(int hq, int n, const float* pmap, uint32_t tau_num, uint32_t ta
 // the slash direction (the "sink-aware" part: a sink cannot raise the
 // diagonal noise floor). Written element by element, independent of any tiling.
 int oracle_vs_masses(int hq, int n, const float* pmap, uint64_t* vmass, uint64_t* smass, int nthreads) {
-  if (hq <= 0 || n < 2 * kB || n % kB) return 1;
-  const int nb = n / kB;
+  if (hq <= 0 || n < 2 * kB) return 1;
+  const int nb = num_blocks(n);
   parallel_for(hq, nthreads, [&](int64_t hh) {
     const int h = static_cast<int>(hh);
     uint64_t* v = vmass + static_cast<int64_t>(h) * nb;
@@ -371,27 +377,30 @@ int oracle_route_jsd(int hq, int nb, const uint64_t* vmass, const float* pbar_la
 // ---------------------------------------------------------------------------
 // A5. Pooled-Estimation map (the PE route CRISP keeps from FlexPrefill;
 // ai.info, Overview/Methodology). Reading: mean-pool queries and keys over
-// each B-token block, logits scale * Qbar[b] . Kbar[c] for c <= b, softmax
-// over c in [0, b] per row; entries c > b are 0.
+// each block (a short last block over its own tokens), logits
+// scale * Qbar[b] . Kbar[c] for c <= b, softmax over c in [0, b] per row;
+// entries c > b are 0.
 // out: double [hq][nb][nb].
 int oracle_pe_map(int hq, int hkv, int n, const uint16_t* q, const uint16_t* k, double scale, double* out,
                   int nthreads) {
-  if (hq <= 0 || hkv <= 0 || hq % hkv || n < kB || n % kB) return 1;
-  const int G = hq / hkv, nb = n / kB;
+  if (hq <= 0 || hkv <= 0 || hq % hkv || n < 1) return 1;
+  const int G = hq / hkv, nb = num_blocks(n);
   std::vector<double> qbar(static_cast<size_t>(hq) * nb * kD, 0.0), kbar(static_cast<size_t>(hkv) * nb * kD, 0.0);
   parallel_for(static_cast<int64_t>(hq) * nb, nthreads, [&](int64_t t) {
     double* dst = &qbar[t * kD];
     const int64_t h = t / nb, b = t % nb;
-    for (int r = 0; r < kB; ++r)
+    const int len = block_len(n, static_cast<int>(b));
+    for (int r = 0; r < len; ++r)
       for (int c = 0; c < kD; ++c) dst[c] += bf16_to_double(q[((h * n) + b * kB + r) * kD + c]);
-    for (int c = 0; c < kD; ++c) dst[c] /= kB;
+    for (int c = 0; c < kD; ++c) dst[c] /= len;
   });
   parallel_for(static_cast<int64_t>(hkv) * nb, nthreads, [&](int64_t t) {
     double* dst = &kbar[t * kD];
     const int64_t g = t / nb, b = t % nb;
-    for (int r = 0; r < kB; ++r)
+    const int len = block_len(n, static_cast<int>(b));
+    for (int r = 0; r < len; ++r)
       for (int c = 0; c < kD; ++c) dst[c] += bf16_to_double(k[((g * n) + b * kB + r) * kD + c]);
-    for (int c = 0; c < kD; ++c) dst[c] /= kB;
+    for (int c = 0; c < kD; ++c) dst[c] /= len;
   });
   parallel_for(static_cast<int64_t>(hq) * nb, nthreads, [&](int64_t t) {
     const int64_t h = t / nb, b = t % nb, g = h / G;
@@ -412,8 +421,8 @@ int oracle_pe_map(int hq, int hkv, int n, const uint16_t* q, const uint16_t* k, 
 // requested (head, b). out: double [count][nb].
 int oracle_pe_rows(int hq, int hkv, int n, const uint16_t* q, const uint16_t* k, double scale, int64_t count,
                    const int32_t* heads, const int32_t* blocks, double* out, int nthreads) {
-  if (hq <= 0 || hkv <= 0 || hq % hkv || n < kB || n % kB) return 1;
-  const int G = hq / hkv, nb = n / kB;
+  if (hq <= 0 || hkv <= 0 || hq % hkv || n < 1) return 1;
+  const int G = hq / hkv, nb = num_blocks(n);
   for (int64_t t = 0; t < count; ++t)
     if (heads[t] < 0 || heads[t] >= hq || blocks[t] < 0 || blocks[t] >= nb) return 2;
   // Mean-pooled keys of every block of every kv head (needed by any row).
@@ -421,16 +430,18 @@ int oracle_pe_rows(int hq, int hkv, int n, const uint16_t* q, const uint16_t* k,
   parallel_for(static_cast<int64_t>(hkv) * nb, nthreads, [&](int64_t t) {
     double* dst = &kbar[t * kD];
     const int64_t g = t / nb, c = t % nb;
-    for (int r = 0; r < kB; ++r)
+    const int len = block_len(n, static_cast<int>(c));
+    for (int r = 0; r < len; ++r)
       for (int e = 0; e < kD; ++e) dst[e] += bf16_to_double(k[((g * n) + c * kB + r) * kD + e]);
-    for (int e = 0; e < kD; ++e) dst[e] /= kB;
+    for (int e = 0; e < kD; ++e) dst[e] /= len;
   });
   parallel_for(count, nthreads, [&](int64_t t) {
     const int64_t h = heads[t], b = blocks[t], g = h / G;
     double qbar[kD] = {};
-    for (int r = 0; r < kB; ++r)
+    const int len = block_len(n, static_cast<int>(b));
+    for (int r = 0; r < len; ++r)
       for (int e = 0; e < kD; ++e) qbar[e] += bf16_to_double(q[((h * n) + b * kB + r) * kD + e]);
-    for (int e = 0; e < kD; ++e) qbar[e] /= kB;
+    for (int e = 0; e < kD; ++e) qbar[e] /= len;
     std::vector<double> s(b + 1);
     for (int64_t c = 0; c <= b; ++c) {
       double acc = 0.0;
@@ -547,8 +558,8 @@ int oracle_build_mask(int hq, int nb, const uint8_t* route, const uint32_t* vbit
 int oracle_attention_rows(int hq, int hkv, int n, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                           double scale, const uint32_t* rowbits, int64_t count, const int32_t* heads,
                           const int32_t* tokens, double* out, int nthreads) {
-  if (hq <= 0 || hkv <= 0 || hq % hkv || n < kB || n % kB) return 1;
-  const int G = hq / hkv, nb = n / kB, W = (nb + 31) / 32;
+  if (hq <= 0 || hkv <= 0 || hq % hkv || n < 1) return 1;
+  const int G = hq / hkv, nb = num_blocks(n), W = (nb + 31) / 32;
   for (int64_t t = 0; t < count; ++t)
     if (heads[t] < 0 || heads[t] >= hq || tokens[t] < 0 || tokens[t] >= n) return 2;
   parallel_for(count, nthreads, [&](int64_t t) {
@@ -579,15 +590,17 @@ int oracle_attention_rows(int hq, int hkv, int n, const uint16_t* q, const uint1
 }
 
 // Number of (row, key) pairs the attention over `rowbits` visits, i.e. the
-// causal pairs of every selected block: B*B off the diagonal, B(B+1)/2 on it.
-int64_t oracle_selected_pairs(int hq, int nb, const uint32_t* rowbits) {
-  const int W = (nb + 31) / 32;
+// causal pairs of every selected block of n tokens: len(qb)*len(kb) off the
+// diagonal, len(qb)(len(qb)+1)/2 on it (len = B except a short last block).
+int64_t oracle_selected_pairs(int hq, int n, const uint32_t* rowbits) {
+  const int nb = num_blocks(n), W = (nb + 31) / 32;
   int64_t pairs = 0;
   for (int h = 0; h < hq; ++h)
     for (int qb = 0; qb < nb; ++qb) {
       const uint32_t* rb = rowbits + (static_cast<int64_t>(h) * nb + qb) * W;
+      const int64_t lq = block_len(n, qb);
       for (int kb = 0; kb <= qb; ++kb)
-        if (bit(rb, kb)) pairs += kb == qb ? static_cast<int64_t>(kB) * (kB + 1) / 2 : static_cast<int64_t>(kB) * kB;
+        if (bit(rb, kb)) pairs += kb == qb ? lq * (lq + 1) / 2 : lq * block_len(n, kb);
     }
   return pairs;
 }

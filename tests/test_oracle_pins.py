@@ -442,7 +442,7 @@ def test_select_all_equals_dense_and_pair_count():
     a = oracle.attention_rows(q, k, v, h, t, rowbits=rb)
     d = oracle.attention_rows(q, k, v, h, t)
     assert np.array_equal(a, d)
-    assert oracle.selected_pairs(rb) == hq * n * (n + 1) // 2
+    assert oracle.selected_pairs(rb, n) == hq * n * (n + 1) // 2
 
 
 def test_empty_row_mask_gives_zero_output():
@@ -450,6 +450,110 @@ def test_empty_row_mask_gives_zero_output():
     rb = np.zeros((1, 2, 1), np.uint32)
     out = oracle.attention_rows(q, k, v, np.zeros(3, np.int32), np.array([0, 130, 255], np.int32), rowbits=rb)
     assert np.all(out == 0.0)
+
+
+# ----------------------------------------------------------------- ragged lengths
+# n need not be a multiple of 128: blocks stay aligned at token 0 and only the
+# last block is short; the proxy rows are the last 128 tokens (straddling two
+# blocks); sink and recency are the token ranges [0, 128) and [n-128, n).
+RAGGED = [257, 300, 383, 700]
+
+
+@pytest.mark.parametrize("n", RAGGED)
+def test_ragged_proxy_matches_torch_softmax(n):
+    q, k, _ = rand_qkv(2, 1, n, 40 + n)
+    P = oracle.proxy_map(q, k)
+    Q = bits_to_f64(q)[:, -B:, :]
+    K = bits_to_f64(k).repeat_interleave(2, dim=0)
+    S = torch.einsum("hrd,hjd->hrj", Q, K) / np.sqrt(128.0)
+    i = torch.arange(n - B, n)[:, None]
+    S = S.masked_fill(torch.arange(n)[None, :] > i, float("-inf"))
+    assert np.max(np.abs(torch.softmax(S, dim=-1).numpy() - P)) < 1e-13
+    assert np.allclose(P.sum(-1), 1.0, atol=1e-12)
+
+
+@pytest.mark.parametrize("n", RAGGED)
+def test_ragged_cstruct_and_mass_invariants(n):
+    w = synth.small("ragged", 2, 1, n, 50 + n)
+    q, k, _ = w.generate()
+    P = oracle.proxy_map(q, k).astype(np.float32)
+    S, T, _ = oracle.route(P)
+    Qm = np.rint(P.astype(np.float64) * 2.0 ** 32).astype(np.uint64)
+    assert S.tolist() == (Qm[:, :, :128].sum(axis=(1, 2)) + Qm[:, :, n - 128:].sum(axis=(1, 2))).tolist()
+    vm, sm = oracle.vs_masses(P)
+    nb = -(-n // B)
+    assert vm.shape == (2, nb)
+    # vertical masses: plain column sums over each block's own columns
+    for c in range(nb):
+        assert vm[:, c].tolist() == Qm[:, :, c * B:min(n, c * B + B)].sum(axis=(1, 2)).tolist()
+    assert vm.sum(axis=1).tolist() == T.tolist()
+    assert sm.sum(axis=1).tolist() == (T - vm[:, 0]).tolist()
+    assert np.all(sm[:, -1] == 0)
+
+
+@pytest.mark.parametrize("n,r,j", [(300, 0, 172), (300, 1, 44), (300, 127, 299), (300, 50, 128),
+                                   (700, 3, 575), (700, 127, 130), (700, 0, 200), (383, 127, 382)])
+def test_ragged_vs_masses_single_entry_closed_form(n, r, j):
+    i = n - B + r
+    assert j <= i
+    nb = -(-n // B)
+    P = np.zeros((1, B, n), np.float32)
+    P[0, r, j] = 1.0
+    vm, sm = oracle.vs_masses(P)
+    want_v = np.zeros(nb, np.uint64)
+    want_v[j // B] = 2 ** 32
+    want_s = np.zeros(nb, np.uint64)
+    if j >= 128:
+        want_s[(i - j) // B] = 2 ** 32
+    assert vm[0].tolist() == want_v.tolist()
+    assert sm[0].tolist() == want_s.tolist()
+
+
+@pytest.mark.parametrize("n", [300, 700])
+def test_ragged_pe_map_uses_block_means_over_own_tokens(n):
+    # Independent statement: numpy block means over each block's tokens (the
+    # short last block over its t tokens), torch softmax over c <= b.
+    hq, hkv = 2, 1
+    q, k, _ = rand_qkv(hq, hkv, n, 60 + n)
+    got = oracle.pe_map(q, k)
+    nb = -(-n // B)
+    Q, K = bits_to_f64(q).numpy(), bits_to_f64(k).numpy()
+    qb = np.stack([Q[:, b * B:min(n, b * B + B)].mean(axis=1) for b in range(nb)], axis=1)
+    kb = np.stack([K[:, b * B:min(n, b * B + B)].mean(axis=1) for b in range(nb)], axis=1)
+    Z = torch.from_numpy(np.einsum("hbd,hcd->hbc", qb, np.repeat(kb, hq // hkv, axis=0)) / np.sqrt(128.0))
+    Z = Z.masked_fill(torch.arange(nb)[None, :] > torch.arange(nb)[:, None], float("-inf"))
+    assert np.max(np.abs(torch.softmax(Z, dim=-1).numpy() - got)) < 1e-13
+    # a short last block scaled to 128 tokens would differ: the means are not diluted
+    t = n - (nb - 1) * B
+    assert t < B and np.allclose(kb[:, -1], K[:, (nb - 1) * B:].sum(axis=1) / t)
+
+
+@pytest.mark.parametrize("n", [130, 300, 383])
+def test_ragged_dense_attention_matches_sdpa(n):
+    hq, hkv = 2, 1
+    q, k, v = rand_qkv(hq, hkv, n, 70 + n)
+    h, t = _all_tokens(hq, n)
+    got = oracle.attention_rows(q, k, v, h, t).reshape(hq, n, 128)
+    Q, K, V = bits_to_f64(q), bits_to_f64(k), bits_to_f64(v)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        Q[None], K.repeat_interleave(2, 0)[None], V.repeat_interleave(2, 0)[None], is_causal=True)[0].numpy()
+    assert np.max(np.abs(ref - got)) < 1e-12
+
+
+def test_ragged_selected_pairs_closed_form():
+    # Every block of every row: n(n+1)/2 causal pairs per head; one row of
+    # just the short diagonal block: t(t+1)/2.
+    n, hq = 300, 2
+    nb = 3
+    rb = np.zeros((hq, nb, 1), np.uint32)
+    for qb in range(nb):
+        rb[:, qb, 0] = (1 << (qb + 1)) - 1
+    assert oracle.selected_pairs(rb, n) == hq * n * (n + 1) // 2
+    rb[:] = 0
+    rb[0, 2, 0] = 1 << 2
+    assert oracle.selected_pairs(rb, n) == 44 * 45 // 2
+    rb[0, 2, 0] = 1 << 0
+    assert oracle.selected_pairs(rb, n) == 44 * 128
 
 
 # ----------------------------------------------------------------- row samplers
