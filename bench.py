@@ -153,14 +153,20 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- accounting
-def selected_pairs(rowbits: np.ndarray, nb: int) -> int:
-    """(row, key) pairs of the selected blocks: B*B off the diagonal block,
-    B(B+1)/2 on it (the causal half)."""
-    hq = rowbits.shape[0]
+def num_blocks(n: int) -> int:
+    """128-token blocks of an n-token layer (the last one short when 128 does not divide n)."""
+    return (n + B - 1) // B
+
+
+def selected_pairs(rowbits: np.ndarray, n: int) -> int:
+    """(row, key) pairs of the selected blocks of an n-token layer:
+    len(qb)*len(kb) below the diagonal block, len(qb)(len(qb)+1)/2 on it (the
+    causal half); len = B except a short last block."""
+    nb = num_blocks(n)
     bits = np.unpackbits(rowbits.view(np.uint8), axis=-1, bitorder="little")[..., :nb]  # [hq][nb][nb]
-    total = int(bits.sum())
-    diag = int(bits[:, np.arange(nb), np.arange(nb)].sum())
-    return (total - diag) * B * B + diag * B * (B + 1) // 2
+    ln = np.minimum(B, n - B * np.arange(nb)).astype(np.int64)
+    wgt = np.tril(np.outer(ln, ln), -1) + np.diag(ln * (ln + 1) // 2)
+    return int((bits.sum(axis=0).astype(np.int64) * wgt).sum())
 
 
 def profiled_traffic(kernel_src: str, profile: str):
@@ -198,7 +204,7 @@ def cpu_sample(w, q, k, v, params_alpha, nthreads=None):
     import oracle
     G = w.hq // w.hkv
     heads = list(range(G))
-    nb = w.n // B
+    nb = num_blocks(w.n)
     t0 = time.perf_counter()
     P = oracle.proxy_map(q[heads], k[:1], nthreads=nthreads).astype(np.float32)
     vm, sm = oracle.vs_masses(P)
@@ -221,7 +227,7 @@ def cpu_sample(w, q, k, v, params_alpha, nthreads=None):
     # Pairs visited by the sampled rows vs by every row of the sampled heads.
     counts = np.unpackbits(rb.view(np.uint8), axis=-1, bitorder="little")[..., :nb]
     sampled_keys = sum(int(counts[h, t // B, : t // B].sum()) * B + (t % B + 1) for h, t in zip(hh, tt))
-    all_pairs = selected_pairs(rb, nb)
+    all_pairs = selected_pairs(rb, w.n)
     layer_s = (t_select + t_attn * all_pairs / max(sampled_keys, 1)) * (w.hq / len(heads))
     return {
         "layer_ms": layer_s * 1e3,
@@ -236,7 +242,7 @@ def cpu_sample(w, q, k, v, params_alpha, nthreads=None):
 def cpu_full_layer(w, q, k, v, params_alpha):
     """The whole layer through the fp64 oracle on one core (small layers)."""
     import oracle
-    nb = w.n // B
+    nb = num_blocks(w.n)
     t0 = time.perf_counter()
     P = oracle.proxy_map(q, k, nthreads=1).astype(np.float32)
     vm, sm = oracle.vs_masses(P, nthreads=1)
@@ -295,7 +301,8 @@ def run_crisp(args):
     w = workload(synth, args.config)
     alpha = tuple(int(x) for x in args.alpha.split("/"))
     hq, hkv, n = w.hq, w.hkv, w.n
-    nb, W = n // B, (n // B + 31) // 32
+    nb = num_blocks(n)
+    W = (nb + 31) // 32
 
     # Inputs: generated on the host into pinned buffers (also the e2e source).
     qh = torch.empty((hq, n, 128), dtype=torch.int16, pin_memory=True)
@@ -313,8 +320,8 @@ def run_crisp(args):
     ws = torch.empty(crisp.workspace_size(s), dtype=torch.uint8, device=dev)
     crisp.workspace_init(ws)
     E = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
-    pmap = E((hq, B, n), torch.float32)
-    vmass, smass = E((hq, nb), torch.int64), E((hq, nb), torch.int64)
+    pmap = E((hq, B, crisp.map_ld(n)), torch.float32)
+    vmass, smass, rmass = E((hq, nb), torch.int64), E((hq, nb), torch.int64), E((hq,), torch.int64)
     cstruct, total, route = E((hq,), torch.int64), E((hq,), torch.int64), E((hq,), torch.uint8)
     vbits, sbits = E((hq, W), torch.int32), E((hq, W), torch.int32)
     pbar = E((hq, nb, nb), torch.float32)
@@ -324,8 +331,8 @@ def run_crisp(args):
 
     stages = ["proxy_masses", "route", "select_vs", "pe_map", "select_pe", "mask", "attention"]
     calls = [
-        lambda: crisp.proxy_masses(s, qd, kd, vmass, smass, ws, stream),
-        lambda: crisp.route_cstruct(s, params, vmass, cstruct, total, route, stream),
+        lambda: crisp.proxy_masses(s, qd, kd, vmass, smass, rmass, ws, stream),
+        lambda: crisp.route_cstruct(s, params, vmass, rmass, cstruct, total, route, stream),
         lambda: crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws, stream),
         lambda: crisp.pe_map(s, qd, kd, route, pbar, ws, stream),
         lambda: crisp.select_pe(s, params, pbar, route, pebits, ws, stream),
@@ -391,7 +398,7 @@ def run_crisp(args):
 
     # Algorithmic work of the step's results.
     rb = rowbits.cpu().numpy().view(np.uint32)
-    pairs = selected_pairs(rb, nb)
+    pairs = selected_pairs(rb, n)
     flops = 4 * 128 * pairs
     dense_pairs = hq * n * (n + 1) // 2
     routes = route.cpu().numpy()
@@ -413,7 +420,7 @@ def run_crisp(args):
         ue[0].record(stream)
         crisp.proxy_map(s, qd, kd, pmap, ws, stream)
         ue[1].record(stream)
-        crisp.block_masses(s, pmap, vmass, smass, ws, stream)
+        crisp.block_masses(s, pmap, vmass, smass, rmass, ws, stream)
         ue[2].record(stream)
         torch.cuda.synchronize()
         unf["proxy"].append(ue[0].elapsed_time(ue[1]))
@@ -536,7 +543,8 @@ def time_layer(w, params, reps, dense=True):
     dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
     qd, kd, vd = dev(q), dev(k), dev(v)
     hq, hkv, n = w.hq, w.hkv, w.n
-    nb, W = n // B, (n // B + 31) // 32
+    nb = num_blocks(n)
+    W = (nb + 31) // 32
     out = torch.empty((hq, n, 128), dtype=torch.bfloat16, device="cuda")
     s = crisp.make_shape(hq, hkv, n, qd, kd, out)
     ws = torch.empty(crisp.layer_workspace_size(s), dtype=torch.uint8, device="cuda")
@@ -569,7 +577,7 @@ def time_layer(w, params, reps, dense=True):
     rb = grab("rowbits", (hq, nb, W), torch.int32).view(np.uint32)
     route = grab("route", (hq,), torch.uint8)
     counts = grab("counts", (hq, nb), torch.int32)
-    pairs = selected_pairs(rb, nb)
+    pairs = selected_pairs(rb, n)
     dense_pairs = hq * n * (n + 1) // 2
     r = {"seq_len": n, "layer_ms": layer_ms, "density": pairs / dense_pairs, "routes_vs": int(route.sum()),
          "blocks_per_row": float(counts.mean())}

@@ -18,6 +18,16 @@ _lib = None
 B = 128
 D = 128
 
+
+def num_blocks(n: int) -> int:
+    """Blocks of an n-token layer: ceil(n / 128), the last one short when 128 does not divide n."""
+    return (n + B - 1) // B
+
+
+def map_ld(n: int) -> int:
+    """Row stride (floats) of the proxy map: 128 * num_blocks(n)."""
+    return num_blocks(n) * B
+
 STATUS_NAMES = {0: "CRISP_OK", 1: "CRISP_ERR_INVALID_ARG", 2: "CRISP_ERR_SHAPE", 3: "CRISP_ERR_ALIGN",
                 4: "CRISP_ERR_WORKSPACE", 5: "CRISP_ERR_CUDA", 6: "CRISP_ERR_TIMEOUT", 7: "CRISP_ERR_DEVICE"}
 PE_GAMMA, PE_NOISE = 0, 1
@@ -52,7 +62,7 @@ class Params(ctypes.Structure):
 
 class LayerViews(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in
-                ("vmass", "smass", "cstruct", "total", "route", "vbits", "sbits", "pbar", "pebits",
+                ("vmass", "smass", "rmass", "cstruct", "total", "route", "vbits", "sbits", "pbar", "pebits",
                  "rowbits", "counts", "order")]
 
 
@@ -72,12 +82,12 @@ def lib():
         L.crisp_workspace_init.argtypes = [vp, sz, st]
         L.crisp_proxy_map.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
         L.crisp_proxy_map_noalloc.argtypes = [P(Shape), vp, vp, vp, st]
-        L.crisp_block_masses.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
-        L.crisp_proxy_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
+        L.crisp_block_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
+        L.crisp_proxy_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, st]
         L.crisp_host_pipeline_create.argtypes = [P(vp)]
         L.crisp_host_pipeline_destroy.argtypes = [vp]
         L.crisp_prefill_layer_host.argtypes = [vp, P(Shape), P(Params)] + [vp] * 9 + [sz, st]
-        L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
+        L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, st]
         L.crisp_route_jsd.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
         L.crisp_wait_selftest.argtypes = [vp, sz, ctypes.c_int64, st]
         L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
@@ -179,20 +189,20 @@ def proxy_map_noalloc(shape, q, k, pmap, stream=None):
            "crisp_proxy_map_noalloc")
 
 
-def block_masses(shape, pmap, vmass, smass, ws, stream=None):
-    _check(lib().crisp_block_masses(ctypes.byref(shape), _ptr(pmap), _ptr(vmass), _ptr(smass), _ptr(ws), _nbytes(ws),
-                                    _stream(stream)), "crisp_block_masses")
+def block_masses(shape, pmap, vmass, smass, rmass, ws, stream=None):
+    _check(lib().crisp_block_masses(ctypes.byref(shape), _ptr(pmap), _ptr(vmass), _ptr(smass), _ptr(rmass), _ptr(ws),
+                                    _nbytes(ws), _stream(stream)), "crisp_block_masses")
 
 
-def proxy_masses(shape, q, k, vmass, smass, ws, stream=None):
+def proxy_masses(shape, q, k, vmass, smass, rmass, ws, stream=None):
     """Block masses of the proxy map straight from q and k (the map is not stored)."""
-    _check(lib().crisp_proxy_masses(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(vmass), _ptr(smass), _ptr(ws),
-                                    _nbytes(ws), _stream(stream)), "crisp_proxy_masses")
+    _check(lib().crisp_proxy_masses(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(vmass), _ptr(smass), _ptr(rmass),
+                                    _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_proxy_masses")
 
 
-def route_cstruct(shape, params, vmass, cstruct, total, route, stream=None):
-    _check(lib().crisp_route_cstruct(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(cstruct),
-                                     _ptr(total), _ptr(route), _stream(stream)), "crisp_route_cstruct")
+def route_cstruct(shape, params, vmass, rmass, cstruct, total, route, stream=None):
+    _check(lib().crisp_route_cstruct(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(rmass),
+                                     _ptr(cstruct), _ptr(total), _ptr(route), _stream(stream)), "crisp_route_cstruct")
 
 
 def route_jsd(shape, params, vmass, pbar, jsd, route, stream=None):

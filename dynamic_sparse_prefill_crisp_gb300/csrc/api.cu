@@ -18,18 +18,23 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-crisp_status check_shape(const crisp_shape* s) {
+// The method's steps need the sink block and at least one more (n >= 256);
+// attention and the whole layer take any n from 0 (an empty input) up.
+constexpr int kMinSeqMethod = 2 * kB;
+
+crisp_status check_shape(const crisp_shape* s, int min_n = kMinSeqMethod) {
   if (!s) return CRISP_ERR_INVALID_ARG;
   if (s->hq <= 0 || s->hkv <= 0 || s->hq % s->hkv != 0) return CRISP_ERR_SHAPE;
   if (s->head_dim != kD || s->block != kB) return CRISP_ERR_SHAPE;
-  if (s->seq_len < 2 * kB || s->seq_len > kMaxSeq || s->seq_len % kB != 0) return CRISP_ERR_SHAPE;
+  if (s->seq_len < min_n || s->seq_len > kMaxSeq) return CRISP_ERR_SHAPE;
   if (s->hq > 4096) return CRISP_ERR_SHAPE;
+  if (!(s->scale >= 0.f) || std::isinf(s->scale)) return CRISP_ERR_INVALID_ARG;
+  if (s->seq_len == 0) return CRISP_OK;  // an empty input addresses no element: strides are not used
   const int64_t strides[6] = {s->q_head_stride, s->q_tok_stride, s->kv_head_stride,
                               s->kv_tok_stride, s->o_head_stride, s->o_tok_stride};
   for (int64_t st : strides)
     if (st <= 0 || st % 8 != 0 || st > (int64_t(1) << 38)) return CRISP_ERR_ALIGN;
   if (s->q_tok_stride < kD || s->kv_tok_stride < kD || s->o_tok_stride < kD) return CRISP_ERR_SHAPE;
-  if (!(s->scale >= 0.f) || std::isinf(s->scale)) return CRISP_ERR_INVALID_ARG;
   return CRISP_OK;
 }
 
@@ -116,6 +121,8 @@ ScratchLayout scratch_layout(const crisp_shape& s) {
   L.proxy_stats = o; o = up(o + hq * kB * sizeof(float2));
   L.mass_lower = o;  o = up(o + hq * nb * 8);
   L.mass_upper = o;  o = up(o + hq * nb * 8);
+  L.mass_upper2 = o; o = up(o + hq * nb * 8);
+  L.mass_rec = o;    o = up(o + hq * 8);
   L.qbar = o;        o = up(o + hq * nb * kD * 4);
   L.kbar = o;        o = up(o + hkv * nb * kD * 4);
   L.srev = o;        o = up(o + hq * (W + 2) * 4);
@@ -129,6 +136,7 @@ LayerLayout layer_layout(const crisp_shape& s) {
   size_t o = scratch_layout(s).total;
   L.vmass = o;      o = up(o + hq * nb * 8);
   L.smass = o;      o = up(o + hq * nb * 8);
+  L.rmass = o;      o = up(o + hq * 8);
   L.cstruct = o;    o = up(o + hq * 8);
   L.total_mass = o; o = up(o + hq * 8);
   L.route = o;      o = up(o + hq);
@@ -168,7 +176,7 @@ void crisp_params_default(crisp_params* p) {
 }
 
 crisp_status crisp_workspace_size(const crisp_shape* shape, size_t* bytes) {
-  crisp_status st = check_shape(shape);
+  crisp_status st = check_shape(shape, 0);
   if (st != CRISP_OK) return st;
   if (!bytes) return CRISP_ERR_INVALID_ARG;
   *bytes = scratch_layout(*shape).total;
@@ -176,7 +184,7 @@ crisp_status crisp_workspace_size(const crisp_shape* shape, size_t* bytes) {
 }
 
 crisp_status crisp_layer_workspace_size(const crisp_shape* shape, size_t* bytes) {
-  crisp_status st = check_shape(shape);
+  crisp_status st = check_shape(shape, 0);
   if (st != CRISP_OK) return st;
   if (!bytes) return CRISP_ERR_INVALID_ARG;
   *bytes = layer_layout(*shape).total;
@@ -266,23 +274,24 @@ crisp_status crisp_proxy_map_noalloc(const crisp_shape* shape, const void* q, co
 }
 
 crisp_status crisp_block_masses(const crisp_shape* shape, const float* pmap, uint64_t* vmass, uint64_t* smass,
-                                void* ws, size_t ws_bytes, crisp_stream_t stream) {
+                                uint64_t* rmass, void* ws, size_t ws_bytes, crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
   if (st != CRISP_OK) return st;
-  if (!pmap || !vmass || !smass) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(pmap) || !aligned(vmass, 8) || !aligned(smass, 8)) return CRISP_ERR_ALIGN;
+  if (!pmap || !vmass || !smass || !rmass) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(pmap) || !aligned(vmass, 8) || !aligned(smass, 8) || !aligned(rmass, 8)) return CRISP_ERR_ALIGN;
   const crisp_shape s = normalised(*shape);
   if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_block_masses(s, pmap, vmass, smass, static_cast<char*>(ws), stream));
+  return from_cuda(launch_block_masses(s, pmap, vmass, smass, rmass, static_cast<char*>(ws), stream));
 }
 
 crisp_status crisp_proxy_masses(const crisp_shape* shape, const void* q, const void* k, uint64_t* vmass,
-                                uint64_t* smass, void* ws, size_t ws_bytes, crisp_stream_t stream) {
+                                uint64_t* smass, uint64_t* rmass, void* ws, size_t ws_bytes, crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
   if (st != CRISP_OK) return st;
-  if (!q || !k || !vmass || !smass) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned(vmass, 8) || !aligned(smass, 8)) return CRISP_ERR_ALIGN;
+  if (!q || !k || !vmass || !smass || !rmass) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned(vmass, 8) || !aligned(smass, 8) || !aligned(rmass, 8))
+    return CRISP_ERR_ALIGN;
   const crisp_shape s = normalised(*shape);
   if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
@@ -290,18 +299,19 @@ crisp_status crisp_proxy_masses(const crisp_shape* shape, const void* q, const v
   if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
   if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
   maps.v = maps.k;
-  return from_cuda(launch_proxy_masses(s, maps, vmass, smass, static_cast<char*>(ws), stream));
+  return from_cuda(launch_proxy_masses(s, maps, vmass, smass, rmass, static_cast<char*>(ws), stream));
 }
 
 crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
-                                 uint64_t* cstruct, uint64_t* total, uint8_t* route, crisp_stream_t stream) {
+                                 const uint64_t* rmass, uint64_t* cstruct, uint64_t* total, uint8_t* route,
+                                 crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
   if (st != CRISP_OK) return st;
   if ((st = check_params(params)) != CRISP_OK) return st;
-  if (!vmass || !cstruct || !total || !route) return CRISP_ERR_INVALID_ARG;
-  if (!aligned(vmass, 8) || !aligned(cstruct, 8) || !aligned(total, 8)) return CRISP_ERR_ALIGN;
+  if (!vmass || !rmass || !cstruct || !total || !route) return CRISP_ERR_INVALID_ARG;
+  if (!aligned(vmass, 8) || !aligned(rmass, 8) || !aligned(cstruct, 8) || !aligned(total, 8)) return CRISP_ERR_ALIGN;
   if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_route(normalised(*shape), *params, vmass, cstruct, total, route, stream));
+  return from_cuda(launch_route(normalised(*shape), *params, vmass, rmass, cstruct, total, route, stream));
 }
 
 crisp_status crisp_route_jsd(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
@@ -374,8 +384,9 @@ crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t* route, co
 static crisp_status attention_common(const crisp_shape* shape, const void* q, const void* k, const void* v,
                                      const uint32_t* rowbits, const int32_t* order, void* out, void* ws,
                                      size_t ws_bytes, crisp_stream_t stream, bool dense) {
-  crisp_status st = check_shape(shape);
+  crisp_status st = check_shape(shape, 0);
   if (st != CRISP_OK) return st;
+  if (shape->seq_len == 0) return CRISP_OK;  // an empty input: nothing to compute
   if (!q || !k || !v || !out || (!dense && !rowbits)) return CRISP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
   if (!dense && (!aligned(rowbits, 4) || !aligned(order, 4))) return CRISP_ERR_ALIGN;
@@ -401,13 +412,14 @@ crisp_status crisp_dense_prefill(const crisp_shape* shape, const void* q, const 
 }
 
 crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws, crisp_layer_views* views) {
-  crisp_status st = check_shape(shape);
+  crisp_status st = check_shape(shape, 0);
   if (st != CRISP_OK) return st;
   if (!ws || !views) return CRISP_ERR_INVALID_ARG;
   const LayerLayout L = layer_layout(*shape);
   char* b = static_cast<char*>(ws);
   views->vmass = reinterpret_cast<uint64_t*>(b + L.vmass);
   views->smass = reinterpret_cast<uint64_t*>(b + L.smass);
+  views->rmass = reinterpret_cast<uint64_t*>(b + L.rmass);
   views->cstruct = reinterpret_cast<uint64_t*>(b + L.cstruct);
   views->total = reinterpret_cast<uint64_t*>(b + L.total_mass);
   views->route = reinterpret_cast<uint8_t*>(b + L.route);
@@ -437,10 +449,12 @@ crisp_status run_layer(const crisp_shape& s, const crisp_params& p, const void* 
   if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
   if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
   char* wsb = static_cast<char*>(ws);
-  // Length gate: below it the layer is plain dense attention.
-  if (s.seq_len < p.dense_below)
+  // Length gate: below it the layer is plain dense attention. Below two
+  // blocks the method has no candidates (and k_min keeps every block of up
+  // to 8), so such layers are dense too.
+  if (s.seq_len < p.dense_below || s.seq_len < kMinSeqMethod)
     return from_cuda(launch_attention(s, maps, nullptr, nullptr, out, wsb, true, stream));
-  if (launch_proxy_masses(s, maps, w.vmass, w.smass, wsb, stream) != cudaSuccess) return CRISP_ERR_CUDA;
+  if (launch_proxy_masses(s, maps, w.vmass, w.smass, w.rmass, wsb, stream) != cudaSuccess) return CRISP_ERR_CUDA;
   if (p.route_mode == CRISP_ROUTE_JSD) {
     // The comparator needs the pooled estimate of every head before routing
     // (a zero route array selects all heads), then routes by divergence.
@@ -448,7 +462,7 @@ crisp_status run_layer(const crisp_shape& s, const crisp_params& p, const void* 
         launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess ||
         launch_route_jsd(s, p, w.vmass, w.pbar, nullptr, w.route, stream) != cudaSuccess)
       return CRISP_ERR_CUDA;
-  } else if (launch_route(s, p, w.vmass, w.cstruct, w.total, w.route, stream) != cudaSuccess ||
+  } else if (launch_route(s, p, w.vmass, w.rmass, w.cstruct, w.total, w.route, stream) != cudaSuccess ||
              launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess) {
     return CRISP_ERR_CUDA;
   }
@@ -488,9 +502,10 @@ extern "C" {
 
 crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* params, const void* q, const void* k,
                                  const void* v, void* out, void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
+  crisp_status st = check_shape(shape, 0);
   if (st != CRISP_OK) return st;
   if ((st = check_params(params)) != CRISP_OK) return st;
+  if (shape->seq_len == 0) return CRISP_OK;  // an empty input: nothing to compute
   if (!q || !k || !v || !out) return CRISP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
   const crisp_shape s = normalised(*shape);
@@ -546,9 +561,10 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
                                       const void* v_host, void* out_host, void* q, void* k, void* v, void* out,
                                       void* ws, size_t ws_bytes, crisp_stream_t stream) {
   if (!pipeline) return CRISP_ERR_INVALID_ARG;
-  crisp_status st = check_shape(shape);
+  crisp_status st = check_shape(shape, 0);
   if (st != CRISP_OK) return st;
   if ((st = check_params(params)) != CRISP_OK) return st;
+  if (shape->seq_len == 0) return CRISP_OK;  // an empty input: nothing to compute
   if (!q_host || !k_host || !v_host || !out_host || !q || !k || !v || !out) return CRISP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
   const crisp_shape s = normalised(*shape);

@@ -9,7 +9,9 @@
 //   P  = 2^(S*c - m)     softmax warps: TMEM -> registers -> bf16 -> TMEM (each warp
 //                        over its own S columns)
 //   O += P V_kb          tcgen05.mma, A = P (TMEM), B = V (smem, MN-major), D = O (TMEM)
-// K and V tiles arrive by TMA at row coordinate kb*128 (gather by block index).
+// K and V tiles arrive by TMA at row coordinate kb*128 (gather by block index);
+// rows past n in a short last block are filled with zeros, the causal mask
+// hides those keys and their query rows are not stored.
 // The reference max m is raised lazily: each block is first exponentiated at
 // the current m; only if some row's block sum exceeds 2^8 (so possibly one p
 // > 2^8) do the warps take the exact row max, move m, rescale O and the row
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ Bars bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = n / kB, W = (nb + 31) / 32;
+  const int nb = (n + kB - 1) / kB, W = (nb + 31) / 32;  // a short last block when 128 does not divide n
   // Work item: the schedule order[] or, without one, query blocks descending.
   int item;
   if (order != nullptr) {
@@ -398,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int R = it * 4 + (lane >> 3);
       const uint4 u = stg[R * 8 + (chunk ^ (R & 7))];
       const int tok = qb * kB + quarter * 32 + R;
+      if (tok >= n) continue;  // rows past the end of a short last block
       uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * o_hs + static_cast<int64_t>(tok) * o_ts +
                                             half * 64);
       dst[chunk] = u;

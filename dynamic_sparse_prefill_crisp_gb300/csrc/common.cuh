@@ -46,7 +46,12 @@ __device__ __forceinline__ uint64_t q32(float p) {
   return x < kTwo23 ? static_cast<uint64_t>(q32_small(x)) : q32_large(x);
 }
 
-inline int num_blocks(int n) { return n / kB; }
+// Blocks are aligned at token 0; when 128 does not divide n the last block
+// is short: it holds tail_len(n) in [1, 128] tokens.
+inline int num_blocks(int n) { return (n + kB - 1) / kB; }
+inline int tail_len(int n) { return n - (num_blocks(n) - 1) * kB; }
+// Row stride (floats) of the proxy map: whole 128-column tiles.
+inline int64_t map_ld(int n) { return static_cast<int64_t>(num_blocks(n)) * kB; }
 inline int bit_words(int nb) { return (nb + 31) / 32; }
 inline int proxy_chunks(int nb) { return (nb + kProxyChunk - 1) / kProxyChunk; }
 
@@ -55,8 +60,10 @@ struct ScratchLayout {
   size_t status;       // DevStatus
   size_t proxy_part;   // float2 [hq][128][chunks]  per-chunk (max, sum) in log2 units
   size_t proxy_stats;  // float2 [hq][128]          (row max, 1/row sum)
-  size_t mass_lower;   // uint64 [hq][nb]  lower-triangle slash part of tile c
-  size_t mass_upper;   // uint64 [hq][nb]  strict-upper slash part of tile c
+  size_t mass_lower;   // uint64 [hq][nb]  tile c's entries with slash block nb-1-c
+  size_t mass_upper;   // uint64 [hq][nb]  tile c's entries with slash block nb-2-c
+  size_t mass_upper2;  // uint64 [hq][nb]  tile c's entries with slash block nb-3-c (short last block only)
+  size_t mass_rec;     // uint64 [hq]      recency columns [n-128, n) that lie in tile nb-2
   size_t qbar;         // float  [hq][nb][128]
   size_t kbar;         // float  [hkv][nb][128]
   size_t srev;         // uint32 [hq][W + 2]  slash bits reversed
@@ -65,7 +72,7 @@ struct ScratchLayout {
 
 // Intermediates of crisp_prefill_layer, placed after the scratch.
 struct LayerLayout {
-  size_t vmass, smass, cstruct, total_mass, route, vbits, sbits, pbar, pebits, rowbits, counts, order;
+  size_t vmass, smass, rmass, cstruct, total_mass, route, vbits, sbits, pbar, pebits, rowbits, counts, order;
   size_t total;
 };
 
@@ -78,14 +85,14 @@ struct TmaMaps {
 
 // ---- launchers (one per translation unit); return cudaSuccess or the launch error
 cudaError_t launch_proxy(const crisp_shape& s, const TmaMaps& maps, float* pmap, char* ws, cudaStream_t st);
-cudaError_t launch_proxy_masses(const crisp_shape& s, const TmaMaps& maps, uint64_t* vmass, uint64_t* smass, char* ws,
-                                cudaStream_t st);
-cudaError_t launch_assemble_slash(const crisp_shape& s, const uint64_t* lower, const uint64_t* upper, uint64_t* smass,
-                                  cudaStream_t st);
-cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_t* vmass, uint64_t* smass, char* ws,
-                                cudaStream_t st);
-cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, uint64_t* cstruct,
-                         uint64_t* total, uint8_t* route, cudaStream_t st);
+cudaError_t launch_proxy_masses(const crisp_shape& s, const TmaMaps& maps, uint64_t* vmass, uint64_t* smass,
+                                uint64_t* rmass, char* ws, cudaStream_t st);
+cudaError_t launch_assemble_slash(const crisp_shape& s, const uint64_t* vmass, char* ws, uint64_t* smass,
+                                  uint64_t* rmass, cudaStream_t st);
+cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_t* vmass, uint64_t* smass,
+                                uint64_t* rmass, char* ws, cudaStream_t st);
+cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const uint64_t* rmass,
+                         uint64_t* cstruct, uint64_t* total, uint8_t* route, cudaStream_t st);
 cudaError_t launch_route_jsd(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const float* pbar,
                              double* jsd, uint8_t* route, cudaStream_t st);
 cudaError_t launch_select_vs(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass,

@@ -14,28 +14,40 @@ namespace {
 
 constexpr int kMassThreads = 256;
 
-// One CTA per 128x128 tile (key block c, head h) of the proxy map. Thread t
-// reads columns 4*(t%32)..+3 of rows 16*(t/32)..+15 (coalesced 512-byte rows)
-// and sums the quanta three ways: the whole tile (vertical mass of block c),
-// the lower triangle r >= jj (slash offset block nb-1-c) and the strict upper
-// triangle r < jj (slash offset block nb-2-c).
-__global__ void __launch_bounds__(kMassThreads) mass_tiles(const float* __restrict__ pmap, int n,
+// One CTA per 128x128 tile (key block c, head h) of the proxy map (row
+// stride ld floats). Thread t reads columns 4*(t%32)..+3 of rows
+// 16*(t/32)..+15 (coalesced 512-byte rows) and sums the quanta by slash
+// block. Row r is token i = n-128+r = (nb-2)*128 + tail + r and column jj
+// of the tile is token j = 128c + jj, so the diagonal offset i - j falls in
+// slash block nb-2-c + floor((tail + r - jj) / 128):
+//   nb-1-c  where jj - r <= tail - 128   (the lower triangle when 128 | n)
+//   nb-2-c  where tail - 128 < jj - r <= tail
+//   nb-3-c  where jj - r > tail          (empty when 128 | n)
+// The whole tile is the vertical mass of block c. Tile nb-2 also sums its
+// columns jj >= tail, the part of the recency columns [n-128, n) that lies
+// before the (short) last block. kRagged = false fixes tail = 128 (128
+// divides n), where the third band and the recency part fold away.
+template <bool kRagged>
+__global__ void __launch_bounds__(kMassThreads) mass_tiles(const float* __restrict__ pmap, int64_t ld, int tail_arg,
                                                            uint64_t* __restrict__ vmass,
                                                            uint64_t* __restrict__ lower,
-                                                           uint64_t* __restrict__ upper) {
-  __shared__ uint64_t red[3][kMassThreads / 32];
+                                                           uint64_t* __restrict__ upper,
+                                                           uint64_t* __restrict__ upper2,
+                                                           uint64_t* __restrict__ rec) {
+  __shared__ uint64_t red[4][kMassThreads / 32];
+  const int tail = kRagged ? tail_arg : kB;
   const int c = blockIdx.x, h = blockIdx.y, nb = gridDim.x;
   const int cq = threadIdx.x & 31, rg = threadIdx.x >> 5;
-  const float* base = pmap + static_cast<size_t>(h) * kB * n + static_cast<size_t>(c) * kB + cq * 4;
+  const float* base = pmap + static_cast<size_t>(h) * kB * ld + static_cast<size_t>(c) * kB + cq * 4;
   float4 p[16];
 #pragma unroll
   for (int k = 0; k < 16; ++k)
-    p[k] = __ldcs(reinterpret_cast<const float4*>(base + static_cast<size_t>(rg * 16 + k) * n));
+    p[k] = __ldcs(reinterpret_cast<const float4*>(base + static_cast<size_t>(rg * 16 + k) * ld));
   // Quanta below 2^23 (nearly all of them) are summed in 32 bits: 64 of them
   // stay below 2^29. Larger ones go to 64-bit sums.
-  uint32_t all32 = 0, lo32 = 0;
-  uint64_t all64 = 0, lo64 = 0;
-  const int jj = cq * 4;
+  uint32_t all32 = 0, lo32 = 0, hi32 = 0;
+  uint64_t all64 = 0, lo64 = 0, hi64 = 0;
+  const int jj = cq * 4, b_lo = tail - kB, b_hi = tail;
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
     const int r = rg * 16 + k;
@@ -43,51 +55,76 @@ __global__ void __launch_bounds__(kMassThreads) mass_tiles(const float* __restri
                         p[k].w * 4294967296.0f};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const bool lower = r >= jj + e;
+      const int dj = jj + e - r;
+      const bool in_lo = dj <= b_lo, in_hi = kRagged && dj > b_hi;
       if (x[e] < kTwo23) {
         const uint32_t f = q32_small(x[e]);
         all32 += f;
-        lo32 += lower ? f : 0u;
+        lo32 += in_lo ? f : 0u;
+        hi32 += in_hi ? f : 0u;
       } else {
         const uint64_t f = q32_large(x[e]);
         all64 += f;
-        lo64 += lower ? f : 0ull;
+        lo64 += in_lo ? f : 0ull;
+        hi64 += in_hi ? f : 0ull;
       }
     }
   }
-  const uint64_t all = all64 + all32, lo = lo64 + lo32;
-  uint64_t v[3] = {all, lo, all - lo};
+  const bool rec_tile = c == nb - 2 && tail < kB;
+  uint64_t rs = 0;
+  if (rec_tile) {
 #pragma unroll
-  for (int t = 0; t < 3; ++t) v[t] = warp_sum(v[t]);
+    for (int k = 0; k < 16; ++k) {
+      const float x[4] = {p[k].x * 4294967296.0f, p[k].y * 4294967296.0f, p[k].z * 4294967296.0f,
+                          p[k].w * 4294967296.0f};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (jj + e >= tail) rs += x[e] < kTwo23 ? static_cast<uint64_t>(q32_small(x[e])) : q32_large(x[e]);
+    }
+  }
+  uint64_t v[4] = {all64 + all32, lo64 + lo32, hi64 + hi32, rs};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) v[t] = warp_sum(v[t]);
   if ((threadIdx.x & 31) == 0)
-    for (int t = 0; t < 3; ++t) red[t][threadIdx.x >> 5] = v[t];
+    for (int t = 0; t < 4; ++t) red[t][threadIdx.x >> 5] = v[t];
   __syncthreads();
-  if (threadIdx.x < 3) {
-    uint64_t s = 0;
-    for (int w = 0; w < kMassThreads / 32; ++w) s += red[threadIdx.x][w];
-    uint64_t* out = threadIdx.x == 0 ? vmass : (threadIdx.x == 1 ? lower : upper);
-    out[static_cast<size_t>(h) * nb + c] = s;
+  if (threadIdx.x == 0) {
+    uint64_t sum[4] = {0, 0, 0, 0};
+    for (int t = 0; t < 4; ++t)
+      for (int w = 0; w < kMassThreads / 32; ++w) sum[t] += red[t][w];
+    const size_t idx = static_cast<size_t>(h) * nb + c;
+    vmass[idx] = sum[0];
+    lower[idx] = sum[1];
+    upper[idx] = sum[0] - sum[1] - sum[2];
+    upper2[idx] = sum[2];
+    if (rec_tile) rec[h] = sum[3];
   }
 }
 
-// smass[h][s] = lower[nb-1-s] (tile nb-1-s >= 1) + upper[nb-2-s] (tile >= 1).
-// Tile 0 holds the sink columns j < 128, which the slash direction leaves out.
-__global__ void assemble_slash(const uint64_t* __restrict__ lower, const uint64_t* __restrict__ upper, int nb,
-                               uint64_t* __restrict__ smass) {
+// smass[h][s] = lower[nb-1-s] + upper[nb-2-s] + upper2[nb-3-s], each over
+// tiles >= 1: tile 0 holds the sink columns j < 128, which the slash
+// direction leaves out. Thread s = 0 also forms the recency mass, the
+// columns [n-128, n): the last block plus, when it is short, the rest of
+// tile nb-2.
+__global__ void assemble_slash(const uint64_t* __restrict__ vmass, const uint64_t* __restrict__ lower,
+                               const uint64_t* __restrict__ upper, const uint64_t* __restrict__ upper2,
+                               const uint64_t* __restrict__ rec, int nb, int tail, uint64_t* __restrict__ smass,
+                               uint64_t* __restrict__ rmass) {
   const int h = blockIdx.y;
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= nb) return;
-  const uint64_t* lo = lower + static_cast<size_t>(h) * nb;
-  const uint64_t* up = upper + static_cast<size_t>(h) * nb;
-  const int cl = nb - 1 - s, cu = nb - 2 - s;
-  smass[static_cast<size_t>(h) * nb + s] = (cl >= 1 ? lo[cl] : 0ull) + (cu >= 1 ? up[cu] : 0ull);
+  const size_t o = static_cast<size_t>(h) * nb;
+  const int c1 = nb - 1 - s, c2 = nb - 2 - s, c3 = nb - 3 - s;
+  smass[o + s] = (c1 >= 1 ? lower[o + c1] : 0ull) + (c2 >= 1 ? upper[o + c2] : 0ull) +
+                 (c3 >= 1 ? upper2[o + c3] : 0ull);
+  if (s == 0) rmass[h] = vmass[o + nb - 1] + (tail < kB ? rec[h] : 0ull);
 }
 
-// C_struct = vmass[0] + vmass[nb-1] (columns [0,128) and [n-128,n)), total =
-// sum of vmass; VS iff tau_den * C_struct >= tau_num * total.
-__global__ void route_kernel(const uint64_t* __restrict__ vmass, int nb, uint32_t tau_num, uint32_t tau_den,
-                             uint64_t* __restrict__ cstruct, uint64_t* __restrict__ total,
-                             uint8_t* __restrict__ route) {
+// C_struct = vmass[0] + rmass (columns [0,128) and [n-128,n), disjoint for
+// n >= 256), total = sum of vmass; VS iff tau_den * C_struct >= tau_num * total.
+__global__ void route_kernel(const uint64_t* __restrict__ vmass, const uint64_t* __restrict__ rmass, int nb,
+                             uint32_t tau_num, uint32_t tau_den, uint64_t* __restrict__ cstruct,
+                             uint64_t* __restrict__ total, uint8_t* __restrict__ route) {
   __shared__ uint64_t scratch[32];
   const int h = blockIdx.x;
   const uint64_t* v = vmass + static_cast<size_t>(h) * nb;
@@ -95,7 +132,7 @@ __global__ void route_kernel(const uint64_t* __restrict__ vmass, int nb, uint32_
   for (int c = threadIdx.x; c < nb; c += blockDim.x) s += v[c];
   const uint64_t T = block_sum(s, scratch);
   if (threadIdx.x == 0) {
-    const uint64_t S = v[0] + v[nb - 1];
+    const uint64_t S = v[0] + rmass[h];
     cstruct[h] = S;
     total[h] = T;
     route[h] = static_cast<unsigned __int128>(tau_den) * S >= static_cast<unsigned __int128>(tau_num) * T ? 1 : 0;
@@ -216,27 +253,34 @@ __global__ void jsd_route_kernel(const uint64_t* __restrict__ vmass, const float
 
 }  // namespace
 
-cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_t* vmass, uint64_t* smass, char* ws,
-                                cudaStream_t st) {
+cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_t* vmass, uint64_t* smass,
+                                uint64_t* rmass, char* ws, cudaStream_t st) {
   const ScratchLayout L = scratch_layout(s);
   const int nb = num_blocks(s.seq_len);
-  auto* lower = reinterpret_cast<uint64_t*>(ws + L.mass_lower);
-  auto* upper = reinterpret_cast<uint64_t*>(ws + L.mass_upper);
-  mass_tiles<<<dim3(nb, s.hq), kMassThreads, 0, st>>>(pmap, s.seq_len, vmass, lower, upper);
+  auto* kern = tail_len(s.seq_len) == kB ? mass_tiles<false> : mass_tiles<true>;
+  kern<<<dim3(nb, s.hq), kMassThreads, 0, st>>>(
+      pmap, map_ld(s.seq_len), tail_len(s.seq_len), vmass, reinterpret_cast<uint64_t*>(ws + L.mass_lower),
+      reinterpret_cast<uint64_t*>(ws + L.mass_upper), reinterpret_cast<uint64_t*>(ws + L.mass_upper2),
+      reinterpret_cast<uint64_t*>(ws + L.mass_rec));
   const cudaError_t e = cudaGetLastError();
-  return e != cudaSuccess ? e : launch_assemble_slash(s, lower, upper, smass, st);
+  return e != cudaSuccess ? e : launch_assemble_slash(s, vmass, ws, smass, rmass, st);
 }
 
-cudaError_t launch_assemble_slash(const crisp_shape& s, const uint64_t* lower, const uint64_t* upper, uint64_t* smass,
-                                  cudaStream_t st) {
+cudaError_t launch_assemble_slash(const crisp_shape& s, const uint64_t* vmass, char* ws, uint64_t* smass,
+                                  uint64_t* rmass, cudaStream_t st) {
+  const ScratchLayout L = scratch_layout(s);
   const int nb = num_blocks(s.seq_len);
-  assemble_slash<<<dim3((nb + 255) / 256, s.hq), 256, 0, st>>>(lower, upper, nb, smass);
+  assemble_slash<<<dim3((nb + 255) / 256, s.hq), 256, 0, st>>>(
+      vmass, reinterpret_cast<const uint64_t*>(ws + L.mass_lower), reinterpret_cast<const uint64_t*>(ws + L.mass_upper),
+      reinterpret_cast<const uint64_t*>(ws + L.mass_upper2), reinterpret_cast<const uint64_t*>(ws + L.mass_rec), nb,
+      tail_len(s.seq_len), smass, rmass);
   return cudaGetLastError();
 }
 
-cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, uint64_t* cstruct,
-                         uint64_t* total, uint8_t* route, cudaStream_t st) {
-  route_kernel<<<s.hq, 256, 0, st>>>(vmass, num_blocks(s.seq_len), p.tau_num, p.tau_den, cstruct, total, route);
+cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const uint64_t* rmass,
+                         uint64_t* cstruct, uint64_t* total, uint8_t* route, cudaStream_t st) {
+  route_kernel<<<s.hq, 256, 0, st>>>(vmass, rmass, num_blocks(s.seq_len), p.tau_num, p.tau_den, cstruct, total,
+                                     route);
   return cudaGetLastError();
 }
 

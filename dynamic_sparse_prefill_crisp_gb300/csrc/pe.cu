@@ -3,7 +3,8 @@
 // "Methodology in Plain English": the PE path keeps FlexPrefill's pooled
 // estimate and uses gamma = 0.95 coverage).
 //
-// A5: qbar_b / kbar_c = means over each 128-token block; pbar[b][c] = softmax
+// A5: qbar_b / kbar_c = means over each block's tokens (128, or fewer in a
+// short last block); pbar[b][c] = softmax
 // over c <= b of scale * qbar_b . kbar_c (fp32; c > b stored as 0).
 // A6: per row b, gamma coverage (or the noise floor) over Q32 quanta of pbar.
 #include <cuda_bf16.h>
@@ -20,7 +21,7 @@ namespace {
 // only), otherwise kv head y - hq (when any of its query heads is PE).
 __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat162* __restrict__ q,
                                                    const __nv_bfloat162* __restrict__ k, const uint8_t* __restrict__ route,
-                                                   int hq, int hkv, int64_t q_hs, int64_t q_ts, int64_t kv_hs,
+                                                   int hq, int hkv, int n, int64_t q_hs, int64_t q_ts, int64_t kv_hs,
                                                    int64_t kv_ts, float* __restrict__ qbar, float* __restrict__ kbar) {
   __shared__ float2 red[4][64];
   const int b = blockIdx.x, y = blockIdx.y, nb = gridDim.x;
@@ -38,8 +39,9 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat162* __restr
   const __nv_bfloat162* src = is_q ? q + (static_cast<int64_t>(y) * q_hs + static_cast<int64_t>(b) * kB * q_ts) / 2
                                    : k + (static_cast<int64_t>(y - hq) * kv_hs + static_cast<int64_t>(b) * kB * kv_ts) / 2;
   const int64_t ts = (is_q ? q_ts : kv_ts) / 2;
+  const int len = min(kB, n - b * kB);  // tokens of block b
   float2 acc = make_float2(0.f, 0.f);
-  for (int r = rg * 32; r < rg * 32 + 32; ++r) {
+  for (int r = rg * 32; r < min(rg * 32 + 32, len); ++r) {
     const float2 v = __bfloat1622float2(src[r * ts + pair]);
     acc.x += v.x;
     acc.y += v.y;
@@ -53,8 +55,9 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat162* __restr
       s.y += red[t][pair].y;
     }
     float* dst = is_q ? qbar + (static_cast<size_t>(y) * nb + b) * kD : kbar + (static_cast<size_t>(y - hq) * nb + b) * kD;
-    dst[2 * pair] = s.x * (1.0f / kB);
-    dst[2 * pair + 1] = s.y * (1.0f / kB);
+    const float inv = 1.0f / static_cast<float>(len);  // exact for a whole block
+    dst[2 * pair] = s.x * inv;
+    dst[2 * pair + 1] = s.y * inv;
   }
 }
 
@@ -223,7 +226,7 @@ cudaError_t launch_pe_map(const crisp_shape& s, const void* q, const void* k, co
   auto* kbar = reinterpret_cast<float*>(ws + L.kbar);
   pool_kernel<<<dim3(nb, s.hq + s.hkv), 256, 0, st>>>(static_cast<const __nv_bfloat162*>(q),
                                                       static_cast<const __nv_bfloat162*>(k), route, s.hq, s.hkv,
-                                                      s.q_head_stride, s.q_tok_stride, s.kv_head_stride,
+                                                      s.seq_len, s.q_head_stride, s.q_tok_stride, s.kv_head_stride,
                                                       s.kv_tok_stride, qbar, kbar);
   const int tiles = (nb + kPT - 1) / kPT;
   pooled_scores<<<dim3(tiles, tiles, s.hq), 256, 0, st>>>(qbar, kbar, route, nb, s.hq / s.hkv,

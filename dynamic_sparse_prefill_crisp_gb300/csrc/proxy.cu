@@ -4,6 +4,10 @@
 //
 //   pmap[h][r][j] = softmax_j( scale * q_{n-128+r} . k_j ),  j <= n-128+r
 //
+// Key tiles are the 128-token blocks aligned at token 0 (the last one short
+// when 128 does not divide n; TMA fills its missing rows with zeros and the
+// causal mask hides them); the query rows are the last 128 tokens.
+//
 // Two passes over the keys with the same tile engine: pass 1 computes per-row
 // (max, sum of exp) over each chunk of key blocks, a tiny kernel combines the
 // chunks, pass 2 recomputes the logits and writes the normalised fp32 map.
@@ -67,12 +71,15 @@ struct ProxyCfg {
 };
 
 // grid: (hq, chunks). CTA (h, chunk) covers key blocks [chunk*C, chunk*C + C).
-template <int kMode>
+// kRagged: 128 does not divide n. The whole-block instantiation has the tail
+// fixed at 128, so the third slash band and the recency part fold away.
+template <int kMode, bool kRagged>
 __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
     proxy_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk, int n, int group,
-                 float c_log2, float* __restrict__ pmap, float2* __restrict__ part,
+                 float c_log2, float* __restrict__ pmap, int64_t ld, float2* __restrict__ part,
                  const float2* __restrict__ stats, uint64_t* __restrict__ vmass, uint64_t* __restrict__ lower,
-                 uint64_t* __restrict__ upper, DevStatus* status) {
+                 uint64_t* __restrict__ upper, uint64_t* __restrict__ upper2, uint64_t* __restrict__ rec,
+                 DevStatus* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
@@ -80,19 +87,21 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
   constexpr int kStages = ProxyCfg<kMode>::kStages;
   float* sStage = reinterpret_cast<float*>(base + kTile + kStages * kTile);
   __shared__ Bars bars;
-  __shared__ unsigned long long tile_acc[2][2];  // [tile parity][whole, lower triangle]
+  __shared__ unsigned long long tile_acc[2][4];  // [tile parity][whole, band lo, band hi, recency part]
   __shared__ unsigned int tile_cnt[2];           // warps that have added to the slot
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, chunk = blockIdx.y, nchunks = gridDim.y;
   const int g = h / group;
-  const int nb = n / kB;
+  const int nb = (n + kB - 1) / kB;
+  const int tail = kRagged ? n - (nb - 1) * kB : kB;  // tokens of the last block, in [1, 128]
   const int kb0 = chunk * kProxyChunk;
   const int T = min(nb, kb0 + kProxyChunk) - kb0;
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
-    tile_acc[0][0] = tile_acc[0][1] = tile_acc[1][0] = tile_acc[1][1] = 0ull;
+    for (int b = 0; b < 2; ++b)
+      for (int k = 0; k < 4; ++k) tile_acc[b][k] = 0ull;
     tile_cnt[0] = tile_cnt[1] = 0u;
     mbar_init(&bars.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
@@ -195,11 +204,16 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
       }
       tc_fence_after();
       const int kb = kb0 + t;
-      const bool diag = (kb == nb - 1);  // causal edge: keys j > n-128+r are masked
+      // Row r is token n-128+r = (nb-2)*128 + tail + r and column jj of this
+      // tile is token 128*kb + jj: visible iff jj - r <= lim (causal edge in
+      // the last one or two tiles).
+      const int lim = (nb - 2 - kb) * kB + tail;
+      const bool edge = lim < kB - 1;
+      const bool rec_tile = kb == nb - 2 && tail < kB;  // holds recency columns jj >= tail
       // Q32 quanta of this row's 64 probabilities of the tile: below 2^23 in
       // 32 bits (64 of them stay below 2^29), larger ones in 64 bits.
-      uint32_t all32 = 0, lo32 = 0;
-      uint64_t all64 = 0, lo64 = 0;
+      uint32_t all32 = 0, lo32 = 0, hi32 = 0;
+      uint64_t all64 = 0, lo64 = 0, hi64 = 0, rec64 = 0;
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = half * 64 + cc * 32;
@@ -209,10 +223,10 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
         float x[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(v[e]);
-        if (diag) {
+        if (edge) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (col0 + e > r) x[e] = -INFINITY;
+            if (col0 + e - r > lim) x[e] = -INFINITY;
         }
         if (kMode == kStats) {
           // Running (max, sum) in base-2 units: m = c_log2 * max S, l = sum
@@ -256,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
           for (int it = 0; it < 8; ++it) {
             const int R = it * 4 + (lane >> 3);
             const float4 p = reinterpret_cast<const float4*>(stg + R * 32)[c4 ^ (R & 7)];
-            float* dst = pmap + (static_cast<size_t>(h) * kB + quarter * 32 + R) * static_cast<size_t>(n) +
+            float* dst = pmap + (static_cast<size_t>(h) * kB + quarter * 32 + R) * static_cast<size_t>(ld) +
                          static_cast<size_t>(kb) * kB + col0 + c4 * 4;
             *reinterpret_cast<float4*>(dst) = p;
           }
@@ -270,39 +284,55 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
 #pragma unroll
           for (int i = 0; i < 8; ++i) t[i] = fmax3(xq[4 * i], xq[4 * i + 1], fmaxf(xq[4 * i + 2], xq[4 * i + 3]));
           const float mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
-          // Lower triangle r >= jj of the tile: this warp's rows are
-          // 32*quarter.., its columns col0..; both multiples of 32, so the
-          // chunk is wholly below (col0 < 32*quarter), wholly above, or on
-          // the diagonal (jj = col0 + e <= r iff e <= lane).
-          const bool on_diag = col0 == quarter * 32, below = col0 < quarter * 32;
+          // Slash bands of the tile (as the mass pass over the map sums
+          // them): band lo = entries with jj - r <= tail-128 (slash block
+          // nb-1-kb; the lower triangle when 128 | n), band hi = jj - r >
+          // tail (block nb-3-kb; empty when 128 | n), the rest block
+          // nb-2-kb. Here jj - r = D0 + e - lane with D0 = col0 - 32*quarter,
+          // so each band holds none, all or the e - lane side of a
+          // warp-uniform threshold.
+          const int D0 = col0 - quarter * 32;
+          const int th_lo = tail - kB - D0, th_hi = tail - D0;
+          const bool lo_all = th_lo >= 31, lo_part = !lo_all && th_lo >= -31;
+          const bool hi_all = kRagged && th_hi < -31, hi_part = kRagged && !hi_all && th_hi < 31;
           if (!__any_sync(0xffffffffu, mx >= kTwo23)) {
             // Every quantum below 2^23: the bits of xq + 2^23 minus those of
             // 2^23, with the 32 subtractions taken once at the end (mod 2^32;
             // the true sums stay below 2^28).
-            uint32_t a4[4] = {0u, 0u, 0u, 0u}, lo = 0;
+            uint32_t a4[4] = {0u, 0u, 0u, 0u}, lo = 0, hi = 0;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const uint32_t u = __float_as_uint(xq[e] + kTwo23);
               a4[e & 3] += u;
-              if (on_diag) lo += e <= lane ? u : 0x4B000000u;
+              if (lo_part) lo += e - lane <= th_lo ? u : 0x4B000000u;
+              if (hi_part) hi += e - lane > th_hi ? u : 0x4B000000u;
             }
             const uint32_t a = (a4[0] + a4[1]) + (a4[2] + a4[3]) - 32u * 0x4B000000u;
             all32 += a;
-            lo32 += on_diag ? lo - 32u * 0x4B000000u : (below ? a : 0u);
+            lo32 += lo_part ? lo - 32u * 0x4B000000u : (lo_all ? a : 0u);
+            hi32 += hi_part ? hi - 32u * 0x4B000000u : (hi_all ? a : 0u);
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const bool in_lower = r >= col0 + e;
+              const bool in_lo = e - lane <= th_lo, in_hi = kRagged && e - lane > th_hi;
               if (xq[e] < kTwo23) {
                 const uint32_t f = q32_small(xq[e]);
                 all32 += f;
-                lo32 += in_lower ? f : 0u;
+                lo32 += in_lo ? f : 0u;
+                hi32 += in_hi ? f : 0u;
               } else {
                 const uint64_t f = q32_large(xq[e]);
                 all64 += f;
-                lo64 += in_lower ? f : 0ull;
+                lo64 += in_lo ? f : 0ull;
+                hi64 += in_hi ? f : 0ull;
               }
             }
+          }
+          if (rec_tile) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (col0 + e >= tail)
+                rec64 += xq[e] < kTwo23 ? static_cast<uint64_t>(q32_small(xq[e])) : q32_large(xq[e]);
           }
         }
       }
@@ -311,25 +341,36 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
         // by shared-memory atomics into the slot of this tile's parity; the
         // last warp to add publishes the sums and clears the slot (before it
         // releases S, so the slot's next use, two tiles later, sees it clear).
-        unsigned long long all = all64 + all32, lo = lo64 + lo32;
+        unsigned long long all = all64 + all32, lo = lo64 + lo32, hi = hi64 + hi32, rc = rec64;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
           all += __shfl_xor_sync(0xffffffffu, all, o);
           lo += __shfl_xor_sync(0xffffffffu, lo, o);
+          if (kRagged) hi += __shfl_xor_sync(0xffffffffu, hi, o);
+        }
+        if (rec_tile) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) rc += __shfl_xor_sync(0xffffffffu, rc, o);
         }
         if (lane == 0) {
           atomicAdd(&tile_acc[b][0], all);
           atomicAdd(&tile_acc[b][1], lo);
+          if (kRagged) atomicAdd(&tile_acc[b][2], hi);
+          if (rec_tile) atomicAdd(&tile_acc[b][3], rc);
           __threadfence_block();
           if (atomicAdd(&tile_cnt[b], 1u) == kEpiWarps - 1) {
             __threadfence_block();
             const unsigned long long sa = atomicExch(&tile_acc[b][0], 0ull);
             const unsigned long long sl = atomicExch(&tile_acc[b][1], 0ull);
+            const unsigned long long sh = kRagged ? atomicExch(&tile_acc[b][2], 0ull) : 0ull;
+            const unsigned long long sr = atomicExch(&tile_acc[b][3], 0ull);
             atomicExch(&tile_cnt[b], 0u);
             const size_t idx = static_cast<size_t>(h) * nb + kb;
             vmass[idx] = sa;
             lower[idx] = sl;
-            upper[idx] = sa - sl;
+            upper[idx] = sa - sl - sh;
+            upper2[idx] = sh;
+            if (rec_tile) rec[h] = sr;
           }
         }
       }
@@ -369,12 +410,12 @@ static cudaError_t proxy_stats(const crisp_shape& s, const TmaMaps& maps, char* 
   auto* part = reinterpret_cast<float2*>(ws + L.proxy_part);
   auto* stats = reinterpret_cast<float2*>(ws + L.proxy_stats);
   auto* status = reinterpret_cast<DevStatus*>(ws + L.status);
-  cudaError_t e = cudaFuncSetAttribute(proxy_kernel<kStats>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           ProxyCfg<kStats>::kSmem);
+  auto* kern = tail_len(s.seq_len) == kB ? proxy_kernel<kStats, false> : proxy_kernel<kStats, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ProxyCfg<kStats>::kSmem);
   if (e != cudaSuccess) return e;
-  proxy_kernel<kStats><<<dim3(s.hq, chunks), kThreads, ProxyCfg<kStats>::kSmem, st>>>(
-      maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, nullptr, part, stats, nullptr, nullptr,
-      nullptr, status);
+  kern<<<dim3(s.hq, chunks), kThreads, ProxyCfg<kStats>::kSmem, st>>>(
+      maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, nullptr, 0, part, stats, nullptr,
+      nullptr, nullptr, nullptr, nullptr, status);
   const int rows = s.hq * kB;
   proxy_combine<<<(rows + 127) / 128, 128, 0, st>>>(part, stats, rows, 2 * chunks);
   return cudaGetLastError();
@@ -385,34 +426,34 @@ cudaError_t launch_proxy(const crisp_shape& s, const TmaMaps& maps, float* pmap,
   if (e != cudaSuccess) return e;
   const ScratchLayout L = scratch_layout(s);
   const int chunks = proxy_chunks(num_blocks(s.seq_len));
-  e = cudaFuncSetAttribute(proxy_kernel<kWriteMap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           ProxyCfg<kWriteMap>::kSmem);
+  auto* kern = tail_len(s.seq_len) == kB ? proxy_kernel<kWriteMap, false> : proxy_kernel<kWriteMap, true>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ProxyCfg<kWriteMap>::kSmem);
   if (e != cudaSuccess) return e;
-  proxy_kernel<kWriteMap><<<dim3(s.hq, chunks), kThreads, ProxyCfg<kWriteMap>::kSmem, st>>>(
-      maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, pmap,
+  kern<<<dim3(s.hq, chunks), kThreads, ProxyCfg<kWriteMap>::kSmem, st>>>(
+      maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, pmap, map_ld(s.seq_len),
       reinterpret_cast<float2*>(ws + L.proxy_part), reinterpret_cast<const float2*>(ws + L.proxy_stats), nullptr,
-      nullptr, nullptr, reinterpret_cast<DevStatus*>(ws + L.status));
+      nullptr, nullptr, nullptr, nullptr, reinterpret_cast<DevStatus*>(ws + L.status));
   return cudaGetLastError();
 }
 
-cudaError_t launch_proxy_masses(const crisp_shape& s, const TmaMaps& maps, uint64_t* vmass, uint64_t* smass, char* ws,
-                                cudaStream_t st) {
+cudaError_t launch_proxy_masses(const crisp_shape& s, const TmaMaps& maps, uint64_t* vmass, uint64_t* smass,
+                                uint64_t* rmass, char* ws, cudaStream_t st) {
   cudaError_t e = proxy_stats(s, maps, ws, st);
   if (e != cudaSuccess) return e;
   const ScratchLayout L = scratch_layout(s);
   const int chunks = proxy_chunks(num_blocks(s.seq_len));
-  auto* lower = reinterpret_cast<uint64_t*>(ws + L.mass_lower);
-  auto* upper = reinterpret_cast<uint64_t*>(ws + L.mass_upper);
-  e = cudaFuncSetAttribute(proxy_kernel<kMasses>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           ProxyCfg<kMasses>::kSmem);
+  auto* kern = tail_len(s.seq_len) == kB ? proxy_kernel<kMasses, false> : proxy_kernel<kMasses, true>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ProxyCfg<kMasses>::kSmem);
   if (e != cudaSuccess) return e;
-  proxy_kernel<kMasses><<<dim3(s.hq, chunks), kThreads, ProxyCfg<kMasses>::kSmem, st>>>(
-      maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, nullptr,
-      reinterpret_cast<float2*>(ws + L.proxy_part), reinterpret_cast<const float2*>(ws + L.proxy_stats), vmass, lower,
-      upper, reinterpret_cast<DevStatus*>(ws + L.status));
+  kern<<<dim3(s.hq, chunks), kThreads, ProxyCfg<kMasses>::kSmem, st>>>(
+      maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, nullptr, 0,
+      reinterpret_cast<float2*>(ws + L.proxy_part), reinterpret_cast<const float2*>(ws + L.proxy_stats), vmass,
+      reinterpret_cast<uint64_t*>(ws + L.mass_lower), reinterpret_cast<uint64_t*>(ws + L.mass_upper),
+      reinterpret_cast<uint64_t*>(ws + L.mass_upper2), reinterpret_cast<uint64_t*>(ws + L.mass_rec),
+      reinterpret_cast<DevStatus*>(ws + L.status));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_assemble_slash(s, lower, upper, smass, st);
+  return launch_assemble_slash(s, vmass, ws, smass, rmass, st);
 }
 
 }  // namespace crisp

@@ -34,7 +34,12 @@
  *    out) are recorded in the workspace status word; read it with
  *    crisp_read_status. No C++ exception crosses this boundary.
  *  - Fixed sizes: head_dim = 128, block = 128 tokens, batch 1 (a batch is a
- *    loop over calls). seq_len is a multiple of 128, 256 <= seq_len <= 2^20.
+ *    loop over calls). seq_len = n <= 2^20, any n: blocks are aligned at
+ *    token 0, nb = ceil(n/128), and when 128 does not divide n the last block
+ *    is short (n - 128*(nb-1) tokens). The method's steps (A1..A7) need
+ *    n >= 256 (the sink block and at least one more); attention, the whole
+ *    layer and the workspace sizes take any n >= 0, and n = 0 (an empty
+ *    input) launches nothing and returns CRISP_OK.
  *  - bf16 tensors are [heads][tokens][128] with element strides per head and
  *    per token (the 128 features contiguous). For the TMA copies every
  *    pointer must be 16-byte aligned and every stride a multiple of 8
@@ -140,11 +145,12 @@ CRISP_API crisp_status crisp_workspace_init(void* ws, size_t ws_bytes, crisp_str
 
 /* A1. Proxy attention map of the last query block (ai.info page, "Key
  * Contributions" 2 and "Methodology": routing reads the proxy attention map
- * the method already computes). For q-head h (kv head h/G) and the last
- * block's rows i = n-128+r, r in [0,128):
+ * the method already computes). For q-head h (kv head h/G) and the rows
+ * i = n-128+r, r in [0,128) (the last 128 tokens):
  *   pmap[h][r][j] = softmax_j(scale * q_i . k_j) over j <= i, and 0 for j > i.
  * q: bf16 [hq][n][128] (only the last 128 rows are read); k: bf16
- * [hkv][n][128]; pmap: fp32 [hq][128][n] contiguous, 16-byte aligned. */
+ * [hkv][n][128]; pmap: fp32 [hq][128][ld], ld = 128*nb (= n when 128
+ * divides n; columns n..ld-1 are written as 0), contiguous, 16-byte aligned. */
 CRISP_API crisp_status crisp_proxy_map(const crisp_shape* shape, const void* q, const void* k, float* pmap, void* ws,
                              size_t ws_bytes, crisp_stream_t stream);
 
@@ -173,36 +179,43 @@ CRISP_API crisp_status crisp_proxy_map_noalloc(const crisp_shape* shape, const v
                                                crisp_stream_t stream);
 
 /* A3. Block masses of the proxy map ("mass at Vertical-Slash compatible
- * positions", ai-feeds page, "方法"). With q(p) the Q32 quantum:
+ * positions", ai-feeds page, "方法"). With q(p) the Q32 quantum and row r
+ * standing for token i = n-128+r:
  *   vmass[h][c] = sum over rows r and key columns j of block c of q(pmap[h][r][j])
  *   smass[h][s] = sum over (r, j) with j <= i, j >= 128 and
  *                 floor((i - j)/128) == s of q(pmap[h][r][j])
+ *   rmass[h]    = sum over rows r and the recency columns j in [n-128, n)
+ *                 (= vmass[h][nb-1] when 128 divides n)
  * Sink columns (j < 128) are left out of the slash masses, so the sink cannot
- * raise the slash noise floor. pmap fp32 [hq][128][n]; vmass, smass: uint64
- * [hq][nb]. */
+ * raise the slash noise floor. pmap fp32 [hq][128][ld] as crisp_proxy_map
+ * writes it; vmass, smass: uint64 [hq][nb]; rmass: uint64 [hq]. */
 CRISP_API crisp_status crisp_block_masses(const crisp_shape* shape, const float* pmap, uint64_t* vmass, uint64_t* smass,
-                                void* ws, size_t ws_bytes, crisp_stream_t stream);
+                                uint64_t* rmass, void* ws, size_t ws_bytes, crisp_stream_t stream);
 
 /* A1 and A3 in one pass: the block masses of the proxy map, computed from q
  * and k without storing the map (routing and Vertical-Slash selection read
  * only these masses; ai.info page, "Key Contributions" 2; ai-feeds page,
  * "方法"). Each fp32 probability is formed exactly as crisp_proxy_map stores
  * it and quantised exactly as crisp_block_masses reads it, so vmass and
- * smass are bit-identical to crisp_block_masses(crisp_proxy_map(q, k)).
- * q, k as for crisp_proxy_map; vmass, smass uint64 [hq][nb], 8-byte aligned.
- * Saves the 4*hq*128*n-byte map write and its re-read. */
+ * smass (and rmass) are bit-identical to crisp_block_masses(crisp_proxy_map(q,
+ * k)). q, k as for crisp_proxy_map; vmass, smass uint64 [hq][nb], rmass
+ * uint64 [hq], 8-byte aligned. Saves the 4*hq*128*n-byte map write and its
+ * re-read. */
 CRISP_API crisp_status crisp_proxy_masses(const crisp_shape* shape, const void* q, const void* k, uint64_t* vmass,
-                                          uint64_t* smass, void* ws, size_t ws_bytes, crisp_stream_t stream);
+                                          uint64_t* smass, uint64_t* rmass, void* ws, size_t ws_bytes,
+                                          crisp_stream_t stream);
 
 /* A2. C_struct routing (ai.info page, "Key Contributions" 2: mass at the
- * first 128 and the last 128 tokens of the proxy map; tau_proxy = 0.2). With
- * B = 128 those slices are key blocks 0 and nb-1, so
- *   cstruct[h] = vmass[h][0] + vmass[h][nb-1],  total[h] = sum_c vmass[h][c],
+ * first 128 and the last 128 tokens of the proxy map; tau_proxy = 0.2). The
+ * first 128 tokens are key block 0, the last 128 the recency mass rmass
+ * (key block nb-1 when 128 divides n), disjoint for n >= 256:
+ *   cstruct[h] = vmass[h][0] + rmass[h],  total[h] = sum_c vmass[h][c],
  *   route[h]   = 1 (Vertical-Slash) iff tau_den * cstruct >= tau_num * total,
  *                0 (Pooled-Estimation) otherwise.
- * vmass uint64 [hq][nb]; cstruct, total uint64 [hq]; route uint8 [hq]. */
+ * vmass uint64 [hq][nb]; rmass, cstruct, total uint64 [hq]; route uint8 [hq]. */
 CRISP_API crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
-                                 uint64_t* cstruct, uint64_t* total, uint8_t* route, crisp_stream_t stream);
+                                           const uint64_t* rmass, uint64_t* cstruct, uint64_t* total, uint8_t* route,
+                                           crisp_stream_t stream);
 
 /* A2 comparator: FlexPrefill's routing, which CRISP replaces (ai.info page,
  * "Methodology in Plain English": a pooled attention estimate compared with
@@ -236,7 +249,7 @@ CRISP_API crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_par
 
 /* A5. Pooled attention estimate for PE heads (the Pooled-Estimation route
  * CRISP keeps from FlexPrefill; ai.info page, "Overview"): block means of q
- * and k, pbar[h][b][c] = softmax over c <= b of scale * qbar_b . kbar_c, and 0
+ * and k (a short last block averaged over its own tokens), pbar[h][b][c] = softmax over c <= b of scale * qbar_b . kbar_c, and 0
  * for c > b. Rows of VS heads are not written. q, k bf16; pbar fp32
  * [hq][nb][nb], 16-byte aligned. */
 CRISP_API crisp_status crisp_pe_map(const crisp_shape* shape, const void* q, const void* k, const uint8_t* route, float* pbar,
@@ -276,7 +289,7 @@ CRISP_API crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t*
  *   out_i = sum_{j in A(i)} softmax_j(scale * q_i . k_j) v_j,
  *   A(i) = { j <= i : block(j) in rowbits[h][qb] }.
  * Bits above the diagonal block are ignored; rows with an empty A(i) are
- * written as zeros. q bf16 [hq][n][128]; k, v bf16 [hkv][n][128]; rowbits
+ * written as zeros; only rows i < n are written. q bf16 [hq][n][128]; k, v bf16 [hkv][n][128]; rowbits
  * from crisp_build_mask; order: the schedule from crisp_build_mask, or NULL
  * for query blocks in descending order (any permutation of the row ids gives
  * the same result); out bf16 [hq][n][128] (o strides). */
@@ -291,7 +304,7 @@ CRISP_API crisp_status crisp_dense_prefill(const crisp_shape* shape, const void*
 
 /* Device views of the intermediates crisp_prefill_layer leaves in `ws`. */
 typedef struct crisp_layer_views {
-  uint64_t *vmass, *smass, *cstruct, *total;
+  uint64_t *vmass, *smass, *rmass, *cstruct, *total;
   uint8_t* route;
   uint32_t *vbits, *sbits;
   float* pbar;
@@ -306,8 +319,10 @@ CRISP_API crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws,
  * the map itself is never stored), routing, VS and PE selection, mask,
  * sparse attention. ws must hold crisp_layer_workspace_size bytes. With
  * route_mode = CRISP_ROUTE_JSD the pooled map is computed for every head and
- * routing is crisp_route_jsd. If seq_len < params->dense_below the layer is
- * dense attention only and the workspace intermediates are not written. */
+ * routing is crisp_route_jsd. If seq_len < params->dense_below, or
+ * seq_len < 256 (too short for the method, and every block would be kept
+ * anyway), the layer is dense attention only and the workspace
+ * intermediates are not written. seq_len = 0 launches nothing. */
 CRISP_API crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* params, const void* q, const void* k,
                                  const void* v, void* out, void* ws, size_t ws_bytes, crisp_stream_t stream);
 

@@ -38,7 +38,7 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
     as all-ones words so that an entry it fails to write shows."""
     hq, n, _ = q.shape
     hkv = k.shape[0]
-    nb = n // B
+    nb = crisp.num_blocks(n)
     W = (nb + 31) // 32
     qd = to_dev(q) if q_dev is None else q_dev
     kd = to_dev(k) if k_dev is None else k_dev
@@ -46,9 +46,10 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
     out = empty((hq, n, 128), torch.bfloat16)
     s = crisp.make_shape(hq, hkv, n, qd, kd, out)
     ws = new_workspace(s)
-    pmap = empty((hq, B, n), torch.float32)
+    pmap = torch.full((hq, B, crisp.map_ld(n)), float("nan"), dtype=torch.float32, device="cuda")
     vmass = empty((hq, nb), torch.int64)
     smass = empty((hq, nb), torch.int64)
+    rmass = empty((hq,), torch.int64)
     cstruct = empty((hq,), torch.int64)
     total = empty((hq,), torch.int64)
     route = empty((hq,), torch.uint8)
@@ -61,10 +62,11 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
     order = empty((hq * nb,), torch.int32)
     vmass_f = torch.full((hq, nb), -1, dtype=torch.int64, device="cuda")
     smass_f = torch.full((hq, nb), -1, dtype=torch.int64, device="cuda")
-    crisp.proxy_masses(s, qd, kd, vmass_f, smass_f, ws)
+    rmass_f = torch.full((hq,), -1, dtype=torch.int64, device="cuda")
+    crisp.proxy_masses(s, qd, kd, vmass_f, smass_f, rmass_f, ws)
     crisp.proxy_map(s, qd, kd, pmap, ws)
-    crisp.block_masses(s, pmap, vmass, smass, ws)
-    crisp.route_cstruct(s, params, vmass, cstruct, total, route)
+    crisp.block_masses(s, pmap, vmass, smass, rmass, ws)
+    crisp.route_cstruct(s, params, vmass, rmass, cstruct, total, route)
     crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws)
     crisp.pe_map(s, qd, kd, route, pbar, ws)
     crisp.select_pe(s, params, pbar, route, pebits, ws)
@@ -74,8 +76,12 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
     assert_status_ok(ws)
     u64 = lambda t: t.cpu().numpy().view(np.uint64)
     u32 = lambda t: t.cpu().numpy().view(np.uint32)
-    return dict(pmap=pmap.cpu().numpy(), vmass=u64(vmass), smass=u64(smass), vmass_fused=u64(vmass_f),
-                smass_fused=u64(smass_f), cstruct=u64(cstruct), total=u64(total),
+    pm = pmap.cpu().numpy()
+    # columns n..ld-1 of the map are written as zeros; the oracle's map has n columns
+    assert np.all(pm[:, :, n:] == 0.0)
+    return dict(pmap=np.ascontiguousarray(pm[:, :, :n]), vmass=u64(vmass), smass=u64(smass), rmass=u64(rmass),
+                vmass_fused=u64(vmass_f), smass_fused=u64(smass_f), rmass_fused=u64(rmass_f),
+                cstruct=u64(cstruct), total=u64(total),
                 route=route.cpu().numpy(), vbits=u32(vbits), sbits=u32(sbits), pbar=pbar.cpu().numpy(),
                 pebits=u32(pebits), rowbits=u32(rowbits), counts=counts.cpu().numpy(), order=order.cpu().numpy(),
                 out=out)

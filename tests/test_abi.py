@@ -72,8 +72,8 @@ def test_workspace_sizes(L):
 
 
 @pytest.mark.parametrize("field,value,code", [
-    ("hq", 6, 2), ("hkv", 0, 2), ("head_dim", 64, 2), ("block", 64, 2), ("seq_len", 200, 2),
-    ("seq_len", 128, 2), ("seq_len", (1 << 20) + 128, 2), ("q_tok_stride", 100, 3), ("kv_head_stride", 0, 3),
+    ("hq", 6, 2), ("hkv", 0, 2), ("head_dim", 64, 2), ("block", 64, 2), ("seq_len", -1, 2),
+    ("seq_len", (1 << 20) + 128, 2), ("q_tok_stride", 100, 3), ("kv_head_stride", 0, 3),
     ("scale", float("nan"), 1), ("scale", -1.0, 1)])
 def test_shape_validation(L, field, value, code):
     s = crisp.make_shape(8, 4, 1024)
@@ -96,7 +96,7 @@ def test_params_validation(L, field, value):
     p = crisp.params_default()
     setattr(p, field, value)
     rc = L.crisp_route_cstruct(ctypes.byref(s), ctypes.byref(p), ctypes.c_void_p(256), ctypes.c_void_p(256),
-                               ctypes.c_void_p(256), ctypes.c_void_p(256), None)
+                               ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256), None)
     assert rc == 1
 
 
@@ -109,9 +109,18 @@ def test_null_and_misaligned_pointers(L):
                                   None) == 1
     assert L.crisp_sparse_prefill(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(18), vp(16), vp(256), 1 << 30,
                                   None) == 3
-    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), None, vp(16), vp(256), 1 << 30, None) == 1
-    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(20), vp(256), 1 << 30, None) == 3
-    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(256), 64, None) == 4
+    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), None, vp(16), vp(16), vp(256), 1 << 30, None) == 1
+    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), None, vp(256), 1 << 30, None) == 1
+    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(20), vp(16), vp(256), 1 << 30,
+                                None) == 3
+    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(20), vp(256), 1 << 30,
+                                None) == 3
+    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(16), vp(256), 64, None) == 4
+    assert L.crisp_block_masses(ctypes.byref(s), vp(16), vp(16), vp(16), None, vp(256), 1 << 30, None) == 1
+    assert L.crisp_route_cstruct(ctypes.byref(s), ctypes.byref(crisp.params_default()), vp(256), None, vp(256),
+                                 vp(256), vp(256), None) == 1
+    assert L.crisp_route_cstruct(ctypes.byref(s), ctypes.byref(crisp.params_default()), vp(256), vp(260), vp(256),
+                                 vp(256), vp(256), None) == 3
     # divergence routing and fused masses: argument errors before any CUDA call
     pd = ctypes.byref(crisp.params_default())
     assert L.crisp_route_jsd(ctypes.byref(s), pd, None, vp(256), None, vp(256), None) == 1
@@ -134,6 +143,45 @@ def test_null_and_misaligned_pointers(L):
     assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), vp(256), 64, None) == 4
     assert L.crisp_prefill_layer(ctypes.byref(s), ctypes.byref(crisp.params_default()), vp(16), vp(16), vp(16),
                                  vp(16), vp(256), 1024, None) == 4
+
+
+@pytest.mark.parametrize("n", [300, 1000, 2049, 524287])
+def test_ragged_lengths_are_accepted(L, n):
+    # 128 need not divide n: every step passes the shape check (and then
+    # stops at its first pointer check, before any CUDA call)
+    s = crisp.make_shape(8, 4, n)
+    size = ctypes.c_size_t()
+    assert L.crisp_workspace_size(ctypes.byref(s), ctypes.byref(size)) == 0
+    nb = -(-n // 128)
+    assert size.value >= 8 * nb * 8  # per-tile mass scratch of every head
+    assert L.crisp_proxy_map(ctypes.byref(s), None, ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(256),
+                             1 << 30, None) == 1
+    assert L.crisp_proxy_masses(ctypes.byref(s), ctypes.c_void_p(16), ctypes.c_void_p(16), None, ctypes.c_void_p(16),
+                                ctypes.c_void_p(16), ctypes.c_void_p(256), 1 << 30, None) == 1
+
+
+@pytest.mark.parametrize("n", [0, 1, 100, 128, 255])
+def test_short_and_empty_lengths(L, n):
+    # The method's steps need two blocks; attention and the layer take any n,
+    # and an empty input (n = 0) returns OK without launching anything.
+    s = crisp.make_shape(8, 4, n)
+    size = ctypes.c_size_t()
+    assert L.crisp_workspace_size(ctypes.byref(s), ctypes.byref(size)) == 0
+    assert L.crisp_layer_workspace_size(ctypes.byref(s), ctypes.byref(size)) == 0
+    vp = ctypes.c_void_p
+    assert L.crisp_proxy_map(ctypes.byref(s), vp(16), vp(16), vp(16), vp(256), 1 << 30, None) == 2
+    assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(16), vp(256), 1 << 30, None) == 2
+    p = ctypes.byref(crisp.params_default())
+    if n == 0:
+        # nothing to compute: OK with null buffers and no device
+        assert L.crisp_prefill_layer(ctypes.byref(s), p, None, None, None, None, None, 0, None) == 0
+        assert L.crisp_dense_prefill(ctypes.byref(s), None, None, None, None, None, 0, None) == 0
+        assert L.crisp_sparse_prefill(ctypes.byref(s), None, None, None, None, None, None, None, 0, None) == 0
+        assert L.crisp_prefill_layer_host(vp(256), ctypes.byref(s), p, *([None] * 9), 0, None) == 0
+    else:
+        # past the shape check: the first pointer check answers
+        assert L.crisp_dense_prefill(ctypes.byref(s), None, vp(16), vp(16), vp(16), vp(256), 1 << 30, None) == 1
+        assert L.crisp_prefill_layer(ctypes.byref(s), p, None, vp(16), vp(16), vp(16), vp(256), 1 << 30, None) == 1
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -63,4 +63,6 @@ def test_selected_pairs_counts_the_causal_half_of_the_diagonal():
     rb[0, 0, 0] = 0b001  # diagonal only
     rb[0, 1, 0] = 0b011  # one off-diagonal + diagonal
     rb[0, 2, 0] = 0b001  # one off-diagonal, no diagonal
-    assert bench.selected_pairs(rb, nb) == 2 * (128 * 129 // 2) + 2 * 128 * 128
+    assert bench.selected_pairs(rb, nb * 128) == 2 * (128 * 129 // 2) + 2 * 128 * 128
+    # a short last block (n = 300: 44 tokens): its row counts 44 query rows
+    assert bench.selected_pairs(rb, 300) == 2 * (128 * 129 // 2) + 128 * 128 + 44 * 128

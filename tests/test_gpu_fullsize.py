@@ -52,7 +52,7 @@ def _check_layer(w, index, params=None):
     ph, pr = _proxy_samples(w.hq, seed)
     check_map(r["pmap"][ph, pr], oracle.proxy_rows(q, k, ph, pr))
     rb, route = check_index_sets(r, params)
-    nb = w.n // B
+    nb = crisp.num_blocks(w.n)
     if (route == 0).any():
         eh, eb = _pe_samples(route, nb, seed)
         check_map(r["pbar"][eh, eb], oracle.pe_rows(q, k, eh, eb))
@@ -94,6 +94,14 @@ def test_max_length_one_million_tokens():
     w = synth.small("max-1m", 4, 1, 1 << 20, 77, d_sink=12.0)  # sink strong enough to dominate 1M keys
     route = _check_layer(w, 77)
     assert route.tolist() == [1, 0, 1, 0]
+
+
+def test_ragged_long_sequence():
+    # 128k + 77 tokens: a short last block of 77 keys, the proxy rows spread
+    # over blocks 1024 and 1025, recency columns in two proxy CTAs' tiles.
+    w = synth.small("ragged-128k", 8, 2, 131072 + 77, 78, d_sink=8.0)  # sink strong enough for 128k keys
+    route = _check_layer(w, 78)
+    assert route.any() and not route.all()  # both routes
 
 
 def test_cfg5_512k_dense_sampled_rows():

@@ -36,8 +36,11 @@ def check_index_sets(r, params):
     # the fused pass that never stores the map gives the same integers
     assert np.array_equal(vm, r["vmass_fused"])
     assert np.array_equal(sm, r["smass_fused"])
+    assert np.array_equal(r["rmass"], r["rmass_fused"])
     S, T, route = oracle.route(r["pmap"], tau=(params.tau_num, params.tau_den))
     assert np.array_equal(S, r["cstruct"]) and np.array_equal(T, r["total"])
+    # recency mass: the columns [n-128, n) (C_struct less the sink block)
+    assert np.array_equal(r["rmass"], S - vm[:, 0])
     assert np.array_equal(route, r["route"])
     vb, sb = oracle.select_vs(vm, sm, route, alpha=(params.alpha_num, params.alpha_den), kmin=params.kmin_blocks)
     assert np.array_equal(vb, r["vbits"])
@@ -92,6 +95,13 @@ CASES = [
     ("gqa7-1152", 7, 1, 1152, 6, [0, 3, 6]),
     ("nb33-4224", 4, 2, 4224, 7, None),
     ("all-pe-2k", 4, 2, 2048, 8, []),
+    # 128 does not divide n: a short last block of t tokens (t = 44, 104, 1,
+    # 127, 4); at 2049 the recency columns straddle two proxy CTAs
+    ("ragged-300", 2, 1, 300, 31, None),
+    ("ragged-1000", 4, 2, 1000, 32, None),
+    ("ragged-2049", 4, 1, 2049, 33, [0]),
+    ("ragged-2175", 4, 2, 2175, 34, None),
+    ("ragged-4100", 8, 2, 4100, 35, None),
 ]
 
 
@@ -124,7 +134,8 @@ def test_parameter_variants(overrides):
 
 
 def test_dense_prefill_matches_oracle():
-    for hq, hkv, n, seed in ((4, 1, 1024, 21), (6, 2, 640, 22), (2, 2, 256, 23)):
+    for hq, hkv, n, seed in ((4, 1, 1024, 21), (6, 2, 640, 22), (2, 2, 256, 23), (2, 1, 1, 24), (4, 2, 100, 25),
+                             (2, 1, 129, 26), (4, 2, 777, 27)):
         w = synth.small("dense", hq, hkv, n, seed)
         q, k, v = w.generate()
         qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
@@ -198,7 +209,7 @@ def test_strided_token_major_layout():
 
 
 def test_prefill_layer_matches_steps():
-    for hq, hkv, n, seed in ((8, 2, 2048, 51), (4, 1, 640, 52)):
+    for hq, hkv, n, seed in ((8, 2, 2048, 51), (4, 1, 640, 52), (4, 2, 1337, 53)):
         w = synth.small("layer", hq, hkv, n, seed)
         q, k, v = w.generate()
         params = crisp.params_default()
@@ -211,7 +222,8 @@ def test_prefill_layer_matches_steps():
         torch.cuda.synchronize()
         assert_status_ok(ws)
         views = crisp.layer_views(s, ws)
-        nb, W = n // B, (n // B + 31) // 32
+        nb = crisp.num_blocks(n)
+        W = (nb + 31) // 32
 
         def grab(name, shape, dtype):
             t = torch.empty(shape, dtype=dtype, device="cuda")
@@ -223,6 +235,7 @@ def test_prefill_layer_matches_steps():
 
         assert np.array_equal(grab("vmass", (hq, nb), torch.int64).view(np.uint64), steps["vmass"])
         assert np.array_equal(grab("smass", (hq, nb), torch.int64).view(np.uint64), steps["smass"])
+        assert np.array_equal(grab("rmass", (hq,), torch.int64).view(np.uint64), steps["rmass"])
         assert np.array_equal(grab("route", (hq,), torch.uint8), steps["route"])
         assert np.array_equal(grab("rowbits", (hq, nb, W), torch.int32).view(np.uint32), steps["rowbits"])
         assert torch.equal(out, steps["out"])
@@ -233,7 +246,8 @@ def test_prefill_layer_host_matches_device_layer():
     # overlapped: bit-identical to the device-resident layer.
     pipe = crisp.HostPipeline()
     # 128k tokens with an even group size: half-group chunks
-    for hq, hkv, n, seed in ((8, 2, 2048, 71), (7, 1, 1152, 72), (4, 4, 640, 73), (4, 2, 131072, 74)):
+    for hq, hkv, n, seed in ((8, 2, 2048, 71), (7, 1, 1152, 72), (4, 4, 640, 73), (4, 2, 131072, 74),
+                             (4, 2, 1001, 75), (2, 1, 200, 76)):
         w = synth.small("host", hq, hkv, n, seed)
         q, k, v = w.generate()
         params = crisp.params_default()
@@ -288,19 +302,21 @@ def run_comparator_steps(q, k, v, params):
     A4..A8 as in the layer; returns numpy copies and the output."""
     hq, n, _ = q.shape
     hkv = k.shape[0]
-    nb, W = n // B, (n // B + 31) // 32
+    nb = crisp.num_blocks(n)
+    W = (nb + 31) // 32
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
     out = empty((hq, n, 128), torch.bfloat16)
     s = crisp.make_shape(hq, hkv, n, qd, kd, out)
     ws = new_workspace(s)
     vmass, smass = empty((hq, nb), torch.int64), empty((hq, nb), torch.int64)
+    rmass = empty((hq,), torch.int64)
     route = torch.zeros((hq,), dtype=torch.uint8, device="cuda")
     jsd = empty((hq,), torch.float64)
     vbits, sbits = empty((hq, W), torch.int32), empty((hq, W), torch.int32)
     pbar = torch.zeros((hq, nb, nb), dtype=torch.float32, device="cuda")
     pebits, rowbits = empty((hq, nb, W), torch.int32), empty((hq, nb, W), torch.int32)
     counts, order = empty((hq, nb), torch.int32), empty((hq * nb,), torch.int32)
-    crisp.proxy_masses(s, qd, kd, vmass, smass, ws)
+    crisp.proxy_masses(s, qd, kd, vmass, smass, rmass, ws)
     crisp.pe_map(s, qd, kd, route, pbar, ws)  # route all zeros: every head's pooled map
     crisp.route_jsd(s, params, vmass, pbar, jsd, route)
     crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws)
@@ -322,6 +338,7 @@ COMPARATOR_CASES = [
     ("gqa4-4k-t01", 4, 1, 4096, 9, 0.1, (95, 100)),
     ("gqa7-1152-t02", 7, 1, 1152, 6, 0.2, (97, 100)),
     ("nb33-4224-t03", 4, 2, 4224, 7, 0.3, (9, 10)),
+    ("ragged-2100-t02", 4, 2, 2100, 36, 0.2, (95, 100)),
 ]
 
 
@@ -331,7 +348,7 @@ def test_flexprefill_comparators_match_oracle(name, hq, hkv, n, seed, tau, vg):
     q, k, v = w.generate()
     params = crisp.params_default(route_mode=crisp.ROUTE_JSD, vs_mode=crisp.VS_GAMMA, jsd_tau=tau, vs_gamma=vg)
     r = run_comparator_steps(q, k, v, params)
-    nb = n // B
+    nb = crisp.num_blocks(n)
     # masses as in the CRISP path (the fused pass is checked elsewhere)
     ref_map = run_steps(q, k, v, crisp.params_default())
     assert np.array_equal(r["vmass"], ref_map["vmass"]) and np.array_equal(r["smass"], ref_map["smass"])
@@ -384,6 +401,28 @@ def test_length_gate_runs_dense():
     crisp.prefill_layer(s, crisp.params_default(dense_below=n), qd, kd, vd, out, ws)  # not below: sparse
     torch.cuda.synchronize()
     assert not torch.equal(out, ref)
+
+
+def test_short_and_empty_layers():
+    # n = 0 launches nothing; below two blocks the layer is dense attention
+    # (bit-identical to crisp_dense_prefill); a ragged short layer too.
+    params = crisp.params_default()
+    for hq, hkv, n, seed in ((4, 2, 0, 0), (4, 2, 1, 93), (2, 1, 100, 94), (4, 1, 200, 95)):
+        qd = torch.randn((hq, n, 128), device="cuda").to(torch.bfloat16)
+        kd = torch.randn((hkv, n, 128), device="cuda").to(torch.bfloat16)
+        vd = torch.randn((hkv, n, 128), device="cuda").to(torch.bfloat16)
+        out = torch.full((hq, n, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+        ref = empty((hq, n, 128), torch.bfloat16)
+        s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+        ws = new_workspace(s, layer=True)
+        crisp.prefill_layer(s, params, qd, kd, vd, out, ws)
+        crisp.dense_prefill(s, qd, kd, vd, ref, ws)
+        torch.cuda.synchronize()
+        assert_status_ok(ws)
+        assert torch.equal(out, ref)
+        if n:
+            q, k, v = (bf16_to_u16(t) for t in (qd, kd, vd))
+            check_attention(q, k, v, out, None)
 
 
 def test_attention_is_deterministic_under_load():
