@@ -579,9 +579,11 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
   // The layer in chunks of query heads within a kv group, the group's K and
   // V uploaded with its first chunk: the upload of chunk c+1 and the
   // download of chunk c-1 overlap the compute of chunk c. Long sequences use
-  // half a group per chunk (when G is even), so that the pipeline fills and
-  // drains with half a group; shorter ones a whole group, where the extra
-  // launches and copies would cost more than the shorter fill.
+  // half a group per chunk (when G is even), and the first and last half
+  // groups of the layer go one head at a time, so that the pipeline fills
+  // and drains with a single head; shorter ones a whole group per chunk,
+  // where the extra launches and copies would cost more than the shorter
+  // fill.
   const int G = s.hq / s.hkv;
   const int hc = (G % 2 == 0 && s.seq_len >= kHalfGroupChunkLen) ? G / 2 : G;  // query heads per chunk
   const size_t plane = static_cast<size_t>(s.seq_len) * kD * 2;  // bytes of one head
@@ -596,24 +598,28 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
   if (cudaEventRecord(p->start, cs) != cudaSuccess || cudaStreamWaitEvent(p->in, p->start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(p->out, p->start, 0) != cudaSuccess)
     return CRISP_ERR_CUDA;
-  const int chunks = s.hq / hc;
-  for (int c = 0; c < chunks; ++c) {
+  const bool split_ends = hc > 1 && s.seq_len >= kHalfGroupChunkLen;
+  int c = 0;
+  for (int h0 = 0; h0 < s.hq; ++c) {
+    const int size = (split_ends && (h0 < hc || h0 >= s.hq - hc)) ? 1 : hc;  // heads in this chunk
+    sub.hq = size;
     const int e = c % crisp_host_pipeline::kRing;
-    const int g = (c * hc) / G;  // the chunk's kv group
-    const size_t kv_off = static_cast<size_t>(g) * plane, q_off = static_cast<size_t>(c) * hc * plane;
-    if (c * hc % G == 0 &&
+    const int g = h0 / G;  // the chunk's kv group
+    const size_t kv_off = static_cast<size_t>(g) * plane, q_off = static_cast<size_t>(h0) * plane;
+    if (h0 % G == 0 &&
         (cudaMemcpyAsync(mb(k, kv_off), cb(k_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
          cudaMemcpyAsync(mb(v, kv_off), cb(v_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess))
       return CRISP_ERR_CUDA;
-    if (cudaMemcpyAsync(mb(q, q_off), cb(q_host, q_off), hc * plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+    if (cudaMemcpyAsync(mb(q, q_off), cb(q_host, q_off), size * plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
         cudaEventRecord(p->ev_in[e], p->in) != cudaSuccess || cudaStreamWaitEvent(cs, p->ev_in[e], 0) != cudaSuccess)
       return CRISP_ERR_CUDA;
     if ((st = run_layer(sub, *params, mb(q, q_off), mb(k, kv_off), mb(v, kv_off), mb(out, q_off), ws, cs)) !=
         CRISP_OK)
       return st;
     if (cudaEventRecord(p->ev_comp[e], cs) != cudaSuccess || cudaStreamWaitEvent(p->out, p->ev_comp[e], 0) != cudaSuccess ||
-        cudaMemcpyAsync(mb(out_host, q_off), cb(out, q_off), hc * plane, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
+        cudaMemcpyAsync(mb(out_host, q_off), cb(out, q_off), size * plane, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
       return CRISP_ERR_CUDA;
+    h0 += size;
   }
   // `stream` completes after the last download.
   if (cudaEventRecord(p->done, p->out) != cudaSuccess || cudaStreamWaitEvent(cs, p->done, 0) != cudaSuccess)

@@ -245,8 +245,8 @@ def test_prefill_layer_host_matches_device_layer():
     # Host buffers in, host buffer out, one kv group at a time with the copies
     # overlapped: bit-identical to the device-resident layer.
     pipe = crisp.HostPipeline()
-    # 128k tokens with an even group size: half-group chunks
-    for hq, hkv, n, seed in ((8, 2, 2048, 71), (7, 1, 1152, 72), (4, 4, 640, 73), (4, 2, 131072, 74),
+    # 128k tokens with group size 4: half-group chunks, single heads at both ends
+    for hq, hkv, n, seed in ((8, 2, 2048, 71), (7, 1, 1152, 72), (4, 4, 640, 73), (8, 2, 131072, 74),
                              (4, 2, 1001, 75), (2, 1, 200, 76)):
         w = synth.small("host", hq, hkv, n, seed)
         q, k, v = w.generate()
