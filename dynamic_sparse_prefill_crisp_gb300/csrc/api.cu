@@ -493,8 +493,8 @@ constexpr int kHalfGroupChunkLen = 131072;
 struct crisp_host_pipeline {
   static constexpr int kRing = 4;  // events are reused round-robin across kv groups
   int device;
-  cudaStream_t in, out;
-  cudaEvent_t start, done;
+  cudaStream_t in, out, comp;  // comp: the second compute stream
+  cudaEvent_t start, done, comp_done;
   cudaEvent_t ev_in[kRing], ev_comp[kRing];
 };
 
@@ -526,8 +526,10 @@ crisp_status crisp_host_pipeline_create(crisp_host_pipeline** pipeline) {
   bool ok = cudaGetDevice(&p->device) == cudaSuccess &&
             cudaStreamCreateWithFlags(&p->in, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&p->out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->comp, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&p->start, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming) == cudaSuccess;
+            cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&p->comp_done, cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; ok && i < crisp_host_pipeline::kRing; ++i)
     ok = cudaEventCreateWithFlags(&p->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
          cudaEventCreateWithFlags(&p->ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
@@ -544,17 +546,37 @@ crisp_status crisp_host_pipeline_destroy(crisp_host_pipeline* p) {
   // Objects never created are null handles; destroying those is skipped.
   if (p->in) cudaStreamSynchronize(p->in);
   if (p->out) cudaStreamSynchronize(p->out);
+  if (p->comp) cudaStreamSynchronize(p->comp);
   for (int i = 0; i < crisp_host_pipeline::kRing; ++i) {
     if (p->ev_in[i]) cudaEventDestroy(p->ev_in[i]);
     if (p->ev_comp[i]) cudaEventDestroy(p->ev_comp[i]);
   }
   if (p->start) cudaEventDestroy(p->start);
   if (p->done) cudaEventDestroy(p->done);
+  if (p->comp_done) cudaEventDestroy(p->comp_done);
+  if (p->comp) cudaStreamDestroy(p->comp);
   if (p->in) cudaStreamDestroy(p->in);
   if (p->out) cudaStreamDestroy(p->out);
   delete p;
   return CRISP_OK;
 }
+
+}  // extern "C"
+
+namespace crisp {
+namespace {
+// The second sub-workspace's status word folded into the caller's (the
+// first error stays).
+__global__ void merge_status_kernel(DevStatus* dst, const DevStatus* src) {
+  if (dst->code == 0 && src->code != 0) {
+    dst->detail = src->detail;
+    dst->code = src->code;
+  }
+}
+}  // namespace
+}  // namespace crisp
+
+extern "C" {
 
 crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp_shape* shape,
                                       const crisp_params* params, const void* q_host, const void* k_host,
@@ -578,7 +600,10 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
 
   // The layer in chunks of query heads within a kv group, the group's K and
   // V uploaded with its first chunk: the upload of chunk c+1 and the
-  // download of chunk c-1 overlap the compute of chunk c. Long sequences use
+  // download of chunk c-1 overlap the compute of chunk c, and consecutive
+  // chunks alternate between two compute streams (each with its own part of
+  // the workspace), so that one chunk's short selection kernels run beside
+  // the previous chunk's attention. Long sequences use
   // half a group per chunk (when G is even), and the first and last half
   // groups of the layer go one head at a time, so that the pipeline fills
   // and drains with a single head; shorter ones a whole group per chunk,
@@ -594,9 +619,16 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
   cudaStream_t cs = stream;
   auto cb = [](const void* b, size_t off) { return static_cast<const char*>(b) + off; };
   auto mb = [](void* b, size_t off) { return static_cast<char*>(b) + off; };
+  // Two compute streams, each with its own part of the workspace, when it
+  // holds two chunks' intermediates and there are several chunks.
+  const size_t sub_bytes = up(layer_layout(sub).total);
+  const bool dual = hc < s.hq && 2 * sub_bytes <= ws_bytes;
+  void* ws1 = static_cast<char*>(ws) + sub_bytes;
   // Work already on `stream` (earlier users of these buffers) comes first.
   if (cudaEventRecord(p->start, cs) != cudaSuccess || cudaStreamWaitEvent(p->in, p->start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(p->out, p->start, 0) != cudaSuccess)
+      cudaStreamWaitEvent(p->out, p->start, 0) != cudaSuccess ||
+      (dual && (cudaStreamWaitEvent(p->comp, p->start, 0) != cudaSuccess ||
+                cudaMemsetAsync(ws1, 0, sizeof(DevStatus), p->comp) != cudaSuccess)))
     return CRISP_ERR_CUDA;
   const bool split_ends = hc > 1 && s.seq_len >= kHalfGroupChunkLen;
   int c = 0;
@@ -610,18 +642,27 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
         (cudaMemcpyAsync(mb(k, kv_off), cb(k_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
          cudaMemcpyAsync(mb(v, kv_off), cb(v_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess))
       return CRISP_ERR_CUDA;
+    cudaStream_t sc = (dual && (c & 1)) ? p->comp : cs;
+    void* wsc = (dual && (c & 1)) ? ws1 : ws;
     if (cudaMemcpyAsync(mb(q, q_off), cb(q_host, q_off), size * plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
-        cudaEventRecord(p->ev_in[e], p->in) != cudaSuccess || cudaStreamWaitEvent(cs, p->ev_in[e], 0) != cudaSuccess)
+        cudaEventRecord(p->ev_in[e], p->in) != cudaSuccess || cudaStreamWaitEvent(sc, p->ev_in[e], 0) != cudaSuccess)
       return CRISP_ERR_CUDA;
-    if ((st = run_layer(sub, *params, mb(q, q_off), mb(k, kv_off), mb(v, kv_off), mb(out, q_off), ws, cs)) !=
+    if ((st = run_layer(sub, *params, mb(q, q_off), mb(k, kv_off), mb(v, kv_off), mb(out, q_off), wsc, sc)) !=
         CRISP_OK)
       return st;
-    if (cudaEventRecord(p->ev_comp[e], cs) != cudaSuccess || cudaStreamWaitEvent(p->out, p->ev_comp[e], 0) != cudaSuccess ||
+    if (cudaEventRecord(p->ev_comp[e], sc) != cudaSuccess || cudaStreamWaitEvent(p->out, p->ev_comp[e], 0) != cudaSuccess ||
         cudaMemcpyAsync(mb(out_host, q_off), cb(out, q_off), size * plane, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
       return CRISP_ERR_CUDA;
     h0 += size;
   }
-  // `stream` completes after the last download.
+  // `stream` completes after the last download, with the second compute
+  // stream's status folded into the caller's.
+  if (dual) {
+    if (cudaEventRecord(p->comp_done, p->comp) != cudaSuccess || cudaStreamWaitEvent(cs, p->comp_done, 0) != cudaSuccess)
+      return CRISP_ERR_CUDA;
+    merge_status_kernel<<<1, 1, 0, cs>>>(static_cast<DevStatus*>(ws), static_cast<const DevStatus*>(ws1));
+    if (cudaGetLastError() != cudaSuccess) return CRISP_ERR_CUDA;
+  }
   if (cudaEventRecord(p->done, p->out) != cudaSuccess || cudaStreamWaitEvent(cs, p->done, 0) != cudaSuccess)
     return CRISP_ERR_CUDA;
   return CRISP_OK;

@@ -26,7 +26,7 @@
  *  - Pointers are DEVICE pointers unless marked "host". The caller owns and
  *    allocates every buffer, including the workspace; the library allocates
  *    and frees no memory, and creates CUDA objects only in
- *    crisp_host_pipeline_create (two streams and their events).
+ *    crisp_host_pipeline_create (three streams and their events).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream); calls return without synchronising, except crisp_read_status.
  *  - Argument errors are detected on the host, returned synchronously, and
@@ -336,11 +336,15 @@ CRISP_API crisp_status crisp_host_pipeline_destroy(crisp_host_pipeline* pipeline
 
 /* crisp_prefill_layer with q, k, v read from host memory and out written to
  * host memory. The layer is processed in chunks of the query heads of one
- * kv group (half of its G heads when G is even and n >= 131072, else all G;
- * every step of the method is per head), the group's K and V uploaded with its first
- * chunk: the upload of chunk c+1 and the download of chunk c-1 run on the
- * pipeline's two streams while chunk c computes on `stream`, so the copies
- * overlap the compute.
+ * kv group (half of its G heads when G is even and n >= 131072, with the
+ * first and last half group of the layer one head at a time; else all G;
+ * every step of the method is per head), the group's K and V uploaded with
+ * its first chunk: the upload of chunk c+1 and the download of chunk c-1 run
+ * on two of the pipeline's streams while chunk c computes, so the copies
+ * overlap the compute. Consecutive chunks compute alternately on `stream`
+ * and on the pipeline's third stream, each with its own half of `ws` (when
+ * ws holds two chunks' intermediates, as a layer workspace of several
+ * chunks does); errors from both land in the status word of `ws`.
  * Results are bit-identical to crisp_prefill_layer.
  * q_host, k_host, v_host, out_host: host, contiguous [heads][n][128] bf16,
  * page-locked for the copies to be asynchronous. q, k, v, out: device
