@@ -8,7 +8,7 @@ the proxy map (fused: the map is never stored), C_struct routing, VS
 selection, pooled estimate and PE selection, mask + schedule, block-sparse
 attention. The unfused map path (map write, then the mass pass) is timed
 separately after the step. Inputs (6 GiB) are larger than L2, so no flush
-between steps; for workloads whose inputs fit in L2 (--config cfg1) a
+between steps; for workloads whose inputs fit in L2 (--config gqa4x1-2k) a
 512 MiB buffer is written before each timed step, outside its events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl crisp|reference]
@@ -44,15 +44,15 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["crisp", "reference"], default="crisp")
-    ap.add_argument("--config", default="cfg5", help="cfg1, cfg2, cfg3, cfg4-L0..cfg4-L3, cfg5")
+    ap.add_argument("--config", default="llama8b-512k", help="gqa4x1-2k, llama8b-32k, qwen7b-128k, llama8b-256k-L0..llama8b-256k-L3, llama8b-512k")
     ap.add_argument("--alpha", default="1/1")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention baseline launch")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--sweep", choices=["lengths", "alpha", "pe", "flex"], default=None,
-                    help="instead of the step: sparse layer vs dense attention over sequence lengths (cfg2 "
-                         "recipe, 2k-128k), over alpha (cfg5), PE gamma vs noise-floor rule (cfg2), or CRISP "
-                         "vs the FlexPrefill rules it replaces (cfg5 and cfg2)")
+                    help="instead of the step: sparse layer vs dense attention over sequence lengths (the "
+                         "llama8b-32k recipe, 2k-128k), over alpha (llama8b-512k), PE gamma vs noise-floor rule "
+                         "(llama8b-32k), or CRISP vs the FlexPrefill rules it replaces (llama8b-512k and llama8b-32k)")
     return ap.parse_args(argv)
 
 
@@ -64,9 +64,9 @@ def workload_config(w, args, world):
 
 
 def workload(synth, name):
-    """A named workload; cfg4-L0..cfg4-L3 are the layers of the 4-layer stack."""
-    if name.startswith("cfg4-L"):
-        return synth.WORKLOADS["cfg4"].layer(int(name[len("cfg4-L"):]))
+    """A named workload; llama8b-256k-L0..L3 are the layers of the 4-layer stack."""
+    if name.startswith("llama8b-256k-L"):
+        return synth.WORKLOADS["llama8b-256k-stack"].layer(int(name[len("llama8b-256k-L"):]))
     return synth.WORKLOADS[name]
 
 
@@ -404,7 +404,7 @@ def run_crisp(args):
     routes = route.cpu().numpy()
     hbm_peak, tf_peak, peak_kind = measured_peaks()
     traffic = profiled_traffic("dynamic_sparse_prefill_crisp_gb300/csrc/attention.cu",
-                               "profiles/attention_cfg5_512k_traffic.md")
+                               "profiles/attention_llama8b_512k_traffic.md")
     attn_ms = stage_ms["attention"]
     achieved_tf = flops / (attn_ms * 1e-3) / 1e12
     proxy_bytes = 4 * hq * B * n + 2 * (2 * hkv * n * 128) + 2 * hq * B * 128
@@ -507,8 +507,8 @@ def run_crisp(args):
             "eff_tflops": achieved_tf,
             "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": achieved_tf, "peak": tf_peak,
                          "unit": "TFLOP/s", "frac": achieved_tf / tf_peak,
-                         "traffic": traffic if w.name == "cfg5-512k-llama8b" else None,
-                         "traffic_source": "profiles/attention_cfg5_512k_traffic.md",
+                         "traffic": traffic if w.name == "llama8b-512k" else None,
+                         "traffic_source": "profiles/attention_llama8b_512k_traffic.md",
                          "peak_kind": f"bf16 dense, {peak_kind} (sustained)"},
             "unfused_map_path": {
                 "proxy_ms": unf_proxy_ms, "masses_ms": unf_masses_ms,
@@ -596,13 +596,13 @@ def run_sweep(args):
     torch.cuda.set_device(0)
     rows = []
     if args.sweep == "lengths":
-        base = synth.WORKLOADS["cfg2"]
+        base = synth.WORKLOADS["llama8b-32k"]
         for n in (2048, 4096, 8192, 16384, 32768, 65536, 131072):
-            w = synth.Workload(**{**base.__dict__, "name": f"cfg2-recipe-{n}", "n": n})
+            w = synth.Workload(**{**base.__dict__, "name": f"llama8b-recipe-{n}", "n": n})
             rows.append(time_layer(w, crisp.params_default(), reps=5))
-        workload = "cfg2 recipe (32 q / 8 kv heads, half sink-type, half diffuse) at 2k-128k tokens"
+        workload = "llama8b-32k recipe (32 q / 8 kv heads, half sink-type, half diffuse) at 2k-128k tokens"
     elif args.sweep == "alpha":
-        w = synth.WORKLOADS["cfg5"]
+        w = synth.WORKLOADS["llama8b-512k"]
         for i, a in enumerate(((1, 1), (5, 4), (3, 2))):
             r = time_layer(w, crisp.params_default(alpha=a), reps=3, dense=(i == 0))
             r["alpha"] = f"{a[0]}/{a[1]}"
@@ -610,7 +610,7 @@ def run_sweep(args):
         d = rows[0]["dense_ms"]
         for r in rows:
             r["speedup_vs_dense"] = d / r["layer_ms"]
-        workload = "cfg5 (512k tokens, 32 q / 8 kv heads)"
+        workload = "llama8b-512k (512k tokens, 32 q / 8 kv heads)"
     elif args.sweep == "flex":
         variants = [("CRISP (C_struct, noise floor alpha 1)", crisp.params_default()),
                     ("CRISP alpha 5/4", crisp.params_default(alpha=(5, 4))),
@@ -618,7 +618,7 @@ def run_sweep(args):
                      crisp.params_default(route_mode=crisp.ROUTE_JSD, vs_mode=crisp.VS_GAMMA, vs_gamma=(95, 100))),
                     ("FlexPrefill rules gamma 0.97",
                      crisp.params_default(route_mode=crisp.ROUTE_JSD, vs_mode=crisp.VS_GAMMA, vs_gamma=(97, 100)))]
-        for cfg in ("cfg5", "cfg2"):
+        for cfg in ("llama8b-512k", "llama8b-32k"):
             w = synth.WORKLOADS[cfg]
             for i, (label, p) in enumerate(variants):
                 r = time_layer(w, p, reps=3, dense=(i == 0))
@@ -627,14 +627,14 @@ def run_sweep(args):
             d = rows[-len(variants)]["dense_ms"]
             for r in rows[-len(variants):]:
                 r["speedup_vs_dense"] = d / r["layer_ms"]
-        workload = "cfg5 (512k, all heads sink-type) and cfg2 (32k, half diffuse); same kernels, rules differ"
+        workload = "llama8b-512k (all heads sink-type) and llama8b-32k (half diffuse); same kernels, rules differ"
     else:
-        w = synth.WORKLOADS["cfg2"]
+        w = synth.WORKLOADS["llama8b-32k"]
         for mode in (crisp.PE_GAMMA, crisp.PE_NOISE):
             r = time_layer(w, crisp.params_default(pe_mode=mode), reps=5, dense=(mode == crisp.PE_GAMMA))
             r["pe_mode"] = "gamma 19/20" if mode == crisp.PE_GAMMA else "noise floor (alpha 1)"
             rows.append(r)
-        workload = "cfg2 (32k tokens, 16 sink-type + 16 diffuse heads)"
+        workload = "llama8b-32k (32k tokens, 16 sink-type + 16 diffuse heads)"
     print(json.dumps({"sweep": args.sweep, "workload": workload, "unit": "ms", "rows": rows}), flush=True)
     return 0
 

@@ -146,21 +146,21 @@ def _alternating(hq):
 WORKLOADS = {
     # 4 q / 1 kv, 2k tokens, all heads sink-type: 64 sink keys at +4 logit,
     # a local band of width 64, 3 needle columns, no sharp slash.
-    "cfg1": Workload("cfg1-2k-gqa4x1", 4, 1, 2048, 0, [0, 1, 2, 3], sink_tokens=64, d_sink=4.0, n_needles=3,
+    "gqa4x1-2k": Workload("gqa4x1-2k", 4, 1, 2048, 0, [0, 1, 2, 3], sink_tokens=64, d_sink=4.0, n_needles=3,
                      d_needle=7.0, n_slash=0, band_w=64, d_band=3.0),
     # Llama-shaped, 32k: even heads sink+2 slashes+8 needles, odd heads diffuse.
-    "cfg2": Workload("cfg2-32k-llama8b", 32, 8, 32768, 1, _alternating(32), d_sink=7.0, n_needles=8,
+    "llama8b-32k": Workload("llama8b-32k", 32, 8, 32768, 1, _alternating(32), d_sink=7.0, n_needles=8,
                      d_needle=9.0, n_slash=2, d_slash=9.0),
     # Qwen-shaped, 128k: even heads sink/recency dominated (no sharp slash),
     # odd heads diffuse; 16 needles.
-    "cfg3": Workload("cfg3-128k-qwen7b", 28, 4, 131072, 2, _alternating(28), d_sink=8.0, n_needles=16,
+    "qwen7b-128k": Workload("qwen7b-128k", 28, 4, 131072, 2, _alternating(28), d_sink=8.0, n_needles=16,
                      d_needle=9.5, n_slash=0),
     # Llama-shaped 4-layer stack, 256k: 25/50/75/90% sink-type heads per layer.
-    "cfg4": Workload("cfg4-256k-llama8b-4layer", 32, 8, 262144, 4000, list(range(32)), d_sink=8.5, n_needles=8,
+    "llama8b-256k-stack": Workload("llama8b-256k-stack", 32, 8, 262144, 4000, list(range(32)), d_sink=8.5, n_needles=8,
                      d_needle=10.0, n_slash=2, d_slash=10.0, layers=4,
                      extra={"vs_fraction": [0.25, 0.50, 0.75, 0.90]}),
     # Llama-shaped, 512k, every head sink-type with 2 slashes and 32 needles.
-    "cfg5": Workload("cfg5-512k-llama8b", 32, 8, 524288, 5, list(range(32)), d_sink=10.0, n_needles=32,
+    "llama8b-512k": Workload("llama8b-512k", 32, 8, 524288, 5, list(range(32)), d_sink=10.0, n_needles=32,
                      d_needle=10.0, n_slash=2, d_slash=10.0),
 }
 

@@ -64,27 +64,27 @@ def _check_layer(w, index, params=None):
     return route
 
 
-def test_cfg2_32k_llama_shape():
-    route = _check_layer(synth.WORKLOADS["cfg2"], 2)
+def test_llama8b_32k():
+    route = _check_layer(synth.WORKLOADS["llama8b-32k"], 2)
     assert route.tolist() == [1 - (h % 2) for h in range(32)]  # even heads sink-type, odd diffuse
 
 
-def test_cfg3_128k_qwen_shape():
-    route = _check_layer(synth.WORKLOADS["cfg3"], 3)
+def test_qwen7b_128k():
+    route = _check_layer(synth.WORKLOADS["qwen7b-128k"], 3)
     assert route.tolist() == [1 - (h % 2) for h in range(28)]
 
 
 @pytest.mark.parametrize("layer", [0, 1, 2, 3])
-def test_cfg4_256k_stack_layer(layer):
-    w = synth.WORKLOADS["cfg4"].layer(layer)
+def test_llama8b_256k_stack_layer(layer):
+    w = synth.WORKLOADS["llama8b-256k-stack"].layer(layer)
     route = _check_layer(w, 4 * 16 + layer)
     want = np.zeros(w.hq, np.uint8)
     want[w.vs_heads] = 1
     assert np.array_equal(route, want)
 
 
-def test_cfg5_512k_llama_shape():
-    route = _check_layer(synth.WORKLOADS["cfg5"], 5)
+def test_llama8b_512k():
+    route = _check_layer(synth.WORKLOADS["llama8b-512k"], 5)
     assert route.all()
 
 
@@ -104,8 +104,8 @@ def test_ragged_long_sequence():
     assert route.any() and not route.all()  # both routes
 
 
-def test_cfg5_512k_dense_sampled_rows():
-    w = synth.WORKLOADS["cfg5"]
+def test_llama8b_512k_dense_sampled_rows():
+    w = synth.WORKLOADS["llama8b-512k"]
     q, k, v = w.generate()
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
     out = empty((w.hq, w.n, 128), torch.bfloat16)

@@ -271,8 +271,8 @@ def test_prefill_layer_host_matches_device_layer():
     pipe.close()
 
 
-def test_cfg1_full_layer():
-    w = synth.WORKLOADS["cfg1"]
+def test_gqa4x1_2k_full_layer():
+    w = synth.WORKLOADS["gqa4x1-2k"]
     q, k, v = w.generate()
     params = crisp.params_default()
     r = run_steps(q, k, v, params)
