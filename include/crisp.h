@@ -272,12 +272,12 @@ CRISP_API crisp_status crisp_select_pe(const crisp_shape* shape, const crisp_par
  *            (a 128-wide diagonal band at offset block s crosses key blocks
  *            qb-s and qb-s-1);
  *   PE head: pebits row qb within [0, qb].
- * and the attention schedule: query blocks descending, heads ascending within
- * a query block (a causal row's block count grows with qb, so the longest
- * rows run first, and the heads of one query block, which gather the same
- * kv-group blocks, run next to each other).
+ * and the attention schedule: kv group by kv group (g = h / G), within a
+ * group query blocks descending and the group's heads ascending (a causal
+ * row's block count grows with qb, so each group's longest rows run first,
+ * and the CTAs in flight gather one kv group's blocks, which stay in L2).
  * rowbits: uint32 [hq][nb][W]; counts: int32 [hq][nb] = blocks per row;
- * order: int32 [hq*nb], order[(nb-1-qb)*hq + h] = h*nb + qb. */
+ * order: int32 [hq*nb], order[(g*nb + nb-1-qb)*G + h%G] = h*nb + qb. */
 CRISP_API crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t* route, const uint32_t* vbits,
                                         const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits,
                                         int32_t* counts, int32_t* order, void* ws, size_t ws_bytes,

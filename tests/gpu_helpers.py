@@ -84,7 +84,7 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
                 cstruct=u64(cstruct), total=u64(total),
                 route=route.cpu().numpy(), vbits=u32(vbits), sbits=u32(sbits), pbar=pbar.cpu().numpy(),
                 pebits=u32(pebits), rowbits=u32(rowbits), counts=counts.cpu().numpy(), order=order.cpu().numpy(),
-                out=out)
+                group=hq // hkv, out=out)
 
 
 def attn_error(out_dev_or_np, ref):

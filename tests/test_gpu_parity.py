@@ -54,10 +54,15 @@ def check_index_sets(r, params):
     assert np.array_equal(rb, r["rowbits"])
     pop = np.unpackbits(rb.view(np.uint8), axis=-1).sum(-1).astype(np.int64)
     assert np.array_equal(pop, r["counts"])
-    # schedule: query blocks descending, heads ascending within a query block
+    # schedule: kv group by kv group; within a group query blocks descending,
+    # the group's heads ascending
     hq, nb = pop.shape
-    t = np.arange(hq * nb)
-    assert np.array_equal(r["order"], (t % hq) * nb + (nb - 1 - t // hq))
+    G = r["group"]
+    want = np.empty(hq * nb, np.int64)
+    for h in range(hq):
+        for qb in range(nb):
+            want[((h // G) * nb + nb - 1 - qb) * G + h % G] = h * nb + qb
+    assert np.array_equal(r["order"], want)
     return rb, route
 
 
