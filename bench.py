@@ -169,13 +169,14 @@ def selected_pairs(rowbits: np.ndarray, n: int) -> int:
     return int((bits.sum(axis=0).astype(np.int64) * wgt).sum())
 
 
-def profiled_traffic(kernel_src: str, profile: str):
-    """DRAM bytes per launch from a committed ncu summary, or None when the
-    kernel source has changed since the counters were taken."""
+def profiled_traffic(sources, profile: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when a
+    source that decides the traffic (the kernel, its work order) has changed
+    since the counters were taken (sha256 over the files in order)."""
     import hashlib
     try:
         text = open(os.path.join(ROOT, profile)).read()
-        src = open(os.path.join(ROOT, kernel_src), "rb").read()
+        src = b"".join(open(os.path.join(ROOT, f), "rb").read() for f in sources)
     except OSError:
         return None
     fields = dict(line.split(": ", 1) for line in text.splitlines() if ": " in line and " " not in line.split(": ")[0])
@@ -185,6 +186,11 @@ def profiled_traffic(kernel_src: str, profile: str):
         return int(fields["traffic_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+
+
+# The attention kernel and the kernel that writes its work order.
+TRAFFIC_SOURCES = ("dynamic_sparse_prefill_crisp_gb300/csrc/attention.cu",
+                   "dynamic_sparse_prefill_crisp_gb300/csrc/mask.cu")
 
 
 def measured_peaks():
@@ -403,8 +409,7 @@ def run_crisp(args):
     dense_pairs = hq * n * (n + 1) // 2
     routes = route.cpu().numpy()
     hbm_peak, tf_peak, peak_kind = measured_peaks()
-    traffic = profiled_traffic("dynamic_sparse_prefill_crisp_gb300/csrc/attention.cu",
-                               "profiles/attention_llama8b_512k_traffic.md")
+    traffic = profiled_traffic(TRAFFIC_SOURCES, "profiles/attention_llama8b_512k_traffic.md")
     attn_ms = stage_ms["attention"]
     achieved_tf = flops / (attn_ms * 1e-3) / 1e12
     proxy_bytes = 4 * hq * B * n + 2 * (2 * hkv * n * 128) + 2 * hq * B * 128
