@@ -99,7 +99,7 @@ __device__ __forceinline__ uint32_t row_word(const uint32_t* row, bool dense, in
 
 __global__ void __launch_bounds__(kThreads, 2)
     attention_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                     const __grid_constant__ CUtensorMap tv, int n, int hq, int group, float c_log2,
+                     const __grid_constant__ CUtensorMap tv, int n, int group, float c_log2,
                      const uint32_t* __restrict__ rowbits, const int32_t* __restrict__ order, int dense,
                      __nv_bfloat16* __restrict__ out, int64_t o_hs, int64_t o_ts, DevStatus* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -111,13 +111,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = (n + kB - 1) / kB, W = (nb + 31) / 32;  // a short last block when 128 does not divide n
-  // Work item: the schedule order[] or, without one, query blocks descending.
+  // Work item: the schedule order[] or, without one, the same kv-group-major
+  // order (kv group by kv group, query blocks descending within a group).
   int item;
   if (order != nullptr) {
     item = order[blockIdx.x];
   } else {
-    const int qb_desc = nb - 1 - static_cast<int>(blockIdx.x) / hq;
-    item = (static_cast<int>(blockIdx.x) % hq) * nb + qb_desc;
+    const int t = static_cast<int>(blockIdx.x), per_group = group * nb;
+    const int rem = t % per_group;
+    item = ((t / per_group) * group + rem % group) * nb + (nb - 1 - rem / group);
   }
   const int h = item / nb, qb = item % nb;
   const int g = h / group;
@@ -425,7 +427,7 @@ cudaError_t launch_attention(const crisp_shape& s, const TmaMaps& maps, const ui
   if (e != cudaSuccess) return e;
   const int items = s.hq * nb;
   attention_kernel<<<items, kThreads, kSmemBytes, st>>>(
-      maps.q, maps.k, maps.v, s.seq_len, s.hq, s.hq / s.hkv, s.scale * 1.4426950408889634f,
+      maps.q, maps.k, maps.v, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f,
       dense ? nullptr : rowbits, order, dense ? 1 : 0, static_cast<__nv_bfloat16*>(out), s.o_head_stride,
       s.o_tok_stride, status);
   return cudaGetLastError();

@@ -291,7 +291,7 @@ CRISP_API crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t*
  * Bits above the diagonal block are ignored; rows with an empty A(i) are
  * written as zeros; only rows i < n are written. q bf16 [hq][n][128]; k, v bf16 [hkv][n][128]; rowbits
  * from crisp_build_mask; order: the schedule from crisp_build_mask, or NULL
- * for query blocks in descending order (any permutation of the row ids gives
+ * for the same kv-group-major order (any permutation of the row ids gives
  * the same result); out bf16 [hq][n][128] (o strides). */
 CRISP_API crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v,
                                             const uint32_t* rowbits, const int32_t* order, void* out, void* ws,
