@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kPeThreads) select_pe_kernel(const float* __re
   __shared__ uint32_t chosen[kMaxBlocks / 32];
   __shared__ uint64_t scratch64[32];
   __shared__ int scratch32[32];
-  __shared__ unsigned long long hist[256], bcast[2];
+  __shared__ unsigned long long hist[256], bcast[4];
   const int b = blockIdx.x, h = blockIdx.y;
   const int W = (nb + 31) / 32;
   uint32_t* out = pebits + (static_cast<size_t>(h) * nb + b) * W;

@@ -41,16 +41,20 @@ __device__ __forceinline__ uint64_t sel_key(uint64_t m, int c) {
 // unique keys and a reach that grows with W, this x is the key of the last
 // member of the (key descending) prefix that first reaches the goal: the
 // same answer as a bit-by-bit search from the top, found one 8-bit digit
-// per pass (six passes) from a shared-memory histogram of weights. Digit 0,
-// where most small masses fall in the first passes, is summed per warp
-// before its one shared atomic. Keys must be < 2^48; reach(total eligible
-// weight) must hold (then every pass finds a digit). If reach(0) holds the
-// result is 2^48 - 1 (no key reaches it). All threads of the block call it.
-// hist: 256 entries; bcast: 2 entries (shared memory).
+// per pass (at most six passes) from a shared-memory histogram of weights.
+// Each bin also counts its keys (bits 40 and up of the entry); once the
+// chosen bin holds a single eligible key, that key is the answer and the
+// remaining passes are skipped. Digit 0, where most small masses fall in the
+// first passes, is summed per warp before its one shared atomic. Keys must be
+// < 2^48 and the total eligible weight < 2^40; reach(total eligible weight)
+// must hold (then every pass finds a digit). If reach(0) holds the result is
+// 2^48 - 1 (no key reaches it). All threads of the block call it.
+// hist: 256 entries; bcast: 4 entries (shared memory).
 template <typename KeyFn, typename WeightFn, typename EligFn, typename ReachFn>
 __device__ __forceinline__ uint64_t radix_max_key(int len, KeyFn key_of, WeightFn weight_of, EligFn eligible,
                                                   ReachFn reach, unsigned long long* hist,
                                                   unsigned long long* bcast) {
+  constexpr unsigned long long kOne = 1ull << 40, kWeight = kOne - 1;  // count unit, weight field
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t prefix = 0;            // digits decided so far
   unsigned long long above = 0;   // weight of eligible keys above the current bucket
@@ -63,7 +67,7 @@ __device__ __forceinline__ uint64_t radix_max_key(int len, KeyFn key_of, WeightF
       const uint64_t key = key_of(c);
       if ((key >> (shift + 8)) != prefix) continue;
       const int d = static_cast<int>((key >> shift) & 255u);
-      const unsigned long long w = weight_of(c);
+      const unsigned long long w = kOne + weight_of(c);
       if (d == 0)
         w0 += w;
       else
@@ -75,10 +79,12 @@ __device__ __forceinline__ uint64_t radix_max_key(int len, KeyFn key_of, WeightF
     if (warp == 0) {
       // Lane l holds bins 255-8l .. 248-8l (descending); cumulative weights
       // from the top find the largest digit whose suffix reaches the goal.
-      unsigned long long v[8], mine = 0;
+      unsigned long long v[8], cnt[8], mine = 0;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        v[k] = hist[255 - 8 * lane - k];
+        const unsigned long long e = hist[255 - 8 * lane - k];
+        v[k] = e & kWeight;
+        cnt[k] = e >> 40;
         mine += v[k];
       }
       unsigned long long before = mine;  // inclusive scan over lanes, then exclusive
@@ -90,12 +96,13 @@ __device__ __forceinline__ uint64_t radix_max_key(int len, KeyFn key_of, WeightF
       before -= mine;
       unsigned long long run = above + before;
       int found = -1;
-      unsigned long long run_above = 0;
+      unsigned long long run_above = 0, found_cnt = 0;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         if (found < 0 && reach(run + v[k])) {
           found = 255 - 8 * lane - k;
           run_above = run;
+          found_cnt = cnt[k];
         }
         run += v[k];
       }
@@ -104,11 +111,22 @@ __device__ __forceinline__ uint64_t radix_max_key(int len, KeyFn key_of, WeightF
       if (lane == first) {
         bcast[0] = static_cast<unsigned long long>(found >= 0 ? found : 0);
         bcast[1] = found >= 0 ? run_above : above;
+        bcast[2] = found >= 0 ? found_cnt : 0ull;
       }
     }
     __syncthreads();
     prefix = (prefix << 8) | bcast[0];
     above = bcast[1];
+    if (bcast[2] == 1ull && shift > 0) {
+      // One eligible key carries the decided digits: the goal is reached at
+      // it and not above it, so it is the answer.
+      for (int c = threadIdx.x; c < len; c += blockDim.x)
+        if (eligible(c) && (key_of(c) >> shift) == prefix) bcast[3] = key_of(c);
+      __syncthreads();
+      const uint64_t x = bcast[3];
+      __syncthreads();  // bcast is free for the caller's next search
+      return x;
+    }
     __syncthreads();
   }
   return prefix;
