@@ -387,18 +387,22 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Combines the per-chunk (max, sum) pairs of each row: M = max m_c,
-// L = sum l_c * 2^(m_c - M); stores (M, 1/L).
+// Combines the per-chunk (max, sum) pairs of each row, one warp per row:
+// M = max m_c, L = sum l_c * 2^(m_c - M); stores (M, 1/L).
 __global__ void proxy_combine(const float2* __restrict__ part, float2* __restrict__ stats, int rows, int nparts) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= rows) return;
-  const float2* p = part + static_cast<size_t>(idx) * nparts;
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (row >= rows) return;  // whole warps
+  const float2* p = part + static_cast<size_t>(row) * nparts;
   float M = -INFINITY;
-  for (int c = 0; c < nparts; ++c) M = fmaxf(M, p[c].x);
+  for (int c = lane; c < nparts; c += 32) M = fmaxf(M, p[c].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float L = 0.f;
-  for (int c = 0; c < nparts; ++c)
+  for (int c = lane; c < nparts; c += 32)
     if (p[c].x != -INFINITY) L += p[c].y * ex2_approx(p[c].x - M);
-  stats[idx] = make_float2(M, 1.0f / L);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  if (lane == 0) stats[row] = make_float2(M, 1.0f / L);
 }
 
 }  // namespace
@@ -417,7 +421,7 @@ static cudaError_t proxy_stats(const crisp_shape& s, const TmaMaps& maps, char* 
       maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, nullptr, 0, part, stats, nullptr,
       nullptr, nullptr, nullptr, nullptr, status);
   const int rows = s.hq * kB;
-  proxy_combine<<<(rows + 127) / 128, 128, 0, st>>>(part, stats, rows, 2 * chunks);
+  proxy_combine<<<(rows + 7) / 8, 256, 0, st>>>(part, stats, rows, 2 * chunks);  // 8 rows (warps) per CTA
   return cudaGetLastError();
 }
 
