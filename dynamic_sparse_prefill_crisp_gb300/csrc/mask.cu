@@ -46,13 +46,17 @@ __device__ __forceinline__ uint32_t window32(const uint32_t* v, int p) {
   return __funnelshift_r(v[p >> 5], v[(p >> 5) + 1], p & 31);
 }
 
-// grid (nb, hq); one thread per bitset word.
+// One warp per row (h, qb), rows of a head consecutive; a lane per bitset
+// word (strided).
+constexpr int kMaskRowsPerCta = 8;
 __global__ void mask_kernel(const uint8_t* __restrict__ route, const uint32_t* __restrict__ vbits,
-                            const uint32_t* __restrict__ srev, const uint32_t* __restrict__ pebits, int nb,
+                            const uint32_t* __restrict__ srev, const uint32_t* __restrict__ pebits, int hq, int nb,
                             int group, uint32_t* __restrict__ rowbits, int32_t* __restrict__ counts,
                             int32_t* __restrict__ order) {
-  __shared__ int scratch[32];
-  const int qb = blockIdx.x, h = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int rowid = blockIdx.x * kMaskRowsPerCta + (threadIdx.x >> 5);
+  if (rowid >= hq * nb) return;  // whole warps
+  const int h = rowid / nb, qb = rowid % nb;
   const int W = (nb + 31) / 32, wq = qb >> 5;
   const bool vs = route[h] != 0;
   const uint32_t* V = vbits + static_cast<size_t>(h) * W;
@@ -60,7 +64,7 @@ __global__ void mask_kernel(const uint8_t* __restrict__ route, const uint32_t* _
   const uint32_t* PE = pebits + (static_cast<size_t>(h) * nb + qb) * W;
   uint32_t* out = rowbits + (static_cast<size_t>(h) * nb + qb) * W;
   int cnt = 0;
-  for (int w = threadIdx.x; w < W; w += blockDim.x) {
+  for (int w = lane; w < W; w += 32) {
     uint32_t word = 0;
     if (w <= wq) {
       if (vs) {
@@ -74,8 +78,8 @@ __global__ void mask_kernel(const uint8_t* __restrict__ route, const uint32_t* _
     out[w] = word;
     cnt += __popc(word);
   }
-  const int total = block_sum(cnt, scratch);
-  if (threadIdx.x == 0) {
+  const int total = warp_sum(cnt);
+  if (lane == 0) {
     counts[static_cast<size_t>(h) * nb + qb] = total;
     const size_t g = h / group, j = h % group;
     order[(g * nb + (nb - 1 - qb)) * group + j] = h * nb + qb;
@@ -91,8 +95,9 @@ cudaError_t launch_build_mask(const crisp_shape& s, const uint8_t* route, const 
   const int nb = num_blocks(s.seq_len);
   auto* srev = reinterpret_cast<uint32_t*>(ws + L.srev);
   srev_kernel<<<s.hq, 128, 0, st>>>(sbits, route, nb, srev);
-  mask_kernel<<<dim3(nb, s.hq), 128, 0, st>>>(route, vbits, srev, pebits, nb, s.hq / s.hkv, rowbits, counts,
-                                              order);
+  const int rows = s.hq * nb;
+  mask_kernel<<<(rows + kMaskRowsPerCta - 1) / kMaskRowsPerCta, 32 * kMaskRowsPerCta, 0, st>>>(
+      route, vbits, srev, pebits, s.hq, nb, s.hq / s.hkv, rowbits, counts, order);
   return cudaGetLastError();
 }
 

@@ -137,7 +137,9 @@ __global__ void pooled_softmax(const uint8_t* __restrict__ route, int hq, int nb
   for (int c = lane; c <= b; c += 32) z[c] = ptx::ex2_approx(z[c] - mx) * inv;
 }
 
-// A6: one CTA per (head, query block b). The row's selection keys
+// A6: one CTA per head and `rows` consecutive query blocks b (rows of one
+// head have similar lengths; a VS head's CTA only writes empty rows, so long
+// sequences group rows to launch fewer of those). Each row's selection keys
 // (quantum << 13 | 8191 - c) are formed once into shared memory (nb x 8
 // bytes, dynamic); every search pass then reads them from there.
 constexpr int kPeThreads = 256;
@@ -145,75 +147,80 @@ __global__ void __launch_bounds__(kPeThreads) select_pe_kernel(const float* __re
                                                                const uint8_t* __restrict__ route, int nb,
                                                                int pe_mode, uint32_t gamma_num, uint32_t gamma_den,
                                                                uint32_t alpha_num, uint32_t alpha_den, int kmin,
-                                                               uint32_t* __restrict__ pebits) {
+                                                               int rows, uint32_t* __restrict__ pebits) {
   extern __shared__ unsigned long long keys[];  // [b + 1]
   __shared__ uint32_t chosen[kMaxBlocks / 32];
   __shared__ uint64_t scratch64[32];
   __shared__ int scratch32[32];
   __shared__ unsigned long long hist[256], bcast[4];
-  const int b = blockIdx.x, h = blockIdx.y;
+  const int h = blockIdx.y;
   const int W = (nb + 31) / 32;
-  uint32_t* out = pebits + (static_cast<size_t>(h) * nb + b) * W;
-  for (int w = threadIdx.x; w < W; w += blockDim.x) chosen[w] = 0u;
+  const int b_end = min(nb, (static_cast<int>(blockIdx.x) + 1) * rows);
   if (route[h]) {
-    for (int w = threadIdx.x; w < W; w += blockDim.x) out[w] = 0u;
+    for (int i = blockIdx.x * rows * W + threadIdx.x; i < b_end * W; i += blockDim.x)
+      pebits[static_cast<size_t>(h) * nb * W + i] = 0u;
     return;
   }
-  const float* z = pbar + (static_cast<size_t>(h) * nb + b) * nb;
-  // Pooled quanta are <= 2^33, so the keys fit in 48 bits and key >> 13 is
-  // the quantum.
-  uint64_t part = 0;
-  for (int c = threadIdx.x; c <= b; c += blockDim.x) {
-    const uint64_t m = q32(z[c]);
-    keys[c] = sel_key(m, c);
-    if (pe_mode == CRISP_PE_GAMMA || (c >= 1 && c <= b - 1)) part += m;
-  }
-  const uint64_t T = block_sum(part, scratch64);  // also orders the key writes before the reads below
-  auto key_of = [&](int c) { return static_cast<uint64_t>(keys[c]); };
-  if (pe_mode == CRISP_PE_GAMMA) {
-    const unsigned __int128 goal = static_cast<unsigned __int128>(gamma_num) * T;
-    // Largest key x whose suffix mass reaches gamma of the row: the last
-    // member of the shortest (mass desc, index asc) prefix.
-    const uint64_t x = radix_max_key(
-        b + 1, key_of, [&](int c) { return keys[c] >> 13; }, [](int) { return true; },
-        [&](unsigned long long f) { return static_cast<unsigned __int128>(gamma_den) * f >= goal; }, hist, bcast);
-    for (int c = threadIdx.x; c <= b; c += blockDim.x)
-      if (keys[c] >= x) atomicOr(&chosen[c >> 5], 1u << (c & 31));
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      chosen[0] |= 1u;
-      chosen[b >> 5] |= 1u << (b & 31);
+  for (int b = blockIdx.x * rows; b < b_end; ++b) {
+    uint32_t* out = pebits + (static_cast<size_t>(h) * nb + b) * W;
+    __syncthreads();  // the previous row's reads of keys and chosen are done
+    for (int w = threadIdx.x; w < W; w += blockDim.x) chosen[w] = 0u;
+    const float* z = pbar + (static_cast<size_t>(h) * nb + b) * nb;
+    // Pooled quanta are <= 2^33, so the keys fit in 48 bits and key >> 13 is
+    // the quantum.
+    uint64_t part = 0;
+    for (int c = threadIdx.x; c <= b; c += blockDim.x) {
+      const uint64_t m = q32(z[c]);
+      keys[c] = sel_key(m, c);
+      if (pe_mode == CRISP_PE_GAMMA || (c >= 1 && c <= b - 1)) part += m;
     }
-  } else {
-    const int N = max(0, b - 1);  // candidates [1, b-1]; T is their mass
-    const unsigned __int128 rhs = static_cast<unsigned __int128>(alpha_num) * T;
-    for (int c = 1 + threadIdx.x; c <= b - 1; c += blockDim.x) {
-      const unsigned __int128 lhs = static_cast<unsigned __int128>(keys[c] >> 13) * static_cast<unsigned>(N) * alpha_den;
-      if (lhs > rhs) atomicOr(&chosen[c >> 5], 1u << (c & 31));
+    const uint64_t T = block_sum(part, scratch64);  // also orders the key writes before the reads below
+    auto key_of = [&](int c) { return static_cast<uint64_t>(keys[c]); };
+    if (pe_mode == CRISP_PE_GAMMA) {
+      const unsigned __int128 goal = static_cast<unsigned __int128>(gamma_num) * T;
+      // Largest key x whose suffix mass reaches gamma of the row: the last
+      // member of the shortest (mass desc, index asc) prefix.
+      const uint64_t x = radix_max_key(
+          b + 1, key_of, [&](int c) { return keys[c] >> 13; }, [](int) { return true; },
+          [&](unsigned long long f) { return static_cast<unsigned __int128>(gamma_den) * f >= goal; }, hist, bcast);
+      for (int c = threadIdx.x; c <= b; c += blockDim.x)
+        if (keys[c] >= x) atomicOr(&chosen[c >> 5], 1u << (c & 31));
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        chosen[0] |= 1u;
+        chosen[b >> 5] |= 1u << (b & 31);
+      }
+    } else {
+      const int N = max(0, b - 1);  // candidates [1, b-1]; T is their mass
+      const unsigned __int128 rhs = static_cast<unsigned __int128>(alpha_num) * T;
+      for (int c = 1 + threadIdx.x; c <= b - 1; c += blockDim.x) {
+        const unsigned __int128 lhs = static_cast<unsigned __int128>(keys[c] >> 13) * static_cast<unsigned>(N) * alpha_den;
+        if (lhs > rhs) atomicOr(&chosen[c >> 5], 1u << (c & 31));
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        chosen[0] |= 1u;
+        chosen[b >> 5] |= 1u << (b & 31);
+      }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      chosen[0] |= 1u;
-      chosen[b >> 5] |= 1u << (b & 31);
+    int pc = 0;
+    for (int w = threadIdx.x; w < W; w += blockDim.x) pc += __popc(chosen[w]);
+    const int count = block_sum(pc, scratch32);
+    const int need = min(kmin, b + 1) - count;
+    if (need > 0) {
+      // k_min fill: the `need` unchosen blocks with the largest keys.
+      auto unchosen = [&](int c) { return !((chosen[c >> 5] >> (c & 31)) & 1u); };
+      const uint64_t x = radix_max_key(
+          b + 1, key_of, [](int) { return 1ull; }, unchosen,
+          [&](unsigned long long cnt) { return cnt >= static_cast<unsigned long long>(need); }, hist, bcast);
+      __syncthreads();
+      for (int c = threadIdx.x; c <= b; c += blockDim.x)
+        if (unchosen(c) && keys[c] >= x) atomicOr(&chosen[c >> 5], 1u << (c & 31));
     }
-  }
-  __syncthreads();
-  int pc = 0;
-  for (int w = threadIdx.x; w < W; w += blockDim.x) pc += __popc(chosen[w]);
-  const int count = block_sum(pc, scratch32);
-  const int need = min(kmin, b + 1) - count;
-  if (need > 0) {
-    // k_min fill: the `need` unchosen blocks with the largest keys.
-    auto unchosen = [&](int c) { return !((chosen[c >> 5] >> (c & 31)) & 1u); };
-    const uint64_t x = radix_max_key(
-        b + 1, key_of, [](int) { return 1ull; }, unchosen,
-        [&](unsigned long long cnt) { return cnt >= static_cast<unsigned long long>(need); }, hist, bcast);
     __syncthreads();
-    for (int c = threadIdx.x; c <= b; c += blockDim.x)
-      if (unchosen(c) && keys[c] >= x) atomicOr(&chosen[c >> 5], 1u << (c & 31));
+    for (int w = threadIdx.x; w < W; w += blockDim.x) out[w] = chosen[w];
   }
-  __syncthreads();
-  for (int w = threadIdx.x; w < W; w += blockDim.x) out[w] = chosen[w];
 }
 
 }  // namespace
@@ -243,9 +250,11 @@ cudaError_t launch_select_pe(const crisp_shape& s, const crisp_params& p, const 
   cudaError_t e = cudaFuncSetAttribute(select_pe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(key_bytes));
   if (e != cudaSuccess) return e;
-  select_pe_kernel<<<dim3(nb, s.hq), kPeThreads, key_bytes, st>>>(pbar, route, nb, p.pe_mode, p.gamma_num,
-                                                                  p.gamma_den, p.alpha_num, p.alpha_den,
-                                                                  p.kmin_blocks, pebits);
+  // Four rows per CTA from 1024 blocks (measured: 512k with no PE heads
+  // 0.13 -> 0.03 ms); one below, where a CTA per row keeps more in flight.
+  const int rows = nb >= 1024 ? 4 : 1;
+  select_pe_kernel<<<dim3((nb + rows - 1) / rows, s.hq), kPeThreads, key_bytes, st>>>(
+      pbar, route, nb, p.pe_mode, p.gamma_num, p.gamma_den, p.alpha_num, p.alpha_den, p.kmin_blocks, rows, pebits);
   return cudaGetLastError();
 }
 
