@@ -233,7 +233,7 @@ def build_mask(shape, route, vbits, sbits, pebits, rowbits, counts, order, ws, s
 
 
 def sparse_prefill(shape, q, k, v, rowbits, order, out, ws, stream=None):
-    """order: the schedule from build_mask, or None (query blocks descending)."""
+    """order: the schedule from build_mask, or None (the same kv-group-major order)."""
     _check(lib().crisp_sparse_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(rowbits), _ptr(order),
                                       _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_sparse_prefill")
 

@@ -181,7 +181,7 @@ def test_sparse_prefill_arbitrary_masks():
     s = crisp.make_shape(hq, hkv, n, qd, kd, out)
     ws = new_workspace(s)
     rbd = torch.from_numpy(rb.view(np.int32)).cuda()
-    crisp.sparse_prefill(s, qd, kd, vd, rbd, None, out, ws)  # default order: query blocks descending
+    crisp.sparse_prefill(s, qd, kd, vd, rbd, None, out, ws)  # default order: kv-group-major
     torch.cuda.synchronize()
     assert_status_ok(ws)
     rb_causal = rb.copy()
