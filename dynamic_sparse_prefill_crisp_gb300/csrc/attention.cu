@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int pair_bar = 1 + quarter;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + half * 64;        // 64 S columns
-    const uint32_t p_addr = tmem + lane_addr + half * 64;        // 32 P columns (bf16 pairs), over own S
+    const uint32_t p_addr = s_addr;                              // 32 P columns (bf16 pairs) over the first of them
     const uint32_t o_addr = tmem + lane_addr + 128 + half * 64;  // 64 O columns
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
