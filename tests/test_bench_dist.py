@@ -66,3 +66,24 @@ def test_selected_pairs_counts_the_causal_half_of_the_diagonal():
     assert bench.selected_pairs(rb, nb * 128) == 2 * (128 * 129 // 2) + 2 * 128 * 128
     # a short last block (n = 300: 44 tokens): its row counts 44 query rows
     assert bench.selected_pairs(rb, 300) == 2 * (128 * 129 // 2) + 128 * 128 + 44 * 128
+
+
+def test_profiled_traffic_is_dropped_once_a_source_changes(tmp_path, monkeypatch):
+    # The DRAM-traffic figure of a committed ncu summary is reported only
+    # while the sources that decide it hash to the recorded value.
+    import hashlib
+    (tmp_path / "a.cu").write_bytes(b"kernel")
+    (tmp_path / "b.cu").write_bytes(b"order")
+    sha = hashlib.sha256(b"kernel" + b"order").hexdigest()
+    (tmp_path / "p.md").write_text(f"# summary\n\ntraffic_bytes_per_launch: 1234\nsource_sha256: {sha}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic(("a.cu", "b.cu"), "p.md") == 1234
+    (tmp_path / "b.cu").write_bytes(b"order changed")
+    assert bench.profiled_traffic(("a.cu", "b.cu"), "p.md") is None
+    assert bench.profiled_traffic(("a.cu", "missing.cu"), "p.md") is None
+
+
+def test_committed_traffic_summary_names_the_guarded_sources():
+    text = open(os.path.join(bench.ROOT, "profiles", "attention_llama8b_512k_traffic.md")).read()
+    assert "source_sha256:" in text and "traffic_bytes_per_launch:" in text
+    assert all(os.path.exists(os.path.join(bench.ROOT, f)) for f in bench.TRAFFIC_SOURCES)
