@@ -33,29 +33,33 @@ def _p(a):
     return ctypes.c_void_p(a.ctypes.data)
 
 
+def _configure(lib):
+    """Declares the argument types of the oracle's C entry points on `lib`."""
+    i, vp, d, u32, i64 = ctypes.c_int, ctypes.c_void_p, ctypes.c_double, ctypes.c_uint32, ctypes.c_int64
+    lib.oracle_proxy_map.argtypes = [i, i, i, vp, vp, d, vp, i]
+    lib.oracle_quantize.argtypes = [vp, i64, vp]
+    lib.oracle_quantize.restype = None
+    lib.oracle_proxy_rows.argtypes = [i, i, i, vp, vp, d, i64, vp, vp, vp, i]
+    lib.oracle_route.argtypes = [i, i, vp, u32, u32, vp, vp, vp, i]
+    lib.oracle_vs_masses.argtypes = [i, i, vp, vp, vp, i]
+    lib.oracle_pe_rows.argtypes = [i, i, i, vp, vp, d, i64, vp, vp, vp, i]
+    lib.oracle_select_vs.argtypes = [i, i, vp, vp, vp, u32, u32, i, vp, vp]
+    lib.oracle_select_vs_gamma.argtypes = [i, i, vp, vp, vp, u32, u32, i, vp, vp]
+    lib.oracle_route_jsd.argtypes = [i, i, vp, vp, d, vp, vp]
+    lib.oracle_pe_map.argtypes = [i, i, i, vp, vp, d, vp, i]
+    lib.oracle_select_pe.argtypes = [i, i, vp, vp, i, u32, u32, u32, u32, i, vp, i]
+    lib.oracle_build_mask.argtypes = [i, i, vp, vp, vp, vp, vp]
+    lib.oracle_attention_rows.argtypes = [i, i, i, vp, vp, vp, d, vp, i64, vp, vp, vp, i]
+    lib.oracle_selected_pairs.argtypes = [i, i, vp]
+    lib.oracle_selected_pairs.restype = ctypes.c_int64
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
         build()
-        lib = ctypes.CDLL(_LIB)
-        i, vp, d, u32, i64 = ctypes.c_int, ctypes.c_void_p, ctypes.c_double, ctypes.c_uint32, ctypes.c_int64
-        lib.oracle_proxy_map.argtypes = [i, i, i, vp, vp, d, vp, i]
-        lib.oracle_quantize.argtypes = [vp, i64, vp]
-        lib.oracle_quantize.restype = None
-        lib.oracle_proxy_rows.argtypes = [i, i, i, vp, vp, d, i64, vp, vp, vp, i]
-        lib.oracle_route.argtypes = [i, i, vp, u32, u32, vp, vp, vp, i]
-        lib.oracle_vs_masses.argtypes = [i, i, vp, vp, vp, i]
-        lib.oracle_pe_rows.argtypes = [i, i, i, vp, vp, d, i64, vp, vp, vp, i]
-        lib.oracle_select_vs.argtypes = [i, i, vp, vp, vp, u32, u32, i, vp, vp]
-        lib.oracle_select_vs_gamma.argtypes = [i, i, vp, vp, vp, u32, u32, i, vp, vp]
-        lib.oracle_route_jsd.argtypes = [i, i, vp, vp, d, vp, vp]
-        lib.oracle_pe_map.argtypes = [i, i, i, vp, vp, d, vp, i]
-        lib.oracle_select_pe.argtypes = [i, i, vp, vp, i, u32, u32, u32, u32, i, vp, i]
-        lib.oracle_build_mask.argtypes = [i, i, vp, vp, vp, vp, vp]
-        lib.oracle_attention_rows.argtypes = [i, i, i, vp, vp, vp, d, vp, i64, vp, vp, vp, i]
-        lib.oracle_selected_pairs.argtypes = [i, i, vp]
-        lib.oracle_selected_pairs.restype = ctypes.c_int64
-        _lib = lib
+        _lib = _configure(ctypes.CDLL(_LIB))
     return _lib
 
 
