@@ -32,7 +32,7 @@ def assert_status_ok(ws):
     assert st == 0, crisp.status_string(st)
 
 
-def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_only=True):
+def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_only=True, out_dev=None, scale=0.0):
     """Runs A1..A8 through the step entry points; returns numpy copies. Also
     runs the fused A1+A3 pass (vmass_fused, smass_fused), whose outputs start
     as all-ones words so that an entry it fails to write shows."""
@@ -43,8 +43,8 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
     qd = to_dev(q) if q_dev is None else q_dev
     kd = to_dev(k) if k_dev is None else k_dev
     vd = to_dev(v) if v_dev is None else v_dev
-    out = empty((hq, n, 128), torch.bfloat16)
-    s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+    out = empty((hq, n, 128), torch.bfloat16) if out_dev is None else out_dev
+    s = crisp.make_shape(hq, hkv, n, qd, kd, out, scale=scale)
     ws = new_workspace(s)
     pmap = torch.full((hq, B, crisp.map_ld(n)), float("nan"), dtype=torch.float32, device="cuda")
     vmass = empty((hq, nb), torch.int64)

@@ -77,14 +77,14 @@ def sample_rows(hq, n, count, seed):
     return np.array(heads, np.int32), np.array(toks, np.int32)
 
 
-def check_attention(q, k, v, out, rowbits, rows=None):
+def check_attention(q, k, v, out, rowbits, rows=None, scale=None):
     hq, n, _ = q.shape
     if rows is None:
         h, t = np.meshgrid(np.arange(hq), np.arange(n), indexing="ij")
         h, t = h.ravel().astype(np.int32), t.ravel().astype(np.int32)
     else:
         h, t = rows
-    ref = oracle.attention_rows(q, k, v, h, t, rowbits=rowbits)
+    ref = oracle.attention_rows(q, k, v, h, t, rowbits=rowbits, scale=scale)
     got = out.float().cpu().numpy()[h, t]
     mx, mean = attn_error(got, ref)
     assert mx <= ATT_MAX and mean <= ATT_MEAN, (mx, mean)
@@ -211,6 +211,24 @@ def test_strided_token_major_layout():
     assert np.array_equal(got["pmap"], ref["pmap"])
     assert np.array_equal(got["rowbits"], ref["rowbits"])
     assert torch.equal(got["out"], ref["out"])
+
+
+def test_custom_scale_and_mixed_layouts():
+    # A softmax scale other than 1/sqrt(128); q contiguous, k and v
+    # token-major ([n][heads][128] storage) and the output token-major too.
+    hq, hkv, n, scale = 4, 2, 1536, 0.05
+    w = synth.small("scale", hq, hkv, n, 81)
+    q, k, v = w.generate()
+    params = crisp.params_default()
+    kt = to_dev(np.ascontiguousarray(k.transpose(1, 0, 2))).permute(1, 0, 2)
+    vt = to_dev(np.ascontiguousarray(v.transpose(1, 0, 2))).permute(1, 0, 2)
+    ot = torch.empty((n, hq, 128), dtype=torch.bfloat16, device="cuda").permute(1, 0, 2)
+    r = run_steps(q, k, v, params, k_dev=kt, v_dev=vt, out_dev=ot, scale=scale)
+    check_map(r["pmap"], oracle.proxy_map(q, k, scale=scale))
+    rb, route = check_index_sets(r, params)
+    if (route == 0).any():
+        check_map(r["pbar"][route == 0], oracle.pe_map(q, k, scale=scale)[route == 0])
+    check_attention(q, k, v, r["out"], rb, scale=scale)
 
 
 def test_prefill_layer_matches_steps():
