@@ -295,3 +295,31 @@ def read_status(ws, stream=None) -> int:
     s = ctypes.c_int()
     _check(lib().crisp_read_status(_ptr(ws), _stream(stream), ctypes.byref(s)), "crisp_read_status")
     return s.value
+
+
+def attention(q, k, v, params=None, scale=0.0, stream=None, check=True):
+    """One CRISP sparse-prefill layer on torch tensors: q [hq][n][128], k and v
+    [hkv][n][128], bf16, on the current CUDA device, features contiguous (any
+    head and token strides that are multiples of 8 elements). Allocates the
+    output (contiguous [hq][n][128] bf16) and a layer workspace with torch,
+    runs crisp_prefill_layer on `stream` and returns the output. params: a
+    Params (default: the paper's universal configuration); scale 0 means
+    1/sqrt(128). With check=True the stream is synchronised and a device-side
+    error raises CrispError."""
+    import torch
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape:
+        raise ValueError("attention: q must be [hq][n][128], k and v [hkv][n][128]")
+    hq, n, _ = q.shape
+    hkv = k.shape[0]
+    out = torch.empty((hq, n, D), dtype=torch.bfloat16, device=q.device)
+    shape = make_shape(hq, hkv, n, q, k, out, scale=scale)
+    if k.stride() != v.stride():
+        raise ValueError("attention: k and v must share their strides")
+    ws = torch.empty(max(layer_workspace_size(shape), 256), dtype=torch.uint8, device=q.device)
+    workspace_init(ws, stream)
+    prefill_layer(shape, params if params is not None else params_default(), q, k, v, out, ws, stream)
+    if check:
+        st = read_status(ws, stream)
+        if st != 0:
+            raise CrispError(st, "crisp_prefill_layer (device)")
+    return out

@@ -231,6 +231,22 @@ def test_custom_scale_and_mixed_layouts():
     check_attention(q, k, v, r["out"], rb, scale=scale)
 
 
+def test_attention_convenience_call_matches_the_layer():
+    # crisp.attention allocates the output and workspace with torch and runs
+    # the same layer call: identical bits, ragged length included.
+    for hq, hkv, n, seed in ((8, 2, 2048, 54), (4, 1, 1000, 55)):
+        w = synth.small("conv", hq, hkv, n, seed)
+        q, k, v = w.generate()
+        qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+        got = crisp.attention(qd, kd, vd)
+        ref = empty((hq, n, 128), torch.bfloat16)
+        s = crisp.make_shape(hq, hkv, n, qd, kd, ref)
+        ws = new_workspace(s, layer=True)
+        crisp.prefill_layer(s, crisp.params_default(), qd, kd, vd, ref, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+
+
 def test_prefill_layer_matches_steps():
     for hq, hkv, n, seed in ((8, 2, 2048, 51), (4, 1, 640, 52), (4, 2, 1337, 53)):
         w = synth.small("layer", hq, hkv, n, seed)
