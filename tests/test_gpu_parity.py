@@ -247,6 +247,23 @@ def test_attention_convenience_call_matches_the_layer():
         assert torch.equal(got, ref)
 
 
+@pytest.mark.parametrize("scale", [1.0, 1e-3])
+def test_extreme_softmax_scales(scale):
+    # scale 1: logits with a spread of ~11 (rows ruled by single keys; the
+    # lazy reference max must move, through the exact path); scale 1e-3:
+    # nearly uniform rows.
+    hq, hkv, n = 4, 2, 1280
+    w = synth.small("scales", hq, hkv, n, 82)
+    q, k, v = w.generate()
+    params = crisp.params_default()
+    r = run_steps(q, k, v, params, scale=scale)
+    check_map(r["pmap"], oracle.proxy_map(q, k, scale=scale))
+    rb, route = check_index_sets(r, params)
+    if (route == 0).any():
+        check_map(r["pbar"][route == 0], oracle.pe_map(q, k, scale=scale)[route == 0])
+    check_attention(q, k, v, r["out"], rb, scale=scale)
+
+
 def test_prefill_layer_matches_steps():
     for hq, hkv, n, seed in ((8, 2, 2048, 51), (4, 1, 640, 52), (4, 2, 1337, 53)):
         w = synth.small("layer", hq, hkv, n, seed)
