@@ -100,6 +100,8 @@ CASES = [
     ("gqa7-1152", 7, 1, 1152, 6, [0, 3, 6]),
     ("nb33-4224", 4, 2, 4224, 7, None),
     ("all-pe-2k", 4, 2, 2048, 8, []),
+    ("single-head-512", 1, 1, 512, 12, None),
+    ("gqa16-640", 16, 1, 640, 13, None),
     # 128 does not divide n: a short last block of t tokens (t = 44, 104, 1,
     # 127, 4); at 2049 the recency columns straddle two proxy CTAs
     ("ragged-300", 2, 1, 300, 31, None),
