@@ -603,12 +603,11 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
   // download of chunk c-1 overlap the compute of chunk c, and consecutive
   // chunks alternate between two compute streams (each with its own part of
   // the workspace), so that one chunk's short selection kernels run beside
-  // the previous chunk's attention. Long sequences use
-  // half a group per chunk (when G is even), and the first and last half
-  // groups of the layer go one head at a time, so that the pipeline fills
-  // and drains with a single head; shorter ones a whole group per chunk,
-  // where the extra launches and copies would cost more than the shorter
-  // fill.
+  // the previous chunk's attention. Long sequences use half a group per
+  // chunk (when G is even), and the first and last half groups of the layer
+  // go one head at a time, so that the pipeline fills and drains with a
+  // single head; shorter ones a whole group per chunk, where the extra
+  // launches and copies would cost more than the shorter fill.
   const int G = s.hq / s.hkv;
   const int hc = (G % 2 == 0 && s.seq_len >= kHalfGroupChunkLen) ? G / 2 : G;  // query heads per chunk
   const size_t plane = static_cast<size_t>(s.seq_len) * kD * 2;  // bytes of one head
