@@ -189,3 +189,13 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(crisp, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         crisp.lib()
+
+
+def test_readme_names_exist_in_the_binding():
+    # Every crisp.<name> the README shows is part of the binding.
+    import re
+    text = open(os.path.join(os.path.dirname(__file__), "..", "README.md")).read()
+    names = set(re.findall(r"crisp\.([a-z_A-Z]+)\(", text))
+    assert names, "README shows no calls"
+    missing = sorted(n for n in names if not hasattr(crisp, n))
+    assert not missing, missing
