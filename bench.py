@@ -338,12 +338,12 @@ def run_crisp(args):
     stages = ["proxy_masses", "route", "select_vs", "pe_map", "select_pe", "mask", "attention"]
     calls = [
         lambda: crisp.proxy_masses(s, qd, kd, vmass, smass, rmass, ws, stream),
-        lambda: crisp.route_cstruct(s, params, vmass, rmass, cstruct, total, route, stream),
-        lambda: crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws, stream),
-        lambda: crisp.pe_map(s, qd, kd, route, pbar, ws, stream),
+        lambda: crisp.route_cstruct_masses(s, params, vmass, rmass, cstruct, total, route, ws, stream),
+        lambda: crisp.select_vs_masses(s, params, vmass, smass, route, vbits, sbits, ws, stream),
+        lambda: crisp.pe_pool(s, qd, kd, route, pbar, ws, stream),
         lambda: crisp.select_pe(s, params, pbar, route, pebits, ws, stream),
         lambda: crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, ws, stream),
-        lambda: crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws, stream),
+        lambda: crisp.sparse_prefill_mask(s, qd, kd, vd, rowbits, order, out, ws, stream),
     ]
     # our kernel launches per step: proxy statistics 2, fused masses 2,
     # route 1, select_vs 1, pe_map 3, select_pe 1, mask+schedule 2, attention 1
@@ -444,7 +444,7 @@ def run_crisp(args):
         d_ms = e0.elapsed_time(e1)
         dense = {"ms": d_ms, "tflops": 4 * 128 * dense_pairs / (d_ms * 1e-3) / 1e12,
                  "attention_speedup": d_ms / attn_ms, "layer_speedup": d_ms / ms_per_step}
-        crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws, stream)
+        crisp.sparse_prefill_mask(s, qd, kd, vd, rowbits, order, out, ws, stream)
 
     # End to end through the public API with HOST buffers: one call of
     # crisp_prefill_layer_host per step, which uploads q, k, v from pinned

@@ -29,7 +29,8 @@ def map_ld(n: int) -> int:
     return num_blocks(n) * B
 
 STATUS_NAMES = {0: "CRISP_OK", 1: "CRISP_ERR_INVALID_ARG", 2: "CRISP_ERR_SHAPE", 3: "CRISP_ERR_ALIGN",
-                4: "CRISP_ERR_WORKSPACE", 5: "CRISP_ERR_CUDA", 6: "CRISP_ERR_TIMEOUT", 7: "CRISP_ERR_DEVICE"}
+                4: "CRISP_ERR_WORKSPACE", 5: "CRISP_ERR_CUDA", 6: "CRISP_ERR_TIMEOUT", 7: "CRISP_ERR_DEVICE",
+                8: "CRISP_ERR_BOUNDS"}
 PE_GAMMA, PE_NOISE = 0, 1
 ROUTE_CSTRUCT, ROUTE_JSD = 0, 1
 VS_NOISE, VS_GAMMA = 0, 1
@@ -57,7 +58,8 @@ class Params(ctypes.Structure):
                 ("kmin_blocks", ctypes.c_int32), ("pe_mode", ctypes.c_int32),
                 ("route_mode", ctypes.c_int32), ("vs_mode", ctypes.c_int32),
                 ("vs_gamma_num", ctypes.c_uint32), ("vs_gamma_den", ctypes.c_uint32),
-                ("jsd_tau", ctypes.c_float), ("dense_below", ctypes.c_int32)]
+                ("jsd_tau", ctypes.c_float), ("dense_below", ctypes.c_int32),
+                ("sink_tokens", ctypes.c_int32), ("recency_tokens", ctypes.c_int32)]
 
 
 class LayerViews(ctypes.Structure):
@@ -82,19 +84,23 @@ def lib():
         L.crisp_workspace_init.argtypes = [vp, sz, st]
         L.crisp_proxy_map.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
         L.crisp_proxy_map_noalloc.argtypes = [P(Shape), vp, vp, vp, st]
+        L.crisp_noalloc_read_status.argtypes = [st, P(ctypes.c_int)]
         L.crisp_block_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
         L.crisp_proxy_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, st]
         L.crisp_host_pipeline_create.argtypes = [P(vp)]
         L.crisp_host_pipeline_destroy.argtypes = [vp]
         L.crisp_prefill_layer_host.argtypes = [vp, P(Shape), P(Params)] + [vp] * 9 + [sz, st]
-        L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, st]
-        L.crisp_route_jsd.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, st]
+        L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, sz, st]
+        L.crisp_route_cstruct_masses.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
+        L.crisp_route_jsd.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, sz, st]
         L.crisp_wait_selftest.argtypes = [vp, sz, ctypes.c_int64, st]
-        L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
-        L.crisp_pe_map.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
+        L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, vp, sz, st]
+        L.crisp_select_vs_masses.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
+        L.crisp_pe_pool.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
         L.crisp_select_pe.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, sz, st]
         L.crisp_build_mask.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, vp, sz, st]
-        L.crisp_sparse_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, st]
+        L.crisp_sparse_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, st]
+        L.crisp_sparse_prefill_mask.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, st]
         L.crisp_dense_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
         L.crisp_layer_views_get.argtypes = [P(Shape), vp, P(LayerViews)]
         L.crisp_prefill_layer.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, sz, st]
@@ -102,9 +108,10 @@ def lib():
         L.crisp_status_string.argtypes = [ctypes.c_int]
         L.crisp_status_string.restype = ctypes.c_char_p
         for name in ("crisp_workspace_size", "crisp_layer_workspace_size", "crisp_workspace_init", "crisp_proxy_map",
-                     "crisp_proxy_map_noalloc",
-                     "crisp_block_masses", "crisp_proxy_masses", "crisp_route_cstruct", "crisp_route_jsd", "crisp_select_vs", "crisp_pe_map",
-                     "crisp_select_pe", "crisp_build_mask", "crisp_sparse_prefill", "crisp_dense_prefill",
+                     "crisp_proxy_map_noalloc", "crisp_noalloc_read_status", "crisp_block_masses",
+                     "crisp_proxy_masses", "crisp_route_cstruct", "crisp_route_cstruct_masses", "crisp_route_jsd",
+                     "crisp_select_vs", "crisp_select_vs_masses", "crisp_pe_pool", "crisp_select_pe",
+                     "crisp_build_mask", "crisp_sparse_prefill", "crisp_sparse_prefill_mask", "crisp_dense_prefill",
                      "crisp_layer_views_get", "crisp_prefill_layer", "crisp_read_status",
                      "crisp_host_pipeline_create", "crisp_host_pipeline_destroy", "crisp_prefill_layer_host",
                      "crisp_wait_selftest"):
@@ -189,6 +196,13 @@ def proxy_map_noalloc(shape, q, k, pmap, stream=None):
            "crisp_proxy_map_noalloc")
 
 
+def noalloc_read_status(stream=None) -> int:
+    """The status word of proxy_map_noalloc's static scratch (syncs the stream)."""
+    s = ctypes.c_int()
+    _check(lib().crisp_noalloc_read_status(_stream(stream), ctypes.byref(s)), "crisp_noalloc_read_status")
+    return s.value
+
+
 def block_masses(shape, pmap, vmass, smass, rmass, ws, stream=None):
     _check(lib().crisp_block_masses(ctypes.byref(shape), _ptr(pmap), _ptr(vmass), _ptr(smass), _ptr(rmass), _ptr(ws),
                                     _nbytes(ws), _stream(stream)), "crisp_block_masses")
@@ -200,25 +214,44 @@ def proxy_masses(shape, q, k, vmass, smass, rmass, ws, stream=None):
                                     _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_proxy_masses")
 
 
-def route_cstruct(shape, params, vmass, rmass, cstruct, total, route, stream=None):
-    _check(lib().crisp_route_cstruct(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(rmass),
-                                     _ptr(cstruct), _ptr(total), _ptr(route), _stream(stream)), "crisp_route_cstruct")
+def route_cstruct(shape, params, pmap, cstruct, total, route, ws, stream=None):
+    """A2 from the proxy map (any sink / recency slice widths of params)."""
+    _check(lib().crisp_route_cstruct(ctypes.byref(shape), ctypes.byref(params), _ptr(pmap), _ptr(cstruct),
+                                     _ptr(total), _ptr(route), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "crisp_route_cstruct")
 
 
-def route_jsd(shape, params, vmass, pbar, jsd, route, stream=None):
+def route_cstruct_masses(shape, params, vmass, rmass, cstruct, total, route, ws, stream=None):
+    """A2 from the block masses (both slices one block wide)."""
+    _check(lib().crisp_route_cstruct_masses(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(rmass),
+                                            _ptr(cstruct), _ptr(total), _ptr(route), _ptr(ws), _nbytes(ws),
+                                            _stream(stream)), "crisp_route_cstruct_masses")
+
+
+def route_jsd(shape, params, vmass, pbar, jsd, route, ws, stream=None):
     """FlexPrefill's divergence routing (comparator); pbar must hold row nb-1 of every head."""
     _check(lib().crisp_route_jsd(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(pbar), _ptr(jsd),
-                                 _ptr(route), _stream(stream)), "crisp_route_jsd")
+                                 _ptr(route), _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_route_jsd")
 
 
-def select_vs(shape, params, vmass, smass, route, vbits, sbits, ws, stream=None):
-    _check(lib().crisp_select_vs(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(smass), _ptr(route),
-                                 _ptr(vbits), _ptr(sbits), _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_select_vs")
+def select_vs(shape, params, pmap, route, vmass, smass, vbits, sbits, ws, stream=None):
+    """A4 from the proxy map (writes the block masses too)."""
+    _check(lib().crisp_select_vs(ctypes.byref(shape), ctypes.byref(params), _ptr(pmap), _ptr(route), _ptr(vmass),
+                                 _ptr(smass), _ptr(vbits), _ptr(sbits), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "crisp_select_vs")
 
 
-def pe_map(shape, q, k, route, pbar, ws, stream=None):
-    _check(lib().crisp_pe_map(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(route), _ptr(pbar), _ptr(ws), _nbytes(ws),
-                              _stream(stream)), "crisp_pe_map")
+def select_vs_masses(shape, params, vmass, smass, route, vbits, sbits, ws, stream=None):
+    """A4 from the block masses."""
+    _check(lib().crisp_select_vs_masses(ctypes.byref(shape), ctypes.byref(params), _ptr(vmass), _ptr(smass),
+                                        _ptr(route), _ptr(vbits), _ptr(sbits), _ptr(ws), _nbytes(ws),
+                                        _stream(stream)), "crisp_select_vs_masses")
+
+
+def pe_pool(shape, q, k, route, pbar, ws, stream=None):
+    """A5: the pooled estimate of the PE heads (route[h] == 0)."""
+    _check(lib().crisp_pe_pool(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(route), _ptr(pbar), _ptr(ws), _nbytes(ws),
+                               _stream(stream)), "crisp_pe_pool")
 
 
 def select_pe(shape, params, pbar, route, pebits, ws, stream=None):
@@ -232,10 +265,18 @@ def build_mask(shape, route, vbits, sbits, pebits, rowbits, counts, order, ws, s
            "crisp_build_mask")
 
 
-def sparse_prefill(shape, q, k, v, rowbits, order, out, ws, stream=None):
-    """order: the schedule from build_mask, or None (the same kv-group-major order)."""
-    _check(lib().crisp_sparse_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(rowbits), _ptr(order),
-                                      _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)), "crisp_sparse_prefill")
+def sparse_prefill(shape, q, k, v, route, vbits, sbits, pebits, out, ws, stream=None):
+    """A8 from the index sets (the mask and schedule are built in ws)."""
+    _check(lib().crisp_sparse_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(route), _ptr(vbits),
+                                      _ptr(sbits), _ptr(pebits), _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "crisp_sparse_prefill")
+
+
+def sparse_prefill_mask(shape, q, k, v, rowbits, order, out, ws, stream=None):
+    """A8 over a block mask; order: the schedule from build_mask, or None (the same kv-group-major order)."""
+    _check(lib().crisp_sparse_prefill_mask(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(rowbits),
+                                           _ptr(order), _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "crisp_sparse_prefill_mask")
 
 
 def dense_prefill(shape, q, k, v, out, ws, stream=None):

@@ -50,7 +50,15 @@ crisp_status check_params(const crisp_params* p) {
   if (p->vs_gamma_den == 0 || p->vs_gamma_num > p->vs_gamma_den) return CRISP_ERR_INVALID_ARG;
   if (!(p->jsd_tau >= 0.f && p->jsd_tau <= 1.f)) return CRISP_ERR_INVALID_ARG;
   if (p->dense_below < 0) return CRISP_ERR_INVALID_ARG;
+  if (p->sink_tokens < 0 || p->sink_tokens > kMaxSeq || p->recency_tokens < 0 || p->recency_tokens > kMaxSeq)
+    return CRISP_ERR_INVALID_ARG;
   return CRISP_OK;
+}
+
+// Routing from block masses reads the sink slice as key block 0 and the
+// recency slice as the recency mass: both slices must be one block wide.
+crisp_status check_block_slices(const crisp_params* p) {
+  return (p->sink_tokens == kB && p->recency_tokens == kB) ? CRISP_OK : CRISP_ERR_INVALID_ARG;
 }
 
 crisp_shape normalised(const crisp_shape& s) {
@@ -126,6 +134,10 @@ ScratchLayout scratch_layout(const crisp_shape& s) {
   L.qbar = o;        o = up(o + hq * nb * kD * 4);
   L.kbar = o;        o = up(o + hkv * nb * kD * 4);
   L.srev = o;        o = up(o + hq * (W + 2) * 4);
+  L.rmass = o;       o = up(o + hq * 8);
+  L.rowbits = o;     o = up(o + hq * nb * W * 4);
+  L.counts = o;      o = up(o + hq * nb * 4);
+  L.order = o;       o = up(o + hq * nb * 4);
   L.total = o;
   return L;
 }
@@ -133,7 +145,8 @@ ScratchLayout scratch_layout(const crisp_shape& s) {
 LayerLayout layer_layout(const crisp_shape& s) {
   const size_t hq = s.hq, nb = num_blocks(s.seq_len), W = bit_words(static_cast<int>(nb));
   LayerLayout L{};
-  size_t o = scratch_layout(s).total;
+  const ScratchLayout S = scratch_layout(s);
+  size_t o = S.total;
   L.vmass = o;      o = up(o + hq * nb * 8);
   L.smass = o;      o = up(o + hq * nb * 8);
   L.rmass = o;      o = up(o + hq * 8);
@@ -144,9 +157,10 @@ LayerLayout layer_layout(const crisp_shape& s) {
   L.sbits = o;      o = up(o + hq * W * 4);
   L.pbar = o;       o = up(o + hq * nb * nb * 4);
   L.pebits = o;     o = up(o + hq * nb * W * 4);
-  L.rowbits = o;    o = up(o + hq * nb * W * 4);
-  L.counts = o;     o = up(o + hq * nb * 4);
-  L.order = o;      o = up(o + hq * nb * 4);
+  // The mask and the schedule share the scratch regions crisp_sparse_prefill uses.
+  L.rowbits = S.rowbits;
+  L.counts = S.counts;
+  L.order = S.order;
   L.total = o;
   return L;
 }
@@ -173,6 +187,8 @@ void crisp_params_default(crisp_params* p) {
   p->vs_gamma_den = 100;
   p->jsd_tau = 0.1f;
   p->dense_below = 0;
+  p->sink_tokens = kB;
+  p->recency_tokens = kB;
 }
 
 crisp_status crisp_workspace_size(const crisp_shape* shape, size_t* bytes) {
@@ -273,6 +289,19 @@ crisp_status crisp_proxy_map_noalloc(const crisp_shape* shape, const void* q, co
   return from_cuda(launch_proxy(s, maps, pmap, scratch, stream));
 }
 
+crisp_status crisp_noalloc_read_status(crisp_stream_t stream, crisp_status* status) {
+  if (!status) return CRISP_ERR_INVALID_ARG;
+  char* scratch = nullptr;
+  crisp_status st = noalloc_scratch(&scratch);
+  if (st != CRISP_OK) return st;
+  DevStatus host{};
+  if (cudaMemcpyAsync(&host, scratch, sizeof(host), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return CRISP_ERR_CUDA;
+  *status = static_cast<crisp_status>(host.code);
+  return CRISP_OK;
+}
+
 crisp_status crisp_block_masses(const crisp_shape* shape, const float* pmap, uint64_t* vmass, uint64_t* smass,
                                 uint64_t* rmass, void* ws, size_t ws_bytes, crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
@@ -302,32 +331,52 @@ crisp_status crisp_proxy_masses(const crisp_shape* shape, const void* q, const v
   return from_cuda(launch_proxy_masses(s, maps, vmass, smass, rmass, static_cast<char*>(ws), stream));
 }
 
-crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
-                                 const uint64_t* rmass, uint64_t* cstruct, uint64_t* total, uint8_t* route,
+crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const float* pmap,
+                                 uint64_t* cstruct, uint64_t* total, uint8_t* route, void* ws, size_t ws_bytes,
                                  crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
   if (st != CRISP_OK) return st;
   if ((st = check_params(params)) != CRISP_OK) return st;
+  if (!pmap || !cstruct || !total || !route) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(pmap) || !aligned(cstruct, 8) || !aligned(total, 8)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  return from_cuda(launch_route_map(s, *params, pmap, cstruct, total, route, stream));
+}
+
+crisp_status crisp_route_cstruct_masses(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
+                                        const uint64_t* rmass, uint64_t* cstruct, uint64_t* total, uint8_t* route,
+                                        void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if ((st = check_params(params)) != CRISP_OK) return st;
+  if ((st = check_block_slices(params)) != CRISP_OK) return st;
   if (!vmass || !rmass || !cstruct || !total || !route) return CRISP_ERR_INVALID_ARG;
   if (!aligned(vmass, 8) || !aligned(rmass, 8) || !aligned(cstruct, 8) || !aligned(total, 8)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_route(normalised(*shape), *params, vmass, rmass, cstruct, total, route, stream));
+  return from_cuda(launch_route(s, *params, vmass, rmass, cstruct, total, route, stream));
 }
 
 crisp_status crisp_route_jsd(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
-                             const float* pbar, double* jsd, uint8_t* route, crisp_stream_t stream) {
+                             const float* pbar, double* jsd, uint8_t* route, void* ws, size_t ws_bytes,
+                             crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
   if (st != CRISP_OK) return st;
   if ((st = check_params(params)) != CRISP_OK) return st;
   if (!vmass || !pbar || !route) return CRISP_ERR_INVALID_ARG;
   if (!aligned(vmass, 8) || !aligned(pbar, 4) || (jsd && !aligned(jsd, 8))) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_route_jsd(normalised(*shape), *params, vmass, pbar, jsd, route, stream));
+  return from_cuda(launch_route_jsd(s, *params, vmass, pbar, jsd, route, stream));
 }
 
-crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
-                             const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
-                             void* ws, size_t ws_bytes, crisp_stream_t stream) {
+crisp_status crisp_select_vs_masses(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
+                                    const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
+                                    void* ws, size_t ws_bytes, crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
   if (st != CRISP_OK) return st;
   if ((st = check_params(params)) != CRISP_OK) return st;
@@ -339,8 +388,26 @@ crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* param
   return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, stream));
 }
 
-crisp_status crisp_pe_map(const crisp_shape* shape, const void* q, const void* k, const uint8_t* route, float* pbar,
-                          void* ws, size_t ws_bytes, crisp_stream_t stream) {
+crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* params, const float* pmap,
+                             const uint8_t* route, uint64_t* vmass, uint64_t* smass, uint32_t* vbits,
+                             uint32_t* sbits, void* ws, size_t ws_bytes, crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if ((st = check_params(params)) != CRISP_OK) return st;
+  if (!pmap || !route || !vmass || !smass || !vbits || !sbits) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(pmap) || !aligned(vmass, 8) || !aligned(smass, 8) || !aligned(vbits, 4) || !aligned(sbits, 4))
+    return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  char* wsb = static_cast<char*>(ws);
+  auto* rmass = reinterpret_cast<uint64_t*>(wsb + scratch_layout(s).rmass);
+  if (launch_block_masses(s, pmap, vmass, smass, rmass, wsb, stream) != cudaSuccess) return CRISP_ERR_CUDA;
+  return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, stream));
+}
+
+crisp_status crisp_pe_pool(const crisp_shape* shape, const void* q, const void* k, const uint8_t* route, float* pbar,
+                           void* ws, size_t ws_bytes, crisp_stream_t stream) {
   crisp_status st = check_shape(shape);
   if (st != CRISP_OK) return st;
   if (!q || !k || !route || !pbar) return CRISP_ERR_INVALID_ARG;
@@ -400,10 +467,37 @@ static crisp_status attention_common(const crisp_shape* shape, const void* q, co
   return from_cuda(launch_attention(s, maps, rowbits, order, out, static_cast<char*>(ws), dense, stream));
 }
 
-crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v,
-                                  const uint32_t* rowbits, const int32_t* order, void* out, void* ws,
-                                  size_t ws_bytes, crisp_stream_t stream) {
+crisp_status crisp_sparse_prefill_mask(const crisp_shape* shape, const void* q, const void* k, const void* v,
+                                       const uint32_t* rowbits, const int32_t* order, void* out, void* ws,
+                                       size_t ws_bytes, crisp_stream_t stream) {
   return attention_common(shape, q, k, v, rowbits, order, out, ws, ws_bytes, stream, false);
+}
+
+crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v,
+                                  const uint8_t* route, const uint32_t* vbits, const uint32_t* sbits,
+                                  const uint32_t* pebits, void* out, void* ws, size_t ws_bytes,
+                                  crisp_stream_t stream) {
+  crisp_status st = check_shape(shape);
+  if (st != CRISP_OK) return st;
+  if (!q || !k || !v || !out || !route || !vbits || !sbits || !pebits) return CRISP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
+  if (!aligned(vbits, 4) || !aligned(sbits, 4) || !aligned(pebits, 4)) return CRISP_ERR_ALIGN;
+  const crisp_shape s = normalised(*shape);
+  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+  if ((st = check_device()) != CRISP_OK) return st;
+  // A7 into the workspace, then A8 over that mask in its schedule.
+  char* wsb = static_cast<char*>(ws);
+  const ScratchLayout L = scratch_layout(s);
+  auto* rowbits = reinterpret_cast<uint32_t*>(wsb + L.rowbits);
+  auto* counts = reinterpret_cast<int32_t*>(wsb + L.counts);
+  auto* order = reinterpret_cast<int32_t*>(wsb + L.order);
+  TmaMaps maps;
+  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  if (launch_build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, wsb, stream) != cudaSuccess)
+    return CRISP_ERR_CUDA;
+  return from_cuda(launch_attention(s, maps, rowbits, order, out, wsb, false, stream));
 }
 
 crisp_status crisp_dense_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v, void* out,
@@ -505,6 +599,7 @@ crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* p
   crisp_status st = check_shape(shape, 0);
   if (st != CRISP_OK) return st;
   if ((st = check_params(params)) != CRISP_OK) return st;
+  if ((st = check_block_slices(params)) != CRISP_OK) return st;
   if (shape->seq_len == 0) return CRISP_OK;  // an empty input: nothing to compute
   if (!q || !k || !v || !out) return CRISP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
@@ -586,6 +681,7 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
   crisp_status st = check_shape(shape, 0);
   if (st != CRISP_OK) return st;
   if ((st = check_params(params)) != CRISP_OK) return st;
+  if ((st = check_block_slices(params)) != CRISP_OK) return st;
   if (shape->seq_len == 0) return CRISP_OK;  // an empty input: nothing to compute
   if (!q_host || !k_host || !v_host || !out_host || !q || !k || !v || !out) return CRISP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
@@ -720,6 +816,7 @@ const char* crisp_status_string(crisp_status status) {
     case CRISP_ERR_CUDA: return "CUDA runtime error";
     case CRISP_ERR_TIMEOUT: return "device wait timed out";
     case CRISP_ERR_DEVICE: return "device is not sm_103";
+    case CRISP_ERR_BOUNDS: return "device index outside its buffer (bounds-checking build)";
   }
   return "unknown status";
 }

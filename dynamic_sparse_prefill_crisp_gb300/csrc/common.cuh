@@ -67,6 +67,10 @@ struct ScratchLayout {
   size_t qbar;         // float  [hq][nb][128]
   size_t kbar;         // float  [hkv][nb][128]
   size_t srev;         // uint32 [hq][W + 2]  slash bits reversed
+  size_t rmass;        // uint64 [hq]      recency masses of crisp_select_vs (from the map)
+  size_t rowbits;      // uint32 [hq][nb][W]  block mask built by crisp_sparse_prefill
+  size_t counts;       // int32  [hq][nb]      blocks per row
+  size_t order;        // int32  [hq*nb]       attention schedule
   size_t total;
 };
 
@@ -93,6 +97,8 @@ cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_
                                 uint64_t* rmass, char* ws, cudaStream_t st);
 cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const uint64_t* rmass,
                          uint64_t* cstruct, uint64_t* total, uint8_t* route, cudaStream_t st);
+cudaError_t launch_route_map(const crisp_shape& s, const crisp_params& p, const float* pmap, uint64_t* cstruct,
+                             uint64_t* total, uint8_t* route, cudaStream_t st);
 cudaError_t launch_route_jsd(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const float* pbar,
                              double* jsd, uint8_t* route, cudaStream_t st);
 cudaError_t launch_select_vs(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass,

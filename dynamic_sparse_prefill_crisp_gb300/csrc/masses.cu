@@ -139,6 +139,73 @@ __global__ void route_kernel(const uint64_t* __restrict__ vmass, const uint64_t*
   }
 }
 
+// C_struct from the proxy map itself, for any slice widths: one CTA per
+// 128x128 tile (column block c, head h), 16-byte streaming loads as in
+// mass_tiles; the tile's quanta go to the head's total and, for columns j in
+// [0, sink) U [n - recency, n), to its slice sum (both zeroed beforehand;
+// integer atomics, so the order of the tiles does not matter).
+__global__ void __launch_bounds__(kMassThreads) cstruct_tiles(const float* __restrict__ pmap, int64_t ld, int n,
+                                                              int sink, int recency, uint64_t* __restrict__ cstruct,
+                                                              uint64_t* __restrict__ total) {
+  __shared__ uint64_t red[2][kMassThreads / 32];
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int cq = threadIdx.x & 31, rg = threadIdx.x >> 5;
+  const float* base = pmap + static_cast<size_t>(h) * kB * ld + static_cast<size_t>(c) * kB + cq * 4;
+  const int j0 = c * kB + cq * 4;  // key token of this thread's first column
+  bool in_slice[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) in_slice[e] = j0 + e < sink || (j0 + e >= n - recency && j0 + e < n);
+  float4 p[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+    p[k] = __ldcs(reinterpret_cast<const float4*>(base + static_cast<size_t>(rg * 16 + k) * ld));
+  // As in mass_tiles: quanta below 2^23 summed in 32 bits (64 stay below 2^29).
+  uint32_t all32 = 0, sl32 = 0;
+  uint64_t all64 = 0, sl64 = 0;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float x[4] = {p[k].x * 4294967296.0f, p[k].y * 4294967296.0f, p[k].z * 4294967296.0f,
+                        p[k].w * 4294967296.0f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (x[e] < kTwo23) {
+        const uint32_t f = q32_small(x[e]);
+        all32 += f;
+        sl32 += in_slice[e] ? f : 0u;
+      } else {
+        const uint64_t f = q32_large(x[e]);
+        all64 += f;
+        sl64 += in_slice[e] ? f : 0ull;
+      }
+    }
+  }
+  const uint64_t all = warp_sum(all64 + all32), sl = warp_sum(sl64 + sl32);
+  if (cq == 0) {
+    red[0][rg] = all;
+    red[1][rg] = sl;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint64_t a = 0, b = 0;
+    for (int w = 0; w < kMassThreads / 32; ++w) {
+      a += red[0][w];
+      b += red[1][w];
+    }
+    atomicAdd(reinterpret_cast<unsigned long long*>(total + h), static_cast<unsigned long long>(a));
+    if (b != 0) atomicAdd(reinterpret_cast<unsigned long long*>(cstruct + h), static_cast<unsigned long long>(b));
+  }
+}
+
+// VS iff tau_den * C_struct >= tau_num * total, one thread per head.
+__global__ void route_decide(const uint64_t* __restrict__ cstruct, const uint64_t* __restrict__ total, int hq,
+                             uint32_t tau_num, uint32_t tau_den, uint8_t* __restrict__ route) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= hq) return;
+  route[h] = static_cast<unsigned __int128>(tau_den) * cstruct[h] >= static_cast<unsigned __int128>(tau_num) * total[h]
+                 ? 1
+                 : 0;
+}
+
 // A4 for one (head, direction): direction 0 = vertical (always keeps {0,
 // nb-1}), 1 = slash (always keeps {0}). Noise floor (CRISP): candidates
 // [1, nb-2] above alpha times their mean. Cumulative coverage (FlexPrefill,
@@ -281,6 +348,18 @@ cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint
                          uint64_t* cstruct, uint64_t* total, uint8_t* route, cudaStream_t st) {
   route_kernel<<<s.hq, 256, 0, st>>>(vmass, rmass, num_blocks(s.seq_len), p.tau_num, p.tau_den, cstruct, total,
                                      route);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_map(const crisp_shape& s, const crisp_params& p, const float* pmap, uint64_t* cstruct,
+                             uint64_t* total, uint8_t* route, cudaStream_t st) {
+  const size_t bytes = static_cast<size_t>(s.hq) * sizeof(uint64_t);
+  cudaError_t e = cudaMemsetAsync(cstruct, 0, bytes, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(total, 0, bytes, st);
+  if (e != cudaSuccess) return e;
+  cstruct_tiles<<<dim3(num_blocks(s.seq_len), s.hq), kMassThreads, 0, st>>>(
+      pmap, map_ld(s.seq_len), s.seq_len, p.sink_tokens, p.recency_tokens, cstruct, total);
+  route_decide<<<(s.hq + 127) / 128, 128, 0, st>>>(cstruct, total, s.hq, p.tau_num, p.tau_den, route);
   return cudaGetLastError();
 }
 

@@ -6,21 +6,24 @@
  * per attention head, which 128x128 blocks of the causal attention matrix to
  * compute, then computes exact softmax attention over those blocks:
  *
- *   A1 crisp_proxy_map       proxy attention map of the last query block
- *   A3 crisp_block_masses    vertical / slash block masses of that map
- *   A1+A3 crisp_proxy_masses the same masses straight from q and k (map not stored)
- *   A2 crisp_route_cstruct   C_struct routing: Vertical-Slash or Pooled-Estimation
- *      crisp_route_jsd       FlexPrefill's divergence routing (the rule CRISP replaces)
- *   A4 crisp_select_vs       sink-aware noise-floor selection (VS heads)
- *   A5 crisp_pe_map          pooled attention estimate (PE heads)
- *   A6 crisp_select_pe       PE block selection (gamma coverage or noise floor)
- *   A7 crisp_build_mask      per-head sparse block mask
- *   A8 crisp_sparse_prefill  causal GQA block-sparse attention
- *   A9 crisp_dense_prefill   the same kernel over every causal block
- *   crisp_prefill_layer      A1..A8 in order, intermediates in the workspace
- *   crisp_prefill_layer_host the same from host buffers, copies overlapped with compute
- *   crisp_proxy_map_noalloc  A1 without a caller workspace (static scratch)
- *   crisp_wait_selftest      failure detection: a bounded wait that must time out
+ *   A1 crisp_proxy_map          proxy attention map of the last query block
+ *   A3 crisp_block_masses       vertical / slash block masses of that map
+ *   A1+A3 crisp_proxy_masses    the same masses straight from q and k (map not stored)
+ *   A2 crisp_route_cstruct      C_struct routing from the map: Vertical-Slash or Pooled-Estimation
+ *      crisp_route_cstruct_masses  the same from the block masses (what the layer runs)
+ *      crisp_route_jsd          FlexPrefill's divergence routing (the rule CRISP replaces)
+ *   A4 crisp_select_vs          sink-aware noise-floor selection from the map (VS heads)
+ *      crisp_select_vs_masses   the same from the block masses (what the layer runs)
+ *   A5 crisp_pe_pool            pooled attention estimate (PE heads)
+ *   A6 crisp_select_pe          PE block selection (gamma coverage or noise floor)
+ *   A7 crisp_build_mask         per-head sparse block mask and attention schedule
+ *   A8 crisp_sparse_prefill     causal GQA block-sparse attention over the index sets
+ *      crisp_sparse_prefill_mask  the same over a block mask from crisp_build_mask
+ *   A9 crisp_dense_prefill      the same kernel over every causal block
+ *   crisp_prefill_layer         A1..A8 in order, intermediates in the workspace
+ *   crisp_prefill_layer_host    the same from host buffers, copies overlapped with compute
+ *   crisp_proxy_map_noalloc     A1 without a caller workspace (static scratch)
+ *   crisp_wait_selftest         failure detection: a bounded wait that must time out
  *
  * Conventions (every function):
  *  - Pointers are DEVICE pointers unless marked "host". The caller owns and
@@ -76,7 +79,9 @@ typedef enum crisp_status {
   CRISP_ERR_WORKSPACE = 4,   /* workspace null or smaller than required */
   CRISP_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, copy) */
   CRISP_ERR_TIMEOUT = 6,     /* device: a bounded wait inside a kernel ran out */
-  CRISP_ERR_DEVICE = 7       /* the current device is not sm_103 */
+  CRISP_ERR_DEVICE = 7,      /* the current device is not sm_103 */
+  CRISP_ERR_BOUNDS = 8       /* device, bounds-checking build only: an index fell outside its
+                                buffer; the access was skipped (the release build has no checks) */
 } crisp_status;
 
 typedef enum crisp_pe_mode {
@@ -116,7 +121,15 @@ typedef struct crisp_shape {
  * k_min = 8 blocks (1024 tokens) per direction, pe_mode = CRISP_PE_GAMMA,
  * route_mode = CRISP_ROUTE_CSTRUCT, vs_mode = CRISP_VS_NOISE (the comparator
  * fields default to FlexPrefill's settings as we read them: vs_gamma =
- * 95/100, jsd_tau = 0.1), dense_below = 0 (no length gate). */
+ * 95/100, jsd_tau = 0.1), dense_below = 0 (no length gate; the measured
+ * sparse/dense crossover on GB300 lies between 4096 and 8192 tokens, so
+ * 8192 is the recommended gate), sink_tokens = recency_tokens = 128 (the
+ * paper's two slices: the sink is the first 128 key tokens, the recency
+ * window the last 128).
+ * crisp_route_cstruct (from the map) takes any slice widths; every call that
+ * routes from block masses (crisp_route_cstruct_masses, crisp_prefill_layer,
+ * crisp_prefill_layer_host) needs both at 128, one block, and returns
+ * CRISP_ERR_INVALID_ARG otherwise. */
 typedef struct crisp_params {
   uint32_t tau_num, tau_den;     /* 0 <= tau <= 1, tau_den > 0 */
   uint32_t alpha_num, alpha_den; /* alpha_num, alpha_den <= 65535, alpha_den > 0 */
@@ -128,6 +141,8 @@ typedef struct crisp_params {
   uint32_t vs_gamma_num, vs_gamma_den; /* coverage of CRISP_VS_GAMMA, 0 <= gamma <= 1 */
   float jsd_tau;                 /* CRISP_ROUTE_JSD: VS iff sqrt(JSD) >= jsd_tau; 0 <= jsd_tau <= 1 */
   int32_t dense_below;           /* crisp_prefill_layer*: n < dense_below runs dense attention only */
+  int32_t sink_tokens;           /* C_struct sink slice: key columns [0, sink_tokens), 0 <= . <= 2^20 */
+  int32_t recency_tokens;        /* C_struct recency slice: key columns [n - recency_tokens, n), 0 <= . <= 2^20 */
 } crisp_params;
 
 /* Fills *p (host) with the defaults above. */
@@ -168,15 +183,25 @@ CRISP_API crisp_status crisp_proxy_map(const crisp_shape* shape, const void* q, 
  * bytes of it, rounded up to 256-byte units (the 512k-token, 32-head layer
  * needs about 16.8 MB); larger shapes are rejected with CRISP_ERR_WORKSPACE
  * and nothing is launched. The first call on a device looks up the array's
- * device address (once per device, with that device current), so make that
- * first call before any stream capture. Every call shares the one array:
- * calls whose kernels overlap on the GPU (other streams, other threads)
- * race and corrupt each other's statistics; calls serialised on one stream
- * are safe. The status word in the array is cleared by every call; a device
- * wait that times out is recorded there but cannot be read by the caller.
+ * device address (once per device, with that device current) and keeps it
+ * for the life of the process, so make that first call before any stream
+ * capture, and make no call on a device after cudaDeviceReset on it (the
+ * reset releases the library's static memory and the kept address would
+ * point at memory the process no longer owns). Every call shares the one
+ * array: calls whose kernels overlap on the GPU (other streams, other
+ * threads) race and corrupt each other's statistics; calls serialised on one
+ * stream are safe. The status word in the array is cleared by every call; a
+ * device wait that times out is recorded there: read it with
+ * crisp_noalloc_read_status on the same stream before the next call.
  * Allocates nothing (no cudaMalloc/cudaFree, no allocating library call). */
 CRISP_API crisp_status crisp_proxy_map_noalloc(const crisp_shape* shape, const void* q, const void* k, float* pmap,
                                                crisp_stream_t stream);
+
+/* The status word of crisp_proxy_map_noalloc's static scratch on the current
+ * device: synchronises `stream` and copies the word to *status (host),
+ * CRISP_OK or CRISP_ERR_TIMEOUT after the last call. Allocates nothing.
+ * Returns CRISP_ERR_CUDA if the stream or the copy failed. */
+CRISP_API crisp_status crisp_noalloc_read_status(crisp_stream_t stream, crisp_status* status /* host */);
 
 /* A3. Block masses of the proxy map ("mass at Vertical-Slash compatible
  * positions", ai-feeds page, "方法"). With q(p) the Q32 quantum and row r
@@ -205,17 +230,37 @@ CRISP_API crisp_status crisp_proxy_masses(const crisp_shape* shape, const void* 
                                           uint64_t* smass, uint64_t* rmass, void* ws, size_t ws_bytes,
                                           crisp_stream_t stream);
 
-/* A2. C_struct routing (ai.info page, "Key Contributions" 2: mass at the
- * first 128 and the last 128 tokens of the proxy map; tau_proxy = 0.2). The
- * first 128 tokens are key block 0, the last 128 the recency mass rmass
- * (key block nb-1 when 128 divides n), disjoint for n >= 256:
- *   cstruct[h] = vmass[h][0] + rmass[h],  total[h] = sum_c vmass[h][c],
+/* A2. C_struct routing from the proxy map (ai.info page, "Key Contributions"
+ * 2 and "Methodology in Plain English": the share of the map's mass that sits
+ * in the sink slice, the first 128 key tokens, and the recency slice, the
+ * last 128; tau_proxy = 0.2). With q(p) the Q32 quantum and the slice widths
+ * of params (sink_tokens = S, recency_tokens = R; the paper's 128 and 128):
+ *   cstruct[h] = sum over rows r and columns j in [0, S) U [n-R, n) of
+ *                q(pmap[h][r][j])   (the union: a column in both counts once),
+ *   total[h]   = sum over rows r and all columns j of q(pmap[h][r][j]),
  *   route[h]   = 1 (Vertical-Slash) iff tau_den * cstruct >= tau_num * total,
  *                0 (Pooled-Estimation) otherwise.
- * vmass uint64 [hq][nb]; rmass, cstruct, total uint64 [hq]; route uint8 [hq]. */
-CRISP_API crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
-                                           const uint64_t* rmass, uint64_t* cstruct, uint64_t* total, uint8_t* route,
-                                           crisp_stream_t stream);
+ * Reads the whole map once (HBM-bound). pmap fp32 [hq][128][ld] as
+ * crisp_proxy_map writes it; cstruct, total uint64 [hq], 8-byte aligned;
+ * route uint8 [hq]. */
+CRISP_API crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const float* pmap,
+                                           uint64_t* cstruct, uint64_t* total, uint8_t* route, void* ws,
+                                           size_t ws_bytes, crisp_stream_t stream);
+
+/* A2 from the block masses (what crisp_prefill_layer runs: the masses come
+ * from the fused crisp_proxy_masses pass and the map is never stored). With
+ * both slices 128 tokens wide the sink slice is key block 0 and the recency
+ * slice the recency mass rmass (key block nb-1 when 128 divides n), disjoint
+ * for n >= 256:
+ *   cstruct[h] = vmass[h][0] + rmass[h],  total[h] = sum_c vmass[h][c],
+ *   route[h] as for crisp_route_cstruct; bit-identical to it on the same map.
+ * params->sink_tokens and recency_tokens must be 128 (else
+ * CRISP_ERR_INVALID_ARG). vmass uint64 [hq][nb]; rmass, cstruct, total
+ * uint64 [hq]; route uint8 [hq]. */
+CRISP_API crisp_status crisp_route_cstruct_masses(const crisp_shape* shape, const crisp_params* params,
+                                                  const uint64_t* vmass, const uint64_t* rmass, uint64_t* cstruct,
+                                                  uint64_t* total, uint8_t* route, void* ws, size_t ws_bytes,
+                                                  crisp_stream_t stream);
 
 /* A2 comparator: FlexPrefill's routing, which CRISP replaces (ai.info page,
  * "Methodology in Plain English": a pooled attention estimate compared with
@@ -225,35 +270,48 @@ CRISP_API crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp
  *   e[c] = pbar[h][nb-1][c]                  (the pooled estimate of that block),
  *   D    = (KL(a || m) + KL(e || m)) / 2,  m = (a + e) / 2, natural log, in fp64,
  *   route[h] = 1 (Vertical-Slash) iff sqrt(D) >= jsd_tau, else 0.
- * pbar: fp32 [hq][nb][nb] holding row nb-1 of EVERY head (crisp_pe_map with a
+ * pbar: fp32 [hq][nb][nb] holding row nb-1 of EVERY head (crisp_pe_pool with a
  * route array of zeros computes it); jsd: double [hq] (D), or NULL. */
 CRISP_API crisp_status crisp_route_jsd(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
-                                       const float* pbar, double* jsd, uint8_t* route, crisp_stream_t stream);
+                                       const float* pbar, double* jsd, uint8_t* route, void* ws, size_t ws_bytes,
+                                       crisp_stream_t stream);
 
-/* A4. Sink-aware noise-floor selection for VS heads (ai.info page,
- * "Methodology in Plain English": keep each block whose mass exceeds alpha
- * times the expected background mass of the blocks that are not always
- * retained; "k_min=1024 tokens (8 blocks) per direction"). Per direction:
- * always-retained vertical {0, nb-1}, slash {0}; candidates [1, nb-2], N of
- * them, mass sum M; keep c iff m[c]*N*alpha_den > alpha_num*M; then fill to
- * min(kmin, available) by (mass desc, index asc). PE heads get empty rows.
+/* A4. Sink-aware noise-floor selection for VS heads, from the block masses
+ * (ai.info page, "Methodology in Plain English": a block is kept when its
+ * mass is above alpha times the mean background mass of the blocks that are
+ * not always retained; k_min is 1024 tokens, 8 blocks, in each direction).
+ * Per direction: always-retained vertical {0, nb-1}, slash {0}; candidates
+ * [1, nb-2], N of them, mass sum M; keep c iff m[c]*N*alpha_den >
+ * alpha_num*M; then fill to min(kmin, available) by (mass desc, index asc).
+ * PE heads get empty rows.
  * vs_mode = CRISP_VS_GAMMA (FlexPrefill's cumulative coverage, the rule CRISP
  * replaces): per direction, every block [0, nb-1] is a candidate; keep the
  * shortest (mass desc, index asc) prefix whose mass reaches vs_gamma of the
  * direction's total (vs_gamma_den * prefix >= vs_gamma_num * total), add the
  * always-retained blocks and fill to min(kmin, nb) the same way.
+ * vmass, smass: uint64 [hq][nb] (crisp_block_masses or crisp_proxy_masses);
  * vbits, sbits: uint32 [hq][W]. */
-CRISP_API crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
-                             const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
-                             void* ws, size_t ws_bytes, crisp_stream_t stream);
+CRISP_API crisp_status crisp_select_vs_masses(const crisp_shape* shape, const crisp_params* params,
+                                              const uint64_t* vmass, const uint64_t* smass, const uint8_t* route,
+                                              uint32_t* vbits, uint32_t* sbits, void* ws, size_t ws_bytes,
+                                              crisp_stream_t stream);
+
+/* A4 from the proxy map: crisp_block_masses (A3) then crisp_select_vs_masses,
+ * with the masses written out. pmap fp32 [hq][128][ld] as crisp_proxy_map
+ * writes it; route uint8 [hq]; vmass, smass uint64 [hq][nb] (outputs);
+ * vbits, sbits uint32 [hq][W]. */
+CRISP_API crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* params, const float* pmap,
+                                       const uint8_t* route, uint64_t* vmass, uint64_t* smass, uint32_t* vbits,
+                                       uint32_t* sbits, void* ws, size_t ws_bytes, crisp_stream_t stream);
 
 /* A5. Pooled attention estimate for PE heads (the Pooled-Estimation route
  * CRISP keeps from FlexPrefill; ai.info page, "Overview"): block means of q
- * and k (a short last block averaged over its own tokens), pbar[h][b][c] = softmax over c <= b of scale * qbar_b . kbar_c, and 0
- * for c > b. Rows of VS heads are not written. q, k bf16; pbar fp32
+ * and k (a short last block averaged over its own tokens),
+ * pbar[h][b][c] = softmax over c <= b of scale * qbar_b . kbar_c, and 0 for
+ * c > b. Rows of VS heads are not written. q, k bf16; pbar fp32
  * [hq][nb][nb], 16-byte aligned. */
-CRISP_API crisp_status crisp_pe_map(const crisp_shape* shape, const void* q, const void* k, const uint8_t* route, float* pbar,
-                          void* ws, size_t ws_bytes, crisp_stream_t stream);
+CRISP_API crisp_status crisp_pe_pool(const crisp_shape* shape, const void* q, const void* k, const uint8_t* route,
+                                     float* pbar, void* ws, size_t ws_bytes, crisp_stream_t stream);
 
 /* A6. PE block selection per query block b from pbar (ai.info page,
  * "Methodology in Plain English": gamma = 0.95 for the PE path only).
@@ -284,21 +342,36 @@ CRISP_API crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t*
                                         crisp_stream_t stream);
 
 /* A8. Exact causal GQA softmax attention over the selected blocks (ai.info
- * page, "Why This Matters": exact softmax attention over the blocks it
- * selects): for token i in query block qb of head h,
+ * page, "Why This Matters": the attention is exact softmax over the blocks
+ * the method keeps), from the index sets of A2, A4 and A6: the mask and the
+ * schedule of crisp_build_mask (A7) are built in `ws`, then for token i in
+ * query block qb of head h,
+ *   out_i = sum_{j in A(i)} softmax_j(scale * q_i . k_j) v_j,
+ *   A(i) = { j <= i : block(j) in the head's set for qb (crisp_build_mask) }.
+ * Rows with an empty A(i) are written as zeros; only rows i < n are written.
+ * q bf16 [hq][n][128]; k, v bf16 [hkv][n][128]; route uint8 [hq]; vbits,
+ * sbits uint32 [hq][W]; pebits uint32 [hq][nb][W]; out bf16 [hq][n][128]
+ * (o strides). n >= 256 (the index sets need the method's steps). */
+CRISP_API crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v,
+                                            const uint8_t* route, const uint32_t* vbits, const uint32_t* sbits,
+                                            const uint32_t* pebits, void* out, void* ws, size_t ws_bytes,
+                                            crisp_stream_t stream);
+
+/* A8 over a block mask: for token i in query block qb of head h,
  *   out_i = sum_{j in A(i)} softmax_j(scale * q_i . k_j) v_j,
  *   A(i) = { j <= i : block(j) in rowbits[h][qb] }.
  * Bits above the diagonal block are ignored; rows with an empty A(i) are
- * written as zeros; only rows i < n are written. q bf16 [hq][n][128]; k, v bf16 [hkv][n][128]; rowbits
- * from crisp_build_mask; order: the schedule from crisp_build_mask, or NULL
- * for the same kv-group-major order (any permutation of the row ids gives
- * the same result); out bf16 [hq][n][128] (o strides). */
-CRISP_API crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v,
-                                            const uint32_t* rowbits, const int32_t* order, void* out, void* ws,
-                                            size_t ws_bytes, crisp_stream_t stream);
+ * written as zeros; only rows i < n are written; any n >= 0. rowbits uint32
+ * [hq][nb][W] (crisp_build_mask, or any caller-made mask); order: the
+ * schedule from crisp_build_mask, or NULL for the same kv-group-major order
+ * (any permutation of the row ids gives the same result). */
+CRISP_API crisp_status crisp_sparse_prefill_mask(const crisp_shape* shape, const void* q, const void* k,
+                                                 const void* v, const uint32_t* rowbits, const int32_t* order,
+                                                 void* out, void* ws, size_t ws_bytes, crisp_stream_t stream);
 
-/* A9. Dense causal attention (A(i) = [0, i]): the exact baseline the paper
- * compares against ("FlashAttention (exact dense)", ai.info page). */
+/* A9. Dense causal attention (A(i) = [0, i]): the exact dense
+ * FlashAttention-style baseline the paper measures against (ai.info page,
+ * "Methodology in Plain English"). */
 CRISP_API crisp_status crisp_dense_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v, void* out,
                                  void* ws, size_t ws_bytes, crisp_stream_t stream);
 

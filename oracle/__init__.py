@@ -40,7 +40,7 @@ def _configure(lib):
     lib.oracle_quantize.argtypes = [vp, i64, vp]
     lib.oracle_quantize.restype = None
     lib.oracle_proxy_rows.argtypes = [i, i, i, vp, vp, d, i64, vp, vp, vp, i]
-    lib.oracle_route.argtypes = [i, i, vp, u32, u32, vp, vp, vp, i]
+    lib.oracle_route.argtypes = [i, i, vp, u32, u32, i, i, vp, vp, vp, i]
     lib.oracle_vs_masses.argtypes = [i, i, vp, vp, vp, i]
     lib.oracle_pe_rows.argtypes = [i, i, i, vp, vp, d, i64, vp, vp, vp, i]
     lib.oracle_select_vs.argtypes = [i, i, vp, vp, vp, u32, u32, i, vp, vp]
@@ -129,12 +129,14 @@ def quantize(p):
     return out
 
 
-def route(pmap32, tau=(1, 5), nthreads=None):
-    """A2: (cstruct S, total T, route) from an fp32 map [hq][128][n]."""
+def route(pmap32, tau=(1, 5), sink=128, recency=128, nthreads=None):
+    """A2: (cstruct S, total T, route) from an fp32 map [hq][128][n]; the
+    slices are key columns [0, sink) and [n - recency, n)."""
     pmap32 = np.ascontiguousarray(pmap32, dtype=np.float32)
     hq, _, n = pmap32.shape
     S, T, r = np.empty(hq, np.uint64), np.empty(hq, np.uint64), np.empty(hq, np.uint8)
-    _check(_load().oracle_route(hq, n, _p(pmap32), tau[0], tau[1], _p(S), _p(T), _p(r), _nt(nthreads)), "route")
+    _check(_load().oracle_route(hq, n, _p(pmap32), tau[0], tau[1], int(sink), int(recency), _p(S), _p(T), _p(r),
+                                _nt(nthreads)), "route")
     return S, T, r
 
 

@@ -203,16 +203,18 @@ void oracle_quantize(const float* p, int64_t count, uint64_t* out) {
 }
 
 // ---------------------------------------------------------------------------
-// A2. C_struct routing (ai.info, Key Contributions 2 and Methodology: mass "in
-// the first 128 tokens and the last 128 tokens of the proxy attention map";
-// "tau_proxy=0.2"). Reading: C_struct = S/T with S the quantised mass in
-// columns [0,128) U [n-128,n) (the union, counted once) and T the total
+// A2. C_struct routing (ai.info, Key Contributions 2 and Methodology: the
+// share of the proxy map's mass in the sink slice, the first 128 key tokens,
+// and the recency slice, the last 128; tau_proxy = 0.2). Reading: C_struct =
+// S/T with S the quantised mass in columns [0, sink) U [n - recency, n) (the
+// union, counted once; the pages fix sink = recency = 128, the two widths are
+// parameters here so that other slices can be checked) and T the total
 // quantised mass; a head is Vertical-Slash iff C_struct >= tau, compared in
 // integers as tau_den * S >= tau_num * T.
 // pmap: fp32 [hq][128][n] (the map under test); route[h] = 1 for VS, 0 for PE.
-int oracle_route(int hq, int n, const float* pmap, uint32_t tau_num, uint32_t tau_den, uint64_t* cstruct,
-                 uint64_t* total, uint8_t* route, int nthreads) {
-  if (hq <= 0 || n < 2 * kB || tau_den == 0) return 1;
+int oracle_route(int hq, int n, const float* pmap, uint32_t tau_num, uint32_t tau_den, int sink, int recency,
+                 uint64_t* cstruct, uint64_t* total, uint8_t* route, int nthreads) {
+  if (hq <= 0 || n < 2 * kB || tau_den == 0 || sink < 0 || recency < 0) return 1;
   parallel_for(hq, nthreads, [&](int64_t hh) {
     const int h = static_cast<int>(hh);
     uint64_t S = 0, T = 0;
@@ -221,7 +223,7 @@ int oracle_route(int hq, int n, const float* pmap, uint32_t tau_num, uint32_t ta
       for (int j = 0; j < n; ++j) {
         const uint64_t m = q32(row[j]);
         T += m;
-        if (j < 128 || j >= n - 128) S += m;
+        if (j < sink || j >= n - recency) S += m;
       }
     }
     cstruct[h] = S;

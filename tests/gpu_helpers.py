@@ -66,14 +66,29 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
     crisp.proxy_masses(s, qd, kd, vmass_f, smass_f, rmass_f, ws)
     crisp.proxy_map(s, qd, kd, pmap, ws)
     crisp.block_masses(s, pmap, vmass, smass, rmass, ws)
-    crisp.route_cstruct(s, params, vmass, rmass, cstruct, total, route)
-    crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws)
-    crisp.pe_map(s, qd, kd, route, pbar, ws)
+    # Both forms of A2 and A4: from the map (the survey's calls) and from the
+    # block masses (what the layer runs); they must agree bit for bit.
+    crisp.route_cstruct(s, params, pmap, cstruct, total, route, ws)
+    cstruct_m, total_m, route_m = empty((hq,), torch.int64), empty((hq,), torch.int64), empty((hq,), torch.uint8)
+    crisp.route_cstruct_masses(s, params, vmass, rmass, cstruct_m, total_m, route_m, ws)
+    vmass_s = torch.full((hq, nb), -1, dtype=torch.int64, device="cuda")
+    smass_s = torch.full((hq, nb), -1, dtype=torch.int64, device="cuda")
+    crisp.select_vs(s, params, pmap, route, vmass_s, smass_s, vbits, sbits, ws)
+    vbits_m, sbits_m = empty((hq, W), torch.int32), empty((hq, W), torch.int32)
+    crisp.select_vs_masses(s, params, vmass, smass, route, vbits_m, sbits_m, ws)
+    crisp.pe_pool(s, qd, kd, route, pbar, ws)
     crisp.select_pe(s, params, pbar, route, pebits, ws)
     crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, ws)
-    crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws)
+    crisp.sparse_prefill_mask(s, qd, kd, vd, rowbits, order, out, ws)
+    # A8 from the index sets: the mask is built in the workspace
+    out_sets = empty((hq, n, 128), torch.bfloat16)
+    crisp.sparse_prefill(s, qd, kd, vd, route, vbits, sbits, pebits, out_sets, ws)
     torch.cuda.synchronize()
     assert_status_ok(ws)
+    assert torch.equal(cstruct, cstruct_m) and torch.equal(total, total_m) and torch.equal(route, route_m)
+    assert torch.equal(vmass_s, vmass) and torch.equal(smass_s, smass)
+    assert torch.equal(vbits, vbits_m) and torch.equal(sbits, sbits_m)
+    assert torch.equal(out_sets, out), "A8 from the index sets differs from A8 over the built mask"
     u64 = lambda t: t.cpu().numpy().view(np.uint64)
     u32 = lambda t: t.cpu().numpy().view(np.uint32)
     pm = pmap.cpu().numpy()

@@ -27,10 +27,58 @@ def declared_functions():
 def test_header_declares_the_steps():
     names = declared_functions()
     for want in ("crisp_proxy_map", "crisp_route_cstruct", "crisp_select_vs", "crisp_select_pe",
-                 "crisp_sparse_prefill", "crisp_dense_prefill", "crisp_block_masses", "crisp_pe_map",
+                 "crisp_sparse_prefill", "crisp_dense_prefill", "crisp_block_masses", "crisp_pe_pool",
                  "crisp_build_mask", "crisp_prefill_layer", "crisp_proxy_masses", "crisp_read_status",
-                 "crisp_status_string"):
+                 "crisp_status_string", "crisp_route_cstruct_masses", "crisp_select_vs_masses",
+                 "crisp_sparse_prefill_mask", "crisp_workspace_size", "crisp_params_default"):
         assert want in names
+
+
+# The survey's boundary table, call by call: each row's name and its argument
+# list as this header declares it (the survey's signature plus ws_bytes
+# after every workspace; the workspace size takes the shape only).
+SURVEY_BOUNDARY = {
+    "crisp_proxy_map": ["shape", "q", "k", "pmap", "ws", "ws_bytes", "stream"],
+    "crisp_route_cstruct": ["shape", "params", "pmap", "cstruct", "total", "route", "ws", "ws_bytes", "stream"],
+    "crisp_select_vs": ["shape", "params", "pmap", "route", "vmass", "smass", "vbits", "sbits", "ws", "ws_bytes",
+                        "stream"],
+    "crisp_pe_pool": ["shape", "q", "k", "route", "pbar", "ws", "ws_bytes", "stream"],
+    "crisp_select_pe": ["shape", "params", "pbar", "route", "pebits", "ws", "ws_bytes", "stream"],
+    "crisp_sparse_prefill": ["shape", "q", "k", "v", "route", "vbits", "sbits", "pebits", "out", "ws", "ws_bytes",
+                             "stream"],
+    "crisp_dense_prefill": ["shape", "q", "k", "v", "out", "ws", "ws_bytes", "stream"],
+    "crisp_prefill_layer": ["shape", "params", "q", "k", "v", "out", "ws", "ws_bytes", "stream"],
+    "crisp_read_status": ["ws", "stream", "status"],
+    "crisp_status_string": ["status"],
+    "crisp_params_default": ["p"],
+    "crisp_workspace_size": ["shape", "bytes"],
+}
+
+
+def declared_arguments(name):
+    text = open(os.path.join(ROOT, "include", "crisp.h")).read()
+    m = re.search(r"CRISP_API[\w\s\*]*?\b" + name + r"\s*\(([^)]*)\)", text)
+    assert m, name
+    args = []
+    for a in m.group(1).split(","):
+        a = re.sub(r"/\*.*?\*/", "", a).strip()
+        args.append(re.findall(r"\w+", a)[-1])
+    return args
+
+
+@pytest.mark.parametrize("name", sorted(SURVEY_BOUNDARY))
+def test_survey_boundary_calls_are_declared(name):
+    assert declared_arguments(name) == SURVEY_BOUNDARY[name]
+
+
+def test_survey_boundary_fields_and_codes():
+    text = open(os.path.join(ROOT, "include", "crisp.h")).read()
+    for field in ("tau_num", "tau_den", "alpha_num", "alpha_den", "gamma_num", "gamma_den", "kmin_blocks",
+                  "sink_tokens", "recency_tokens", "pe_mode"):
+        assert re.search(r"\b" + field + r"\b", text), field
+    for code in ("CRISP_OK", "CRISP_ERR_INVALID_ARG", "CRISP_ERR_SHAPE", "CRISP_ERR_ALIGN", "CRISP_ERR_WORKSPACE",
+                 "CRISP_ERR_CUDA", "CRISP_ERR_TIMEOUT", "CRISP_ERR_BOUNDS"):
+        assert re.search(r"\b" + code + r"\s*=", text), code
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -52,10 +100,11 @@ def test_params_default_is_the_universal_configuration(L):
     assert p.route_mode == crisp.ROUTE_CSTRUCT and p.vs_mode == crisp.VS_NOISE
     assert (p.vs_gamma_num, p.vs_gamma_den) == (95, 100) and abs(p.jsd_tau - 0.1) < 1e-7
     assert p.dense_below == 0
+    assert p.sink_tokens == 128 and p.recency_tokens == 128
 
 
 def test_status_strings(L):
-    for code in range(8):
+    for code in range(9):
         assert crisp.status_string(code)
     assert crisp.status_string(99) == "unknown status"
 
@@ -90,14 +139,35 @@ def test_shape_validation(L, field, value, code):
                                          ("gamma_num", 21), ("kmin_blocks", -1), ("kmin_blocks", 9000),
                                          ("pe_mode", 2), ("route_mode", 2), ("vs_mode", -1), ("vs_gamma_den", 0),
                                          ("vs_gamma_num", 101), ("jsd_tau", -0.1), ("jsd_tau", 1.5),
-                                         ("jsd_tau", float("nan")), ("dense_below", -1)])
+                                         ("jsd_tau", float("nan")), ("dense_below", -1), ("sink_tokens", -1),
+                                         ("recency_tokens", (1 << 20) + 1)])
 def test_params_validation(L, field, value):
     s = crisp.make_shape(8, 4, 1024)
     p = crisp.params_default()
     setattr(p, field, value)
-    rc = L.crisp_route_cstruct(ctypes.byref(s), ctypes.byref(p), ctypes.c_void_p(256), ctypes.c_void_p(256),
-                               ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256), None)
+    vp = ctypes.c_void_p
+    rc = L.crisp_route_cstruct(ctypes.byref(s), ctypes.byref(p), vp(256), vp(256), vp(256), vp(256), vp(256),
+                               1 << 30, None)
     assert rc == 1
+
+
+@pytest.mark.parametrize("sink,recency", [(64, 128), (128, 200), (0, 0)])
+def test_mass_routing_needs_block_wide_slices(L, sink, recency):
+    # Routing from block masses (and the layer, which does so) reads the sink
+    # slice as block 0 and the recency slice as the recency mass: other widths
+    # are refused on the host; the map-reading route accepts them.
+    s = crisp.make_shape(8, 4, 1024)
+    p = crisp.params_default(sink_tokens=sink, recency_tokens=recency)
+    vp = ctypes.c_void_p
+    assert L.crisp_route_cstruct_masses(ctypes.byref(s), ctypes.byref(p), vp(256), vp(256), vp(256), vp(256),
+                                        vp(256), vp(256), 1 << 30, None) == 1
+    assert L.crisp_prefill_layer(ctypes.byref(s), ctypes.byref(p), vp(16), vp(16), vp(16), vp(16), vp(256), 1 << 30,
+                                 None) == 1
+    assert L.crisp_prefill_layer_host(vp(256), ctypes.byref(s), ctypes.byref(p), *([vp(256)] * 9), 1 << 30,
+                                      None) == 1
+    # past the parameter check, the map-reading route stops at its first null pointer
+    assert L.crisp_route_cstruct(ctypes.byref(s), ctypes.byref(p), None, vp(256), vp(256), vp(256), vp(256),
+                                 1 << 30, None) == 1
 
 
 def test_null_and_misaligned_pointers(L):
@@ -105,10 +175,27 @@ def test_null_and_misaligned_pointers(L):
     vp = ctypes.c_void_p
     assert L.crisp_proxy_map(ctypes.byref(s), None, vp(16), vp(16), vp(256), 1 << 30, None) == 1
     assert L.crisp_proxy_map(ctypes.byref(s), vp(8), vp(16), vp(16), vp(256), 1 << 30, None) == 3
-    assert L.crisp_sparse_prefill(ctypes.byref(s), vp(16), vp(16), vp(16), None, vp(16), vp(16), vp(256), 1 << 30,
-                                  None) == 1
-    assert L.crisp_sparse_prefill(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(18), vp(16), vp(256), 1 << 30,
-                                  None) == 3
+    assert L.crisp_sparse_prefill_mask(ctypes.byref(s), vp(16), vp(16), vp(16), None, vp(16), vp(16), vp(256),
+                                       1 << 30, None) == 1
+    assert L.crisp_sparse_prefill_mask(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(18), vp(16), vp(256),
+                                       1 << 30, None) == 3
+    # the index-set form: route, vbits, sbits, pebits checked before any launch
+    assert L.crisp_sparse_prefill(ctypes.byref(s), vp(16), vp(16), vp(16), None, vp(16), vp(16), vp(16), vp(16),
+                                  vp(256), 1 << 30, None) == 1
+    assert L.crisp_sparse_prefill(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(18), vp(16), vp(16), vp(16),
+                                  vp(256), 1 << 30, None) == 3
+    assert L.crisp_sparse_prefill(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16),
+                                  vp(256), 64, None) == 4
+    assert L.crisp_sparse_prefill(ctypes.byref(s), None, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16),
+                                  vp(256), 1 << 30, None) == 1
+    # A4 from the map
+    pd0 = ctypes.byref(crisp.params_default())
+    assert L.crisp_select_vs(ctypes.byref(s), pd0, None, vp(16), vp(16), vp(16), vp(16), vp(16), vp(256), 1 << 30,
+                             None) == 1
+    assert L.crisp_select_vs(ctypes.byref(s), pd0, vp(16), vp(16), vp(20), vp(16), vp(16), vp(16), vp(256), 1 << 30,
+                             None) == 3
+    assert L.crisp_select_vs_masses(ctypes.byref(s), pd0, vp(16), vp(16), None, vp(16), vp(16), vp(256), 1 << 30,
+                                    None) == 1
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), None, vp(16), vp(16), vp(256), 1 << 30, None) == 1
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), None, vp(256), 1 << 30, None) == 1
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(20), vp(16), vp(256), 1 << 30,
@@ -117,17 +204,26 @@ def test_null_and_misaligned_pointers(L):
                                 None) == 3
     assert L.crisp_proxy_masses(ctypes.byref(s), vp(16), vp(16), vp(16), vp(16), vp(16), vp(256), 64, None) == 4
     assert L.crisp_block_masses(ctypes.byref(s), vp(16), vp(16), vp(16), None, vp(256), 1 << 30, None) == 1
-    assert L.crisp_route_cstruct(ctypes.byref(s), ctypes.byref(crisp.params_default()), vp(256), None, vp(256),
-                                 vp(256), vp(256), None) == 1
-    assert L.crisp_route_cstruct(ctypes.byref(s), ctypes.byref(crisp.params_default()), vp(256), vp(260), vp(256),
-                                 vp(256), vp(256), None) == 3
-    # divergence routing and fused masses: argument errors before any CUDA call
     pd = ctypes.byref(crisp.params_default())
-    assert L.crisp_route_jsd(ctypes.byref(s), pd, None, vp(256), None, vp(256), None) == 1
-    assert L.crisp_route_jsd(ctypes.byref(s), pd, vp(260), vp(256), None, vp(256), None) == 3
-    assert L.crisp_route_jsd(ctypes.byref(s), pd, vp(256), vp(256), vp(260), vp(256), None) == 3
+    assert L.crisp_route_cstruct_masses(ctypes.byref(s), pd, vp(256), None, vp(256), vp(256), vp(256), vp(256),
+                                        1 << 30, None) == 1
+    assert L.crisp_route_cstruct_masses(ctypes.byref(s), pd, vp(256), vp(260), vp(256), vp(256), vp(256), vp(256),
+                                        1 << 30, None) == 3
+    assert L.crisp_route_cstruct_masses(ctypes.byref(s), pd, vp(256), vp(256), vp(256), vp(256), vp(256), None,
+                                        1 << 30, None) == 4
+    assert L.crisp_route_cstruct(ctypes.byref(s), pd, vp(256), None, vp(256), vp(256), vp(256), 1 << 30, None) == 1
+    assert L.crisp_route_cstruct(ctypes.byref(s), pd, vp(260), vp(256), vp(256), vp(256), vp(256), 1 << 30,
+                                 None) == 3
+    assert L.crisp_route_cstruct(ctypes.byref(s), pd, vp(256), vp(256), vp(256), vp(256), vp(256), 64, None) == 4
+    # divergence routing and fused masses: argument errors before any CUDA call
+    assert L.crisp_route_jsd(ctypes.byref(s), pd, None, vp(256), None, vp(256), vp(256), 1 << 30, None) == 1
+    assert L.crisp_route_jsd(ctypes.byref(s), pd, vp(260), vp(256), None, vp(256), vp(256), 1 << 30, None) == 3
+    assert L.crisp_route_jsd(ctypes.byref(s), pd, vp(256), vp(256), vp(260), vp(256), vp(256), 1 << 30, None) == 3
     bad = crisp.params_default(route_mode=7)
-    assert L.crisp_route_jsd(ctypes.byref(s), ctypes.byref(bad), vp(256), vp(256), None, vp(256), None) == 1
+    assert L.crisp_route_jsd(ctypes.byref(s), ctypes.byref(bad), vp(256), vp(256), None, vp(256), vp(256), 1 << 30,
+                             None) == 1
+    # the allocation-free map's status reader needs a destination
+    assert L.crisp_noalloc_read_status(None, None) == 1
     # failure-detection self-test: argument errors before any CUDA call
     assert L.crisp_wait_selftest(None, 1 << 20, 1000000, None) == 4
     assert L.crisp_wait_selftest(vp(256), 1 << 20, 0, None) == 1
@@ -176,7 +272,9 @@ def test_short_and_empty_lengths(L, n):
         # nothing to compute: OK with null buffers and no device
         assert L.crisp_prefill_layer(ctypes.byref(s), p, None, None, None, None, None, 0, None) == 0
         assert L.crisp_dense_prefill(ctypes.byref(s), None, None, None, None, None, 0, None) == 0
-        assert L.crisp_sparse_prefill(ctypes.byref(s), None, None, None, None, None, None, None, 0, None) == 0
+        assert L.crisp_sparse_prefill_mask(ctypes.byref(s), None, None, None, None, None, None, None, 0, None) == 0
+        # the index-set form needs the method's steps (n >= 256)
+        assert L.crisp_sparse_prefill(ctypes.byref(s), *([None] * 9), 0, None) == 2
         assert L.crisp_prefill_layer_host(vp(256), ctypes.byref(s), p, *([None] * 9), 0, None) == 0
     else:
         # past the shape check: the first pointer check answers

@@ -183,7 +183,7 @@ def test_sparse_prefill_arbitrary_masks():
     s = crisp.make_shape(hq, hkv, n, qd, kd, out)
     ws = new_workspace(s)
     rbd = torch.from_numpy(rb.view(np.int32)).cuda()
-    crisp.sparse_prefill(s, qd, kd, vd, rbd, None, out, ws)  # default order: kv-group-major
+    crisp.sparse_prefill_mask(s, qd, kd, vd, rbd, None, out, ws)  # default order: kv-group-major
     torch.cuda.synchronize()
     assert_status_ok(ws)
     rb_causal = rb.copy()
@@ -375,12 +375,12 @@ def run_comparator_steps(q, k, v, params):
     pebits, rowbits = empty((hq, nb, W), torch.int32), empty((hq, nb, W), torch.int32)
     counts, order = empty((hq, nb), torch.int32), empty((hq * nb,), torch.int32)
     crisp.proxy_masses(s, qd, kd, vmass, smass, rmass, ws)
-    crisp.pe_map(s, qd, kd, route, pbar, ws)  # route all zeros: every head's pooled map
-    crisp.route_jsd(s, params, vmass, pbar, jsd, route)
-    crisp.select_vs(s, params, vmass, smass, route, vbits, sbits, ws)
+    crisp.pe_pool(s, qd, kd, route, pbar, ws)  # route all zeros: every head's pooled map
+    crisp.route_jsd(s, params, vmass, pbar, jsd, route, ws)
+    crisp.select_vs_masses(s, params, vmass, smass, route, vbits, sbits, ws)
     crisp.select_pe(s, params, pbar, route, pebits, ws)
     crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, ws)
-    crisp.sparse_prefill(s, qd, kd, vd, rowbits, order, out, ws)
+    crisp.sparse_prefill_mask(s, qd, kd, vd, rowbits, order, out, ws)
     torch.cuda.synchronize()
     assert_status_ok(ws)
     u64 = lambda t: t.cpu().numpy().view(np.uint64)
@@ -443,6 +443,80 @@ def test_prefill_layer_comparator_mode_matches_steps():
     assert 0 < steps["route"].sum() < 8  # both routes exercised
 
 
+@pytest.mark.parametrize("n", [1024, 1000])
+def test_route_cstruct_other_slice_widths(n):
+    # crisp_route_cstruct reads the map itself, so any slice widths work; bit
+    # for bit against the oracle on the GPU's own map, the overlap of the two
+    # slices counted once.
+    hq, hkv = 4, 2
+    w = synth.small("slices", hq, hkv, n, 81, vs_heads=[0])
+    q, k, _ = w.generate()
+    qd, kd = to_dev(q), to_dev(k)
+    s = crisp.make_shape(hq, hkv, n, qd, kd)
+    ws = new_workspace(s)
+    pmap = empty((hq, B, crisp.map_ld(n)), torch.float32)
+    crisp.proxy_map(s, qd, kd, pmap, ws)
+    pm = np.ascontiguousarray(pmap.cpu().numpy()[:, :, :n])
+    for sink, recency, tau in ((64, 128, (1, 5)), (1, 300, (1, 10)), (0, 128, (1, 5)), (700, 500, (1, 2)),
+                               (2000, 2000, (1, 1)), (128, 128, (1, 5))):
+        params = crisp.params_default(sink_tokens=sink, recency_tokens=recency, tau=tau)
+        cs, tot, route = empty((hq,), torch.int64), empty((hq,), torch.int64), empty((hq,), torch.uint8)
+        crisp.route_cstruct(s, params, pmap, cs, tot, route, ws)
+        torch.cuda.synchronize()
+        assert_status_ok(ws)
+        S, T, r = oracle.route(pm, tau=tau, sink=sink, recency=recency)
+        assert np.array_equal(cs.cpu().numpy().view(np.uint64), S), (sink, recency)
+        assert np.array_equal(tot.cpu().numpy().view(np.uint64), T), (sink, recency)
+        assert np.array_equal(route.cpu().numpy(), r), (sink, recency)
+
+
+# The pages' two ablations ("Main Findings"): routing alone (C_struct with
+# FlexPrefill's coverage selection on VS heads) and sink-aware selection alone
+# (FlexPrefill's divergence routing with CRISP's noise floor).
+ABLATIONS = [("routing-only", crisp.ROUTE_CSTRUCT, crisp.VS_GAMMA), ("selection-only", crisp.ROUTE_JSD, crisp.VS_NOISE)]
+
+
+@pytest.mark.parametrize("name,route_mode,vs_mode", ABLATIONS, ids=[a[0] for a in ABLATIONS])
+def test_prefill_layer_ablation_modes(name, route_mode, vs_mode):
+    hq, hkv, n, seed = 8, 2, 2048, 93
+    w = synth.small("ablation", hq, hkv, n, seed)
+    q, k, v = w.generate()
+    params = crisp.params_default(route_mode=route_mode, vs_mode=vs_mode, jsd_tau=0.2)
+    nb = crisp.num_blocks(n)
+    if route_mode == crisp.ROUTE_JSD:
+        steps = run_comparator_steps(q, k, v, params)
+        D, route = oracle.route_jsd(steps["vmass"], steps["pbar"][:, nb - 1, :], tau=params.jsd_tau)
+        near = np.abs(np.sqrt(np.maximum(D, 0)) - params.jsd_tau) < 1e-9
+        assert np.array_equal(steps["route"][~near], route[~near])
+        route = steps["route"]
+        pbar = steps["pbar"]
+    else:
+        steps = run_steps(q, k, v, params)
+        _, _, route = oracle.route(steps["pmap"])
+        assert np.array_equal(route, steps["route"])
+        pbar = steps["pbar"].copy()
+        pbar[route == 1] = 0.0
+    if vs_mode == crisp.VS_GAMMA:
+        vb, sb = oracle.select_vs_gamma(steps["vmass"], steps["smass"], route, gamma=(95, 100), kmin=8)
+    else:
+        vb, sb = oracle.select_vs(steps["vmass"], steps["smass"], route, kmin=8)
+    assert np.array_equal(vb, steps["vbits"]) and np.array_equal(sb, steps["sbits"])
+    pe = oracle.select_pe(pbar, route)
+    assert np.array_equal(pe, steps["pebits"])
+    rb = oracle.build_mask(route, vb, sb, pe)
+    assert np.array_equal(rb, steps["rowbits"])
+    assert 0 < route.sum() < hq  # both routes exercised
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    out = empty((hq, n, 128), torch.bfloat16)
+    s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+    ws = new_workspace(s, layer=True)
+    crisp.prefill_layer(s, params, qd, kd, vd, out, ws)
+    torch.cuda.synchronize()
+    assert_status_ok(ws)
+    assert torch.equal(out, steps["out"])
+    check_attention(q, k, v, out, rb, rows=sample_rows(hq, n, 24, seed))
+
+
 def test_length_gate_runs_dense():
     n = 4096  # 32 blocks: the sparse selection keeps fewer than all of them
     w = synth.small("gate", 4, 1, n, 92)
@@ -500,7 +574,7 @@ def test_attention_is_deterministic_under_load():
     order = torch.from_numpy(r["order"]).cuda()
     for _ in range(4):
         out = empty((hq, n, 128), torch.bfloat16)
-        crisp.sparse_prefill(s, qd, kd, vd, rb, order, out, ws)
+        crisp.sparse_prefill_mask(s, qd, kd, vd, rb, order, out, ws)
         torch.cuda.synchronize()
         assert_status_ok(ws)
         assert torch.equal(out, r["out"])

@@ -21,8 +21,11 @@ MUTANTS = [
       lambda: pins.test_vs_masses_single_entry_closed_form(127, 640)]),
     ("sink columns kept in the slash masses", "if (j <= i && j >= 128) s[", "if (j <= i && j >= 0) s[",
      [pins.test_vs_masses_sum_invariants, lambda: pins.test_vs_masses_single_entry_closed_form(5, 127)]),
-    ("recency slice one column short", "if (j < 128 || j >= n - 128) S += m;", "if (j < 128 || j > n - 128) S += m;",
-     [pins.test_cstruct_equals_brute_force_slice_sum]),
+    ("recency slice one column short", "if (j < sink || j >= n - recency) S += m;",
+     "if (j < sink || j > n - recency) S += m;", [pins.test_cstruct_equals_brute_force_slice_sum]),
+    ("slice union counted twice", "if (j < sink || j >= n - recency) S += m;",
+     "if (j < sink) S += m;\n        if (j >= n - recency) S += m;",
+     [lambda: pins.test_cstruct_other_slice_widths_brute_force(700, 500)]),
     ("route tie goes to PE", "route[h] = static_cast<unsigned __int128>(tau_den) * S >= ",
      "route[h] = static_cast<unsigned __int128>(tau_den) * S > ", [pins.test_route_tau_tie_goes_to_vs]),
     ("noise floor not strict", "if (lhs > rhs && !chosen[c])", "if (lhs >= rhs && !chosen[c])",

@@ -104,6 +104,25 @@ def test_cstruct_equals_brute_force_slice_sum():
     assert S.tolist() == (vm[:, 0] + vm[:, -1]).tolist()
 
 
+@pytest.mark.parametrize("sink,recency", [(64, 128), (1, 300), (0, 128), (128, 0), (700, 500), (1024, 1024)])
+def test_cstruct_other_slice_widths_brute_force(sink, recency):
+    # The slice widths as parameters (the pages fix both at 128): brute-force
+    # numpy sums over the union of the two column ranges, a column inside
+    # both counted once (n = 1024: 700 + 500 overlap, 1024 + 1024 is all).
+    w, P = _small_map()
+    S, T, _ = oracle.route(P, sink=sink, recency=recency)
+    Q = np.rint(P.astype(np.float64) * 2.0 ** 32).astype(np.uint64)
+    n = w.n
+    cols = np.zeros(n, bool)
+    cols[:sink] = True
+    if recency:
+        cols[max(0, n - recency):] = True
+    assert S.tolist() == Q[:, :, cols].sum(axis=(1, 2)).tolist()
+    assert T.tolist() == Q.sum(axis=(1, 2)).tolist()
+    if sink + recency >= n:
+        assert S.tolist() == T.tolist()
+
+
 def test_route_tau_tie_goes_to_vs():
     # n = 384: sink block 0, middle block 1, recency block 2. Every row puts
     # 1/8 at column 0, 3/4 at column 200 and 1/8 at column 300: C = 1/4.
