@@ -45,29 +45,42 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["crisp", "reference"], default="crisp")
     ap.add_argument("--config", default="llama8b-512k", help="gqa4x1-2k, llama8b-32k, qwen7b-128k, llama8b-256k-L0..llama8b-256k-L3, llama8b-512k")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="run the chosen workload's recipe at this many tokens instead (small profiling cases)")
+    ap.add_argument("--also", default="qwen7b-128k",
+                    help="a second workload timed in the same process and reported under 'also' ('' for none)")
     ap.add_argument("--alpha", default="1/1")
+    ap.add_argument("--pe-mode", choices=["gamma", "noise"], default="gamma",
+                    help="PE selection rule: gamma coverage (the pages' rule) or the noise floor")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention baseline launch")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-map", action="store_true", help="skip the map-reading route/select timing")
     ap.add_argument("--sweep", choices=["lengths", "alpha", "pe", "flex"], default=None,
                     help="instead of the step: sparse layer vs dense attention over sequence lengths (the "
                          "llama8b-32k recipe, 2k-128k), over alpha (llama8b-512k), PE gamma vs noise-floor rule "
-                         "(llama8b-32k), or CRISP vs the FlexPrefill rules it replaces (llama8b-512k and llama8b-32k)")
+                         "(llama8b-32k), or CRISP vs the FlexPrefill rules it replaces and the two ablations "
+                         "(llama8b-512k and llama8b-32k)")
     return ap.parse_args(argv)
 
 
 def workload_config(w, args, world):
-    """The config keys both arms report for a workload."""
+    """The config keys both arms report for a workload (identical in both)."""
     return {"workload": w.name, "hq": w.hq, "hkv": w.hkv, "seq_len": w.n, "head_dim": 128, "block": B,
-            "alpha": args.alpha, "tau": "1/5", "gamma": "19/20", "kmin_blocks": 8,
+            "alpha": args.alpha, "tau": "1/5", "gamma": "19/20", "kmin_blocks": 8, "pe_mode": args.pe_mode,
             "parallelism": f"replicas x{world}"}
 
 
-def workload(synth, name):
-    """A named workload; llama8b-256k-L0..L3 are the layers of the 4-layer stack."""
+def workload(synth, name, seq_len=0):
+    """A named workload; llama8b-256k-L0..L3 are the layers of the 4-layer
+    stack. seq_len > 0: the same recipe at that length (named '<name>@<n>')."""
     if name.startswith("llama8b-256k-L"):
-        return synth.WORKLOADS["llama8b-256k-stack"].layer(int(name[len("llama8b-256k-L"):]))
-    return synth.WORKLOADS[name]
+        w = synth.WORKLOADS["llama8b-256k-stack"].layer(int(name[len("llama8b-256k-L"):]))
+    else:
+        w = synth.WORKLOADS[name]
+    if seq_len:
+        w = synth.Workload(**{**w.__dict__, "name": f"{w.name}@{seq_len}", "n": seq_len})
+    return w
 
 
 # --------------------------------------------------------------- distributed
@@ -169,37 +182,56 @@ def selected_pairs(rowbits: np.ndarray, n: int) -> int:
     return int((bits.sum(axis=0).astype(np.int64) * wgt).sum())
 
 
-def profiled_traffic(sources, profile: str):
-    """DRAM bytes per launch from a committed ncu summary, or None when a
-    source that decides the traffic (the kernel, its work order) has changed
-    since the counters were taken (sha256 over the files in order)."""
+def profiled_traffic(sources, profile: str, w, blocks: int):
+    """DRAM bytes per attention launch from a committed ncu summary, and how
+    they were obtained. The summary holds the counters of one launch on a
+    small case of a workload's recipe and that case's selected key blocks;
+    a run of the same recipe at any length gets the per-block figure times
+    its own selected blocks (the summary states why that scaling holds).
+    None when a source that decides the traffic (the kernel, its work order)
+    has changed since the counters were taken (sha256 over the files in
+    order), or when the run's recipe is another one."""
     import hashlib
     try:
         text = open(os.path.join(ROOT, profile)).read()
         src = b"".join(open(os.path.join(ROOT, f), "rb").read() for f in sources)
     except OSError:
-        return None
+        return None, "no profile"
     fields = dict(line.split(": ", 1) for line in text.splitlines() if ": " in line and " " not in line.split(": ")[0])
     if fields.get("source_sha256", "").strip() != hashlib.sha256(src).hexdigest():
-        return None
+        return None, "kernel changed since the counters were taken"
     try:
-        return int(fields["traffic_bytes_per_launch"])
+        captured = fields["workload"].strip()
+        per_launch = int(fields["traffic_bytes_per_launch"])
+        per_block = float(fields["traffic_bytes_per_selected_block"]) if "traffic_bytes_per_selected_block" in fields \
+            else None
     except (KeyError, ValueError):
-        return None
+        return None, "profile incomplete"
+    if w.name == captured:
+        return per_launch, f"measured on this workload ({captured})"
+    if per_block is not None and w.name.split("@")[0] == captured.split("@")[0]:
+        return int(round(per_block * blocks)), (f"{per_block:.0f} B per selected block measured on {captured}, "
+                                                f"times this run's {blocks} selected blocks")
+    return None, f"profile is for another recipe ({captured})"
 
 
 # The attention kernel and the kernel that writes its work order.
 TRAFFIC_SOURCES = ("dynamic_sparse_prefill_crisp_gb300/csrc/attention.cu",
                    "dynamic_sparse_prefill_crisp_gb300/csrc/mask.cu")
+TRAFFIC_PROFILE = "profiles/attention_llama8b_512k_traffic.md"
 
 
 def measured_peaks():
+    """(HBM GB/s, bf16 burst TFLOP/s, bf16 sustained TFLOP/s, kind). A kernel
+    timed by its own events inside a step of tens of ms is a burst: the burst
+    figure is its denominator; the sustained one is reported beside it."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return p.get("hbm_gbs", 6800.0), p.get("bf16_tflops_sustained", 1700.0), "measured"
-    return 6800.0, 1700.0, "fallback"
+        return p.get("hbm_gbs", 6800.0), p.get("bf16_tflops", 1900.0), p.get("bf16_tflops_sustained", 1700.0), \
+            "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 # ------------------------------------------------------------ CPU baseline
@@ -268,29 +300,340 @@ def run_reference(args):
     if rank != 0:
         return 0
     import synth
-    w = workload(synth, args.config)
+    w = workload(synth, args.config, args.seq_len)
     alpha = tuple(int(x) for x in args.alpha.split("/"))
     q, k, v = w.generate()
     cores = os.cpu_count() or 1
-    times = []
+    times, secs = [], []
     sample = None
     for i in range(args.warmup + args.steps):
         r = cpu_sample(w, q, k, v, alpha, nthreads=cores)
         sample = r["sample"]
         if i >= args.warmup:
             times.append(r["layer_ms"])
+            secs.append(r["seconds"])
     ms = statistics.mean(times)
+    cpu = {"value": ms, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample, "extrapolated": True,
+           "sample_seconds_per_step": statistics.mean(secs)}
     line = {"impl": "reference", "metric": METRIC, "value": ms, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {**workload_config(w, args, 1), "host": "fp64 oracle on the host cores"},
-            "cpu_baseline": {"value": ms, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "config": workload_config(w, args, 1),
+            "host": "fp64 oracle on the host cores (the reference is prose: the oracle stands in for it)",
+            "extrapolated": True,
+            "extrapolation": ("each step times the oracle on a bounded sample of the layer (sample_seconds_per_step "
+                              "of wall time) and scales it to a whole layer by selected (row, key) pairs and by "
+                              "heads; value and ms_per_step are that scaled figure, not wall time"),
+            "sample_seconds_per_step": statistics.mean(secs),
+            "cpu_baseline": cpu,
             "e2e": {"value": ms, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
 # --------------------------------------------------------------- GPU arm
+# our kernel launches per step: proxy statistics 2, fused masses 2, route 1,
+# select_vs 1, pe_pool 3, select_pe 1, mask+schedule 2, attention 1
+LAUNCHES_PER_STEP = 13
+STAGES = ["proxy_masses", "route", "select_vs", "pe_pool", "select_pe", "mask", "attention"]
+
+
+def host_facts(ptrs):
+    """Host-side facts behind the e2e number: CPUs, NUMA nodes, the GPU's
+    node and the node of each pinned buffer's pages (/proc/self/numa_maps)."""
+    facts = {"cpus": os.cpu_count()}
+    try:
+        facts["numa_nodes"] = len([d for d in os.listdir("/sys/devices/system/node") if d.startswith("node")])
+    except OSError:
+        facts["numa_nodes"] = None
+    try:
+        bus = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader", "-i",
+                              os.environ.get("LOCAL_RANK", "0")], capture_output=True, text=True, timeout=20)
+        bus_id = bus.stdout.strip().lower()
+        if len(bus_id.split(":")[0]) > 4:  # nvidia-smi prints an 8-digit domain; sysfs uses 4
+            bus_id = bus_id[len(bus_id.split(":")[0]) - 4:]
+        with open(f"/sys/bus/pci/devices/{bus_id}/numa_node") as f:
+            facts["gpu_numa_node"] = int(f.read())
+    except (OSError, ValueError, subprocess.SubprocessError):
+        facts["gpu_numa_node"] = None
+    try:
+        spans = []
+        with open("/proc/self/maps") as f:
+            for line in f:
+                lo, hi = (int(x, 16) for x in line.split()[0].split("-"))
+                spans.append((lo, hi))
+        nodes = {}
+        with open("/proc/self/numa_maps") as f:
+            numa = {int(line.split()[0], 16): line.split()[1:] for line in f}
+        for name, ptr in ptrs.items():
+            hit = [lo for lo, hi in spans if lo <= ptr < hi]
+            fields = numa.get(hit[0], []) if hit else []
+            nodes[name] = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in fields
+                           if kv.startswith("N") and "=" in kv and kv.split("=")[1].isdigit()}
+        facts["pinned_pages_per_node"] = nodes
+    except (OSError, ValueError, IndexError):
+        facts["pinned_pages_per_node"] = None
+    return facts
+
+
+class Layer:
+    """Device buffers and the step calls of one workload (inputs in HBM)."""
+
+    def __init__(self, crisp, torch, w, params, dev, stream):
+        self.w, self.params, self.stream = w, params, stream
+        hq, hkv, n = w.hq, w.hkv, w.n
+        nb = num_blocks(n)
+        W = (nb + 31) // 32
+        # Inputs: generated on the host into pinned buffers (also the e2e source).
+        self.qh = torch.empty((hq, n, 128), dtype=torch.int16, pin_memory=True)
+        self.kh = torch.empty((hkv, n, 128), dtype=torch.int16, pin_memory=True)
+        self.vh = torch.empty((hkv, n, 128), dtype=torch.int16, pin_memory=True)
+        t0 = time.perf_counter()
+        w.generate(*(t.numpy().view(np.uint16) for t in (self.qh, self.kh, self.vh)))
+        self.gen_s = time.perf_counter() - t0
+        self.qd = self.qh.to(dev).view(torch.bfloat16)
+        self.kd = self.kh.to(dev).view(torch.bfloat16)
+        self.vd = self.vh.to(dev).view(torch.bfloat16)
+        self.out = torch.empty((hq, n, 128), dtype=torch.bfloat16, device=dev)
+        s = self.shape = crisp.make_shape(hq, hkv, n, self.qd, self.kd, self.out)
+        self.ws = torch.empty(crisp.workspace_size(s), dtype=torch.uint8, device=dev)
+        crisp.workspace_init(self.ws)
+        E = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+        self.vmass, self.smass, self.rmass = E((hq, nb), torch.int64), E((hq, nb), torch.int64), E((hq,), torch.int64)
+        self.cstruct, self.total, self.route = E((hq,), torch.int64), E((hq,), torch.int64), E((hq,), torch.uint8)
+        self.vbits, self.sbits = E((hq, W), torch.int32), E((hq, W), torch.int32)
+        self.pbar = E((hq, nb, nb), torch.float32)
+        self.pebits, self.rowbits = E((hq, nb, W), torch.int32), E((hq, nb, W), torch.int32)
+        self.counts, self.order = E((hq, nb), torch.int32), E((hq * nb,), torch.int32)
+        st, ws, p = stream, self.ws, params
+        self.calls = [
+            lambda: crisp.proxy_masses(s, self.qd, self.kd, self.vmass, self.smass, self.rmass, ws, st),
+            lambda: crisp.route_cstruct_masses(s, p, self.vmass, self.rmass, self.cstruct, self.total, self.route,
+                                               ws, st),
+            lambda: crisp.select_vs_masses(s, p, self.vmass, self.smass, self.route, self.vbits, self.sbits, ws, st),
+            lambda: crisp.pe_pool(s, self.qd, self.kd, self.route, self.pbar, ws, st),
+            lambda: crisp.select_pe(s, p, self.pbar, self.route, self.pebits, ws, st),
+            lambda: crisp.build_mask(s, self.route, self.vbits, self.sbits, self.pebits, self.rowbits, self.counts,
+                                     self.order, ws, st),
+            lambda: crisp.sparse_prefill_mask(s, self.qd, self.kd, self.vd, self.rowbits, self.order, self.out, ws,
+                                              st),
+        ]
+
+    def step(self, events=None):
+        for i, c in enumerate(self.calls):
+            if events is not None:
+                events[i].record(self.stream)
+            c()
+        if events is not None:
+            events[-1].record(self.stream)
+
+
+def time_steps(torch, layer, args, world, local, dev):
+    """W warm-up steps, then K steps timed with CUDA events (per stage too),
+    inside a barrier and synchronize on both sides, clocks sampled."""
+    import dynamic_sparse_prefill_crisp_gb300 as crisp
+    for _ in range(args.warmup):
+        layer.step()
+    torch.cuda.synchronize()
+    st = crisp.read_status(layer.ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {crisp.status_string(st)}")
+    w = layer.w
+    in_bytes = (w.hq + 2 * w.hkv) * w.n * 128 * 2
+    l2_bytes = 129 * 2**20
+    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev) if in_bytes < 2 * l2_bytes else None
+    l2_note = (f"inputs ({in_bytes / 2**30:.2f} GiB) larger than L2; no flush" if flush is None else
+               f"inputs ({in_bytes / 2**20:.1f} MiB) smaller than L2: 512 MiB written before each timed step")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(layer.calls) + 1)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    if flush is None:
+        start.record(layer.stream)
+        for i in range(args.steps):
+            layer.step(ev[i])
+        end.record(layer.stream)
+    else:
+        # Inputs smaller than L2: a 512 MiB write evicts them before each
+        # step, outside the timed intervals (the step total is the sum).
+        for i in range(args.steps):
+            flush.zero_()
+            layer.step(ev[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    if flush is None:
+        ms_total = start.elapsed_time(end)
+    else:
+        ms_total = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps))
+    ms_total = max_over_ranks(ms_total, world, dev)
+    stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                for j, name in enumerate(STAGES)}
+    st = crisp.read_status(layer.ws)
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {crisp.status_string(st)}")
+    return ms_total / args.steps, stage_ms, clk, l2_note
+
+
+def attention_roofline(layer, stage_ms, peaks):
+    """The attention kernel's selected-block FLOP rate against the burst bf16
+    peak (the sustained figure beside it), and the layer's work counts."""
+    w = layer.w
+    rb = layer.rowbits.cpu().numpy().view(np.uint32)
+    pairs = selected_pairs(rb, w.n)
+    blocks = int(layer.counts.cpu().numpy().astype(np.int64).sum())
+    flops = 4 * 128 * pairs
+    dense_pairs = w.hq * w.n * (w.n + 1) // 2
+    hbm, burst, sustained, kind = peaks
+    tf = flops / (stage_ms["attention"] * 1e-3) / 1e12
+    routes = layer.route.cpu().numpy()
+    return {"pairs": pairs, "blocks": blocks, "flops": flops, "dense_pairs": dense_pairs, "tflops": tf,
+            "density": pairs / dense_pairs, "routes": {"vs": int(routes.sum()), "pe": int((routes == 0).sum())},
+            "frac_burst": tf / burst, "frac_sustained": tf / sustained, "kind": kind}
+
+
+def dense_run(torch, crisp, layer, attn_ms, ms_per_step):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w, st = layer.w, layer.stream
+    e0.record(st)
+    crisp.dense_prefill(layer.shape, layer.qd, layer.kd, layer.vd, layer.out, layer.ws, st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    d_ms = e0.elapsed_time(e1)
+    dense_pairs = w.hq * w.n * (w.n + 1) // 2
+    # put the sparse output back (the e2e check compares against it)
+    crisp.sparse_prefill_mask(layer.shape, layer.qd, layer.kd, layer.vd, layer.rowbits, layer.order, layer.out,
+                              layer.ws, st)
+    return {"ms": d_ms, "tflops": 4 * 128 * dense_pairs / (d_ms * 1e-3) / 1e12, "attention_speedup": d_ms / attn_ms,
+            "layer_speedup": d_ms / ms_per_step}
+
+
+def map_path(torch, crisp, layer, stage_ms, hbm_peak):
+    """The survey's map-reading calls on the same inputs, after the step: the
+    proxy map written to HBM, C_struct routing from it, VS selection from it
+    (each reads the whole map once). Their masses, routes and bitsets must
+    equal the step's."""
+    w, s, st, ws, p = layer.w, layer.shape, layer.stream, layer.ws, layer.params
+    dev = layer.qd.device
+    pmap = torch.empty((w.hq, B, num_blocks(w.n) * B), dtype=torch.float32, device=dev)
+    E = lambda t: torch.empty_like(t)
+    cs, tot, route = E(layer.cstruct), E(layer.total), E(layer.route)
+    vm, sm, vb, sb = E(layer.vmass), E(layer.smass), E(layer.vbits), E(layer.sbits)
+    ue = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    t = {"proxy": [], "route": [], "select": []}
+    for _ in range(3):
+        ue[0].record(st)
+        crisp.proxy_map(s, layer.qd, layer.kd, pmap, ws, st)
+        ue[1].record(st)
+        crisp.route_cstruct(s, p, pmap, cs, tot, route, ws, st)
+        ue[2].record(st)
+        crisp.select_vs(s, p, pmap, route, vm, sm, vb, sb, ws, st)
+        ue[3].record(st)
+        torch.cuda.synchronize()
+        t["proxy"].append(ue[0].elapsed_time(ue[1]))
+        t["route"].append(ue[1].elapsed_time(ue[2]))
+        t["select"].append(ue[2].elapsed_time(ue[3]))
+    for a, b in ((cs, layer.cstruct), (tot, layer.total), (route, layer.route), (vm, layer.vmass), (sm, layer.smass),
+                 (vb, layer.vbits), (sb, layer.sbits)):
+        assert torch.equal(a, b), "the map-reading calls differ from the fused step"
+    med = {k: statistics.median(v) for k, v in t.items()}
+    map_bytes = 4 * w.hq * B * num_blocks(w.n) * B
+    proxy_bytes = map_bytes + 2 * (2 * w.hkv * w.n * 128) + 2 * w.hq * B * 128
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+    del pmap
+    return {"proxy_map_ms": med["proxy"], "route_cstruct_ms": med["route"], "select_vs_ms": med["select"],
+            "proxy_map_gbs": gbs(proxy_bytes, med["proxy"]), "route_cstruct_gbs": gbs(map_bytes, med["route"]),
+            "select_vs_gbs": gbs(map_bytes, med["select"]), "peak_gbs": hbm_peak,
+            "route_cstruct_frac": gbs(map_bytes, med["route"]) / hbm_peak,
+            "select_vs_frac": gbs(map_bytes, med["select"]) / hbm_peak,
+            "route_select_frac": gbs(2 * map_bytes, med["route"] + med["select"]) / hbm_peak,
+            "bytes_note": "each call reads the fp32 map once (4*hq*128*ld bytes)",
+            "fused_saving_ms": med["proxy"] + med["route"] + med["select"]
+            - (stage_ms["proxy_masses"] + stage_ms["route"] + stage_ms["select_vs"])}
+
+
+def e2e_run(torch, crisp, layer, args, world, local, dev):
+    """End to end through the public API with HOST buffers: one call of
+    crisp_prefill_layer_host per step, which uploads q, k, v from pinned host
+    memory, runs the whole layer and downloads the output, one kv group at a
+    time with the copies overlapped with the compute."""
+    s, st = layer.shape, layer.stream
+    lws = torch.empty(crisp.layer_workspace_size(s), dtype=torch.uint8, device=dev)
+    crisp.workspace_init(lws)
+    oh = torch.empty(tuple(layer.out.shape), dtype=torch.int16, pin_memory=True)
+    qx, kx, vx = torch.empty_like(layer.qd), torch.empty_like(layer.kd), torch.empty_like(layer.vd)
+    ox = torch.empty_like(layer.out)
+    pipe = crisp.HostPipeline()
+    facts = host_facts({"q": layer.qh.data_ptr(), "k": layer.kh.data_ptr(), "v": layer.vh.data_ptr(),
+                        "out": oh.data_ptr()})
+
+    def copy_probe():
+        # one 1 GiB upload and one 1 GiB download between pinned and device memory
+        nel = min(layer.qh.numel(), 2**29)
+        src, dst = layer.qh.view(-1)[:nel], qx.view(torch.int16).view(-1)[:nel]
+        c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        c0.record(st)
+        dst.copy_(src, non_blocking=True)
+        c1.record(st)
+        oh.view(-1)[:nel].copy_(dst, non_blocking=True)
+        c2.record(st)
+        torch.cuda.synchronize()
+        return {"h2d": nel * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9, "d2h": nel * 2 / (c1.elapsed_time(c2) * 1e-3) / 1e9,
+                "bytes": nel * 2}
+
+    def e2e_step():
+        crisp.prefill_layer_host(pipe, s, layer.params, layer.qh, layer.kh, layer.vh, oh, qx, kx, vx, ox, lws, st)
+
+    probe_before = copy_probe()
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    # Three windows of K steps; the value is their median (the host-side
+    # copy path of a shared machine varies between windows, so all three
+    # are reported).
+    windows = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(st)
+        torch.cuda.synchronize()
+        windows.append(max_over_ranks(a.elapsed_time(b) / args.steps, world, dev))
+    clk = clocks.stop()
+    if crisp.read_status(lws) != 0:
+        raise RuntimeError("device status after e2e")
+    assert torch.equal(oh.view(torch.bfloat16).to(dev), layer.out), "e2e output differs from the device-resident run"
+    probe_after = copy_probe()
+    pipe.close()
+    h2d = (layer.qh.numel() + layer.kh.numel() + layer.vh.numel()) * 2
+    return {"value": statistics.median(windows) / world, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": oh.numel() * 2, "api": "crisp_prefill_layer_host",
+            "windows_ms": [round(x / world, 3) for x in windows],
+            "host_buffers_pinned": all(t.is_pinned() for t in (layer.qh, layer.kh, layer.vh, oh)), "clocks": clk,
+            "copy_gbs_before": probe_before, "copy_gbs_after": probe_after,
+            "copy_bound_ms": (h2d / probe_before["h2d"] + oh.numel() * 2 / probe_before["d2h"]) / 1e6,
+            "host": facts}
+
+
+def cpu_baseline(layer, alpha):
+    w = layer.w
+    r = cpu_sample(w, *(t.numpy().view(np.uint16) for t in (layer.qh, layer.kh, layer.vh)), alpha,
+                   nthreads=os.cpu_count())
+    cpu = {"value": r["layer_ms"], "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": r["sample"],
+           "extrapolated": True, "sample_seconds": r["seconds"]}
+    if w.n <= 8192:  # small layers: also the whole layer through the oracle on one core, no sampling
+        cpu["full_layer_1core_ms"] = cpu_full_layer(w, *(t.numpy().view(np.uint16) for t in (layer.qh, layer.kh,
+                                                                                               layer.vh)), alpha)
+    return cpu
+
+
 def run_crisp(args):
     import torch
     import dynamic_sparse_prefill_crisp_gb300 as crisp
@@ -304,238 +647,70 @@ def run_crisp(args):
         crisp_build.build()
     barrier(world)
     dev = torch.device("cuda", local)
-    w = workload(synth, args.config)
     alpha = tuple(int(x) for x in args.alpha.split("/"))
-    hq, hkv, n = w.hq, w.hkv, w.n
-    nb = num_blocks(n)
-    W = (nb + 31) // 32
-
-    # Inputs: generated on the host into pinned buffers (also the e2e source).
-    qh = torch.empty((hq, n, 128), dtype=torch.int16, pin_memory=True)
-    kh = torch.empty((hkv, n, 128), dtype=torch.int16, pin_memory=True)
-    vh = torch.empty((hkv, n, 128), dtype=torch.int16, pin_memory=True)
-    t0 = time.perf_counter()
-    w.generate(qh.numpy().view(np.uint16), kh.numpy().view(np.uint16), vh.numpy().view(np.uint16))
-    gen_s = time.perf_counter() - t0
-    qd = qh.to(dev).view(torch.bfloat16)
-    kd = kh.to(dev).view(torch.bfloat16)
-    vd = vh.to(dev).view(torch.bfloat16)
-    out = torch.empty((hq, n, 128), dtype=torch.bfloat16, device=dev)
-    s = crisp.make_shape(hq, hkv, n, qd, kd, out)
-    params = crisp.params_default(alpha=alpha)
-    ws = torch.empty(crisp.workspace_size(s), dtype=torch.uint8, device=dev)
-    crisp.workspace_init(ws)
-    E = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
-    pmap = E((hq, B, crisp.map_ld(n)), torch.float32)
-    vmass, smass, rmass = E((hq, nb), torch.int64), E((hq, nb), torch.int64), E((hq,), torch.int64)
-    cstruct, total, route = E((hq,), torch.int64), E((hq,), torch.int64), E((hq,), torch.uint8)
-    vbits, sbits = E((hq, W), torch.int32), E((hq, W), torch.int32)
-    pbar = E((hq, nb, nb), torch.float32)
-    pebits, rowbits = E((hq, nb, W), torch.int32), E((hq, nb, W), torch.int32)
-    counts, order = E((hq, nb), torch.int32), E((hq * nb,), torch.int32)
+    pe_mode = crisp.PE_GAMMA if args.pe_mode == "gamma" else crisp.PE_NOISE
+    params = crisp.params_default(alpha=alpha, pe_mode=pe_mode)
     stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    hbm_peak, burst_peak, sustained_peak, peak_kind = peaks
 
-    stages = ["proxy_masses", "route", "select_vs", "pe_map", "select_pe", "mask", "attention"]
-    calls = [
-        lambda: crisp.proxy_masses(s, qd, kd, vmass, smass, rmass, ws, stream),
-        lambda: crisp.route_cstruct_masses(s, params, vmass, rmass, cstruct, total, route, ws, stream),
-        lambda: crisp.select_vs_masses(s, params, vmass, smass, route, vbits, sbits, ws, stream),
-        lambda: crisp.pe_pool(s, qd, kd, route, pbar, ws, stream),
-        lambda: crisp.select_pe(s, params, pbar, route, pebits, ws, stream),
-        lambda: crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, ws, stream),
-        lambda: crisp.sparse_prefill_mask(s, qd, kd, vd, rowbits, order, out, ws, stream),
-    ]
-    # our kernel launches per step: proxy statistics 2, fused masses 2,
-    # route 1, select_vs 1, pe_map 3, select_pe 1, mask+schedule 2, attention 1
-    launches_per_step = 13
+    w = workload(synth, args.config, args.seq_len)
+    layer = Layer(crisp, torch, w, params, dev, stream)
+    ms_per_step, stage_ms, clk, l2_note = time_steps(torch, layer, args, world, local, dev)
+    roof = attention_roofline(layer, stage_ms, peaks)
+    traffic, traffic_how = profiled_traffic(TRAFFIC_SOURCES, TRAFFIC_PROFILE, w, roof["blocks"])
+    mp = None if args.no_map else map_path(torch, crisp, layer, stage_ms, hbm_peak)
+    dense = None if args.no_dense else dense_run(torch, crisp, layer, stage_ms["attention"], ms_per_step)
+    e2e = None if args.no_e2e else e2e_run(torch, crisp, layer, args, world, local, dev)
+    cpu = cpu_baseline(layer, alpha) if rank == 0 and world == 1 and not args.no_cpu else None
+    gen_s = layer.gen_s
+    del layer
+    torch.cuda.empty_cache()
 
-    def step(events=None):
-        for i, c in enumerate(calls):
-            if events is not None:
-                events[i].record(stream)
-            c()
-        if events is not None:
-            events[-1].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st = crisp.read_status(ws)
-    if st != 0:
-        raise RuntimeError(f"device status after warm-up: {crisp.status_string(st)}")
-
-    in_bytes = (hq + 2 * hkv) * n * 128 * 2
-    l2_bytes = 129 * 2**20
-    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev) if in_bytes < 2 * l2_bytes else None
-    l2_note = (f"inputs ({in_bytes / 2**30:.2f} GiB) larger than L2; no flush" if flush is None else
-               f"inputs ({in_bytes / 2**20:.1f} MiB) smaller than L2: 512 MiB written before each timed step")
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    if flush is None:
-        start.record(stream)
-        for i in range(args.steps):
-            step(ev[i])
-        end.record(stream)
-    else:
-        # Inputs smaller than L2: a 512 MiB write evicts them before each
-        # step, outside the timed intervals (the step total is the sum).
-        for i in range(args.steps):
-            flush.zero_()
-            step(ev[i])
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    if flush is None:
-        ms_total = start.elapsed_time(end)
-    else:
-        ms_total = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps))
-    ms_total = max_over_ranks(ms_total, world, dev)
-    ms_per_step = ms_total / args.steps
-    stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
-                for j, name in enumerate(stages)}
-    st = crisp.read_status(ws)
-    if st != 0:
-        raise RuntimeError(f"device status after timing: {crisp.status_string(st)}")
-
-    # Algorithmic work of the step's results.
-    rb = rowbits.cpu().numpy().view(np.uint32)
-    pairs = selected_pairs(rb, n)
-    flops = 4 * 128 * pairs
-    dense_pairs = hq * n * (n + 1) // 2
-    routes = route.cpu().numpy()
-    hbm_peak, tf_peak, peak_kind = measured_peaks()
-    traffic = profiled_traffic(TRAFFIC_SOURCES, "profiles/attention_llama8b_512k_traffic.md")
-    attn_ms = stage_ms["attention"]
-    achieved_tf = flops / (attn_ms * 1e-3) / 1e12
-    proxy_bytes = 4 * hq * B * n + 2 * (2 * hkv * n * 128) + 2 * hq * B * 128
-    masses_bytes = 4 * hq * B * n
-
-    # The unfused map path on the same inputs: the proxy map written to HBM,
-    # then the mass pass reading it back (the map-reading route/select
-    # roofline); its masses must equal the fused ones.
-    vm_fused, sm_fused = vmass.clone(), smass.clone()
-    ue = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    unf = {"proxy": [], "masses": []}
-    for _ in range(3):
-        ue[0].record(stream)
-        crisp.proxy_map(s, qd, kd, pmap, ws, stream)
-        ue[1].record(stream)
-        crisp.block_masses(s, pmap, vmass, smass, rmass, ws, stream)
-        ue[2].record(stream)
-        torch.cuda.synchronize()
-        unf["proxy"].append(ue[0].elapsed_time(ue[1]))
-        unf["masses"].append(ue[1].elapsed_time(ue[2]))
-    assert torch.equal(vm_fused, vmass) and torch.equal(sm_fused, smass), "fused masses differ from the map path"
-    unf_proxy_ms, unf_masses_ms = statistics.median(unf["proxy"]), statistics.median(unf["masses"])
-
-    # Dense attention over every causal block, same inputs, same run.
-    dense = None
-    if not args.no_dense:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        crisp.dense_prefill(s, qd, kd, vd, out, ws, stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        d_ms = e0.elapsed_time(e1)
-        dense = {"ms": d_ms, "tflops": 4 * 128 * dense_pairs / (d_ms * 1e-3) / 1e12,
-                 "attention_speedup": d_ms / attn_ms, "layer_speedup": d_ms / ms_per_step}
-        crisp.sparse_prefill_mask(s, qd, kd, vd, rowbits, order, out, ws, stream)
-
-    # End to end through the public API with HOST buffers: one call of
-    # crisp_prefill_layer_host per step, which uploads q, k, v from pinned
-    # host memory, runs the whole layer and downloads the output, one kv
-    # group at a time with the copies overlapped with the compute.
-    e2e = None
-    if not args.no_e2e:
-        lws = torch.empty(crisp.layer_workspace_size(s), dtype=torch.uint8, device=dev)
-        crisp.workspace_init(lws)
-        oh = torch.empty((hq, n, 128), dtype=torch.int16, pin_memory=True)
-        qx, kx, vx = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-        ox = torch.empty_like(out)
-        pipe = crisp.HostPipeline()
-
-        def e2e_step():
-            crisp.prefill_layer_host(pipe, s, params, qh, kh, vh, oh, qx, kx, vx, ox, lws, stream)
-
-        e2e_step()
-        torch.cuda.synchronize()
-        barrier(world)
-        # Three windows of K steps; the value is their median (the host-side
-        # copy path of a shared machine varies between windows, so all three
-        # are reported).
-        windows = []
-        e2e_clocks = ClockSampler(local)
-        e2e_clocks.start()
-        time.sleep(0.3)
-        for _ in range(3):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(args.steps):
-                e2e_step()
-            b.record(stream)
-            torch.cuda.synchronize()
-            windows.append(max_over_ranks(a.elapsed_time(b) / args.steps, world, dev))
-        e2e_ms = statistics.median(windows)
-        e2e_clk = e2e_clocks.stop()
-        if crisp.read_status(lws) != 0:
-            raise RuntimeError("device status after e2e")
-        assert torch.equal(oh.view(torch.bfloat16).to(dev), out), "e2e output differs from the device-resident run"
-        h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
-        e2e = {"value": e2e_ms / world, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": oh.numel() * 2,
-               "api": "crisp_prefill_layer_host", "windows_ms": [round(x / world, 3) for x in windows],
-               "host_buffers_pinned": all(t.is_pinned() for t in (qh, kh, vh, oh)), "clocks": e2e_clk}
-        # Raw copy rates on this machine, for context: one 4 GiB upload, one download.
-        c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        c0.record(stream)
-        qx.view(torch.int16).copy_(qh, non_blocking=True)
-        c1.record(stream)
-        oh.copy_(ox.view(torch.int16), non_blocking=True)
-        c2.record(stream)
-        torch.cuda.synchronize()
-        e2e["copy_gbs"] = {"h2d": qh.numel() * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9,
-                           "d2h": oh.numel() * 2 / (c1.elapsed_time(c2) * 1e-3) / 1e9}
-        pipe.close()
-        del lws, qx, kx, vx, ox
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        r = cpu_sample(w, qh.numpy().view(np.uint16), kh.numpy().view(np.uint16), vh.numpy().view(np.uint16), alpha,
-                       nthreads=os.cpu_count())
-        cpu = {"value": r["layer_ms"], "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": r["sample"]}
-        if n <= 8192:  # small layers: also the whole layer through the oracle on one core, no sampling
-            cpu["full_layer_1core_ms"] = cpu_full_layer(w, qh.numpy().view(np.uint16), kh.numpy().view(np.uint16),
-                                                        vh.numpy().view(np.uint16), alpha)
+    # The other workload the metric is quoted on, same process, same timing.
+    also = None
+    if args.also and args.also != args.config and not args.seq_len:
+        w2 = workload(synth, args.also)
+        l2 = Layer(crisp, torch, w2, params, dev, stream)
+        ms2, stages2, clk2, l2note2 = time_steps(torch, l2, args, world, local, dev)
+        roof2 = attention_roofline(l2, stages2, peaks)
+        dense2 = None if args.no_dense else dense_run(torch, crisp, l2, stages2["attention"], ms2)
+        cpu2 = cpu_baseline(l2, alpha) if rank == 0 and world == 1 and not args.no_cpu else None
+        also = {"config": workload_config(w2, args, world), "l2_note": l2note2, "ms_per_layer": ms2,
+                "stages_ms": {k: round(v, 4) for k, v in stages2.items()}, "routes": roof2["routes"],
+                "density": roof2["density"], "eff_tflops": roof2["tflops"],
+                "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": roof2["tflops"],
+                             "peak": burst_peak, "unit": "TFLOP/s", "frac": roof2["frac_burst"],
+                             "frac_sustained": roof2["frac_sustained"],
+                             "peak_kind": f"bf16 dense, {peak_kind} burst"},
+                "dense": dense2, "clocks": clk2, "cpu_baseline": cpu2,
+                "gpu_launches": LAUNCHES_PER_STEP * args.steps}
+        del l2
+        torch.cuda.empty_cache()
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": ms_per_step / world, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, planted sink/slash/needle structure)",
-            "config": {**workload_config(w, args, world), "l2": l2_note},
+            "config": workload_config(w, args, world),
+            "l2_note": l2_note,
             "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-            "routes": {"vs": int(routes.sum()), "pe": int((routes == 0).sum())},
-            "density": pairs / dense_pairs,
-            "eff_tflops": achieved_tf,
-            "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": achieved_tf, "peak": tf_peak,
-                         "unit": "TFLOP/s", "frac": achieved_tf / tf_peak,
-                         "traffic": traffic if w.name == "llama8b-512k" else None,
-                         "traffic_source": "profiles/attention_llama8b_512k_traffic.md",
-                         "peak_kind": f"bf16 dense, {peak_kind} (sustained)"},
-            "unfused_map_path": {
-                "proxy_ms": unf_proxy_ms, "masses_ms": unf_masses_ms,
-                "proxy_gbs": proxy_bytes / (unf_proxy_ms * 1e-3) / 1e9,
-                "masses_gbs": masses_bytes / (unf_masses_ms * 1e-3) / 1e9, "peak_gbs": hbm_peak,
-                "route_select_frac": (masses_bytes / ((unf_masses_ms + stage_ms["route"] + stage_ms["select_vs"])
-                                                     * 1e-3) / 1e9) / hbm_peak,
-                "fused_saving_ms": unf_proxy_ms + unf_masses_ms - stage_ms["proxy_masses"]},
+            "routes": roof["routes"],
+            "density": roof["density"],
+            "eff_tflops": roof["tflops"],
+            "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": roof["tflops"],
+                         "peak": burst_peak, "unit": "TFLOP/s", "frac": roof["frac_burst"], "traffic": traffic,
+                         "traffic_source": TRAFFIC_PROFILE, "traffic_how": traffic_how,
+                         "peak_kind": f"bf16 dense, {peak_kind} burst (the kernel is timed alone by its own "
+                                      f"events inside a ~{ms_per_step:.0f} ms step)",
+                         "peak_sustained": sustained_peak, "frac_sustained": roof["frac_sustained"],
+                         "algorithmic_flops": roof["flops"], "selected_blocks": roof["blocks"]},
+            "map_path": mp,
             "dense": dense,
             "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps,
+            "also": also,
+            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
             "gen_seconds": gen_s,
@@ -633,7 +808,12 @@ def run_sweep(args):
                     ("FlexPrefill rules gamma 0.95 (JSD routing, coverage on VS heads)",
                      crisp.params_default(route_mode=crisp.ROUTE_JSD, vs_mode=crisp.VS_GAMMA, vs_gamma=(95, 100))),
                     ("FlexPrefill rules gamma 0.97",
-                     crisp.params_default(route_mode=crisp.ROUTE_JSD, vs_mode=crisp.VS_GAMMA, vs_gamma=(97, 100)))]
+                     crisp.params_default(route_mode=crisp.ROUTE_JSD, vs_mode=crisp.VS_GAMMA, vs_gamma=(97, 100))),
+                    # the pages' two ablations: each of CRISP's two changes alone
+                    ("routing only (C_struct routing, coverage 0.95 on VS heads)",
+                     crisp.params_default(vs_mode=crisp.VS_GAMMA, vs_gamma=(95, 100))),
+                    ("sink-aware selection only (JSD routing, noise floor on VS heads)",
+                     crisp.params_default(route_mode=crisp.ROUTE_JSD))]
         for cfg in ("llama8b-512k", "llama8b-32k"):
             w = synth.WORKLOADS[cfg]
             for i, (label, p) in enumerate(variants):
@@ -643,7 +823,8 @@ def run_sweep(args):
             d = rows[-len(variants)]["dense_ms"]
             for r in rows[-len(variants):]:
                 r["speedup_vs_dense"] = d / r["layer_ms"]
-        workload = "llama8b-512k (all heads sink-type) and llama8b-32k (half diffuse); same kernels, rules differ"
+        workload = ("llama8b-512k (all heads sink-type) and llama8b-32k (half diffuse); same kernels, rules differ; "
+                    "the last two rows are the pages' ablations")
     else:
         w = synth.WORKLOADS["llama8b-32k"]
         for mode in (crisp.PE_GAMMA, crisp.PE_NOISE):

@@ -81,7 +81,7 @@ def run_steps(q, k, v, params, q_dev=None, k_dev=None, v_dev=None, pbar_rows_pe_
     crisp.build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, ws)
     crisp.sparse_prefill_mask(s, qd, kd, vd, rowbits, order, out, ws)
     # A8 from the index sets: the mask is built in the workspace
-    out_sets = empty((hq, n, 128), torch.bfloat16)
+    out_sets = torch.empty_strided(tuple(out.shape), out.stride(), dtype=torch.bfloat16, device="cuda")
     crisp.sparse_prefill(s, qd, kd, vd, route, vbits, sbits, pebits, out_sets, ws)
     torch.cuda.synchronize()
     assert_status_ok(ws)

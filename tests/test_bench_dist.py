@@ -70,20 +70,39 @@ def test_selected_pairs_counts_the_causal_half_of_the_diagonal():
 
 def test_profiled_traffic_is_dropped_once_a_source_changes(tmp_path, monkeypatch):
     # The DRAM-traffic figure of a committed ncu summary is reported only
-    # while the sources that decide it hash to the recorded value.
+    # while the sources that decide it hash to the recorded value; a run of
+    # the same recipe at another length gets the per-block figure scaled by
+    # its own selected blocks; another recipe gets none.
     import hashlib
+    from types import SimpleNamespace as NS
     (tmp_path / "a.cu").write_bytes(b"kernel")
     (tmp_path / "b.cu").write_bytes(b"order")
     sha = hashlib.sha256(b"kernel" + b"order").hexdigest()
-    (tmp_path / "p.md").write_text(f"# summary\n\ntraffic_bytes_per_launch: 1234\nsource_sha256: {sha}\n")
+    (tmp_path / "p.md").write_text(f"# summary\n\nworkload: llama8b-512k@65536\ntraffic_bytes_per_launch: 1234\n"
+                                   f"selected_blocks: 100\ntraffic_bytes_per_selected_block: 12.34\n"
+                                   f"source_sha256: {sha}\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.profiled_traffic(("a.cu", "b.cu"), "p.md") == 1234
+    same = NS(name="llama8b-512k@65536")
+    full = NS(name="llama8b-512k")
+    other = NS(name="qwen7b-128k")
+    assert bench.profiled_traffic(("a.cu", "b.cu"), "p.md", same, 100)[0] == 1234
+    assert bench.profiled_traffic(("a.cu", "b.cu"), "p.md", full, 1000)[0] == 12340
+    assert bench.profiled_traffic(("a.cu", "b.cu"), "p.md", other, 1000)[0] is None
     (tmp_path / "b.cu").write_bytes(b"order changed")
-    assert bench.profiled_traffic(("a.cu", "b.cu"), "p.md") is None
-    assert bench.profiled_traffic(("a.cu", "missing.cu"), "p.md") is None
+    assert bench.profiled_traffic(("a.cu", "b.cu"), "p.md", same, 100)[0] is None
+    assert bench.profiled_traffic(("a.cu", "missing.cu"), "p.md", same, 100)[0] is None
 
 
 def test_committed_traffic_summary_names_the_guarded_sources():
-    text = open(os.path.join(bench.ROOT, "profiles", "attention_llama8b_512k_traffic.md")).read()
-    assert "source_sha256:" in text and "traffic_bytes_per_launch:" in text
+    text = open(os.path.join(bench.ROOT, bench.TRAFFIC_PROFILE)).read()
+    for key in ("source_sha256:", "traffic_bytes_per_launch:", "workload:"):
+        assert key in text, key
     assert all(os.path.exists(os.path.join(bench.ROOT, f)) for f in bench.TRAFFIC_SOURCES)
+
+
+def test_bench_arms_report_identical_configs():
+    # Both arms put the same keys and values in `config` for a workload.
+    from types import SimpleNamespace as NS
+    args = bench.parse_args([])
+    w = NS(name="llama8b-512k", hq=32, hkv=8, n=524288)
+    assert bench.workload_config(w, args, 1) == bench.workload_config(w, bench.parse_args(["--impl", "reference"]), 1)
