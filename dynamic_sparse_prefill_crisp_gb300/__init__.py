@@ -74,50 +74,56 @@ def lib():
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with dynamic_sparse_prefill_crisp_gb300.build.build()")
-        L = ctypes.CDLL(LIB_PATH)
-        vp, sz, st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
-        P = ctypes.POINTER
-        L.crisp_params_default.argtypes = [P(Params)]
-        L.crisp_params_default.restype = None
-        L.crisp_workspace_size.argtypes = [P(Shape), P(sz)]
-        L.crisp_layer_workspace_size.argtypes = [P(Shape), P(sz)]
-        L.crisp_workspace_init.argtypes = [vp, sz, st]
-        L.crisp_proxy_map.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
-        L.crisp_proxy_map_noalloc.argtypes = [P(Shape), vp, vp, vp, st]
-        L.crisp_noalloc_read_status.argtypes = [st, P(ctypes.c_int)]
-        L.crisp_block_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
-        L.crisp_proxy_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, st]
-        L.crisp_host_pipeline_create.argtypes = [P(vp)]
-        L.crisp_host_pipeline_destroy.argtypes = [vp]
-        L.crisp_prefill_layer_host.argtypes = [vp, P(Shape), P(Params)] + [vp] * 9 + [sz, st]
-        L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, sz, st]
-        L.crisp_route_cstruct_masses.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
-        L.crisp_route_jsd.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, sz, st]
-        L.crisp_wait_selftest.argtypes = [vp, sz, ctypes.c_int64, st]
-        L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, vp, sz, st]
-        L.crisp_select_vs_masses.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
-        L.crisp_pe_pool.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
-        L.crisp_select_pe.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, sz, st]
-        L.crisp_build_mask.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, vp, sz, st]
-        L.crisp_sparse_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, st]
-        L.crisp_sparse_prefill_mask.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, st]
-        L.crisp_dense_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
-        L.crisp_layer_views_get.argtypes = [P(Shape), vp, P(LayerViews)]
-        L.crisp_prefill_layer.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, sz, st]
-        L.crisp_read_status.argtypes = [vp, st, P(ctypes.c_int)]
-        L.crisp_status_string.argtypes = [ctypes.c_int]
-        L.crisp_status_string.restype = ctypes.c_char_p
-        for name in ("crisp_workspace_size", "crisp_layer_workspace_size", "crisp_workspace_init", "crisp_proxy_map",
-                     "crisp_proxy_map_noalloc", "crisp_noalloc_read_status", "crisp_block_masses",
-                     "crisp_proxy_masses", "crisp_route_cstruct", "crisp_route_cstruct_masses", "crisp_route_jsd",
-                     "crisp_select_vs", "crisp_select_vs_masses", "crisp_pe_pool", "crisp_select_pe",
-                     "crisp_build_mask", "crisp_sparse_prefill", "crisp_sparse_prefill_mask", "crisp_dense_prefill",
-                     "crisp_layer_views_get", "crisp_prefill_layer", "crisp_read_status",
-                     "crisp_host_pipeline_create", "crisp_host_pipeline_destroy", "crisp_prefill_layer_host",
-                     "crisp_wait_selftest"):
-            getattr(L, name).restype = ctypes.c_int
-        _lib = L
+        _lib = load_library(LIB_PATH)
     return _lib
+
+
+def load_library(path):
+    """Loads a build of the library (e.g. the bounds-checking one) with the
+    argument types declared; the module's calls keep using lib()."""
+    L = ctypes.CDLL(path)
+    vp, sz, st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
+    P = ctypes.POINTER
+    L.crisp_params_default.argtypes = [P(Params)]
+    L.crisp_params_default.restype = None
+    L.crisp_workspace_size.argtypes = [P(Shape), P(sz)]
+    L.crisp_layer_workspace_size.argtypes = [P(Shape), P(sz)]
+    L.crisp_workspace_init.argtypes = [vp, sz, st]
+    L.crisp_proxy_map.argtypes = [P(Shape), vp, vp, vp, vp, sz, st]
+    L.crisp_proxy_map_noalloc.argtypes = [P(Shape), vp, vp, vp, st]
+    L.crisp_noalloc_read_status.argtypes = [st, P(ctypes.c_int)]
+    L.crisp_block_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
+    L.crisp_proxy_masses.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, sz, st]
+    L.crisp_host_pipeline_create.argtypes = [P(vp)]
+    L.crisp_host_pipeline_destroy.argtypes = [vp]
+    L.crisp_prefill_layer_host.argtypes = [vp, P(Shape), P(Params)] + [vp] * 9 + [sz, st]
+    L.crisp_route_cstruct.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, sz, st]
+    L.crisp_route_cstruct_masses.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
+    L.crisp_route_jsd.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, sz, st]
+    L.crisp_wait_selftest.argtypes = [vp, sz, ctypes.c_int64, st]
+    L.crisp_select_vs.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, vp, sz, st]
+    L.crisp_select_vs_masses.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, vp, sz, st]
+    L.crisp_pe_pool.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
+    L.crisp_select_pe.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, sz, st]
+    L.crisp_build_mask.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, vp, sz, st]
+    L.crisp_sparse_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, st]
+    L.crisp_sparse_prefill_mask.argtypes = [P(Shape), vp, vp, vp, vp, vp, vp, vp, sz, st]
+    L.crisp_dense_prefill.argtypes = [P(Shape), vp, vp, vp, vp, vp, sz, st]
+    L.crisp_layer_views_get.argtypes = [P(Shape), vp, P(LayerViews)]
+    L.crisp_prefill_layer.argtypes = [P(Shape), P(Params), vp, vp, vp, vp, vp, sz, st]
+    L.crisp_read_status.argtypes = [vp, st, P(ctypes.c_int)]
+    L.crisp_status_string.argtypes = [ctypes.c_int]
+    L.crisp_status_string.restype = ctypes.c_char_p
+    for name in ("crisp_workspace_size", "crisp_layer_workspace_size", "crisp_workspace_init", "crisp_proxy_map",
+                 "crisp_proxy_map_noalloc", "crisp_noalloc_read_status", "crisp_block_masses",
+                 "crisp_proxy_masses", "crisp_route_cstruct", "crisp_route_cstruct_masses", "crisp_route_jsd",
+                 "crisp_select_vs", "crisp_select_vs_masses", "crisp_pe_pool", "crisp_select_pe",
+                 "crisp_build_mask", "crisp_sparse_prefill", "crisp_sparse_prefill_mask", "crisp_dense_prefill",
+                 "crisp_layer_views_get", "crisp_prefill_layer", "crisp_read_status",
+                 "crisp_host_pipeline_create", "crisp_host_pipeline_destroy", "crisp_prefill_layer_host",
+                 "crisp_wait_selftest"):
+        getattr(L, name).restype = ctypes.c_int
+    return L
 
 
 def status_string(status: int) -> str:

@@ -12,10 +12,14 @@
 // K and V tiles arrive by TMA at row coordinate kb*128 (gather by block index);
 // rows past n in a short last block are filled with zeros, the causal mask
 // hides those keys and their query rows are not stored.
-// The reference max m is raised lazily: each block is first exponentiated at
-// the current m; only if some row's block sum exceeds 2^8 (so possibly one p
-// > 2^8) do the warps take the exact row max, move m, rescale O and the row
-// sum, and recompute the block. Every p stays <= 2^8 and O/l is exact.
+// The reference max m is the first block's exact row max and is raised
+// lazily after that: each later block is exponentiated at the current m and
+// stored chunk by chunk, with no agreement between the two warps of a row;
+// only a warp that finds some chunk's row sum past 2^8 (so possibly one
+// p > 2^8) holds back, waits for its partner's P, moves m to the max of its
+// unstored scores, rescales the row's stored P, O and its row sum, and
+// recomputes the rest; the partner follows the new m at its next block.
+// Every p stays <= 2^8 and O/l is exact.
 //
 // Warp roles: 0-7 softmax + epilogue (warp w owns TMEM lanes / rows
 // 32*(w%4)..+31 and columns 64*(w/4)..+63), 8 TMA producer, 9 MMA issuer (and
@@ -37,16 +41,18 @@ constexpr uint32_t kTile = kB * kD * 2;  // 32 KB bf16 tile
 constexpr uint32_t kHalf = kTile / 2;
 constexpr uint32_t kSmemBytes = 1024 + 3 * kTile;  // Q, K, V (+ alignment slack)
 constexpr uint32_t kTmemCols = 256;                // S/P [0,128), O [128,256)
-constexpr float kRescaleSum = 256.0f;  // 2^8: the largest block row sum kept at the current reference
+constexpr float kRescaleSum = 256.0f;  // 2^8: the largest chunk row sum kept at the current reference
 
 struct Bars {
-  uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, o_full, drain;
+  uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, drain;
+  uint64_t qdone[4];     // per lane quarter: both warps have stored their P of the block
   uint32_t tmem_base;
   int count;
   int has_diag;
   int abort;
-  float xmax[2][2][kB];  // [block parity][column half][row]: partial row maxima
-  int flag[2][4][2];     // [block parity][lane quarter][column half]: needs the exact max
+  uint32_t qov[4][2];    // [lane quarter][column half]: j + 1 when that warp's block j needed a new reference
+  float mrow[kB];        // the reference m of each row, as last moved
+  float xmax[2][2][kB];  // [first block / both halves redone][column half][row]: partial row maxima
   float xsum[2][kB];     // [column half][row]: partial row sums (epilogue)
 };
 
@@ -88,6 +94,106 @@ __device__ __forceinline__ void load_s32(uint32_t taddr, bool diag, int col0, in
     for (int e = 0; e < 32; ++e)
       if (col0 + e > r) sv[e] = 0xff800000u;  // -inf
   }
+}
+
+// Keys above the row on the diagonal block (column index col0 + e > r) -> -inf.
+__device__ __forceinline__ void mask_diag32(int col0, int r, uint32_t (&sv)[32]) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (col0 + e > r) sv[e] = 0xff800000u;
+}
+
+// Largest of 32 raw scores.
+__device__ __forceinline__ float max32(const uint32_t (&sv)[32]) {
+  float ma = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+  float mb = fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
+#pragma unroll
+  for (int e = 6; e + 3 < 32; e += 4) {
+    ma = fmax3(ma, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+    mb = fmax3(mb, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+  }
+  return fmax3(fmax3(ma, mb, __uint_as_float(sv[30])), __uint_as_float(sv[31]), -INFINITY);
+}
+
+// 16 columns of bf16 pairs scaled by f (and repacked).
+__device__ __forceinline__ void scale_bf16x32(uint32_t (&pk)[16], float f) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    pk[e] = pack_bf16x2(__uint_as_float(pk[e] << 16) * f, __uint_as_float(pk[e] & 0xffff0000u) * f);
+}
+
+// The reference and sum of one softmax row (a thread's partial sum).
+struct RowState {
+  float m, l;
+};
+
+// A new reference for the rows of lane quarter `quarter` (rare; out of line so
+// that the common loop keeps its registers). Called by a warp in whose block
+// some p would pass 2^8 (a chunk row sum past 2^8), or whose rows' reference
+// the other warp moved in the last block, once the other warp of the rows has
+// stored its P (qdone). The warp's scores are in TMEM: chunk 0 at columns
+// 0..31, chunk 1 (put back) at 32..63. The rows' new reference is the max of
+// the old one and these scores -- of both warps when both are here (then they
+// exchange it through xmax and each fixes its own columns); otherwise this
+// warp also rescales the other warp's P and O columns (TMEM lanes belong to
+// the quarter, so it can) and the other warp follows the new reference (mrow)
+// at its next block. The other warp's stored P holds p <= 2^8 at the old
+// reference and is rescaled in place by f = 2^(m_old - m_new); this warp's P
+// is formed again from its scores (chunk 1 first: its P goes over chunk 1's
+// own scores, chunk 0's over chunk 1's first half). Every p stays below 2^8
+// and O/l is exact. Returns the new reference and the row sum with this
+// block's part.
+__device__ __noinline__ RowState new_reference(RowState st, uint32_t tmem, uint32_t lane_addr, int half, int r,
+                                               bool diag, bool both, float c_log2, float* xmine, const float* xother,
+                                               int pair_bar, float* mrow) {
+  const uint32_t s_addr = tmem + lane_addr + half * 64, p_addr = s_addr + 32;
+  const int col0 = half * 64;
+  uint32_t sv[32], pk[16];
+  float mc = -INFINITY;
+#pragma unroll 1
+  for (int cc = 0; cc < 2; ++cc) {
+    load_s32(s_addr + cc * 32, diag, col0 + cc * 32, r, sv);
+    mc = fmaxf(mc, max32(sv));
+  }
+  if (both) {
+    *xmine = mc;
+    named_bar_sync(pair_bar, 64);
+    mc = fmaxf(mc, *xother);
+  }
+  const float m_new = fmaxf(st.m, mc * c_log2);
+  const float f = ex2_approx(st.m - m_new);
+  float t = 0.f;
+#pragma unroll 1
+  for (int cc = 1; cc >= 0; --cc) {
+    load_s32(s_addr + cc * 32, diag, col0 + cc * 32, r, sv);
+    p_exp32(sv, c_log2, -m_new, pk, t);
+    tmem_st16(p_addr + cc * 16, pk);
+  }
+  // O columns to rescale: this warp's half, and the other half too when the
+  // other warp is not here (then also its stored P).
+  if (!both) {
+    const uint32_t other = tmem + lane_addr + (half ^ 1) * 64 + 32;
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      tmem_ld16(other + cc * 16, pk);
+      scale_bf16x32(pk, f);
+      tmem_st16(other + cc * 16, pk);
+    }
+  }
+#pragma unroll 1
+  for (int oh = 0; oh < (both ? 1 : 2); ++oh) {
+    const uint32_t oa = tmem + lane_addr + 128 + (oh == 0 ? half : half ^ 1) * 64;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      tmem_ld16(oa + cc * 16, pk);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) pk[e] = __float_as_uint(__uint_as_float(pk[e]) * f);
+      tmem_st16(oa + cc * 16, pk);
+    }
+  }
+  *mrow = m_new;
+  tmem_st_wait();
+  return RowState{m_new, st.l * f + t};
 }
 
 // Bits of row word w restricted to key blocks <= qb.
@@ -136,7 +242,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.p_full, kSoftmaxWarps);
     mbar_init(&bars.pv_done, 1);
-    mbar_init(&bars.o_full, 1);
+    for (int qq = 0; qq < 4; ++qq) {
+      mbar_init(&bars.qdone[qq], 2);
+      bars.qov[qq][0] = bars.qov[qq][1] = 0;
+    }
     mbar_init(&bars.drain, 1);
     fence_mbar_init();
   }
@@ -228,7 +337,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         umma_commit(&bars.k_empty);
         umma_commit(&bars.s_full);
-        if (!mbar_wait(&bars.p_full, par, &bars.abort) || !mbar_wait(&bars.v_full, par, &bars.abort)) {
+        const bool got = mbar_wait(&bars.p_full, par, &bars.abort);
+        if (!got || !mbar_wait(&bars.v_full, par, &bars.abort)) {
           fail(&bars.abort, status, 0x205);
           break;
         }
@@ -236,16 +346,19 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           // A = P rows in TMEM (bf16 pairs, 8 columns per 16 keys; keys
-          // 0..63 at columns 0..31, keys 64..127 at columns 64..95);
+          // 0..63 at columns 32..63, keys 64..127 at columns 96..127);
           // B = V, 16 keys x 128 features, MN-major: 16 rows of 128 B per
           // step, the second 64-feature half kHalf bytes further.
-          umma_ts(tmem + 128, tmem + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), idesc_pv,
+          umma_ts(tmem + 128, tmem + (kk >> 2) * 64 + 32 + (kk & 3) * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024),
+                  idesc_pv,
                   (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bars.v_empty);
         umma_commit(&bars.pv_done);
       }
-      umma_commit(&bars.o_full);
+      // The last phase of s_full: O is final. After a failure the softmax
+      // warps leave on the abort flag instead.
+      if (!*reinterpret_cast<volatile int*>(&bars.abort)) umma_commit(&bars.s_full);
       umma_commit(&bars.drain);
       if (!mbar_wait(&bars.drain, 0, &bars.abort)) fail(&bars.abort, status, 0x206);
     }
@@ -259,104 +372,118 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int pair_bar = 1 + quarter;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + half * 64;        // 64 S columns
-    const uint32_t p_addr = s_addr;                              // 32 P columns (bf16 pairs) over the first of them
+    const uint32_t p_addr = s_addr + 32;                         // 32 P columns (bf16 pairs) over the last of them
     const uint32_t o_addr = tmem + lane_addr + 128 + half * 64;  // 64 O columns
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < count; ++j) {
+    // One phase of s_full per block (its scores), then one when O is final.
+    for (int j = 0; count > 0 && j <= count; ++j) {
       if (!warp_wait(&bars.s_full, static_cast<uint32_t>(j) & 1u, &bars.abort)) {
         if (lane == 0) fail(&bars.abort, status, 0x207);
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool diag = bars.has_diag && j == count - 1;  // ascending order: qb is last
-      // Optimistic pass: P at the current reference m (every block after the
-      // first). The reference must move only when some p would exceed 2^8;
-      // a row's block sum above 2^8 (or not finite) covers every such case,
-      // so that sum is the test and no row max is needed on this path. The
-      // two warps of a quarter hold the two column halves of the same rows,
-      // so they agree through shared memory before either stores P. Each
-      // warp stores P only over its own S columns, so neither store can
-      // overwrite scores the other warp has still to read.
-      uint32_t pk[32];
-      float bsum = 0.f;
-      bool need = (j == 0);
-      if (!need) {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t sv[32];
-          load_s32(s_addr + cc * 32, diag, half * 64 + cc * 32, r, sv);
-          p_exp32(sv, c_log2, -m_ref, pk + cc * 16, bsum);
-        }
-        need = __any_sync(0xffffffffu, !(bsum <= kRescaleSum));
+      if (j == count) {
+        // O is final; the row sum follows the last reference of the row.
+        const float mr = bars.mrow[r];
+        if (mr > m_ref) l *= ex2_approx(m_ref - mr);
+        break;
       }
-      if (lane == 0) bars.flag[j & 1][quarter][half] = need ? 1 : 0;
-      tc_fence_before();
-      named_bar_sync(pair_bar, 64);
-      tc_fence_after();
-      need = need || bars.flag[j & 1][quarter][half ^ 1] != 0;  // warp-uniform; alike in both warps
-      bool rescale = false;
-      float f = 1.f;
-      if (need) {
-        // Exact path: both warps reload S (nothing has been stored over it),
-        // exchange partial row maxima and move each row's reference to its
-        // max (first block: set it), then recompute P. Row max on the raw
-        // scores (c > 0, so max(s*c) = max(s)*c).
+      const bool diag = bars.has_diag && j == count - 1;  // ascending order: qb is last
+      const int col0 = half * 64;
+      if (j == 0) {
+        // First block: the exact row max over both column halves (partial
+        // maxima exchanged through shared memory) is the reference m.
         float pm = -INFINITY;
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t sv[32];
-          load_s32(s_addr + cc * 32, diag, half * 64 + cc * 32, r, sv);
-          float ma = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
-          float mb = fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
-#pragma unroll
-          for (int e = 6; e + 3 < 32; e += 4) {
-            ma = fmax3(ma, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-            mb = fmax3(mb, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
-          }
-          pm = fmax3(pm, fmax3(ma, mb, __uint_as_float(sv[30])), __uint_as_float(sv[31]));
+          load_s32(s_addr + cc * 32, diag, col0 + cc * 32, r, sv);
+          pm = fmaxf(pm, max32(sv));
         }
-        bars.xmax[j & 1][half][r] = pm;
+        bars.xmax[0][half][r] = pm;
         named_bar_sync(pair_bar, 64);
-        const float mx = fmaxf(pm, bars.xmax[j & 1][half ^ 1][r]) * c_log2;
-        if (j == 0) {
-          m_ref = mx;
-        } else {
-          const float m_new = fmaxf(m_ref, mx);  // unchanged rows keep f = 1
-          f = ex2_approx(m_ref - m_new);
-          l *= f;
-          m_ref = m_new;
-          rescale = true;
-        }
-        bsum = 0.f;
+        m_ref = fmaxf(pm, bars.xmax[0][half ^ 1][r]) * c_log2;  // c > 0: max(s*c) = max(s)*c
+        if (half == 0) bars.mrow[r] = m_ref;
+        uint32_t pk[32];
+        float bsum = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t sv[32];
-          load_s32(s_addr + cc * 32, diag, half * 64 + cc * 32, r, sv);
+          load_s32(s_addr + cc * 32, diag, col0 + cc * 32, r, sv);
           p_exp32(sv, c_log2, -m_ref, pk + cc * 16, bsum);
         }
+        tmem_st32(p_addr, pk);
+        l = bsum;
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_full);
+        continue;
       }
-      tmem_st32(p_addr, pk);
-      l += bsum;
-      if (rescale) {
-        // O must carry the new reference before PV_j adds to it; PV_{j-1} is
-        // complete (QK_j was issued after it), so O is stable here.
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t v[32];
-          tmem_ld32(o_addr + cc * 32, v);
-          uint32_t a[16], b[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            a[e] = __float_as_uint(__uint_as_float(v[e]) * f);
-            b[e] = __float_as_uint(__uint_as_float(v[16 + e]) * f);
-          }
-          tmem_st16(o_addr + cc * 32, a);
-          tmem_st16(o_addr + cc * 32 + 16, b);
-        }
+      // Later blocks: P at the current reference, each 32-key chunk stored
+      // as soon as it is formed, without waiting for the other warp of the
+      // row and without a test first. P goes over chunk 1's scores (columns
+      // 32..63): chunk 0's P once chunk 1's scores are in registers, chunk
+      // 1's right after. A block in which some chunk row sum passes 2^8 (any
+      // p that could pass 2^8, or a non-finite value), or whose reference
+      // the other warp moved in the last block, takes the slow path below
+      // with chunk 0's scores still in TMEM and chunk 1's put back from
+      // registers.
+      uint32_t sv[32], pk[16], pk1[16];
+      float s0 = 0.f, s1 = 0.f;
+      // The other warp may have moved the rows' reference (and rescaled this
+      // warp's P and O) in the last block; the read overlaps the loads and
+      // the exponentials.
+      tmem_ld32_async(s_addr, sv);
+      const float mr = bars.mrow[r];
+      tmem_ld_wait32(sv);
+      if (diag) mask_diag32(col0, r, sv);
+      p_exp32(sv, c_log2, -m_ref, pk, s0);
+      tmem_ld32_async(s_addr + 32, sv);
+      tmem_ld_wait32(sv);
+      tmem_st16(p_addr, pk);
+      if (diag) mask_diag32(col0 + 32, r, sv);
+      p_exp32(sv, c_log2, -m_ref, pk1, s1);
+      tmem_st16(p_addr + 16, pk1);
+      const bool moved = mr > m_ref;
+      const bool ov = __any_sync(0xffffffffu, !(s0 <= kRescaleSum) || !(s1 <= kRescaleSum) || moved);
+      if (ov) {
+        if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&bars.qov[quarter][half]) = j + 1;
+        tmem_st32(s_addr + 32, sv);  // chunk 1's scores back (masked keys stay masked: -inf)
       }
       tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (!ov) {
+        l += s0 + s1;
+        if (lane == 0) {
+          mbar_arrive(&bars.p_full);
+          mbar_arrive(&bars.qdone[quarter]);
+        }
+        continue;
+      }
+      // A new reference (rare): this warp holds back its arrival on p_full,
+      // so PV waits, until its rows are consistent again. First catch up
+      // with a reference the other warp moved in the last block.
+      if (moved) {
+        l *= ex2_approx(m_ref - mr);
+        m_ref = mr;
+      }
+      if (lane == 0) mbar_arrive(&bars.qdone[quarter]);
+      if (!warp_wait(&bars.qdone[quarter], static_cast<uint32_t>(j - 1) & 1u, &bars.abort)) {
+        if (lane == 0) fail(&bars.abort, status, 0x209);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool both =
+          *reinterpret_cast<volatile uint32_t*>(&bars.qov[quarter][half ^ 1]) == static_cast<uint32_t>(j + 1);
+      const RowState st = new_reference(RowState{m_ref, l}, tmem, lane_addr, half, r, diag, both, c_log2,
+                                        &bars.xmax[1][half][r], &bars.xmax[1][half ^ 1][r], pair_bar, &bars.mrow[r]);
+      m_ref = st.m;
+      l = st.l;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.p_full);
@@ -364,12 +491,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // Epilogue: O / l -> bf16 for this warp's 64 columns, staged per warp
     // through shared memory (the K tile is no longer needed) so that each
     // store instruction writes four 128-byte row segments.
-    bool have = ok && count > 0;
-    if (have && !warp_wait(&bars.o_full, 0, &bars.abort)) {
-      if (lane == 0) fail(&bars.abort, status, 0x208);
-      have = false;
-    }
-    tc_fence_after();
+    const bool have = ok && count > 0;  // the loop ended on O's final phase
     bars.xsum[half][r] = l;
     named_bar_sync(pair_bar, 64);
     const float l_row = l + bars.xsum[half ^ 1][r];

@@ -266,6 +266,44 @@ def test_extreme_softmax_scales(scale):
     check_attention(q, k, v, r["out"], rb, scale=scale)
 
 
+@pytest.mark.parametrize("window", [(100, 110), (5, 15), (60, 70)], ids=["half1-chunk1", "half0-chunk0", "both-halves"])
+def test_attention_reference_rises_block_after_block(window):
+    # The largest scores of each key block grow with the block and sit in one
+    # window of columns, so the row's reference max must move up again and
+    # again (the redo path of the softmax): chunks without the window keep
+    # their stored P (rescaled), the window's chunk is formed again. Dense
+    # and full-mask sparse launches against fp64 attention.
+    hq, hkv, n = 2, 1, 1024
+    rng = np.random.default_rng(7)
+    u = np.zeros(128)
+    u[0] = 1.0
+    q = 8.0 * u + 0.05 * rng.standard_normal((hq, n, 128))
+    t = np.arange(n) % B
+    kb = np.arange(n) // B
+    amp = 3.0 * kb + np.where((t >= window[0]) & (t < window[1]), 6.0, 0.0)
+    k = amp[None, :, None] * u + 0.05 * rng.standard_normal((hkv, n, 128))
+    v = rng.standard_normal((hkv, n, 128))
+    to_bits = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).view(torch.int16) \
+        .numpy().view(np.uint16)
+    q, k, v = to_bits(q), to_bits(k), to_bits(v)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    nb = n // B
+    full = np.zeros((hq, nb, 1), np.uint32)
+    for qb in range(nb):
+        full[:, qb, 0] = (1 << (qb + 1)) - 1
+    for dense in (True, False):
+        out = empty((hq, n, 128), torch.bfloat16)
+        s = crisp.make_shape(hq, hkv, n, qd, kd, out)
+        ws = new_workspace(s)
+        if dense:
+            crisp.dense_prefill(s, qd, kd, vd, out, ws)
+        else:
+            crisp.sparse_prefill_mask(s, qd, kd, vd, torch.from_numpy(full.view(np.int32)).cuda(), None, out, ws)
+        torch.cuda.synchronize()
+        assert_status_ok(ws)
+        check_attention(q, k, v, out, full)
+
+
 def test_prefill_layer_matches_steps():
     for hq, hkv, n, seed in ((8, 2, 2048, 51), (4, 1, 640, 52), (4, 2, 1337, 53)):
         w = synth.small("layer", hq, hkv, n, seed)
