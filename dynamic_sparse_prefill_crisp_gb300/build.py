@@ -2,6 +2,10 @@
 
 Each translation unit is compiled in parallel by nvcc, then linked into a
 shared library next to this file. Objects go to ``_build/`` (git-ignored).
+``build(debug=True)`` builds the bounds-checking library libcrisp_debug.so
+(-DCRISP_DEBUG, objects in ``_build_debug/``): every global index and TMA
+coordinate is checked against its buffer, and a failed check records
+CRISP_ERR_BOUNDS in the status word and skips the access.
 """
 from __future__ import annotations
 
@@ -15,6 +19,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcrisp.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libcrisp_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]
@@ -38,14 +44,17 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    if debug:
+        extra_flags = (*extra_flags, "-DCRISP_DEBUG")
+    os.makedirs(build_dir, exist_ok=True)
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(HERE, "..", "include", "*.h"))
     nvcc = _nvcc()
     jobs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(build_dir, os.path.basename(src).replace(".cu", ".o"))
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
             cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
@@ -63,14 +72,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 sys.stderr.write(p.stdout + p.stderr)
             if p.returncode != 0:
                 raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".{os.getpid()}.tmp"
         subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lrt",
                                "-lpthread"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -117,6 +117,9 @@ crisp_status make_map(CUtensorMap* m, const void* ptr, int heads, int n, int64_t
 
 crisp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CRISP_OK : CRISP_ERR_CUDA; }
 
+// The status word at the start of a workspace.
+DevStatus* status_of(void* ws) { return static_cast<DevStatus*>(ws); }
+
 }  // namespace
 
 ScratchLayout scratch_layout(const crisp_shape& s) {
@@ -342,7 +345,7 @@ crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* p
   const crisp_shape s = normalised(*shape);
   if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_route_map(s, *params, pmap, cstruct, total, route, stream));
+  return from_cuda(launch_route_map(s, *params, pmap, cstruct, total, route, status_of(ws), stream));
 }
 
 crisp_status crisp_route_cstruct_masses(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
@@ -357,7 +360,7 @@ crisp_status crisp_route_cstruct_masses(const crisp_shape* shape, const crisp_pa
   const crisp_shape s = normalised(*shape);
   if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_route(s, *params, vmass, rmass, cstruct, total, route, stream));
+  return from_cuda(launch_route(s, *params, vmass, rmass, cstruct, total, route, status_of(ws), stream));
 }
 
 crisp_status crisp_route_jsd(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
@@ -371,7 +374,7 @@ crisp_status crisp_route_jsd(const crisp_shape* shape, const crisp_params* param
   const crisp_shape s = normalised(*shape);
   if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_route_jsd(s, *params, vmass, pbar, jsd, route, stream));
+  return from_cuda(launch_route_jsd(s, *params, vmass, pbar, jsd, route, status_of(ws), stream));
 }
 
 crisp_status crisp_select_vs_masses(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
@@ -385,7 +388,7 @@ crisp_status crisp_select_vs_masses(const crisp_shape* shape, const crisp_params
   const crisp_shape s = normalised(*shape);
   if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, stream));
+  return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, status_of(ws), stream));
 }
 
 crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* params, const float* pmap,
@@ -403,7 +406,7 @@ crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* param
   char* wsb = static_cast<char*>(ws);
   auto* rmass = reinterpret_cast<uint64_t*>(wsb + scratch_layout(s).rmass);
   if (launch_block_masses(s, pmap, vmass, smass, rmass, wsb, stream) != cudaSuccess) return CRISP_ERR_CUDA;
-  return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, stream));
+  return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, status_of(ws), stream));
 }
 
 crisp_status crisp_pe_pool(const crisp_shape* shape, const void* q, const void* k, const uint8_t* route, float* pbar,
@@ -429,7 +432,7 @@ crisp_status crisp_select_pe(const crisp_shape* shape, const crisp_params* param
   const crisp_shape s = normalised(*shape);
   if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
   if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_select_pe(s, *params, pbar, route, pebits, stream));
+  return from_cuda(launch_select_pe(s, *params, pbar, route, pebits, status_of(ws), stream));
 }
 
 crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t* route, const uint32_t* vbits,
@@ -554,14 +557,14 @@ crisp_status run_layer(const crisp_shape& s, const crisp_params& p, const void* 
     // (a zero route array selects all heads), then routes by divergence.
     if (cudaMemsetAsync(w.route, 0, static_cast<size_t>(s.hq), stream) != cudaSuccess ||
         launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess ||
-        launch_route_jsd(s, p, w.vmass, w.pbar, nullptr, w.route, stream) != cudaSuccess)
+        launch_route_jsd(s, p, w.vmass, w.pbar, nullptr, w.route, status_of(ws), stream) != cudaSuccess)
       return CRISP_ERR_CUDA;
-  } else if (launch_route(s, p, w.vmass, w.rmass, w.cstruct, w.total, w.route, stream) != cudaSuccess ||
+  } else if (launch_route(s, p, w.vmass, w.rmass, w.cstruct, w.total, w.route, status_of(ws), stream) != cudaSuccess ||
              launch_pe_map(s, q, k, w.route, w.pbar, wsb, stream) != cudaSuccess) {
     return CRISP_ERR_CUDA;
   }
-  if (launch_select_vs(s, p, w.vmass, w.smass, w.route, w.vbits, w.sbits, stream) != cudaSuccess ||
-      launch_select_pe(s, p, w.pbar, w.route, w.pebits, stream) != cudaSuccess ||
+  if (launch_select_vs(s, p, w.vmass, w.smass, w.route, w.vbits, w.sbits, status_of(ws), stream) != cudaSuccess ||
+      launch_select_pe(s, p, w.pbar, w.route, w.pebits, status_of(ws), stream) != cudaSuccess ||
       launch_build_mask(s, w.route, w.vbits, w.sbits, w.pebits, w.rowbits, w.counts, w.order, wsb, stream) !=
           cudaSuccess ||
       launch_attention(s, maps, w.rowbits, w.order, out, wsb, false, stream) != cudaSuccess)

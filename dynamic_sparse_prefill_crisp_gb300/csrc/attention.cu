@@ -196,9 +196,10 @@ __device__ __noinline__ RowState new_reference(RowState st, uint32_t tmem, uint3
   return RowState{m_new, st.l * f + t};
 }
 
-// Bits of row word w restricted to key blocks <= qb.
-__device__ __forceinline__ uint32_t row_word(const uint32_t* row, bool dense, int w, int qb) {
-  uint32_t bits = dense ? 0xffffffffu : row[w];
+// Bits of row word w restricted to key blocks <= qb (row: W words).
+__device__ __forceinline__ uint32_t row_word(const uint32_t* row, bool dense, int w, int qb, int W,
+                                             DevStatus* status) {
+  uint32_t bits = dense ? 0xffffffffu : (CRISP_CHECK(w < W, status, 0x211) ? row[w] : 0u);
   if (w == (qb >> 5) && (qb & 31) != 31) bits &= (1u << ((qb & 31) + 1)) - 1u;
   return bits;
 }
@@ -222,6 +223,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   int item;
   if (order != nullptr) {
     item = order[blockIdx.x];
+    // (checking build) a work item outside [0, hq*nb) is replaced by 0
+    if (!CRISP_CHECK(item >= 0 && item < static_cast<int>(gridDim.x), status, 0x210)) item = 0;
   } else {
     const int t = static_cast<int>(blockIdx.x), per_group = group * nb;
     const int rem = t % per_group;
@@ -251,12 +254,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (warp == kTmaWarp) {
     int cnt = 0;
-    for (int w = lane; w <= (qb >> 5); w += 32) cnt += __popc(row_word(row, is_dense, w, qb));
+    for (int w = lane; w <= (qb >> 5); w += 32) cnt += __popc(row_word(row, is_dense, w, qb, W, status));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
     if (lane == 0) {
       bars.count = cnt;
-      bars.has_diag = (row_word(row, is_dense, qb >> 5, qb) >> (qb & 31)) & 1u;
+      bars.has_diag = (row_word(row, is_dense, qb >> 5, qb, W, status) >> (qb & 31)) & 1u;
     }
   }
   if (warp == kMmaWarp) {
@@ -274,13 +277,21 @@ __global__ void __launch_bounds__(kThreads, 2)
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      mbar_arrive_expect_tx(&bars.q_full, kTile);
-      tma_load_3d(sQ, &tq, &bars.q_full, 0, qb * kB, h);
-      tma_load_3d(sQ + kHalf, &tq, &bars.q_full, 64, qb * kB, h);
+      // (checking build) a tile outside q, k or v is not copied; its barrier
+      // phase completes without data and the status word says why.
+      const int hq = static_cast<int>(gridDim.x) / nb;
+      if (CRISP_CHECK(qb * kB < n && h < hq, status, 0x212)) {
+        mbar_arrive_expect_tx(&bars.q_full, kTile);
+        tma_load_3d(sQ, &tq, &bars.q_full, 0, qb * kB, h);
+        tma_load_3d(sQ + kHalf, &tq, &bars.q_full, 64, qb * kB, h);
+      } else {
+        mbar_arrive(&bars.q_full);
+      }
+      const bool kv_ok = CRISP_CHECK(g < hq / group, status, 0x213);
       int j = 0, nk = 0, nv = 0;  // blocks started, K and V loads issued
       bool ok = true;
       for (int w = 0; ok && w <= (qb >> 5); ++w) {
-        uint32_t bits = row_word(row, is_dense, w, qb);
+        uint32_t bits = row_word(row, is_dense, w, qb, W, status);
         while (bits) {
           const int kb = w * 32 + __ffs(bits) - 1;
           bits &= bits - 1;
@@ -290,19 +301,28 @@ __global__ void __launch_bounds__(kThreads, 2)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars.k_full, kTile);
+          const bool tile_ok = kv_ok && CRISP_CHECK(kb * kB < n, status, 0x214);
           ++nk;
-          tma_load_3d(sK, &tk, &bars.k_full, 0, kb * kB, g);
-          tma_load_3d(sK + kHalf, &tk, &bars.k_full, 64, kb * kB, g);
+          if (tile_ok) {
+            mbar_arrive_expect_tx(&bars.k_full, kTile);
+            tma_load_3d(sK, &tk, &bars.k_full, 0, kb * kB, g);
+            tma_load_3d(sK + kHalf, &tk, &bars.k_full, 64, kb * kB, g);
+          } else {
+            mbar_arrive(&bars.k_full);
+          }
           if (!mbar_wait(&bars.v_empty, par, &bars.abort)) {
             fail(&bars.abort, status, 0x202);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars.v_full, kTile);
           ++nv;
-          tma_load_3d(sV, &tv, &bars.v_full, 0, kb * kB, g);
-          tma_load_3d(sV + kHalf, &tv, &bars.v_full, 64, kb * kB, g);
+          if (tile_ok) {
+            mbar_arrive_expect_tx(&bars.v_full, kTile);
+            tma_load_3d(sV, &tv, &bars.v_full, 0, kb * kB, g);
+            tma_load_3d(sV + kHalf, &tv, &bars.v_full, 64, kb * kB, g);
+          } else {
+            mbar_arrive(&bars.v_full);
+          }
           ++j;
         }
       }
@@ -525,9 +545,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint4 u = stg[R * 8 + (chunk ^ (R & 7))];
       const int tok = qb * kB + quarter * 32 + R;
       if (tok >= n) continue;  // rows past the end of a short last block
-      uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * o_hs + static_cast<int64_t>(tok) * o_ts +
-                                            half * 64);
-      dst[chunk] = u;
+      const int64_t idx = static_cast<int64_t>(h) * o_hs + static_cast<int64_t>(tok) * o_ts + half * 64 + chunk * 8;
+      // extent of out under its strides: (hq - 1) * o_hs + (n - 1) * o_ts + 128 elements
+      if (!CRISP_CHECK(idx >= 0 && idx + 8 <= (static_cast<int64_t>(gridDim.x) / nb - 1) * o_hs +
+                                                   static_cast<int64_t>(n - 1) * o_ts + kD,
+                       status, 0x215))
+        continue;
+      *reinterpret_cast<uint4*>(out + idx) = u;
     }
   }
 

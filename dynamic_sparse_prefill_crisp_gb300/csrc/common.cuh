@@ -26,6 +26,22 @@ __device__ __forceinline__ void report_error(DevStatus* st, uint32_t code, uint3
   if (atomicCAS(&st->code, 0u, code) == 0u) atomicExch(&st->detail, detail);
 }
 
+// Bounds checks of the checking build (compiled with -DCRISP_DEBUG): a
+// global index or TMA coordinate outside its buffer records CRISP_ERR_BOUNDS
+// with the site code in the status word (first error wins), and the caller
+// skips the access; nothing traps. Each extent is derived from the shape the
+// kernel was launched with, independently of the index it guards. The
+// release build compiles every check to `true`.
+#ifdef CRISP_DEBUG
+__device__ __forceinline__ bool in_bounds(bool ok, DevStatus* st, uint32_t site) {
+  if (!ok && st != nullptr) report_error(st, CRISP_ERR_BOUNDS, site);
+  return ok;
+}
+#define CRISP_CHECK(cond, st, site) ::crisp::in_bounds((cond), (st), (site))
+#else
+#define CRISP_CHECK(cond, st, site) true
+#endif
+
 // Q32 quantum of a probability: round-half-even(p * 2^32); p * 2^32 is exact
 // in fp32. No float->64-bit conversion instruction is used (on this GPU those
 // run on the FP64 pipe): below 2^23, adding 2^23 in fp32 rounds the value to
@@ -96,18 +112,18 @@ cudaError_t launch_assemble_slash(const crisp_shape& s, const uint64_t* vmass, c
 cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_t* vmass, uint64_t* smass,
                                 uint64_t* rmass, char* ws, cudaStream_t st);
 cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const uint64_t* rmass,
-                         uint64_t* cstruct, uint64_t* total, uint8_t* route, cudaStream_t st);
+                         uint64_t* cstruct, uint64_t* total, uint8_t* route, DevStatus* status, cudaStream_t st);
 cudaError_t launch_route_map(const crisp_shape& s, const crisp_params& p, const float* pmap, uint64_t* cstruct,
-                             uint64_t* total, uint8_t* route, cudaStream_t st);
+                             uint64_t* total, uint8_t* route, DevStatus* status, cudaStream_t st);
 cudaError_t launch_route_jsd(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const float* pbar,
-                             double* jsd, uint8_t* route, cudaStream_t st);
+                             double* jsd, uint8_t* route, DevStatus* status, cudaStream_t st);
 cudaError_t launch_select_vs(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass,
                              const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
-                             cudaStream_t st);
+                             DevStatus* status, cudaStream_t st);
 cudaError_t launch_pe_map(const crisp_shape& s, const void* q, const void* k, const uint8_t* route, float* pbar,
                           char* ws, cudaStream_t st);
 cudaError_t launch_select_pe(const crisp_shape& s, const crisp_params& p, const float* pbar, const uint8_t* route,
-                             uint32_t* pebits, cudaStream_t st);
+                             uint32_t* pebits, DevStatus* status, cudaStream_t st);
 cudaError_t launch_build_mask(const crisp_shape& s, const uint8_t* route, const uint32_t* vbits,
                               const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits, int32_t* counts,
                               int32_t* order, char* ws, cudaStream_t st);

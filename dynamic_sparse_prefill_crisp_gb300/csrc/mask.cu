@@ -23,9 +23,10 @@ namespace crisp {
 namespace {
 
 __global__ void srev_kernel(const uint32_t* __restrict__ sbits, const uint8_t* __restrict__ route, int nb,
-                            uint32_t* __restrict__ srev) {
+                            uint32_t* __restrict__ srev, DevStatus* status) {
   const int h = blockIdx.x;
   const int W = (nb + 31) / 32;
+  if (!CRISP_CHECK(h < static_cast<int>(gridDim.x), status, 0x510)) return;
   const uint32_t* S = sbits + static_cast<size_t>(h) * W;
   for (int w = threadIdx.x; w < W + 2; w += blockDim.x) {
     uint32_t word = 0;
@@ -42,7 +43,9 @@ __global__ void srev_kernel(const uint32_t* __restrict__ sbits, const uint8_t* _
   }
 }
 
-__device__ __forceinline__ uint32_t window32(const uint32_t* v, int p) {
+// 32 bits of v starting at bit p (v holds `words` words).
+__device__ __forceinline__ uint32_t window32(const uint32_t* v, int p, int words, DevStatus* status) {
+  if (!CRISP_CHECK(p >= 0 && (p >> 5) + 1 < words, status, 0x511)) return 0u;
   return __funnelshift_r(v[p >> 5], v[(p >> 5) + 1], p & 31);
 }
 
@@ -52,7 +55,7 @@ constexpr int kMaskRowsPerCta = 8;
 __global__ void mask_kernel(const uint8_t* __restrict__ route, const uint32_t* __restrict__ vbits,
                             const uint32_t* __restrict__ srev, const uint32_t* __restrict__ pebits, int hq, int nb,
                             int group, uint32_t* __restrict__ rowbits, int32_t* __restrict__ counts,
-                            int32_t* __restrict__ order) {
+                            int32_t* __restrict__ order, DevStatus* status) {
   const int lane = threadIdx.x & 31;
   const int rowid = blockIdx.x * kMaskRowsPerCta + (threadIdx.x >> 5);
   if (rowid >= hq * nb) return;  // whole warps
@@ -69,7 +72,7 @@ __global__ void mask_kernel(const uint8_t* __restrict__ route, const uint32_t* _
     if (w <= wq) {
       if (vs) {
         const int p = nb - 1 - qb + 32 * w;
-        word = V[w] | window32(R, p) | window32(R, p + 1);
+        word = V[w] | window32(R, p, W + 2, status) | window32(R, p + 1, W + 2, status);
       } else {
         word = PE[w];
       }
@@ -82,7 +85,8 @@ __global__ void mask_kernel(const uint8_t* __restrict__ route, const uint32_t* _
   if (lane == 0) {
     counts[static_cast<size_t>(h) * nb + qb] = total;
     const size_t g = h / group, j = h % group;
-    order[(g * nb + (nb - 1 - qb)) * group + j] = h * nb + qb;
+    const size_t o = (g * nb + (nb - 1 - qb)) * group + j;
+    if (CRISP_CHECK(o < static_cast<size_t>(hq) * nb, status, 0x512)) order[o] = h * nb + qb;
   }
 }
 
@@ -94,10 +98,11 @@ cudaError_t launch_build_mask(const crisp_shape& s, const uint8_t* route, const 
   const ScratchLayout L = scratch_layout(s);
   const int nb = num_blocks(s.seq_len);
   auto* srev = reinterpret_cast<uint32_t*>(ws + L.srev);
-  srev_kernel<<<s.hq, 128, 0, st>>>(sbits, route, nb, srev);
+  auto* status = reinterpret_cast<DevStatus*>(ws + L.status);
+  srev_kernel<<<s.hq, 128, 0, st>>>(sbits, route, nb, srev, status);
   const int rows = s.hq * nb;
   mask_kernel<<<(rows + kMaskRowsPerCta - 1) / kMaskRowsPerCta, 32 * kMaskRowsPerCta, 0, st>>>(
-      route, vbits, srev, pebits, s.hq, nb, s.hq / s.hkv, rowbits, counts, order);
+      route, vbits, srev, pebits, s.hq, nb, s.hq / s.hkv, rowbits, counts, order, status);
   return cudaGetLastError();
 }
 

@@ -33,16 +33,22 @@ __global__ void __launch_bounds__(kMassThreads) mass_tiles(const float* __restri
                                                            uint64_t* __restrict__ lower,
                                                            uint64_t* __restrict__ upper,
                                                            uint64_t* __restrict__ upper2,
-                                                           uint64_t* __restrict__ rec) {
+                                                           uint64_t* __restrict__ rec, DevStatus* status) {
   __shared__ uint64_t red[4][kMassThreads / 32];
   const int tail = kRagged ? tail_arg : kB;
   const int c = blockIdx.x, h = blockIdx.y, nb = gridDim.x;
   const int cq = threadIdx.x & 31, rg = threadIdx.x >> 5;
-  const float* base = pmap + static_cast<size_t>(h) * kB * ld + static_cast<size_t>(c) * kB + cq * 4;
+  const size_t off = static_cast<size_t>(h) * kB * ld + static_cast<size_t>(c) * kB + cq * 4;
+  // (checking build) the tile must lie inside the map [hq][128][ld]
+  const bool tile_ok = CRISP_CHECK(off + static_cast<size_t>(kB - 1) * ld + 4 <= static_cast<size_t>(gridDim.y) * kB * ld &&
+                                       static_cast<size_t>(c) * kB + kB <= static_cast<size_t>(ld),
+                                   status, 0x310);
+  const float* base = pmap + off;
   float4 p[16];
 #pragma unroll
   for (int k = 0; k < 16; ++k)
-    p[k] = __ldcs(reinterpret_cast<const float4*>(base + static_cast<size_t>(rg * 16 + k) * ld));
+    p[k] = tile_ok ? __ldcs(reinterpret_cast<const float4*>(base + static_cast<size_t>(rg * 16 + k) * ld))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
   // Quanta below 2^23 (nearly all of them) are summed in 32 bits: 64 of them
   // stay below 2^29. Larger ones go to 64-bit sums.
   uint32_t all32 = 0, lo32 = 0, hi32 = 0;
@@ -93,10 +99,12 @@ __global__ void __launch_bounds__(kMassThreads) mass_tiles(const float* __restri
     for (int t = 0; t < 4; ++t)
       for (int w = 0; w < kMassThreads / 32; ++w) sum[t] += red[t][w];
     const size_t idx = static_cast<size_t>(h) * nb + c;
-    vmass[idx] = sum[0];
-    lower[idx] = sum[1];
-    upper[idx] = sum[0] - sum[1] - sum[2];
-    upper2[idx] = sum[2];
+    if (CRISP_CHECK(idx < static_cast<size_t>(gridDim.y) * nb, status, 0x311)) {
+      vmass[idx] = sum[0];
+      lower[idx] = sum[1];
+      upper[idx] = sum[0] - sum[1] - sum[2];
+      upper2[idx] = sum[2];
+    }
     if (rec_tile) rec[h] = sum[3];
   }
 }
@@ -109,12 +117,13 @@ __global__ void __launch_bounds__(kMassThreads) mass_tiles(const float* __restri
 __global__ void assemble_slash(const uint64_t* __restrict__ vmass, const uint64_t* __restrict__ lower,
                                const uint64_t* __restrict__ upper, const uint64_t* __restrict__ upper2,
                                const uint64_t* __restrict__ rec, int nb, int tail, uint64_t* __restrict__ smass,
-                               uint64_t* __restrict__ rmass) {
+                               uint64_t* __restrict__ rmass, DevStatus* status) {
   const int h = blockIdx.y;
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= nb) return;
   const size_t o = static_cast<size_t>(h) * nb;
   const int c1 = nb - 1 - s, c2 = nb - 2 - s, c3 = nb - 3 - s;
+  if (!CRISP_CHECK(o + s < static_cast<size_t>(gridDim.y) * nb && c1 < nb, status, 0x312)) return;
   smass[o + s] = (c1 >= 1 ? lower[o + c1] : 0ull) + (c2 >= 1 ? upper[o + c2] : 0ull) +
                  (c3 >= 1 ? upper2[o + c3] : 0ull);
   if (s == 0) rmass[h] = vmass[o + nb - 1] + (tail < kB ? rec[h] : 0ull);
@@ -124,12 +133,13 @@ __global__ void assemble_slash(const uint64_t* __restrict__ vmass, const uint64_
 // n >= 256), total = sum of vmass; VS iff tau_den * C_struct >= tau_num * total.
 __global__ void route_kernel(const uint64_t* __restrict__ vmass, const uint64_t* __restrict__ rmass, int nb,
                              uint32_t tau_num, uint32_t tau_den, uint64_t* __restrict__ cstruct,
-                             uint64_t* __restrict__ total, uint8_t* __restrict__ route) {
+                             uint64_t* __restrict__ total, uint8_t* __restrict__ route, DevStatus* status) {
   __shared__ uint64_t scratch[32];
   const int h = blockIdx.x;
   const uint64_t* v = vmass + static_cast<size_t>(h) * nb;
   uint64_t s = 0;
-  for (int c = threadIdx.x; c < nb; c += blockDim.x) s += v[c];
+  for (int c = threadIdx.x; c < nb; c += blockDim.x)
+    if (CRISP_CHECK(static_cast<size_t>(h) * nb + c < static_cast<size_t>(gridDim.x) * nb, status, 0x313)) s += v[c];
   const uint64_t T = block_sum(s, scratch);
   if (threadIdx.x == 0) {
     const uint64_t S = v[0] + rmass[h];
@@ -146,11 +156,15 @@ __global__ void route_kernel(const uint64_t* __restrict__ vmass, const uint64_t*
 // integer atomics, so the order of the tiles does not matter).
 __global__ void __launch_bounds__(kMassThreads) cstruct_tiles(const float* __restrict__ pmap, int64_t ld, int n,
                                                               int sink, int recency, uint64_t* __restrict__ cstruct,
-                                                              uint64_t* __restrict__ total) {
+                                                              uint64_t* __restrict__ total, DevStatus* status) {
   __shared__ uint64_t red[2][kMassThreads / 32];
   const int c = blockIdx.x, h = blockIdx.y;
   const int cq = threadIdx.x & 31, rg = threadIdx.x >> 5;
-  const float* base = pmap + static_cast<size_t>(h) * kB * ld + static_cast<size_t>(c) * kB + cq * 4;
+  const size_t off = static_cast<size_t>(h) * kB * ld + static_cast<size_t>(c) * kB + cq * 4;
+  const bool tile_ok = CRISP_CHECK(off + static_cast<size_t>(kB - 1) * ld + 4 <= static_cast<size_t>(gridDim.y) * kB * ld &&
+                                       static_cast<size_t>(c) * kB + kB <= static_cast<size_t>(ld),
+                                   status, 0x314);
+  const float* base = pmap + off;
   const int j0 = c * kB + cq * 4;  // key token of this thread's first column
   bool in_slice[4];
 #pragma unroll
@@ -158,7 +172,8 @@ __global__ void __launch_bounds__(kMassThreads) cstruct_tiles(const float* __res
   float4 p[16];
 #pragma unroll
   for (int k = 0; k < 16; ++k)
-    p[k] = __ldcs(reinterpret_cast<const float4*>(base + static_cast<size_t>(rg * 16 + k) * ld));
+    p[k] = tile_ok ? __ldcs(reinterpret_cast<const float4*>(base + static_cast<size_t>(rg * 16 + k) * ld))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
   // As in mass_tiles: quanta below 2^23 summed in 32 bits (64 stay below 2^29).
   uint32_t all32 = 0, sl32 = 0;
   uint64_t all64 = 0, sl64 = 0;
@@ -218,12 +233,15 @@ __global__ void __launch_bounds__(kSelThreads) select_vs_kernel(const uint64_t* 
                                                                 uint32_t alpha_num, uint32_t alpha_den, int kmin,
                                                                 int vs_mode, uint32_t gamma_num, uint32_t gamma_den,
                                                                 uint32_t* __restrict__ vbits,
-                                                                uint32_t* __restrict__ sbits) {
+                                                                uint32_t* __restrict__ sbits, DevStatus* status) {
   __shared__ uint32_t chosen[kMaxBlocks / 32];
   __shared__ uint64_t scratch64[32];
   __shared__ int scratch32[32];
   const int h = blockIdx.x, dir = blockIdx.y;
   const int W = (nb + 31) / 32;
+  // (checking build) the bit rows fit the shared bitset; the head's mass rows
+  // [h*nb, h*nb + nb) and bit words [h*W, h*W + W) lie inside [hq][nb] / [hq][W]
+  if (!CRISP_CHECK(W <= kMaxBlocks / 32 && h < static_cast<int>(gridDim.x), status, 0x315)) return;
   uint32_t* out = (dir == 0 ? vbits : sbits) + static_cast<size_t>(h) * W;
   for (int w = threadIdx.x; w < W; w += blockDim.x) chosen[w] = 0u;
   __syncthreads();
@@ -294,10 +312,11 @@ __global__ void __launch_bounds__(kSelThreads) select_vs_kernel(const uint64_t* 
 // between the last query block's block-pooled attention a (from the block
 // masses) and its pooled estimate e (row nb-1 of the pooled map), in fp64.
 __global__ void jsd_route_kernel(const uint64_t* __restrict__ vmass, const float* __restrict__ pbar, int nb,
-                                 float tau, double* __restrict__ jsd, uint8_t* __restrict__ route) {
+                                 float tau, double* __restrict__ jsd, uint8_t* __restrict__ route, DevStatus* status) {
   __shared__ uint64_t scratch64[32];
   __shared__ double scratchd[32];
   const int h = blockIdx.x;
+  if (!CRISP_CHECK(h < static_cast<int>(gridDim.x) && nb >= 1, status, 0x316)) return;
   const uint64_t* v = vmass + static_cast<size_t>(h) * nb;
   const float* e = pbar + (static_cast<size_t>(h) * nb + (nb - 1)) * nb;
   uint64_t part = 0;
@@ -328,7 +347,7 @@ cudaError_t launch_block_masses(const crisp_shape& s, const float* pmap, uint64_
   kern<<<dim3(nb, s.hq), kMassThreads, 0, st>>>(
       pmap, map_ld(s.seq_len), tail_len(s.seq_len), vmass, reinterpret_cast<uint64_t*>(ws + L.mass_lower),
       reinterpret_cast<uint64_t*>(ws + L.mass_upper), reinterpret_cast<uint64_t*>(ws + L.mass_upper2),
-      reinterpret_cast<uint64_t*>(ws + L.mass_rec));
+      reinterpret_cast<uint64_t*>(ws + L.mass_rec), reinterpret_cast<DevStatus*>(ws + L.status));
   const cudaError_t e = cudaGetLastError();
   return e != cudaSuccess ? e : launch_assemble_slash(s, vmass, ws, smass, rmass, st);
 }
@@ -340,41 +359,41 @@ cudaError_t launch_assemble_slash(const crisp_shape& s, const uint64_t* vmass, c
   assemble_slash<<<dim3((nb + 255) / 256, s.hq), 256, 0, st>>>(
       vmass, reinterpret_cast<const uint64_t*>(ws + L.mass_lower), reinterpret_cast<const uint64_t*>(ws + L.mass_upper),
       reinterpret_cast<const uint64_t*>(ws + L.mass_upper2), reinterpret_cast<const uint64_t*>(ws + L.mass_rec), nb,
-      tail_len(s.seq_len), smass, rmass);
+      tail_len(s.seq_len), smass, rmass, reinterpret_cast<DevStatus*>(ws + L.status));
   return cudaGetLastError();
 }
 
 cudaError_t launch_route(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const uint64_t* rmass,
-                         uint64_t* cstruct, uint64_t* total, uint8_t* route, cudaStream_t st) {
+                         uint64_t* cstruct, uint64_t* total, uint8_t* route, DevStatus* status, cudaStream_t st) {
   route_kernel<<<s.hq, 256, 0, st>>>(vmass, rmass, num_blocks(s.seq_len), p.tau_num, p.tau_den, cstruct, total,
-                                     route);
+                                     route, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_route_map(const crisp_shape& s, const crisp_params& p, const float* pmap, uint64_t* cstruct,
-                             uint64_t* total, uint8_t* route, cudaStream_t st) {
+                             uint64_t* total, uint8_t* route, DevStatus* status, cudaStream_t st) {
   const size_t bytes = static_cast<size_t>(s.hq) * sizeof(uint64_t);
   cudaError_t e = cudaMemsetAsync(cstruct, 0, bytes, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(total, 0, bytes, st);
   if (e != cudaSuccess) return e;
   cstruct_tiles<<<dim3(num_blocks(s.seq_len), s.hq), kMassThreads, 0, st>>>(
-      pmap, map_ld(s.seq_len), s.seq_len, p.sink_tokens, p.recency_tokens, cstruct, total);
+      pmap, map_ld(s.seq_len), s.seq_len, p.sink_tokens, p.recency_tokens, cstruct, total, status);
   route_decide<<<(s.hq + 127) / 128, 128, 0, st>>>(cstruct, total, s.hq, p.tau_num, p.tau_den, route);
   return cudaGetLastError();
 }
 
 cudaError_t launch_select_vs(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass,
                              const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
-                             cudaStream_t st) {
+                             DevStatus* status, cudaStream_t st) {
   select_vs_kernel<<<dim3(s.hq, 2), kSelThreads, 0, st>>>(vmass, smass, route, num_blocks(s.seq_len), p.alpha_num,
                                                           p.alpha_den, p.kmin_blocks, p.vs_mode, p.vs_gamma_num,
-                                                          p.vs_gamma_den, vbits, sbits);
+                                                          p.vs_gamma_den, vbits, sbits, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_route_jsd(const crisp_shape& s, const crisp_params& p, const uint64_t* vmass, const float* pbar,
-                             double* jsd, uint8_t* route, cudaStream_t st) {
-  jsd_route_kernel<<<s.hq, 256, 0, st>>>(vmass, pbar, num_blocks(s.seq_len), p.jsd_tau, jsd, route);
+                             double* jsd, uint8_t* route, DevStatus* status, cudaStream_t st) {
+  jsd_route_kernel<<<s.hq, 256, 0, st>>>(vmass, pbar, num_blocks(s.seq_len), p.jsd_tau, jsd, route, status);
   return cudaGetLastError();
 }
 

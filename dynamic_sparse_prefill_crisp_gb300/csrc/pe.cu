@@ -22,9 +22,12 @@ namespace {
 __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat162* __restrict__ q,
                                                    const __nv_bfloat162* __restrict__ k, const uint8_t* __restrict__ route,
                                                    int hq, int hkv, int n, int64_t q_hs, int64_t q_ts, int64_t kv_hs,
-                                                   int64_t kv_ts, float* __restrict__ qbar, float* __restrict__ kbar) {
+                                                   int64_t kv_ts, float* __restrict__ qbar, float* __restrict__ kbar,
+                                                   DevStatus* status) {
   __shared__ float2 red[4][64];
   const int b = blockIdx.x, y = blockIdx.y, nb = gridDim.x;
+  // (checking build) the block's tokens lie in [0, n) and the head in q or k
+  if (!CRISP_CHECK(b * kB < n && y < hq + hkv, status, 0x410)) return;
   const int G = hq / hkv;
   const bool is_q = y < hq;
   if (is_q) {
@@ -54,7 +57,9 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat162* __restr
       s.x += red[t][pair].x;
       s.y += red[t][pair].y;
     }
-    float* dst = is_q ? qbar + (static_cast<size_t>(y) * nb + b) * kD : kbar + (static_cast<size_t>(y - hq) * nb + b) * kD;
+    const size_t o = is_q ? (static_cast<size_t>(y) * nb + b) * kD : (static_cast<size_t>(y - hq) * nb + b) * kD;
+    if (!CRISP_CHECK(o + kD <= static_cast<size_t>(is_q ? hq : hkv) * nb * kD, status, 0x411)) return;
+    float* dst = (is_q ? qbar : kbar) + o;
     const float inv = 1.0f / static_cast<float>(len);  // exact for a whole block
     dst[2 * pair] = s.x * inv;
     dst[2 * pair + 1] = s.y * inv;
@@ -66,10 +71,12 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat162* __restr
 constexpr int kPT = 64;
 __global__ void __launch_bounds__(256) pooled_scores(const float* __restrict__ qbar, const float* __restrict__ kbar,
                                                      const uint8_t* __restrict__ route, int nb, int group,
-                                                     float c_log2, float* __restrict__ pbar) {
+                                                     float c_log2, float* __restrict__ pbar, DevStatus* status) {
   __shared__ float As[32][kPT + 1];
   __shared__ float Bs[32][kPT + 1];
   const int bt = blockIdx.y, ct = blockIdx.x, h = blockIdx.z;
+  // (checking build) the tile's rows and columns start inside [0, nb)
+  if (!CRISP_CHECK(bt * kPT < nb && ct * kPT < nb, status, 0x412)) return;
   if (route[h]) return;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   float* out = pbar + static_cast<size_t>(h) * nb * nb;
@@ -119,11 +126,13 @@ __global__ void __launch_bounds__(256) pooled_scores(const float* __restrict__ q
 }
 
 // Row softmax over c <= b (base 2, logits already in log2 units), one warp per row.
-__global__ void pooled_softmax(const uint8_t* __restrict__ route, int hq, int nb, float* __restrict__ pbar) {
+__global__ void pooled_softmax(const uint8_t* __restrict__ route, int hq, int nb, float* __restrict__ pbar,
+                               DevStatus* status) {
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= hq * nb) return;
   const int h = row / nb, b = row % nb;
+  if (!CRISP_CHECK(static_cast<size_t>(row) * nb + b < static_cast<size_t>(hq) * nb * nb, status, 0x413)) return;
   if (route[h]) return;
   float* z = pbar + static_cast<size_t>(row) * nb;
   float mx = -INFINITY;
@@ -147,7 +156,8 @@ __global__ void __launch_bounds__(kPeThreads) select_pe_kernel(const float* __re
                                                                const uint8_t* __restrict__ route, int nb,
                                                                int pe_mode, uint32_t gamma_num, uint32_t gamma_den,
                                                                uint32_t alpha_num, uint32_t alpha_den, int kmin,
-                                                               int rows, uint32_t* __restrict__ pebits) {
+                                                               int rows, uint32_t* __restrict__ pebits,
+                                                               DevStatus* status) {
   extern __shared__ unsigned long long keys[];  // [b + 1]
   __shared__ uint32_t chosen[kMaxBlocks / 32];
   __shared__ uint64_t scratch64[32];
@@ -156,6 +166,9 @@ __global__ void __launch_bounds__(kPeThreads) select_pe_kernel(const float* __re
   const int h = blockIdx.y;
   const int W = (nb + 31) / 32;
   const int b_end = min(nb, (static_cast<int>(blockIdx.x) + 1) * rows);
+  // (checking build) the shared bitset holds a row; the rows [.., b_end) of
+  // head h lie inside pbar [hq][nb][nb] and pebits [hq][nb][W]
+  if (!CRISP_CHECK(W <= kMaxBlocks / 32 && h < static_cast<int>(gridDim.y) && b_end <= nb, status, 0x414)) return;
   if (route[h]) {
     for (int i = blockIdx.x * rows * W + threadIdx.x; i < b_end * W; i += blockDim.x)
       pebits[static_cast<size_t>(h) * nb * W + i] = 0u;
@@ -234,17 +247,18 @@ cudaError_t launch_pe_map(const crisp_shape& s, const void* q, const void* k, co
   pool_kernel<<<dim3(nb, s.hq + s.hkv), 256, 0, st>>>(static_cast<const __nv_bfloat162*>(q),
                                                       static_cast<const __nv_bfloat162*>(k), route, s.hq, s.hkv,
                                                       s.seq_len, s.q_head_stride, s.q_tok_stride, s.kv_head_stride,
-                                                      s.kv_tok_stride, qbar, kbar);
+                                                      s.kv_tok_stride, qbar, kbar, reinterpret_cast<DevStatus*>(ws + L.status));
   const int tiles = (nb + kPT - 1) / kPT;
+  auto* status = reinterpret_cast<DevStatus*>(ws + L.status);
   pooled_scores<<<dim3(tiles, tiles, s.hq), 256, 0, st>>>(qbar, kbar, route, nb, s.hq / s.hkv,
-                                                          s.scale * 1.4426950408889634f, pbar);
+                                                          s.scale * 1.4426950408889634f, pbar, status);
   const int rows = s.hq * nb;
-  pooled_softmax<<<(rows + 7) / 8, 256, 0, st>>>(route, s.hq, nb, pbar);
+  pooled_softmax<<<(rows + 7) / 8, 256, 0, st>>>(route, s.hq, nb, pbar, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_select_pe(const crisp_shape& s, const crisp_params& p, const float* pbar, const uint8_t* route,
-                             uint32_t* pebits, cudaStream_t st) {
+                             uint32_t* pebits, DevStatus* status, cudaStream_t st) {
   const int nb = num_blocks(s.seq_len);
   const size_t key_bytes = static_cast<size_t>(nb) * sizeof(unsigned long long);  // <= 64 KB (nb <= 8192)
   cudaError_t e = cudaFuncSetAttribute(select_pe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -254,7 +268,8 @@ cudaError_t launch_select_pe(const crisp_shape& s, const crisp_params& p, const 
   // 0.13 -> 0.03 ms); one below, where a CTA per row keeps more in flight.
   const int rows = nb >= 1024 ? 4 : 1;
   select_pe_kernel<<<dim3((nb + rows - 1) / rows, s.hq), kPeThreads, key_bytes, st>>>(
-      pbar, route, nb, p.pe_mode, p.gamma_num, p.gamma_den, p.alpha_num, p.alpha_den, p.kmin_blocks, rows, pebits);
+      pbar, route, nb, p.pe_mode, p.gamma_num, p.gamma_den, p.alpha_num, p.alpha_den, p.kmin_blocks, rows, pebits,
+      status);
   return cudaGetLastError();
 }
 

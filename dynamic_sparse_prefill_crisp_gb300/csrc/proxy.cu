@@ -128,9 +128,15 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
-      mbar_arrive_expect_tx(&bars.q_full, kTile);
-      tma_load_3d(sQ, &tq, &bars.q_full, 0, n - kB, h);
-      tma_load_3d(sQ + kHalf, &tq, &bars.q_full, 64, n - kB, h);
+      // (checking build) a tile outside q or k is not copied; its barrier
+      // phase completes without data and the status word says why.
+      if (CRISP_CHECK(n - kB >= 0 && h < static_cast<int>(gridDim.x), status, 0x110)) {
+        mbar_arrive_expect_tx(&bars.q_full, kTile);
+        tma_load_3d(sQ, &tq, &bars.q_full, 0, n - kB, h);
+        tma_load_3d(sQ + kHalf, &tq, &bars.q_full, 64, n - kB, h);
+      } else {
+        mbar_arrive(&bars.q_full);
+      }
       int issued = 0;  // K tiles whose copies were started
       for (int t = 0; t < T; ++t) {
         const int s = t % kStages;
@@ -139,8 +145,12 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
           fail(&bars.abort, status, 0x101);
           break;
         }
-        mbar_arrive_expect_tx(&bars.k_full[s], kTile);
         ++issued;
+        if (!CRISP_CHECK((kb0 + t) * kB < n && g < static_cast<int>(gridDim.x) / group, status, 0x111)) {
+          mbar_arrive(&bars.k_full[s]);
+          continue;
+        }
+        mbar_arrive_expect_tx(&bars.k_full[s], kTile);
         uint8_t* dst = sK + s * kTile;
         tma_load_3d(dst, &tk, &bars.k_full[s], 0, (kb0 + t) * kB, g);
         tma_load_3d(dst + kHalf, &tk, &bars.k_full[s], 64, (kb0 + t) * kB, g);
@@ -187,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     float m_run = -INFINITY, l_run = 0.f;
     float M = 0.f, inv_l = 0.f, inv_l32 = 0.f;
-    if (kMode != kStats) {
+    if (kMode != kStats && CRISP_CHECK(h < static_cast<int>(gridDim.x), status, 0x112)) {
       const float2 st = stats[static_cast<size_t>(h) * kB + r];
       M = st.x;
       inv_l = st.y;
@@ -270,9 +280,12 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
           for (int it = 0; it < 8; ++it) {
             const int R = it * 4 + (lane >> 3);
             const float4 p = reinterpret_cast<const float4*>(stg + R * 32)[c4 ^ (R & 7)];
-            float* dst = pmap + (static_cast<size_t>(h) * kB + quarter * 32 + R) * static_cast<size_t>(ld) +
-                         static_cast<size_t>(kb) * kB + col0 + c4 * 4;
-            *reinterpret_cast<float4*>(dst) = p;
+            const size_t idx = (static_cast<size_t>(h) * kB + quarter * 32 + R) * static_cast<size_t>(ld) +
+                               static_cast<size_t>(kb) * kB + col0 + c4 * 4;
+            if (CRISP_CHECK(idx + 4 <= static_cast<size_t>(gridDim.x) * kB * static_cast<size_t>(ld) &&
+                                static_cast<size_t>(kb) * kB + col0 + c4 * 4 + 4 <= static_cast<size_t>(ld),
+                            status, 0x113))
+              *reinterpret_cast<float4*>(pmap + idx) = p;
           }
           __syncwarp();
         } else if (kMode == kMasses) {
@@ -366,11 +379,13 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
             const unsigned long long sr = atomicExch(&tile_acc[b][3], 0ull);
             atomicExch(&tile_cnt[b], 0u);
             const size_t idx = static_cast<size_t>(h) * nb + kb;
-            vmass[idx] = sa;
-            lower[idx] = sl;
-            upper[idx] = sa - sl - sh;
-            upper2[idx] = sh;
-            if (rec_tile) rec[h] = sr;
+            if (CRISP_CHECK(idx < static_cast<size_t>(gridDim.x) * nb, status, 0x114)) {
+              vmass[idx] = sa;
+              lower[idx] = sl;
+              upper[idx] = sa - sl - sh;
+              upper2[idx] = sh;
+            }
+            if (rec_tile && CRISP_CHECK(h < static_cast<int>(gridDim.x), status, 0x115)) rec[h] = sr;
           }
         }
       }
@@ -378,7 +393,11 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.s_empty[b]);
     }
-    if (kMode == kStats) part[(static_cast<size_t>(h) * kB + r) * (2 * nchunks) + 2 * chunk + half] = make_float2(m_run, l_run);
+    if (kMode == kStats) {
+      const size_t idx = (static_cast<size_t>(h) * kB + r) * (2 * nchunks) + 2 * chunk + half;
+      if (CRISP_CHECK(idx < static_cast<size_t>(gridDim.x) * kB * 2 * nchunks, status, 0x116))
+        part[idx] = make_float2(m_run, l_run);
+    }
   }
 
   tc_fence_before();
@@ -389,9 +408,12 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
 
 // Combines the per-chunk (max, sum) pairs of each row, one warp per row:
 // M = max m_c, L = sum l_c * 2^(m_c - M); stores (M, 1/L).
-__global__ void proxy_combine(const float2* __restrict__ part, float2* __restrict__ stats, int rows, int nparts) {
+__global__ void proxy_combine(const float2* __restrict__ part, float2* __restrict__ stats, int rows, int nparts,
+                              DevStatus* status) {
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (row >= rows) return;  // whole warps
+  if (!CRISP_CHECK(static_cast<size_t>(row) * nparts + nparts <= static_cast<size_t>(rows) * nparts, status, 0x117))
+    return;
   const float2* p = part + static_cast<size_t>(row) * nparts;
   float M = -INFINITY;
   for (int c = lane; c < nparts; c += 32) M = fmaxf(M, p[c].x);
@@ -421,7 +443,7 @@ static cudaError_t proxy_stats(const crisp_shape& s, const TmaMaps& maps, char* 
       maps.q, maps.k, s.seq_len, s.hq / s.hkv, s.scale * 1.4426950408889634f, nullptr, 0, part, stats, nullptr,
       nullptr, nullptr, nullptr, nullptr, status);
   const int rows = s.hq * kB;
-  proxy_combine<<<(rows + 7) / 8, 256, 0, st>>>(part, stats, rows, 2 * chunks);  // 8 rows (warps) per CTA
+  proxy_combine<<<(rows + 7) / 8, 256, 0, st>>>(part, stats, rows, 2 * chunks, status);  // 8 rows (warps) per CTA
   return cudaGetLastError();
 }
 

@@ -90,6 +90,15 @@ def test_library_exports_every_declared_symbol(L):
         assert getattr(L, n) is not None
 
 
+def test_checking_build_exports_every_declared_symbol():
+    # The bounds-checking build (-DCRISP_DEBUG) compiles and keeps the ABI.
+    path = crisp_build.build(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (crisp_\w+)", out))
+    assert not [n for n in declared_functions() if n not in exported]
+    assert crisp.load_library(path).crisp_status_string(8) == b"device index outside its buffer (bounds-checking build)"
+
+
 def test_params_default_is_the_universal_configuration(L):
     p = crisp.params_default()
     assert (p.tau_num, p.tau_den) == (1, 5)
