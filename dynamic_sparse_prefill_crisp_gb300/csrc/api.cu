@@ -1,9 +1,13 @@
 // Host side of the C ABI declared in include/crisp.h: argument validation,
 // workspace layout, TMA descriptors and the launch sequence of each step.
 #include <cmath>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -117,6 +121,33 @@ crisp_status make_map(CUtensorMap* m, const void* ptr, int heads, int n, int64_t
 
 crisp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CRISP_OK : CRISP_ERR_CUDA; }
 
+// Tracing of the entry points: each call runs inside an NVTX range named
+// after it (Nsight tools show the per-stage ranges; without a tool attached
+// the range is a no-op), and with CRISP_LOG=1 in the environment each call
+// writes its name, shape and returned status to stderr.
+bool log_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("CRISP_LOG");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
+}
+
+template <class Body>
+crisp_status traced(const char* name, const crisp_shape* shape, Body&& body) {
+  nvtxRangePushA(name);
+  const crisp_status st = body();
+  nvtxRangePop();
+  if (log_enabled()) {
+    if (shape != nullptr)
+      std::fprintf(stderr, "[crisp] %s hq=%d hkv=%d n=%d -> %d (%s)\n", name, shape->hq, shape->hkv, shape->seq_len,
+                   static_cast<int>(st), crisp_status_string(st));
+    else
+      std::fprintf(stderr, "[crisp] %s -> %d (%s)\n", name, static_cast<int>(st), crisp_status_string(st));
+  }
+  return st;
+}
+
 // The status word at the start of a workspace.
 DevStatus* status_of(void* ws) { return static_cast<DevStatus*>(ws); }
 
@@ -195,41 +226,49 @@ void crisp_params_default(crisp_params* p) {
 }
 
 crisp_status crisp_workspace_size(const crisp_shape* shape, size_t* bytes) {
-  crisp_status st = check_shape(shape, 0);
-  if (st != CRISP_OK) return st;
-  if (!bytes) return CRISP_ERR_INVALID_ARG;
-  *bytes = scratch_layout(*shape).total;
-  return CRISP_OK;
+  return traced("crisp_workspace_size", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape, 0);
+    if (st != CRISP_OK) return st;
+    if (!bytes) return CRISP_ERR_INVALID_ARG;
+    *bytes = scratch_layout(*shape).total;
+    return CRISP_OK;
+  });
 }
 
 crisp_status crisp_layer_workspace_size(const crisp_shape* shape, size_t* bytes) {
-  crisp_status st = check_shape(shape, 0);
-  if (st != CRISP_OK) return st;
-  if (!bytes) return CRISP_ERR_INVALID_ARG;
-  *bytes = layer_layout(*shape).total;
-  return CRISP_OK;
+  return traced("crisp_layer_workspace_size", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape, 0);
+    if (st != CRISP_OK) return st;
+    if (!bytes) return CRISP_ERR_INVALID_ARG;
+    *bytes = layer_layout(*shape).total;
+    return CRISP_OK;
+  });
 }
 
 crisp_status crisp_workspace_init(void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  if (!ws) return CRISP_ERR_WORKSPACE;
-  if (ws_bytes < sizeof(DevStatus)) return CRISP_ERR_WORKSPACE;
-  return from_cuda(cudaMemsetAsync(ws, 0, sizeof(DevStatus), stream));
+  return traced("crisp_workspace_init", nullptr, [&]() -> crisp_status {
+    if (!ws) return CRISP_ERR_WORKSPACE;
+    if (ws_bytes < sizeof(DevStatus)) return CRISP_ERR_WORKSPACE;
+    return from_cuda(cudaMemsetAsync(ws, 0, sizeof(DevStatus), stream));
+  });
 }
 
 crisp_status crisp_proxy_map(const crisp_shape* shape, const void* q, const void* k, float* pmap, void* ws,
                              size_t ws_bytes, crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if (!q || !k || !pmap) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(pmap)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  TmaMaps maps;
-  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
-  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-  maps.v = maps.k;
-  return from_cuda(launch_proxy(s, maps, pmap, static_cast<char*>(ws), stream));
+  return traced("crisp_proxy_map", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if (!q || !k || !pmap) return CRISP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(pmap)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    TmaMaps maps;
+    if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+    if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+    maps.v = maps.k;
+    return from_cuda(launch_proxy(s, maps, pmap, static_cast<char*>(ws), stream));
+  });
 }
 
 }  // extern "C"
@@ -271,184 +310,208 @@ extern "C" {
 
 crisp_status crisp_proxy_map_noalloc(const crisp_shape* shape, const void* q, const void* k, float* pmap,
                                      crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if (!q || !k || !pmap) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(pmap)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  // The proxy kernels touch only the status word and the two statistics
-  // regions, which end where the mass scratch begins.
-  const ScratchLayout L = scratch_layout(s);
-  if (L.mass_lower > kNoAllocScratchBytes) return CRISP_ERR_WORKSPACE;
-  if ((st = check_device()) != CRISP_OK) return st;
-  char* scratch = nullptr;
-  if ((st = noalloc_scratch(&scratch)) != CRISP_OK) return st;
-  TmaMaps maps;
-  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
-  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-  maps.v = maps.k;
-  // The array keeps the previous call's contents: start from a clear status.
-  if (cudaMemsetAsync(scratch + L.status, 0, sizeof(DevStatus), stream) != cudaSuccess) return CRISP_ERR_CUDA;
-  return from_cuda(launch_proxy(s, maps, pmap, scratch, stream));
+  return traced("crisp_proxy_map_noalloc", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if (!q || !k || !pmap) return CRISP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(pmap)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    // The proxy kernels touch only the status word and the two statistics
+    // regions, which end where the mass scratch begins.
+    const ScratchLayout L = scratch_layout(s);
+    if (L.mass_lower > kNoAllocScratchBytes) return CRISP_ERR_WORKSPACE;
+    if ((st = check_device()) != CRISP_OK) return st;
+    char* scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != CRISP_OK) return st;
+    TmaMaps maps;
+    if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+    if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+    maps.v = maps.k;
+    // The array keeps the previous call's contents: start from a clear status.
+    if (cudaMemsetAsync(scratch + L.status, 0, sizeof(DevStatus), stream) != cudaSuccess) return CRISP_ERR_CUDA;
+    return from_cuda(launch_proxy(s, maps, pmap, scratch, stream));
+  });
 }
 
 crisp_status crisp_noalloc_read_status(crisp_stream_t stream, crisp_status* status) {
-  if (!status) return CRISP_ERR_INVALID_ARG;
-  char* scratch = nullptr;
-  crisp_status st = noalloc_scratch(&scratch);
-  if (st != CRISP_OK) return st;
-  DevStatus host{};
-  if (cudaMemcpyAsync(&host, scratch, sizeof(host), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-      cudaStreamSynchronize(stream) != cudaSuccess)
-    return CRISP_ERR_CUDA;
-  *status = static_cast<crisp_status>(host.code);
-  return CRISP_OK;
+  return traced("crisp_noalloc_read_status", nullptr, [&]() -> crisp_status {
+    if (!status) return CRISP_ERR_INVALID_ARG;
+    char* scratch = nullptr;
+    crisp_status st = noalloc_scratch(&scratch);
+    if (st != CRISP_OK) return st;
+    DevStatus host{};
+    if (cudaMemcpyAsync(&host, scratch, sizeof(host), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+      return CRISP_ERR_CUDA;
+    *status = static_cast<crisp_status>(host.code);
+    return CRISP_OK;
+  });
 }
 
 crisp_status crisp_block_masses(const crisp_shape* shape, const float* pmap, uint64_t* vmass, uint64_t* smass,
                                 uint64_t* rmass, void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if (!pmap || !vmass || !smass || !rmass) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(pmap) || !aligned(vmass, 8) || !aligned(smass, 8) || !aligned(rmass, 8)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_block_masses(s, pmap, vmass, smass, rmass, static_cast<char*>(ws), stream));
+  return traced("crisp_block_masses", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if (!pmap || !vmass || !smass || !rmass) return CRISP_ERR_INVALID_ARG;
+    if (!aligned16(pmap) || !aligned(vmass, 8) || !aligned(smass, 8) || !aligned(rmass, 8)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    return from_cuda(launch_block_masses(s, pmap, vmass, smass, rmass, static_cast<char*>(ws), stream));
+  });
 }
 
 crisp_status crisp_proxy_masses(const crisp_shape* shape, const void* q, const void* k, uint64_t* vmass,
                                 uint64_t* smass, uint64_t* rmass, void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if (!q || !k || !vmass || !smass || !rmass) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned(vmass, 8) || !aligned(smass, 8) || !aligned(rmass, 8))
-    return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  TmaMaps maps;
-  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
-  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-  maps.v = maps.k;
-  return from_cuda(launch_proxy_masses(s, maps, vmass, smass, rmass, static_cast<char*>(ws), stream));
+  return traced("crisp_proxy_masses", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if (!q || !k || !vmass || !smass || !rmass) return CRISP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned(vmass, 8) || !aligned(smass, 8) || !aligned(rmass, 8))
+      return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    TmaMaps maps;
+    if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+    if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+    maps.v = maps.k;
+    return from_cuda(launch_proxy_masses(s, maps, vmass, smass, rmass, static_cast<char*>(ws), stream));
+  });
 }
 
 crisp_status crisp_route_cstruct(const crisp_shape* shape, const crisp_params* params, const float* pmap,
                                  uint64_t* cstruct, uint64_t* total, uint8_t* route, void* ws, size_t ws_bytes,
                                  crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if ((st = check_params(params)) != CRISP_OK) return st;
-  if (!pmap || !cstruct || !total || !route) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(pmap) || !aligned(cstruct, 8) || !aligned(total, 8)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_route_map(s, *params, pmap, cstruct, total, route, status_of(ws), stream));
+  return traced("crisp_route_cstruct", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if ((st = check_params(params)) != CRISP_OK) return st;
+    if (!pmap || !cstruct || !total || !route) return CRISP_ERR_INVALID_ARG;
+    if (!aligned16(pmap) || !aligned(cstruct, 8) || !aligned(total, 8)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    return from_cuda(launch_route_map(s, *params, pmap, cstruct, total, route, status_of(ws), stream));
+  });
 }
 
 crisp_status crisp_route_cstruct_masses(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
                                         const uint64_t* rmass, uint64_t* cstruct, uint64_t* total, uint8_t* route,
                                         void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if ((st = check_params(params)) != CRISP_OK) return st;
-  if ((st = check_block_slices(params)) != CRISP_OK) return st;
-  if (!vmass || !rmass || !cstruct || !total || !route) return CRISP_ERR_INVALID_ARG;
-  if (!aligned(vmass, 8) || !aligned(rmass, 8) || !aligned(cstruct, 8) || !aligned(total, 8)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_route(s, *params, vmass, rmass, cstruct, total, route, status_of(ws), stream));
+  return traced("crisp_route_cstruct_masses", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if ((st = check_params(params)) != CRISP_OK) return st;
+    if ((st = check_block_slices(params)) != CRISP_OK) return st;
+    if (!vmass || !rmass || !cstruct || !total || !route) return CRISP_ERR_INVALID_ARG;
+    if (!aligned(vmass, 8) || !aligned(rmass, 8) || !aligned(cstruct, 8) || !aligned(total, 8)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    return from_cuda(launch_route(s, *params, vmass, rmass, cstruct, total, route, status_of(ws), stream));
+  });
 }
 
 crisp_status crisp_route_jsd(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
                              const float* pbar, double* jsd, uint8_t* route, void* ws, size_t ws_bytes,
                              crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if ((st = check_params(params)) != CRISP_OK) return st;
-  if (!vmass || !pbar || !route) return CRISP_ERR_INVALID_ARG;
-  if (!aligned(vmass, 8) || !aligned(pbar, 4) || (jsd && !aligned(jsd, 8))) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_route_jsd(s, *params, vmass, pbar, jsd, route, status_of(ws), stream));
+  return traced("crisp_route_jsd", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if ((st = check_params(params)) != CRISP_OK) return st;
+    if (!vmass || !pbar || !route) return CRISP_ERR_INVALID_ARG;
+    if (!aligned(vmass, 8) || !aligned(pbar, 4) || (jsd && !aligned(jsd, 8))) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    return from_cuda(launch_route_jsd(s, *params, vmass, pbar, jsd, route, status_of(ws), stream));
+  });
 }
 
 crisp_status crisp_select_vs_masses(const crisp_shape* shape, const crisp_params* params, const uint64_t* vmass,
                                     const uint64_t* smass, const uint8_t* route, uint32_t* vbits, uint32_t* sbits,
                                     void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if ((st = check_params(params)) != CRISP_OK) return st;
-  if (!vmass || !smass || !route || !vbits || !sbits) return CRISP_ERR_INVALID_ARG;
-  if (!aligned(vmass, 8) || !aligned(smass, 8) || !aligned(vbits, 4) || !aligned(sbits, 4)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, status_of(ws), stream));
+  return traced("crisp_select_vs_masses", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if ((st = check_params(params)) != CRISP_OK) return st;
+    if (!vmass || !smass || !route || !vbits || !sbits) return CRISP_ERR_INVALID_ARG;
+    if (!aligned(vmass, 8) || !aligned(smass, 8) || !aligned(vbits, 4) || !aligned(sbits, 4)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, status_of(ws), stream));
+  });
 }
 
 crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_params* params, const float* pmap,
                              const uint8_t* route, uint64_t* vmass, uint64_t* smass, uint32_t* vbits,
                              uint32_t* sbits, void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if ((st = check_params(params)) != CRISP_OK) return st;
-  if (!pmap || !route || !vmass || !smass || !vbits || !sbits) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(pmap) || !aligned(vmass, 8) || !aligned(smass, 8) || !aligned(vbits, 4) || !aligned(sbits, 4))
-    return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  char* wsb = static_cast<char*>(ws);
-  auto* rmass = reinterpret_cast<uint64_t*>(wsb + scratch_layout(s).rmass);
-  if (launch_block_masses(s, pmap, vmass, smass, rmass, wsb, stream) != cudaSuccess) return CRISP_ERR_CUDA;
-  return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, status_of(ws), stream));
+  return traced("crisp_select_vs", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if ((st = check_params(params)) != CRISP_OK) return st;
+    if (!pmap || !route || !vmass || !smass || !vbits || !sbits) return CRISP_ERR_INVALID_ARG;
+    if (!aligned16(pmap) || !aligned(vmass, 8) || !aligned(smass, 8) || !aligned(vbits, 4) || !aligned(sbits, 4))
+      return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    char* wsb = static_cast<char*>(ws);
+    auto* rmass = reinterpret_cast<uint64_t*>(wsb + scratch_layout(s).rmass);
+    if (launch_block_masses(s, pmap, vmass, smass, rmass, wsb, stream) != cudaSuccess) return CRISP_ERR_CUDA;
+    return from_cuda(launch_select_vs(s, *params, vmass, smass, route, vbits, sbits, status_of(ws), stream));
+  });
 }
 
 crisp_status crisp_pe_pool(const crisp_shape* shape, const void* q, const void* k, const uint8_t* route, float* pbar,
                            void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if (!q || !k || !route || !pbar) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(pbar)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_pe_map(s, q, k, route, pbar, static_cast<char*>(ws), stream));
+  return traced("crisp_pe_pool", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if (!q || !k || !route || !pbar) return CRISP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(pbar)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    return from_cuda(launch_pe_map(s, q, k, route, pbar, static_cast<char*>(ws), stream));
+  });
 }
 
 crisp_status crisp_select_pe(const crisp_shape* shape, const crisp_params* params, const float* pbar,
                              const uint8_t* route, uint32_t* pebits, void* ws, size_t ws_bytes,
                              crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if ((st = check_params(params)) != CRISP_OK) return st;
-  if (!pbar || !route || !pebits) return CRISP_ERR_INVALID_ARG;
-  if (!aligned(pbar, 4) || !aligned(pebits, 4)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(launch_select_pe(s, *params, pbar, route, pebits, status_of(ws), stream));
+  return traced("crisp_select_pe", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if ((st = check_params(params)) != CRISP_OK) return st;
+    if (!pbar || !route || !pebits) return CRISP_ERR_INVALID_ARG;
+    if (!aligned(pbar, 4) || !aligned(pebits, 4)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    return from_cuda(launch_select_pe(s, *params, pbar, route, pebits, status_of(ws), stream));
+  });
 }
 
 crisp_status crisp_build_mask(const crisp_shape* shape, const uint8_t* route, const uint32_t* vbits,
                               const uint32_t* sbits, const uint32_t* pebits, uint32_t* rowbits, int32_t* counts,
                               int32_t* order, void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if (!route || !vbits || !sbits || !pebits || !rowbits || !counts || !order) return CRISP_ERR_INVALID_ARG;
-  if (!aligned(vbits, 4) || !aligned(sbits, 4) || !aligned(pebits, 4) || !aligned(rowbits, 4) ||
-      !aligned(counts, 4) || !aligned(order, 4))
-    return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  return from_cuda(
-      launch_build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, static_cast<char*>(ws), stream));
+  return traced("crisp_build_mask", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if (!route || !vbits || !sbits || !pebits || !rowbits || !counts || !order) return CRISP_ERR_INVALID_ARG;
+    if (!aligned(vbits, 4) || !aligned(sbits, 4) || !aligned(pebits, 4) || !aligned(rowbits, 4) ||
+        !aligned(counts, 4) || !aligned(order, 4))
+      return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    return from_cuda(
+        launch_build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, static_cast<char*>(ws), stream));
+  });
 }
 
 static crisp_status attention_common(const crisp_shape* shape, const void* q, const void* k, const void* v,
@@ -473,61 +536,69 @@ static crisp_status attention_common(const crisp_shape* shape, const void* q, co
 crisp_status crisp_sparse_prefill_mask(const crisp_shape* shape, const void* q, const void* k, const void* v,
                                        const uint32_t* rowbits, const int32_t* order, void* out, void* ws,
                                        size_t ws_bytes, crisp_stream_t stream) {
-  return attention_common(shape, q, k, v, rowbits, order, out, ws, ws_bytes, stream, false);
+  return traced("crisp_sparse_prefill_mask", shape, [&]() -> crisp_status {
+    return attention_common(shape, q, k, v, rowbits, order, out, ws, ws_bytes, stream, false);
+  });
 }
 
 crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v,
                                   const uint8_t* route, const uint32_t* vbits, const uint32_t* sbits,
                                   const uint32_t* pebits, void* out, void* ws, size_t ws_bytes,
                                   crisp_stream_t stream) {
-  crisp_status st = check_shape(shape);
-  if (st != CRISP_OK) return st;
-  if (!q || !k || !v || !out || !route || !vbits || !sbits || !pebits) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
-  if (!aligned(vbits, 4) || !aligned(sbits, 4) || !aligned(pebits, 4)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
-  if ((st = check_device()) != CRISP_OK) return st;
-  // A7 into the workspace, then A8 over that mask in its schedule.
-  char* wsb = static_cast<char*>(ws);
-  const ScratchLayout L = scratch_layout(s);
-  auto* rowbits = reinterpret_cast<uint32_t*>(wsb + L.rowbits);
-  auto* counts = reinterpret_cast<int32_t*>(wsb + L.counts);
-  auto* order = reinterpret_cast<int32_t*>(wsb + L.order);
-  TmaMaps maps;
-  if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
-  if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-  if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-  if (launch_build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, wsb, stream) != cudaSuccess)
-    return CRISP_ERR_CUDA;
-  return from_cuda(launch_attention(s, maps, rowbits, order, out, wsb, false, stream));
+  return traced("crisp_sparse_prefill", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape);
+    if (st != CRISP_OK) return st;
+    if (!q || !k || !v || !out || !route || !vbits || !sbits || !pebits) return CRISP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
+    if (!aligned(vbits, 4) || !aligned(sbits, 4) || !aligned(pebits, 4)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if ((st = check_ws(s, ws, ws_bytes)) != CRISP_OK) return st;
+    if ((st = check_device()) != CRISP_OK) return st;
+    // A7 into the workspace, then A8 over that mask in its schedule.
+    char* wsb = static_cast<char*>(ws);
+    const ScratchLayout L = scratch_layout(s);
+    auto* rowbits = reinterpret_cast<uint32_t*>(wsb + L.rowbits);
+    auto* counts = reinterpret_cast<int32_t*>(wsb + L.counts);
+    auto* order = reinterpret_cast<int32_t*>(wsb + L.order);
+    TmaMaps maps;
+    if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
+    if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+    if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+    if (launch_build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, wsb, stream) != cudaSuccess)
+      return CRISP_ERR_CUDA;
+    return from_cuda(launch_attention(s, maps, rowbits, order, out, wsb, false, stream));
+  });
 }
 
 crisp_status crisp_dense_prefill(const crisp_shape* shape, const void* q, const void* k, const void* v, void* out,
                                  void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  return attention_common(shape, q, k, v, nullptr, nullptr, out, ws, ws_bytes, stream, true);
+  return traced("crisp_dense_prefill", shape, [&]() -> crisp_status {
+    return attention_common(shape, q, k, v, nullptr, nullptr, out, ws, ws_bytes, stream, true);
+  });
 }
 
 crisp_status crisp_layer_views_get(const crisp_shape* shape, void* ws, crisp_layer_views* views) {
-  crisp_status st = check_shape(shape, 0);
-  if (st != CRISP_OK) return st;
-  if (!ws || !views) return CRISP_ERR_INVALID_ARG;
-  const LayerLayout L = layer_layout(*shape);
-  char* b = static_cast<char*>(ws);
-  views->vmass = reinterpret_cast<uint64_t*>(b + L.vmass);
-  views->smass = reinterpret_cast<uint64_t*>(b + L.smass);
-  views->rmass = reinterpret_cast<uint64_t*>(b + L.rmass);
-  views->cstruct = reinterpret_cast<uint64_t*>(b + L.cstruct);
-  views->total = reinterpret_cast<uint64_t*>(b + L.total_mass);
-  views->route = reinterpret_cast<uint8_t*>(b + L.route);
-  views->vbits = reinterpret_cast<uint32_t*>(b + L.vbits);
-  views->sbits = reinterpret_cast<uint32_t*>(b + L.sbits);
-  views->pbar = reinterpret_cast<float*>(b + L.pbar);
-  views->pebits = reinterpret_cast<uint32_t*>(b + L.pebits);
-  views->rowbits = reinterpret_cast<uint32_t*>(b + L.rowbits);
-  views->counts = reinterpret_cast<int32_t*>(b + L.counts);
-  views->order = reinterpret_cast<int32_t*>(b + L.order);
-  return CRISP_OK;
+  return traced("crisp_layer_views_get", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape, 0);
+    if (st != CRISP_OK) return st;
+    if (!ws || !views) return CRISP_ERR_INVALID_ARG;
+    const LayerLayout L = layer_layout(*shape);
+    char* b = static_cast<char*>(ws);
+    views->vmass = reinterpret_cast<uint64_t*>(b + L.vmass);
+    views->smass = reinterpret_cast<uint64_t*>(b + L.smass);
+    views->rmass = reinterpret_cast<uint64_t*>(b + L.rmass);
+    views->cstruct = reinterpret_cast<uint64_t*>(b + L.cstruct);
+    views->total = reinterpret_cast<uint64_t*>(b + L.total_mass);
+    views->route = reinterpret_cast<uint8_t*>(b + L.route);
+    views->vbits = reinterpret_cast<uint32_t*>(b + L.vbits);
+    views->sbits = reinterpret_cast<uint32_t*>(b + L.sbits);
+    views->pbar = reinterpret_cast<float*>(b + L.pbar);
+    views->pebits = reinterpret_cast<uint32_t*>(b + L.pebits);
+    views->rowbits = reinterpret_cast<uint32_t*>(b + L.rowbits);
+    views->counts = reinterpret_cast<int32_t*>(b + L.counts);
+    views->order = reinterpret_cast<int32_t*>(b + L.order);
+    return CRISP_OK;
+  });
 }
 
 }  // extern "C"
@@ -599,64 +670,70 @@ extern "C" {
 
 crisp_status crisp_prefill_layer(const crisp_shape* shape, const crisp_params* params, const void* q, const void* k,
                                  const void* v, void* out, void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  crisp_status st = check_shape(shape, 0);
-  if (st != CRISP_OK) return st;
-  if ((st = check_params(params)) != CRISP_OK) return st;
-  if ((st = check_block_slices(params)) != CRISP_OK) return st;
-  if (shape->seq_len == 0) return CRISP_OK;  // an empty input: nothing to compute
-  if (!q || !k || !v || !out) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if (!ws) return CRISP_ERR_WORKSPACE;
-  if (!aligned(ws, kAlign)) return CRISP_ERR_ALIGN;
-  if (ws_bytes < layer_layout(s).total) return CRISP_ERR_WORKSPACE;
-  if ((st = check_device()) != CRISP_OK) return st;
-  return run_layer(s, *params, q, k, v, out, ws, stream);
+  return traced("crisp_prefill_layer", shape, [&]() -> crisp_status {
+    crisp_status st = check_shape(shape, 0);
+    if (st != CRISP_OK) return st;
+    if ((st = check_params(params)) != CRISP_OK) return st;
+    if ((st = check_block_slices(params)) != CRISP_OK) return st;
+    if (shape->seq_len == 0) return CRISP_OK;  // an empty input: nothing to compute
+    if (!q || !k || !v || !out) return CRISP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if (!ws) return CRISP_ERR_WORKSPACE;
+    if (!aligned(ws, kAlign)) return CRISP_ERR_ALIGN;
+    if (ws_bytes < layer_layout(s).total) return CRISP_ERR_WORKSPACE;
+    if ((st = check_device()) != CRISP_OK) return st;
+    return run_layer(s, *params, q, k, v, out, ws, stream);
+  });
 }
 
 crisp_status crisp_host_pipeline_create(crisp_host_pipeline** pipeline) {
-  if (!pipeline) return CRISP_ERR_INVALID_ARG;
-  *pipeline = nullptr;
-  crisp_status st = check_device();
-  if (st != CRISP_OK) return st;
-  auto* p = new (std::nothrow) crisp_host_pipeline();
-  if (!p) return CRISP_ERR_CUDA;
-  bool ok = cudaGetDevice(&p->device) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&p->in, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&p->out, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&p->comp, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaEventCreateWithFlags(&p->start, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&p->comp_done, cudaEventDisableTiming) == cudaSuccess;
-  for (int i = 0; ok && i < crisp_host_pipeline::kRing; ++i)
-    ok = cudaEventCreateWithFlags(&p->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&p->ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
-  if (!ok) {
-    crisp_host_pipeline_destroy(p);
-    return CRISP_ERR_CUDA;
-  }
-  *pipeline = p;
-  return CRISP_OK;
+  return traced("crisp_host_pipeline_create", nullptr, [&]() -> crisp_status {
+    if (!pipeline) return CRISP_ERR_INVALID_ARG;
+    *pipeline = nullptr;
+    crisp_status st = check_device();
+    if (st != CRISP_OK) return st;
+    auto* p = new (std::nothrow) crisp_host_pipeline();
+    if (!p) return CRISP_ERR_CUDA;
+    bool ok = cudaGetDevice(&p->device) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p->in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p->out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p->comp, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p->start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p->comp_done, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < crisp_host_pipeline::kRing; ++i)
+      ok = cudaEventCreateWithFlags(&p->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&p->ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      crisp_host_pipeline_destroy(p);
+      return CRISP_ERR_CUDA;
+    }
+    *pipeline = p;
+    return CRISP_OK;
+  });
 }
 
 crisp_status crisp_host_pipeline_destroy(crisp_host_pipeline* p) {
-  if (!p) return CRISP_OK;
-  // Objects never created are null handles; destroying those is skipped.
-  if (p->in) cudaStreamSynchronize(p->in);
-  if (p->out) cudaStreamSynchronize(p->out);
-  if (p->comp) cudaStreamSynchronize(p->comp);
-  for (int i = 0; i < crisp_host_pipeline::kRing; ++i) {
-    if (p->ev_in[i]) cudaEventDestroy(p->ev_in[i]);
-    if (p->ev_comp[i]) cudaEventDestroy(p->ev_comp[i]);
-  }
-  if (p->start) cudaEventDestroy(p->start);
-  if (p->done) cudaEventDestroy(p->done);
-  if (p->comp_done) cudaEventDestroy(p->comp_done);
-  if (p->comp) cudaStreamDestroy(p->comp);
-  if (p->in) cudaStreamDestroy(p->in);
-  if (p->out) cudaStreamDestroy(p->out);
-  delete p;
-  return CRISP_OK;
+  return traced("crisp_host_pipeline_destroy", nullptr, [&]() -> crisp_status {
+    if (!p) return CRISP_OK;
+    // Objects never created are null handles; destroying those is skipped.
+    if (p->in) cudaStreamSynchronize(p->in);
+    if (p->out) cudaStreamSynchronize(p->out);
+    if (p->comp) cudaStreamSynchronize(p->comp);
+    for (int i = 0; i < crisp_host_pipeline::kRing; ++i) {
+      if (p->ev_in[i]) cudaEventDestroy(p->ev_in[i]);
+      if (p->ev_comp[i]) cudaEventDestroy(p->ev_comp[i]);
+    }
+    if (p->start) cudaEventDestroy(p->start);
+    if (p->done) cudaEventDestroy(p->done);
+    if (p->comp_done) cudaEventDestroy(p->comp_done);
+    if (p->comp) cudaStreamDestroy(p->comp);
+    if (p->in) cudaStreamDestroy(p->in);
+    if (p->out) cudaStreamDestroy(p->out);
+    delete p;
+    return CRISP_OK;
+  });
 }
 
 }  // extern "C"
@@ -680,90 +757,92 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
                                       const crisp_params* params, const void* q_host, const void* k_host,
                                       const void* v_host, void* out_host, void* q, void* k, void* v, void* out,
                                       void* ws, size_t ws_bytes, crisp_stream_t stream) {
-  if (!pipeline) return CRISP_ERR_INVALID_ARG;
-  crisp_status st = check_shape(shape, 0);
-  if (st != CRISP_OK) return st;
-  if ((st = check_params(params)) != CRISP_OK) return st;
-  if ((st = check_block_slices(params)) != CRISP_OK) return st;
-  if (shape->seq_len == 0) return CRISP_OK;  // an empty input: nothing to compute
-  if (!q_host || !k_host || !v_host || !out_host || !q || !k || !v || !out) return CRISP_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
-  const crisp_shape s = normalised(*shape);
-  if (!contiguous(s)) return CRISP_ERR_SHAPE;
-  if (!ws) return CRISP_ERR_WORKSPACE;
-  if (!aligned(ws, kAlign)) return CRISP_ERR_ALIGN;
-  if (ws_bytes < layer_layout(s).total) return CRISP_ERR_WORKSPACE;
-  if ((st = check_device()) != CRISP_OK) return st;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev != pipeline->device) return CRISP_ERR_DEVICE;
+  return traced("crisp_prefill_layer_host", shape, [&]() -> crisp_status {
+    if (!pipeline) return CRISP_ERR_INVALID_ARG;
+    crisp_status st = check_shape(shape, 0);
+    if (st != CRISP_OK) return st;
+    if ((st = check_params(params)) != CRISP_OK) return st;
+    if ((st = check_block_slices(params)) != CRISP_OK) return st;
+    if (shape->seq_len == 0) return CRISP_OK;  // an empty input: nothing to compute
+    if (!q_host || !k_host || !v_host || !out_host || !q || !k || !v || !out) return CRISP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CRISP_ERR_ALIGN;
+    const crisp_shape s = normalised(*shape);
+    if (!contiguous(s)) return CRISP_ERR_SHAPE;
+    if (!ws) return CRISP_ERR_WORKSPACE;
+    if (!aligned(ws, kAlign)) return CRISP_ERR_ALIGN;
+    if (ws_bytes < layer_layout(s).total) return CRISP_ERR_WORKSPACE;
+    if ((st = check_device()) != CRISP_OK) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != pipeline->device) return CRISP_ERR_DEVICE;
 
-  // The layer in chunks of query heads within a kv group, the group's K and
-  // V uploaded with its first chunk: the upload of chunk c+1 and the
-  // download of chunk c-1 overlap the compute of chunk c, and consecutive
-  // chunks alternate between two compute streams (each with its own part of
-  // the workspace), so that one chunk's short selection kernels run beside
-  // the previous chunk's attention. Long sequences use half a group per
-  // chunk (when G is even), and the first and last half groups of the layer
-  // go one head at a time, so that the pipeline fills and drains with a
-  // single head; shorter ones a whole group per chunk, where the extra
-  // launches and copies would cost more than the shorter fill.
-  const int G = s.hq / s.hkv;
-  const int hc = (G % 2 == 0 && s.seq_len >= kHalfGroupChunkLen) ? G / 2 : G;  // query heads per chunk
-  const size_t plane = static_cast<size_t>(s.seq_len) * kD * 2;  // bytes of one head
-  crisp_shape sub = s;
-  sub.hq = hc;
-  sub.hkv = 1;
-  auto* p = pipeline;
-  cudaStream_t cs = stream;
-  auto cb = [](const void* b, size_t off) { return static_cast<const char*>(b) + off; };
-  auto mb = [](void* b, size_t off) { return static_cast<char*>(b) + off; };
-  // Two compute streams, each with its own part of the workspace, when it
-  // holds two chunks' intermediates and there are several chunks.
-  const size_t sub_bytes = up(layer_layout(sub).total);
-  const bool dual = hc < s.hq && 2 * sub_bytes <= ws_bytes;
-  void* ws1 = static_cast<char*>(ws) + sub_bytes;
-  // Work already on `stream` (earlier users of these buffers) comes first.
-  if (cudaEventRecord(p->start, cs) != cudaSuccess || cudaStreamWaitEvent(p->in, p->start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(p->out, p->start, 0) != cudaSuccess ||
-      (dual && (cudaStreamWaitEvent(p->comp, p->start, 0) != cudaSuccess ||
-                cudaMemsetAsync(ws1, 0, sizeof(DevStatus), p->comp) != cudaSuccess)))
-    return CRISP_ERR_CUDA;
-  const bool split_ends = hc > 1 && s.seq_len >= kHalfGroupChunkLen;
-  int c = 0;
-  for (int h0 = 0; h0 < s.hq; ++c) {
-    const int size = (split_ends && (h0 < hc || h0 >= s.hq - hc)) ? 1 : hc;  // heads in this chunk
-    sub.hq = size;
-    const int e = c % crisp_host_pipeline::kRing;
-    const int g = h0 / G;  // the chunk's kv group
-    const size_t kv_off = static_cast<size_t>(g) * plane, q_off = static_cast<size_t>(h0) * plane;
-    if (h0 % G == 0 &&
-        (cudaMemcpyAsync(mb(k, kv_off), cb(k_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
-         cudaMemcpyAsync(mb(v, kv_off), cb(v_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess))
+    // The layer in chunks of query heads within a kv group, the group's K and
+    // V uploaded with its first chunk: the upload of chunk c+1 and the
+    // download of chunk c-1 overlap the compute of chunk c, and consecutive
+    // chunks alternate between two compute streams (each with its own part of
+    // the workspace), so that one chunk's short selection kernels run beside
+    // the previous chunk's attention. Long sequences use half a group per
+    // chunk (when G is even), and the first and last half groups of the layer
+    // go one head at a time, so that the pipeline fills and drains with a
+    // single head; shorter ones a whole group per chunk, where the extra
+    // launches and copies would cost more than the shorter fill.
+    const int G = s.hq / s.hkv;
+    const int hc = (G % 2 == 0 && s.seq_len >= kHalfGroupChunkLen) ? G / 2 : G;  // query heads per chunk
+    const size_t plane = static_cast<size_t>(s.seq_len) * kD * 2;  // bytes of one head
+    crisp_shape sub = s;
+    sub.hq = hc;
+    sub.hkv = 1;
+    auto* p = pipeline;
+    cudaStream_t cs = stream;
+    auto cb = [](const void* b, size_t off) { return static_cast<const char*>(b) + off; };
+    auto mb = [](void* b, size_t off) { return static_cast<char*>(b) + off; };
+    // Two compute streams, each with its own part of the workspace, when it
+    // holds two chunks' intermediates and there are several chunks.
+    const size_t sub_bytes = up(layer_layout(sub).total);
+    const bool dual = hc < s.hq && 2 * sub_bytes <= ws_bytes;
+    void* ws1 = static_cast<char*>(ws) + sub_bytes;
+    // Work already on `stream` (earlier users of these buffers) comes first.
+    if (cudaEventRecord(p->start, cs) != cudaSuccess || cudaStreamWaitEvent(p->in, p->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(p->out, p->start, 0) != cudaSuccess ||
+        (dual && (cudaStreamWaitEvent(p->comp, p->start, 0) != cudaSuccess ||
+                  cudaMemsetAsync(ws1, 0, sizeof(DevStatus), p->comp) != cudaSuccess)))
       return CRISP_ERR_CUDA;
-    cudaStream_t sc = (dual && (c & 1)) ? p->comp : cs;
-    void* wsc = (dual && (c & 1)) ? ws1 : ws;
-    if (cudaMemcpyAsync(mb(q, q_off), cb(q_host, q_off), size * plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
-        cudaEventRecord(p->ev_in[e], p->in) != cudaSuccess || cudaStreamWaitEvent(sc, p->ev_in[e], 0) != cudaSuccess)
+    const bool split_ends = hc > 1 && s.seq_len >= kHalfGroupChunkLen;
+    int c = 0;
+    for (int h0 = 0; h0 < s.hq; ++c) {
+      const int size = (split_ends && (h0 < hc || h0 >= s.hq - hc)) ? 1 : hc;  // heads in this chunk
+      sub.hq = size;
+      const int e = c % crisp_host_pipeline::kRing;
+      const int g = h0 / G;  // the chunk's kv group
+      const size_t kv_off = static_cast<size_t>(g) * plane, q_off = static_cast<size_t>(h0) * plane;
+      if (h0 % G == 0 &&
+          (cudaMemcpyAsync(mb(k, kv_off), cb(k_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+           cudaMemcpyAsync(mb(v, kv_off), cb(v_host, kv_off), plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess))
+        return CRISP_ERR_CUDA;
+      cudaStream_t sc = (dual && (c & 1)) ? p->comp : cs;
+      void* wsc = (dual && (c & 1)) ? ws1 : ws;
+      if (cudaMemcpyAsync(mb(q, q_off), cb(q_host, q_off), size * plane, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+          cudaEventRecord(p->ev_in[e], p->in) != cudaSuccess || cudaStreamWaitEvent(sc, p->ev_in[e], 0) != cudaSuccess)
+        return CRISP_ERR_CUDA;
+      if ((st = run_layer(sub, *params, mb(q, q_off), mb(k, kv_off), mb(v, kv_off), mb(out, q_off), wsc, sc)) !=
+          CRISP_OK)
+        return st;
+      if (cudaEventRecord(p->ev_comp[e], sc) != cudaSuccess || cudaStreamWaitEvent(p->out, p->ev_comp[e], 0) != cudaSuccess ||
+          cudaMemcpyAsync(mb(out_host, q_off), cb(out, q_off), size * plane, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
+        return CRISP_ERR_CUDA;
+      h0 += size;
+    }
+    // `stream` completes after the last download, with the second compute
+    // stream's status folded into the caller's.
+    if (dual) {
+      if (cudaEventRecord(p->comp_done, p->comp) != cudaSuccess || cudaStreamWaitEvent(cs, p->comp_done, 0) != cudaSuccess)
+        return CRISP_ERR_CUDA;
+      merge_status_kernel<<<1, 1, 0, cs>>>(static_cast<DevStatus*>(ws), static_cast<const DevStatus*>(ws1));
+      if (cudaGetLastError() != cudaSuccess) return CRISP_ERR_CUDA;
+    }
+    if (cudaEventRecord(p->done, p->out) != cudaSuccess || cudaStreamWaitEvent(cs, p->done, 0) != cudaSuccess)
       return CRISP_ERR_CUDA;
-    if ((st = run_layer(sub, *params, mb(q, q_off), mb(k, kv_off), mb(v, kv_off), mb(out, q_off), wsc, sc)) !=
-        CRISP_OK)
-      return st;
-    if (cudaEventRecord(p->ev_comp[e], sc) != cudaSuccess || cudaStreamWaitEvent(p->out, p->ev_comp[e], 0) != cudaSuccess ||
-        cudaMemcpyAsync(mb(out_host, q_off), cb(out, q_off), size * plane, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
-      return CRISP_ERR_CUDA;
-    h0 += size;
-  }
-  // `stream` completes after the last download, with the second compute
-  // stream's status folded into the caller's.
-  if (dual) {
-    if (cudaEventRecord(p->comp_done, p->comp) != cudaSuccess || cudaStreamWaitEvent(cs, p->comp_done, 0) != cudaSuccess)
-      return CRISP_ERR_CUDA;
-    merge_status_kernel<<<1, 1, 0, cs>>>(static_cast<DevStatus*>(ws), static_cast<const DevStatus*>(ws1));
-    if (cudaGetLastError() != cudaSuccess) return CRISP_ERR_CUDA;
-  }
-  if (cudaEventRecord(p->done, p->out) != cudaSuccess || cudaStreamWaitEvent(cs, p->done, 0) != cudaSuccess)
-    return CRISP_ERR_CUDA;
-  return CRISP_OK;
+    return CRISP_OK;
+  });
 }
 
 }  // extern "C"
@@ -792,21 +871,25 @@ __global__ void wait_selftest_kernel(DevStatus* status, unsigned long long limit
 extern "C" {
 
 crisp_status crisp_wait_selftest(void* ws, size_t ws_bytes, int64_t limit_ns, crisp_stream_t stream) {
-  if (!ws || ws_bytes < sizeof(DevStatus)) return CRISP_ERR_WORKSPACE;
-  if (limit_ns <= 0 || limit_ns > 10000000000ll) return CRISP_ERR_INVALID_ARG;
-  crisp_status st = check_device();
-  if (st != CRISP_OK) return st;
-  wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<DevStatus*>(ws), static_cast<unsigned long long>(limit_ns));
-  return from_cuda(cudaGetLastError());
+  return traced("crisp_wait_selftest", nullptr, [&]() -> crisp_status {
+    if (!ws || ws_bytes < sizeof(DevStatus)) return CRISP_ERR_WORKSPACE;
+    if (limit_ns <= 0 || limit_ns > 10000000000ll) return CRISP_ERR_INVALID_ARG;
+    crisp_status st = check_device();
+    if (st != CRISP_OK) return st;
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<DevStatus*>(ws), static_cast<unsigned long long>(limit_ns));
+    return from_cuda(cudaGetLastError());
+  });
 }
 
 crisp_status crisp_read_status(const void* ws, crisp_stream_t stream, crisp_status* status) {
-  if (!ws || !status) return CRISP_ERR_INVALID_ARG;
-  DevStatus host{};
-  if (cudaMemcpyAsync(&host, ws, sizeof(host), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return CRISP_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return CRISP_ERR_CUDA;
-  *status = static_cast<crisp_status>(host.code);
-  return CRISP_OK;
+  return traced("crisp_read_status", nullptr, [&]() -> crisp_status {
+    if (!ws || !status) return CRISP_ERR_INVALID_ARG;
+    DevStatus host{};
+    if (cudaMemcpyAsync(&host, ws, sizeof(host), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return CRISP_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return CRISP_ERR_CUDA;
+    *status = static_cast<crisp_status>(host.code);
+    return CRISP_OK;
+  });
 }
 
 const char* crisp_status_string(crisp_status status) {

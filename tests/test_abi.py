@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 
@@ -97,6 +98,21 @@ def test_checking_build_exports_every_declared_symbol():
     exported = set(re.findall(r"\bT (crisp_\w+)", out))
     assert not [n for n in declared_functions() if n not in exported]
     assert crisp.load_library(path).crisp_status_string(8) == b"device index outside its buffer (bounds-checking build)"
+
+
+def test_crisp_log_reports_calls_and_statuses(L):
+    # CRISP_LOG=1: every entry point writes its name, shape and returned
+    # status to stderr (here argument errors, no device needed).
+    code = ("import ctypes, dynamic_sparse_prefill_crisp_gb300 as c; L = c.lib(); s = c.make_shape(8, 4, 1024); "
+            "s.head_dim = 64; n = ctypes.c_size_t(); L.crisp_workspace_size(ctypes.byref(s), ctypes.byref(n)); "
+            "L.crisp_read_status(None, None, None)")
+    env = dict(os.environ, CRISP_LOG="1", PYTHONPATH=ROOT)
+    err = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT).stderr
+    assert "[crisp] crisp_workspace_size hq=8 hkv=4 n=1024 -> 2 (unsupported shape)" in err, err
+    assert "[crisp] crisp_read_status -> 1 (invalid argument)" in err, err
+    env.pop("CRISP_LOG")
+    err = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT).stderr
+    assert "[crisp]" not in err
 
 
 def test_params_default_is_the_universal_configuration(L):
