@@ -15,11 +15,11 @@
 // The reference max m is the first block's exact row max and is raised
 // lazily after that: each later block is exponentiated at the current m and
 // stored chunk by chunk, with no agreement between the two warps of a row;
-// only a warp that finds some chunk's row sum past 2^8 (so possibly one
-// p > 2^8) holds back, waits for its partner's P, moves m to the max of its
+// only a warp that finds some chunk's row sum past 2^16 (so possibly one
+// p > 2^16) holds back, waits for its partner's P, moves m to the max of its
 // unstored scores, rescales the row's stored P, O and its row sum, and
 // recomputes the rest; the partner follows the new m at its next block.
-// Every p stays <= 2^8 and O/l is exact.
+// Every p stays <= 2^16 and O/l is exact.
 //
 // Warp roles: 0-7 softmax + epilogue (warp w owns TMEM lanes / rows
 // 32*(w%4)..+31 and columns 64*(w/4)..+63), 8 TMA producer, 9 MMA issuer (and
@@ -41,7 +41,7 @@ constexpr uint32_t kTile = kB * kD * 2;  // 32 KB bf16 tile
 constexpr uint32_t kHalf = kTile / 2;
 constexpr uint32_t kSmemBytes = 1024 + 3 * kTile;  // Q, K, V (+ alignment slack)
 constexpr uint32_t kTmemCols = 256;                // S/P [0,128), O [128,256)
-constexpr float kRescaleSum = 256.0f;  // 2^8: the largest chunk row sum kept at the current reference
+constexpr float kRescaleSum = 65536.0f;  // 2^16: the largest chunk row sum kept at the current reference
 
 struct Bars {
   uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, drain;
@@ -129,7 +129,7 @@ struct RowState {
 
 // A new reference for the rows of lane quarter `quarter` (rare; out of line so
 // that the common loop keeps its registers). Called by a warp in whose block
-// some p would pass 2^8 (a chunk row sum past 2^8), or whose rows' reference
+// some p would pass 2^16 (a chunk row sum past 2^16), or whose rows' reference
 // the other warp moved in the last block, once the other warp of the rows has
 // stored its P (qdone). The warp's scores are in TMEM: chunk 0 at columns
 // 0..31, chunk 1 (put back) at 32..63. The rows' new reference is the max of
@@ -137,10 +137,10 @@ struct RowState {
 // exchange it through xmax and each fixes its own columns); otherwise this
 // warp also rescales the other warp's P and O columns (TMEM lanes belong to
 // the quarter, so it can) and the other warp follows the new reference (mrow)
-// at its next block. The other warp's stored P holds p <= 2^8 at the old
+// at its next block. The other warp's stored P holds p <= 2^16 at the old
 // reference and is rescaled in place by f = 2^(m_old - m_new); this warp's P
 // is formed again from its scores (chunk 1 first: its P goes over chunk 1's
-// own scores, chunk 0's over chunk 1's first half). Every p stays below 2^8
+// own scores, chunk 0's over chunk 1's first half). Every p stays below 2^16
 // and O/l is exact. Returns the new reference and the row sum with this
 // block's part.
 __device__ __noinline__ RowState new_reference(RowState st, uint32_t tmem, uint32_t lane_addr, int half, int r,
@@ -446,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       // as soon as it is formed, without waiting for the other warp of the
       // row and without a test first. P goes over chunk 1's scores (columns
       // 32..63): chunk 0's P once chunk 1's scores are in registers, chunk
-      // 1's right after. A block in which some chunk row sum passes 2^8 (any
-      // p that could pass 2^8, or a non-finite value), or whose reference
+      // 1's right after. A block in which some chunk row sum passes 2^16 (any
+      // p that could pass 2^16, or a non-finite value), or whose reference
       // the other warp moved in the last block, takes the slow path below
       // with chunk 0's scores still in TMEM and chunk 1's put back from
       // registers.

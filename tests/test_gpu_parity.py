@@ -280,7 +280,10 @@ def test_attention_reference_rises_block_after_block(window):
     q = 8.0 * u + 0.05 * rng.standard_normal((hq, n, 128))
     t = np.arange(n) % B
     kb = np.arange(n) // B
-    amp = 3.0 * kb + np.where((t >= window[0]) & (t < window[1]), 6.0, 0.0)
+    # log2 units per raw unit here: 8 * 0.0884 * 1.4427 = 1.02, so each block's
+    # window sits 9.2 above the last one's; the window's chunk sum passes 2^16
+    # two blocks after the reference was set, so every second block is redone
+    amp = 9.0 * kb + np.where((t >= window[0]) & (t < window[1]), 6.0, 0.0)
     k = amp[None, :, None] * u + 0.05 * rng.standard_normal((hkv, n, 128))
     v = rng.standard_normal((hkv, n, 128))
     to_bits = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).view(torch.int16) \
