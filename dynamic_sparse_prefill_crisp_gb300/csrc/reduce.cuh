@@ -132,4 +132,81 @@ __device__ __forceinline__ uint64_t radix_max_key(int len, KeyFn key_of, WeightF
   return prefix;
 }
 
+// The same search by one warp on its own (no block barrier): `hist` is the
+// warp's own 256 entries; weight_of(c, key) is given the key already formed.
+// Every lane of the warp calls it with the same arguments and gets the
+// result.
+template <typename KeyFn, typename WeightFn, typename EligFn, typename ReachFn>
+__device__ __forceinline__ uint64_t warp_radix_max_key(int len, KeyFn key_of, WeightFn weight_of, EligFn eligible,
+                                                       ReachFn reach, unsigned long long* hist) {
+  constexpr unsigned long long kOne = 1ull << 40, kWeight = kOne - 1;
+  const int lane = threadIdx.x & 31;
+  uint64_t prefix = 0;
+  unsigned long long above = 0;
+  for (int shift = 40; shift >= 0; shift -= 8) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) hist[lane + 32 * k] = 0ull;
+    __syncwarp();
+    unsigned long long w0 = 0;
+    for (int c = lane; c < len; c += 32) {
+      if (!eligible(c)) continue;
+      const uint64_t key = key_of(c);
+      if ((key >> (shift + 8)) != prefix) continue;
+      const int d = static_cast<int>((key >> shift) & 255u);
+      const unsigned long long w = kOne + weight_of(c, key);
+      if (d == 0)
+        w0 += w;
+      else
+        atomicAdd(&hist[d], w);
+    }
+    w0 = warp_sum(w0);
+    __syncwarp();
+    if (lane == 0) hist[0] = w0;  // digit 0 takes no atomics
+    __syncwarp();
+    unsigned long long v[8], cnt[8], mine = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const unsigned long long e = hist[255 - 8 * lane - k];
+      v[k] = e & kWeight;
+      cnt[k] = e >> 40;
+      mine += v[k];
+    }
+    unsigned long long before = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(0xffffffffu, before, o);
+      if (lane >= o) before += t;
+    }
+    before -= mine;
+    unsigned long long run = above + before, run_above = 0, found_cnt = 0;
+    int found = -1;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (found < 0 && reach(run + v[k])) {
+        found = 255 - 8 * lane - k;
+        run_above = run;
+        found_cnt = cnt[k];
+      }
+      run += v[k];
+    }
+    const unsigned int hits = __ballot_sync(0xffffffffu, found >= 0);
+    const int first = hits ? __ffs(hits) - 1 : 31;
+    const int digit = __shfl_sync(0xffffffffu, found >= 0 ? found : 0, first);
+    const unsigned long long new_above = __shfl_sync(0xffffffffu, found >= 0 ? run_above : above, first);
+    const unsigned long long single = __shfl_sync(0xffffffffu, found >= 0 ? found_cnt : 0ull, first);
+    prefix = (prefix << 8) | static_cast<uint64_t>(digit);
+    above = new_above;
+    if (single == 1ull && shift > 0) {
+      uint64_t x = 0;
+      for (int c = lane; c < len; c += 32)
+        if (eligible(c) && (key_of(c) >> shift) == prefix) x = key_of(c);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x |= __shfl_xor_sync(0xffffffffu, x, o);
+      return x;
+    }
+    __syncwarp();  // every lane has read hist before the next pass clears it
+  }
+  return prefix;
+}
+
 }  // namespace crisp
