@@ -113,18 +113,19 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
   }
 }
 
-// Pooled logits in log2 units on the lower triangle (c <= b) of 64x64 tiles:
-// items (PE head h, tile t) with t over the T(T+1)/2 tiles (bt, ct <= bt),
-// grid-stride like pool_kernel. Each of 256 threads computes 4x4 outputs from
-// 32-deep slabs (float4 reads of both operands, two fp32 fmas per
-// instruction). Entries above the diagonal are left to pooled_softmax, which
-// writes whole rows.
-constexpr int kPT = 64;
-__global__ void __launch_bounds__(256) pooled_scores(const float* __restrict__ qbar, const float* __restrict__ kbar,
-                                                     const uint8_t* __restrict__ route, int hq, int nb, int group,
-                                                     float c_log2, float* __restrict__ pbar, DevStatus* status) {
-  __shared__ __align__(16) float As[32][kPT + 4];
-  __shared__ __align__(16) float Bs[32][kPT + 4];
+// Pooled logits in log2 units on the lower triangle (c <= b) of 128x128
+// tiles: items (PE head h, tile t) with t over the T(T+1)/2 tiles (bt, ct <=
+// bt), grid-stride like pool_kernel. Each of 256 threads computes 8x8 outputs
+// (two 4x4 quadrants) from 16-deep slabs, double-buffered in shared memory:
+// float4 reads of both operands, two fp32 fmas per instruction, the features
+// added in ascending order. Entries above the diagonal are left to
+// pooled_softmax, which writes whole rows.
+constexpr int kPT = 128, kKS = 16;  // tile edge, depth of a shared-memory slab
+__global__ void __launch_bounds__(256, 2) pooled_scores(const float* __restrict__ qbar, const float* __restrict__ kbar,
+                                                        const uint8_t* __restrict__ route, int hq, int nb, int group,
+                                                        float c_log2, float* __restrict__ pbar, DevStatus* status) {
+  __shared__ __align__(16) float As[2][kKS][kPT + 4];
+  __shared__ __align__(16) float Bs[2][kKS][kPT + 4];
   const int T = (nb + kPT - 1) / kPT;
   const int64_t per_head = static_cast<int64_t>(T) * (T + 1) / 2;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -142,35 +143,67 @@ __global__ void __launch_bounds__(256) pooled_scores(const float* __restrict__ q
       float* out = pbar + static_cast<size_t>(h) * nb * nb;
       const float* A = qbar + static_cast<size_t>(h) * nb * kD;
       const float* Bm = kbar + static_cast<size_t>(h / group) * nb * kD;
-      float acc[4][4] = {};
-      for (int d0 = 0; d0 < kD; d0 += 32) {
-        __syncthreads();  // the previous slab (or item) has been read
-        for (int e = threadIdx.x; e < 32 * kPT; e += 256) {
-          const int row = e / 32, dd = e % 32;
+      // Slab loads: thread f reads 4 consecutive features of row f / 4 (and of
+      // row 64 + f / 4) of both operands with float4 loads.
+      float4 ra[2], rb[2];
+      auto load = [&](int d0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int f = threadIdx.x + 256 * u, row = f >> 2, quad = f & 3;
           const int b = bt * kPT + row, c = ct * kPT + row;
-          As[dd][row] = b < nb ? A[static_cast<size_t>(b) * kD + d0 + dd] : 0.f;
-          Bs[dd][row] = c < nb ? Bm[static_cast<size_t>(c) * kD + d0 + dd] : 0.f;
+          ra[u] = b < nb ? *reinterpret_cast<const float4*>(A + static_cast<size_t>(b) * kD + d0 + 4 * quad)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+          rb[u] = c < nb ? *reinterpret_cast<const float4*>(Bm + static_cast<size_t>(c) * kD + d0 + 4 * quad)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        __syncthreads();
-#pragma unroll 8
-        for (int dd = 0; dd < 32; ++dd) {
-          const float4 a = *reinterpret_cast<const float4*>(&As[dd][ty * 4]);
-          const float4 bb = *reinterpret_cast<const float4*>(&Bs[dd][tx * 4]);
-          const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {bb.x, bb.y, bb.z, bb.w};
+      };
+      auto store = [&](int buf) {
 #pragma unroll
-          for (int r = 0; r < 4; ++r)
+        for (int u = 0; u < 2; ++u) {
+          const int f = threadIdx.x + 256 * u, row = f >> 2, quad = f & 3;
+          As[buf][4 * quad + 0][row] = ra[u].x;
+          As[buf][4 * quad + 1][row] = ra[u].y;
+          As[buf][4 * quad + 2][row] = ra[u].z;
+          As[buf][4 * quad + 3][row] = ra[u].w;
+          Bs[buf][4 * quad + 0][row] = rb[u].x;
+          Bs[buf][4 * quad + 1][row] = rb[u].y;
+          Bs[buf][4 * quad + 2][row] = rb[u].z;
+          Bs[buf][4 * quad + 3][row] = rb[u].w;
+        }
+      };
+      // Rows ty*4 .. +3 and 64 + ty*4 .. +3, columns tx*4 .. +3 and 64 + tx*4 .. +3.
+      float acc[8][8] = {};
+      __syncthreads();  // the previous item's last slab has been read
+      load(0);
+      store(0);
+      __syncthreads();
+      for (int sl = 0; sl < kD / kKS; ++sl) {
+        const int buf = sl & 1;
+        if (sl + 1 < kD / kKS) load((sl + 1) * kKS);
 #pragma unroll
-            for (int j = 0; j < 4; j += 2)
+        for (int kk = 0; kk < kKS; ++kk) {
+          const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+          const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+          const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+          const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
+          const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int j = 0; j < 8; j += 2)
               ptx::ffma2(acc[r][j], acc[r][j + 1], av[r], av[r], bv[j], bv[j + 1], acc[r][j], acc[r][j + 1]);
         }
+        if (sl + 1 < kD / kKS) store(buf ^ 1);  // the other buffer was last read before the previous barrier
+        __syncthreads();
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int b = bt * kPT + ty * 4 + r;
+      for (int r = 0; r < 8; ++r) {
+        const int b = bt * kPT + (r < 4 ? ty * 4 + r : 64 + ty * 4 + r - 4);
         if (b >= nb) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int c = ct * kPT + tx * 4 + j;
+        for (int j = 0; j < 8; ++j) {
+          const int c = ct * kPT + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
           if (c <= b) out[static_cast<size_t>(b) * nb + c] = acc[r][j] * c_log2;
         }
       }

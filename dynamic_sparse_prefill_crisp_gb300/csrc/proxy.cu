@@ -253,14 +253,20 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
           if (m_run != -INFINITY) {
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 32; ++e) s4[e & 3] += ex2_approx(__fmaf_rn(x[e], c_log2, -m_run));
+            for (int e = 0; e < 32; e += 4) {
+              float y[4];
+              ffma2(y[0], y[1], x[e], x[e + 1], c_log2, c_log2, -m_run, -m_run);
+              ffma2(y[2], y[3], x[e + 2], x[e + 3], c_log2, c_log2, -m_run, -m_run);
+              fadd2_acc(s4[0], s4[1], ex2_approx(y[0]), ex2_approx(y[1]));
+              fadd2_acc(s4[2], s4[3], ex2_approx(y[2]), ex2_approx(y[3]));
+            }
             l_run += (s4[0] + s4[1]) + (s4[2] + s4[3]);
           }
         } else {
           // The base-2 exponent c_log2*S - M as one fma, so the map write
           // and the fused masses evaluate p = 2^(c_log2*S - M) / L alike.
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = __fmaf_rn(x[e], c_log2, -M);
+          for (int e = 0; e < 32; e += 2) ffma2(x[e], x[e + 1], x[e], x[e + 1], c_log2, c_log2, -M, -M);
         }
         if (kMode == kWriteMap) {
           // Row `lane` of this warp's 32x32 block into the transpose buffer
@@ -292,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
           // xq = p * 2^32 for the p the map write stores.
           float xq[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) xq[e] = ex2_approx(x[e]) * inv_l32;
+          for (int e = 0; e < 32; e += 2)
+            fmul2(xq[e], xq[e + 1], ex2_approx(x[e]), ex2_approx(x[e + 1]), inv_l32, inv_l32);
           float t[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) t[i] = fmax3(xq[4 * i], xq[4 * i + 1], fmaxf(xq[4 * i + 2], xq[4 * i + 3]));
@@ -314,11 +321,20 @@ __global__ void __launch_bounds__(kThreads, ProxyCfg<kMode>::kCtasPerSm)
             // the true sums stay below 2^28).
             uint32_t a4[4] = {0u, 0u, 0u, 0u}, lo = 0, hi = 0;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const uint32_t u = __float_as_uint(xq[e] + kTwo23);
-              a4[e & 3] += u;
-              if (lo_part) lo += e - lane <= th_lo ? u : 0x4B000000u;
-              if (hi_part) hi += e - lane > th_hi ? u : 0x4B000000u;
+            for (int e = 0; e < 32; e += 2) {
+              float t0, t1;
+              fadd2(t0, t1, xq[e], xq[e + 1], kTwo23, kTwo23);
+              const uint32_t u0 = __float_as_uint(t0), u1 = __float_as_uint(t1);
+              a4[e & 3] += u0;
+              a4[(e + 1) & 3] += u1;
+              if (lo_part) {
+                lo += e - lane <= th_lo ? u0 : 0x4B000000u;
+                lo += e + 1 - lane <= th_lo ? u1 : 0x4B000000u;
+              }
+              if (hi_part) {
+                hi += e - lane > th_hi ? u0 : 0x4B000000u;
+                hi += e + 1 - lane > th_hi ? u1 : 0x4B000000u;
+              }
             }
             const uint32_t a = (a4[0] + a4[1]) + (a4[2] + a4[3]) - 32u * 0x4B000000u;
             all32 += a;
