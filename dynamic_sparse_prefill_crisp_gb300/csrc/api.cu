@@ -104,19 +104,26 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
-// bf16 [heads][n][128] with element strides; boxes of 64 features x 128 tokens
-// (one 128-byte swizzle row per token).
-crisp_status make_map(CUtensorMap* m, const void* ptr, int heads, int n, int64_t hs, int64_t ts) {
+// bf16 [heads][n][128] with element strides; boxes of 64 features x `rows`
+// tokens (one 128-byte swizzle row per token).
+crisp_status make_map(CUtensorMap* m, const void* ptr, int heads, int n, int64_t hs, int64_t ts, int rows = kB) {
   EncodeTiled enc = encode_fn();
   if (!enc) return CRISP_ERR_CUDA;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ts) * 2, static_cast<cuuint64_t>(hs) * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kB), 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CRISP_OK : CRISP_ERR_ALIGN;
+}
+
+// The attention kernel's K and V maps: boxes of 64 tokens (a sub-block).
+crisp_status make_kv_maps(TmaMaps* maps, const void* k, const void* v, const crisp_shape& s) {
+  crisp_status st = make_map(&maps->k64, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride, kB / 2);
+  if (st != CRISP_OK) return st;
+  return make_map(&maps->v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride, kB / 2);
 }
 
 crisp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CRISP_OK : CRISP_ERR_CUDA; }
@@ -529,7 +536,7 @@ static crisp_status attention_common(const crisp_shape* shape, const void* q, co
   TmaMaps maps;
   if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
   if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-  if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_kv_maps(&maps, k, v, s)) != CRISP_OK) return st;
   return from_cuda(launch_attention(s, maps, rowbits, order, out, static_cast<char*>(ws), dense, stream));
 }
 
@@ -563,7 +570,7 @@ crisp_status crisp_sparse_prefill(const crisp_shape* shape, const void* q, const
     TmaMaps maps;
     if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
     if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-    if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+    if ((st = make_kv_maps(&maps, k, v, s)) != CRISP_OK) return st;
     if (launch_build_mask(s, route, vbits, sbits, pebits, rowbits, counts, order, wsb, stream) != cudaSuccess)
       return CRISP_ERR_CUDA;
     return from_cuda(launch_attention(s, maps, rowbits, order, out, wsb, false, stream));
@@ -615,7 +622,7 @@ crisp_status run_layer(const crisp_shape& s, const crisp_params& p, const void* 
   crisp_status st;
   if ((st = make_map(&maps.q, q, s.hq, s.seq_len, s.q_head_stride, s.q_tok_stride)) != CRISP_OK) return st;
   if ((st = make_map(&maps.k, k, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
-  if ((st = make_map(&maps.v, v, s.hkv, s.seq_len, s.kv_head_stride, s.kv_tok_stride)) != CRISP_OK) return st;
+  if ((st = make_kv_maps(&maps, k, v, s)) != CRISP_OK) return st;
   char* wsb = static_cast<char*>(ws);
   // Length gate: below it the layer is plain dense attention. Below two
   // blocks the method has no candidates (and k_min keeps every block of up

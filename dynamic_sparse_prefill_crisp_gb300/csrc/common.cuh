@@ -100,7 +100,7 @@ ScratchLayout scratch_layout(const crisp_shape& s);
 LayerLayout layer_layout(const crisp_shape& s);
 
 struct TmaMaps {
-  CUtensorMap q, k, v;
+  CUtensorMap q, k, v, k64;  // k: 128-token boxes (proxy); k64, v: 64-token boxes (attention)
 };
 
 // ---- launchers (one per translation unit); return cudaSuccess or the launch error

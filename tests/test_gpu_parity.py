@@ -251,8 +251,8 @@ def test_attention_convenience_call_matches_the_layer():
 
 @pytest.mark.parametrize("scale", [1.0, 1e-3])
 def test_extreme_softmax_scales(scale):
-    # scale 1: logits with a spread of ~11 (rows ruled by single keys; the
-    # lazy reference max must move, through the exact path); scale 1e-3:
+    # scale 1: logits with a spread of ~11 (rows ruled by single keys, whose
+    # later blocks sit well above the first sub-block's max); scale 1e-3:
     # nearly uniform rows.
     hq, hkv, n = 4, 2, 1280
     w = synth.small("scales", hq, hkv, n, 82)
@@ -266,14 +266,16 @@ def test_extreme_softmax_scales(scale):
     check_attention(q, k, v, r["out"], rb, scale=scale)
 
 
-@pytest.mark.parametrize("window", [(100, 110), (5, 15), (60, 70)], ids=["half1-chunk1", "half0-chunk0", "both-halves"])
+@pytest.mark.parametrize("window", [(100, 110), (5, 15), (60, 70)],
+                         ids=["second-sub-block", "first-sub-block", "both-sub-blocks"])
 def test_attention_reference_rises_block_after_block(window):
     # The largest scores of each key block grow with the block and sit in one
-    # window of columns, so the row's reference max must move up again and
-    # again (the redo path of the softmax): chunks without the window keep
-    # their stored P (rescaled), the window's chunk is formed again. Dense
-    # and full-mask sparse launches against fp64 attention.
-    hq, hkv, n = 2, 1, 1024
+    # window of columns, so a row's first sub-block sets a reference that
+    # later blocks exceed by far more than 2^64 (the redo path: the row is run
+    # again at its exact max) and, without it, by more than bf16 and fp32
+    # can hold (p = 2^140 in the last block). Dense and full-mask sparse
+    # launches against fp64 attention.
+    hq, hkv, n = 2, 1, 2048
     rng = np.random.default_rng(7)
     u = np.zeros(128)
     u[0] = 1.0
@@ -281,8 +283,8 @@ def test_attention_reference_rises_block_after_block(window):
     t = np.arange(n) % B
     kb = np.arange(n) // B
     # log2 units per raw unit here: 8 * 0.0884 * 1.4427 = 1.02, so each block's
-    # window sits 9.2 above the last one's; the window's chunk sum passes 2^16
-    # two blocks after the reference was set, so every second block is redone
+    # window sits 9.2 above the last one's: 64 above the first block's from
+    # block 7 on, 127 above from block 14 on
     amp = 9.0 * kb + np.where((t >= window[0]) & (t < window[1]), 6.0, 0.0)
     k = amp[None, :, None] * u + 0.05 * rng.standard_normal((hkv, n, 128))
     v = rng.standard_normal((hkv, n, 128))
