@@ -266,16 +266,17 @@ def test_extreme_softmax_scales(scale):
     check_attention(q, k, v, r["out"], rb, scale=scale)
 
 
-@pytest.mark.parametrize("window", [(100, 110), (5, 15), (60, 70)],
-                         ids=["second-sub-block", "first-sub-block", "both-sub-blocks"])
-def test_attention_reference_rises_block_after_block(window):
+@pytest.mark.parametrize("window,n", [((100, 110), 2048), ((5, 15), 2048), ((60, 70), 2048), ((100, 110), 1999)],
+                         ids=["second-sub-block", "first-sub-block", "both-sub-blocks", "ragged-1999"])
+def test_attention_reference_rises_block_after_block(window, n):
     # The largest scores of each key block grow with the block and sit in one
     # window of columns, so a row's first sub-block sets a reference that
     # later blocks exceed by far more than 2^64 (the redo path: the row is run
     # again at its exact max) and, without it, by more than bf16 and fp32
     # can hold (p = 2^140 in the last block). Dense and full-mask sparse
-    # launches against fp64 attention.
-    hq, hkv, n = 2, 1, 2048
+    # launches against fp64 attention; n = 1999 ends in a short block of 79
+    # tokens (zero-filled K/V rows in every pass of the redo).
+    hq, hkv = 2, 1
     rng = np.random.default_rng(7)
     u = np.zeros(128)
     u[0] = 1.0
@@ -292,7 +293,7 @@ def test_attention_reference_rises_block_after_block(window):
         .numpy().view(np.uint16)
     q, k, v = to_bits(q), to_bits(k), to_bits(v)
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
-    nb = n // B
+    nb = (n + B - 1) // B
     full = np.zeros((hq, nb, 1), np.uint32)
     for qb in range(nb):
         full[:, qb, 0] = (1 << (qb + 1)) - 1
