@@ -59,8 +59,9 @@ __device__ __forceinline__ int64_t snake_item(int64_t k, int64_t w, int64_t N) {
 // blockIdx.x, blockIdx.x + gridDim.x, ... of the pooled heads only, so a
 // layer with few PE heads launches no idle CTAs. Thread t sums dims
 // 8(t % 16) .. 8(t % 16) + 7 of rows t / 16, t / 16 + 16, ... with 16-byte
-// loads (eight in flight); the 16 row groups are then added in order
-// through shared memory.
+// loads (eight in flight, the next item's issued before this item's sums
+// are added); the 16 row groups are then added in order through shared
+// memory.
 __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restrict__ q,
                                                    const __nv_bfloat16* __restrict__ k,
                                                    const uint8_t* __restrict__ route, int hq, int hkv, int n, int nb,
@@ -74,29 +75,39 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
     if (!pooled_head(route, hq, G, y)) continue;
     const bool is_q = y < hq;
     const int64_t start = static_cast<int64_t>(y) * nb;
-    for (int64_t i = first_item(start, blockIdx.x, gridDim.x); i < start + nb; i += gridDim.x) {
+    const __nv_bfloat16* base = is_q ? q + static_cast<int64_t>(y) * q_hs : k + static_cast<int64_t>(y - hq) * kv_hs;
+    const int64_t ts = is_q ? q_ts : kv_ts;  // elements, a multiple of 8
+    // The next item's rows are requested before this item's sums go through
+    // shared memory (eight 16-byte loads per thread in flight).
+    uint4 raw[kB / 16];
+    auto fetch = [&](int b) {
+      const __nv_bfloat16* src = base + static_cast<int64_t>(b) * kB * ts;
+      const int len = min(kB, n - b * kB);
+#pragma unroll
+      for (int j = 0; j < kB / 16; ++j) {
+        const int r = rg + 16 * j;
+        raw[j] = r < len ? *reinterpret_cast<const uint4*>(src + r * ts + 8 * seg) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    int64_t i = first_item(start, blockIdx.x, gridDim.x);
+    if (i < start + nb) fetch(static_cast<int>(i - start));
+    for (; i < start + nb; i += gridDim.x) {
       const int b = static_cast<int>(i - start);
       // (checking build) the block's tokens lie in [0, n)
       if (!CRISP_CHECK(b * kB < n, status, 0x410)) return;
-      const __nv_bfloat16* src = is_q ? q + static_cast<int64_t>(y) * q_hs + static_cast<int64_t>(b) * kB * q_ts
-                                      : k + static_cast<int64_t>(y - hq) * kv_hs + static_cast<int64_t>(b) * kB * kv_ts;
-      const int64_t ts = is_q ? q_ts : kv_ts;  // elements, a multiple of 8
       const int len = min(kB, n - b * kB);     // tokens of block b
       float acc[8] = {};
 #pragma unroll
       for (int j = 0; j < kB / 16; ++j) {
-        const int r = rg + 16 * j;
-        if (r < len) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(src + r * ts + 8 * seg);
-          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 v = __bfloat1622float2(h2[e]);
-            acc[2 * e] += v.x;
-            acc[2 * e + 1] += v.y;
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float2 v = __bfloat1622float2(h2[e]);
+          acc[2 * e] += v.x;
+          acc[2 * e + 1] += v.y;
         }
       }
+      if (i + gridDim.x < start + nb) fetch(b + static_cast<int>(gridDim.x));
       __syncthreads();  // the previous item's sums have been read
 #pragma unroll
       for (int e = 0; e < 8; ++e) red[rg][8 * seg + e] = acc[e];
