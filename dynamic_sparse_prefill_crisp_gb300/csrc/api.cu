@@ -788,10 +788,10 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
     // chunks alternate between two compute streams (each with its own part of
     // the workspace), so that one chunk's short selection kernels run beside
     // the previous chunk's attention. Long sequences use half a group per
-    // chunk (when G is even), and the first and last half groups of the layer
-    // go one head at a time, so that the pipeline fills and drains with a
-    // single head; shorter ones a whole group per chunk, where the extra
-    // launches and copies would cost more than the shorter fill.
+    // chunk (when G is even), and ramp the chunks of the first and last
+    // groups, so that the pipeline fills and drains with a single head;
+    // shorter ones a whole group per chunk, where the extra launches and
+    // copies would cost more than the shorter fill.
     const int G = s.hq / s.hkv;
     const int hc = (G % 2 == 0 && s.seq_len >= kHalfGroupChunkLen) ? G / 2 : G;  // query heads per chunk
     const size_t plane = static_cast<size_t>(s.seq_len) * kD * 2;  // bytes of one head
@@ -813,10 +813,45 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
         (dual && (cudaStreamWaitEvent(p->comp, p->start, 0) != cudaSuccess ||
                   cudaMemsetAsync(ws1, 0, sizeof(DevStatus), p->comp) != cudaSuccess)))
       return CRISP_ERR_CUDA;
-    const bool split_ends = hc > 1 && s.seq_len >= kHalfGroupChunkLen;
+    const bool ramp = hc > 1 && s.seq_len >= kHalfGroupChunkLen;
+    // The first kv group ramps up 1, 2, 4, ... heads per chunk and the last
+    // one ramps down the same way (mirrored), so that the pipeline fills and
+    // drains with one head but few chunks are small; the groups between take
+    // hc heads per chunk.
+    auto ramp_size = [&](int i) {  // heads of the chunk at head i (0-based) of the first group
+      int sz = 1;
+      for (int at = 0; at < i;) {
+        at += sz;
+        sz = std::min(2 * sz, hc);
+      }
+      return std::min(sz, G - i);
+    };
     int c = 0;
     for (int h0 = 0; h0 < s.hq; ++c) {
-      const int size = (split_ends && (h0 < hc || h0 >= s.hq - hc)) ? 1 : hc;  // heads in this chunk
+      int size = hc;  // heads in this chunk
+      if (ramp && h0 < G) size = ramp_size(h0);
+      if (ramp && h0 >= s.hq - G && s.hq > G) {
+        // mirrored: the last group's chunks end 4, 2, 1
+        const int i = h0 - (s.hq - G);  // position in the last group
+        int at = 0, sz = 1;
+        int sizes[32], ns = 0;
+        while (at < G && ns < 32) {
+          const int take = std::min(sz, G - at);
+          sizes[ns++] = take;
+          at += take;
+          sz = std::min(2 * sz, hc);
+        }
+        // sizes[] ramps up from the start of the group; walk it backwards
+        int pos = 0;
+        size = sizes[0];
+        for (int t = ns - 1; t >= 0; --t) {
+          if (pos == i) {
+            size = sizes[t];
+            break;
+          }
+          pos += sizes[t];
+        }
+      }
       sub.hq = size;
       const int e = c % crisp_host_pipeline::kRing;
       const int g = h0 / G;  // the chunk's kv group

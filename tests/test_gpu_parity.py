@@ -347,9 +347,11 @@ def test_prefill_layer_host_matches_device_layer():
     # Host buffers in, host buffer out, one kv group at a time with the copies
     # overlapped: bit-identical to the device-resident layer.
     pipe = crisp.HostPipeline()
-    # 128k tokens with group size 4: half-group chunks, single heads at both ends
+    # 128k tokens: group size 4 (half-group chunks, the first and last groups
+    # ramped 1, 2, 1) and group size 7 (whole groups, ramped 1, 2, 4 and
+    # mirrored 4, 2, 1 in the last group)
     for hq, hkv, n, seed in ((8, 2, 2048, 71), (7, 1, 1152, 72), (4, 4, 640, 73), (8, 2, 131072, 74),
-                             (4, 2, 1001, 75), (2, 1, 200, 76)):
+                             (14, 2, 131072, 77), (4, 2, 1001, 75), (2, 1, 200, 76)):
         w = synth.small("host", hq, hkv, n, seed)
         q, k, v = w.generate()
         params = crisp.params_default()
