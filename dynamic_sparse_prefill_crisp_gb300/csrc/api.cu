@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 #include <new>
 
 #include <nvtx3/nvToolsExt.h>
@@ -813,45 +814,28 @@ crisp_status crisp_prefill_layer_host(crisp_host_pipeline* pipeline, const crisp
         (dual && (cudaStreamWaitEvent(p->comp, p->start, 0) != cudaSuccess ||
                   cudaMemsetAsync(ws1, 0, sizeof(DevStatus), p->comp) != cudaSuccess)))
       return CRISP_ERR_CUDA;
+    // Chunk sizes in heads, in order: the first kv group ramps up 1, 2, 4, ...
+    // (each at most hc) and the last ramps down the same way, so that the
+    // pipeline fills and drains with one head but few chunks are small; the
+    // groups between take hc heads per chunk.
     const bool ramp = hc > 1 && s.seq_len >= kHalfGroupChunkLen;
-    // The first kv group ramps up 1, 2, 4, ... heads per chunk and the last
-    // one ramps down the same way (mirrored), so that the pipeline fills and
-    // drains with one head but few chunks are small; the groups between take
-    // hc heads per chunk.
-    auto ramp_size = [&](int i) {  // heads of the chunk at head i (0-based) of the first group
-      int sz = 1;
-      for (int at = 0; at < i;) {
-        at += sz;
-        sz = std::min(2 * sz, hc);
-      }
-      return std::min(sz, G - i);
-    };
+    std::vector<int> up_ramp;
+    for (int at = 0, sz = 1; at < G; sz = std::min(2 * sz, hc)) {
+      up_ramp.push_back(std::min(sz, G - at));
+      at += up_ramp.back();
+    }
+    std::vector<int> sizes;
+    for (int grp = 0; grp < s.hkv; ++grp) {
+      if (ramp && grp == 0)
+        sizes.insert(sizes.end(), up_ramp.begin(), up_ramp.end());
+      else if (ramp && grp == s.hkv - 1)
+        sizes.insert(sizes.end(), up_ramp.rbegin(), up_ramp.rend());
+      else
+        sizes.insert(sizes.end(), G / hc, hc);
+    }
     int c = 0;
     for (int h0 = 0; h0 < s.hq; ++c) {
-      int size = hc;  // heads in this chunk
-      if (ramp && h0 < G) size = ramp_size(h0);
-      if (ramp && h0 >= s.hq - G && s.hq > G) {
-        // mirrored: the last group's chunks end 4, 2, 1
-        const int i = h0 - (s.hq - G);  // position in the last group
-        int at = 0, sz = 1;
-        int sizes[32], ns = 0;
-        while (at < G && ns < 32) {
-          const int take = std::min(sz, G - at);
-          sizes[ns++] = take;
-          at += take;
-          sz = std::min(2 * sz, hc);
-        }
-        // sizes[] ramps up from the start of the group; walk it backwards
-        int pos = 0;
-        size = sizes[0];
-        for (int t = ns - 1; t >= 0; --t) {
-          if (pos == i) {
-            size = sizes[t];
-            break;
-          }
-          pos += sizes[t];
-        }
-      }
+      const int size = sizes[c];  // heads in this chunk (within one kv group)
       sub.hq = size;
       const int e = c % crisp_host_pipeline::kRing;
       const int g = h0 / G;  // the chunk's kv group
