@@ -333,8 +333,8 @@ def run_reference(args):
 
 # --------------------------------------------------------------- GPU arm
 # our kernel launches per step: proxy statistics 2, fused masses 2, route 1,
-# select_vs 1, pe_pool 3, select_pe 1, mask+schedule 2, attention 1
-LAUNCHES_PER_STEP = 13
+# select_vs 1, pe_pool 2, select_pe 1, mask+schedule 2, attention 1
+LAUNCHES_PER_STEP = 12
 STAGES = ["proxy_masses", "route", "select_vs", "pe_pool", "select_pe", "mask", "attention"]
 
 

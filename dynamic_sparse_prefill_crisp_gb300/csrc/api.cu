@@ -173,8 +173,8 @@ ScratchLayout scratch_layout(const crisp_shape& s) {
   L.mass_upper = o;  o = up(o + hq * nb * 8);
   L.mass_upper2 = o; o = up(o + hq * nb * 8);
   L.mass_rec = o;    o = up(o + hq * 8);
-  L.qbar = o;        o = up(o + hq * nb * kD * 4);
-  L.kbar = o;        o = up(o + hkv * nb * kD * 4);
+  L.qbar = o;        o = up(o + hq * nb * kD * 4);   // bf16 hi and lo
+  L.kbar = o;        o = up(o + hkv * nb * kD * 4);  // bf16 hi and lo
   L.srev = o;        o = up(o + hq * (W + 2) * 4);
   L.rmass = o;       o = up(o + hq * 8);
   L.rowbits = o;     o = up(o + hq * nb * W * 4);
@@ -205,6 +205,11 @@ LayerLayout layer_layout(const crisp_shape& s) {
   L.order = S.order;
   L.total = o;
   return L;
+}
+
+// bf16 [heads][rows][128] with 128-row boxes (the pooled estimate's operands).
+bool encode_bf16_rows(CUtensorMap* m, const void* ptr, int heads, int rows) {
+  return make_map(m, ptr, heads, rows, static_cast<int64_t>(rows) * kD, kD, kB) == CRISP_OK;
 }
 
 }  // namespace crisp

@@ -80,8 +80,8 @@ struct ScratchLayout {
   size_t mass_upper;   // uint64 [hq][nb]  tile c's entries with slash block nb-2-c
   size_t mass_upper2;  // uint64 [hq][nb]  tile c's entries with slash block nb-3-c (short last block only)
   size_t mass_rec;     // uint64 [hq]      recency columns [n-128, n) that lie in tile nb-2
-  size_t qbar;         // float  [hq][nb][128]
-  size_t kbar;         // float  [hkv][nb][128]
+  size_t qbar;         // bf16 [hq][nb][128] hi, then the same for lo (block means as hi + lo)
+  size_t kbar;         // bf16 [hkv][nb][128] hi, then lo
   size_t srev;         // uint32 [hq][W + 2]  slash bits reversed
   size_t rmass;        // uint64 [hq]      recency masses of crisp_select_vs (from the map)
   size_t rowbits;      // uint32 [hq][nb][W]  block mask built by crisp_sparse_prefill
@@ -98,6 +98,8 @@ struct LayerLayout {
 
 ScratchLayout scratch_layout(const crisp_shape& s);
 LayerLayout layer_layout(const crisp_shape& s);
+
+bool encode_bf16_rows(CUtensorMap* m, const void* ptr, int heads, int rows);
 
 struct TmaMaps {
   CUtensorMap q, k, v, k64;  // k: 128-token boxes (proxy); k64, v: 64-token boxes (attention)

@@ -5,7 +5,9 @@
 //
 // A5: qbar_b / kbar_c = means over each block's tokens (128, or fewer in a
 // short last block); pbar[b][c] = softmax
-// over c <= b of scale * qbar_b . kbar_c (fp32; c > b stored as 0).
+// over c <= b of scale * qbar_b . kbar_c (fp32; c > b stored as 0). Two
+// kernels: pool_kernel (the means, HBM-bound) and pooled_map (the products
+// on the tensor cores with the row softmax fused).
 // A6: per row b, gamma coverage (or the noise floor) over Q32 quanta of pbar.
 #include <cuda_bf16.h>
 
@@ -61,12 +63,13 @@ __device__ __forceinline__ int64_t snake_item(int64_t k, int64_t w, int64_t N) {
 // 8(t % 16) .. 8(t % 16) + 7 of rows t / 16, t / 16 + 16, ... with 16-byte
 // loads (eight in flight, the next item's issued before this item's sums
 // are added); the 16 row groups are then added in order through shared
-// memory.
+// memory. Each mean m is stored as two bf16 values, hi = bf16(m) and
+// lo = bf16(m - hi), the tensor-core operands of pooled_map.
 __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restrict__ q,
                                                    const __nv_bfloat16* __restrict__ k,
                                                    const uint8_t* __restrict__ route, int hq, int hkv, int n, int nb,
                                                    int64_t q_hs, int64_t q_ts, int64_t kv_hs, int64_t kv_ts,
-                                                   float* __restrict__ qbar, float* __restrict__ kbar,
+                                                   __nv_bfloat16* __restrict__ qbar, __nv_bfloat16* __restrict__ kbar,
                                                    DevStatus* status) {
   __shared__ float red[16][kD + 4];
   const int G = hq / hkv;
@@ -117,140 +120,300 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
 #pragma unroll
         for (int g = 0; g < 16; ++g) sum += red[g][threadIdx.x];
         const size_t o = is_q ? (static_cast<size_t>(y) * nb + b) * kD : (static_cast<size_t>(y - hq) * nb + b) * kD;
-        if (CRISP_CHECK(o + kD <= static_cast<size_t>(is_q ? hq : hkv) * nb * kD, status, 0x411))
-          (is_q ? qbar : kbar)[o + threadIdx.x] = sum * (1.0f / static_cast<float>(len));  // exact for a whole block
-      }
-    }
-  }
-}
-
-// Pooled logits in log2 units on the lower triangle (c <= b) of 128x128
-// tiles: items (PE head h, tile t) with t over the T(T+1)/2 tiles (bt, ct <=
-// bt), grid-stride like pool_kernel. Each of 256 threads computes 8x8 outputs
-// (two 4x4 quadrants) from 16-deep slabs, double-buffered in shared memory:
-// float4 reads of both operands, two fp32 fmas per instruction, the features
-// added in ascending order. Entries above the diagonal are left to
-// pooled_softmax, which writes whole rows.
-constexpr int kPT = 128, kKS = 16;  // tile edge, depth of a shared-memory slab
-__global__ void __launch_bounds__(256, 2) pooled_scores(const float* __restrict__ qbar, const float* __restrict__ kbar,
-                                                        const uint8_t* __restrict__ route, int hq, int nb, int group,
-                                                        float c_log2, float* __restrict__ pbar, DevStatus* status) {
-  __shared__ __align__(16) float As[2][kKS][kPT + 4];
-  __shared__ __align__(16) float Bs[2][kKS][kPT + 4];
-  const int T = (nb + kPT - 1) / kPT;
-  const int64_t per_head = static_cast<int64_t>(T) * (T + 1) / 2;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  for (int h = 0; h < hq; ++h) {
-    if (route[h]) continue;
-    const int64_t start = static_cast<int64_t>(h) * per_head;
-    for (int64_t i = first_item(start, blockIdx.x, gridDim.x); i < start + per_head; i += gridDim.x) {
-      const int t = static_cast<int>(i - start);
-      int bt = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
-      while ((bt + 1) * (bt + 2) / 2 <= t) ++bt;
-      while (bt * (bt + 1) / 2 > t) --bt;
-      const int ct = t - bt * (bt + 1) / 2;
-      // (checking build) the tile lies on or below the diagonal inside [0, nb)
-      if (!CRISP_CHECK(bt < T && ct <= bt, status, 0x412)) return;
-      float* out = pbar + static_cast<size_t>(h) * nb * nb;
-      const float* A = qbar + static_cast<size_t>(h) * nb * kD;
-      const float* Bm = kbar + static_cast<size_t>(h / group) * nb * kD;
-      // Slab loads: thread f reads 4 consecutive features of row f / 4 (and of
-      // row 64 + f / 4) of both operands with float4 loads.
-      float4 ra[2], rb[2];
-      auto load = [&](int d0) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int f = threadIdx.x + 256 * u, row = f >> 2, quad = f & 3;
-          const int b = bt * kPT + row, c = ct * kPT + row;
-          ra[u] = b < nb ? *reinterpret_cast<const float4*>(A + static_cast<size_t>(b) * kD + d0 + 4 * quad)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-          rb[u] = c < nb ? *reinterpret_cast<const float4*>(Bm + static_cast<size_t>(c) * kD + d0 + 4 * quad)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      };
-      auto store = [&](int buf) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int f = threadIdx.x + 256 * u, row = f >> 2, quad = f & 3;
-          As[buf][4 * quad + 0][row] = ra[u].x;
-          As[buf][4 * quad + 1][row] = ra[u].y;
-          As[buf][4 * quad + 2][row] = ra[u].z;
-          As[buf][4 * quad + 3][row] = ra[u].w;
-          Bs[buf][4 * quad + 0][row] = rb[u].x;
-          Bs[buf][4 * quad + 1][row] = rb[u].y;
-          Bs[buf][4 * quad + 2][row] = rb[u].z;
-          Bs[buf][4 * quad + 3][row] = rb[u].w;
-        }
-      };
-      // Rows ty*4 .. +3 and 64 + ty*4 .. +3, columns tx*4 .. +3 and 64 + tx*4 .. +3.
-      float acc[8][8] = {};
-      __syncthreads();  // the previous item's last slab has been read
-      load(0);
-      store(0);
-      __syncthreads();
-      for (int sl = 0; sl < kD / kKS; ++sl) {
-        const int buf = sl & 1;
-        if (sl + 1 < kD / kKS) load((sl + 1) * kKS);
-#pragma unroll
-        for (int kk = 0; kk < kKS; ++kk) {
-          const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
-          const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
-          const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
-          const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
-          const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-          const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-          for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int j = 0; j < 8; j += 2)
-              ptx::ffma2(acc[r][j], acc[r][j + 1], av[r], av[r], bv[j], bv[j + 1], acc[r][j], acc[r][j + 1]);
-        }
-        if (sl + 1 < kD / kKS) store(buf ^ 1);  // the other buffer was last read before the previous barrier
-        __syncthreads();
-      }
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int b = bt * kPT + (r < 4 ? ty * 4 + r : 64 + ty * 4 + r - 4);
-        if (b >= nb) continue;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = ct * kPT + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
-          if (c <= b) out[static_cast<size_t>(b) * nb + c] = acc[r][j] * c_log2;
+        if (CRISP_CHECK(o + kD <= static_cast<size_t>(is_q ? hq : hkv) * nb * kD, status, 0x411)) {
+          // the mean as a sum of two bf16 values (hi + lo carries 16 bits)
+          const float mean = sum * (1.0f / static_cast<float>(len));  // exact for a whole block
+          const __nv_bfloat16 hi = __float2bfloat16_rn(mean);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(mean - __bfloat162float(hi));
+          __nv_bfloat16* dst = is_q ? qbar : kbar;
+          const size_t half = static_cast<size_t>(is_q ? hq : hkv) * nb * kD;  // lo after all hi rows
+          dst[o + threadIdx.x] = hi;
+          dst[half + o + threadIdx.x] = lo;
         }
       }
     }
   }
 }
 
-// Row softmax over c <= b (base 2, logits already in log2 units) and zeros for
-// b < c < nb; one warp per row of a PE head. Rows are numbered b descending
-// (PE heads ascending within a b) and dealt to the warps in snake order.
-__global__ void __launch_bounds__(256) pooled_softmax(const uint8_t* __restrict__ route, int hq, int nb,
-                                                      float* __restrict__ pbar, DevStatus* status) {
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+// Pooled map on the tensor cores, softmax fused: each block mean is held as
+// hi + lo (two bf16 values) and qbar . kbar = hi.hi + hi.lo + lo.hi (the
+// lo.lo term, 2^-16 of the product, is left out): three tcgen05 products of
+// M = N = 128 over the 128 features into an fp32 TMEM accumulator. One CTA
+// per SM takes items (PE head h, row tile bt), bt descending, in snake
+// order. Per item it keeps A = qbar rows [128 bt, +128) in shared memory and
+// walks the column tiles ct <= bt twice: pass 1 keeps each row's running max
+// and sum of 2^(z - max) (z = scale log2(e) qbar . kbar), pass 2 forms the
+// same products again and writes p = 2^(z - max) / sum for c <= b and 0 for
+// b < c < nb, so the logits never go to memory. TMA double-buffers
+// B = kbar rows, the MMA thread alternates two TMEM accumulators, and eight
+// epilogue warps (two per TMEM lane quarter, one per 64-column half) read
+// the accumulators; each 32x16 piece of P goes through shared memory so that
+// it leaves as 64-byte row segments.
+constexpr int kPT = 128;                            // tile edge
+constexpr uint32_t kPTile = kPT * kD * 2;           // 32 KB: one bf16 128x128 operand
+constexpr uint32_t kPHalf = kPTile / 2;             // one 64-feature half
+constexpr int kPStage = 32 * 20;                    // an epilogue warp's 32x16 fp32 transpose (padded rows)
+constexpr int kScoresThreads = 320;                 // TMA warp, MMA warp, 8 epilogue warps
+constexpr uint32_t kScoresSmem = 1024 + 6 * kPTile + 8 * kPStage * 4;  // A, two B stages, eight transposes
+
+struct ScoresBars {
+  uint64_t a_full, a_empty, b_full[2], b_empty[2], d_full[2], d_empty[2], xbar, drain;
+  uint32_t tmem_base;
+  int abort;
+  float2 stats[2][kPT];  // (max, sum) of each row of the item's tile, per column half
+};
+
+__global__ void __launch_bounds__(kScoresThreads, 1)
+    pooled_map(const __grid_constant__ CUtensorMap tq_hi, const __grid_constant__ CUtensorMap tq_lo,
+               const __grid_constant__ CUtensorMap tk_hi, const __grid_constant__ CUtensorMap tk_lo,
+               const uint8_t* __restrict__ route, int hq, int nb, int group, float c_log2,
+               float* __restrict__ pbar, DevStatus* status) {
+  extern __shared__ uint8_t pe_tc_smem[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pe_tc_smem) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;                 // hi, lo
+  uint8_t* sB = base + 2 * kPTile;    // stage s: hi, lo at + 2 * kPTile * s
+  float* sT = reinterpret_cast<float*>(base + 6 * kPTile);  // epilogue warp e: sT + e * kPStage
+  __shared__ ScoresBars bars;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    ptx::mbar_init(&bars.a_full, 1);
+    ptx::mbar_init(&bars.a_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bars.b_full[i], 1);
+      ptx::mbar_init(&bars.b_empty[i], 1);
+      ptx::mbar_init(&bars.d_full[i], 1);
+      ptx::mbar_init(&bars.d_empty[i], 8);
+    }
+    ptx::mbar_init(&bars.xbar, 256);
+    ptx::mbar_init(&bars.drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&bars.tmem_base, 256);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
   int n_pe = 0;
-  for (int base = 0; base < hq; base += 32)
-    n_pe += __popc(__ballot_sync(0xffffffffu, base + lane < hq && route[base + lane] == 0));
-  const int64_t rows = static_cast<int64_t>(n_pe) * nb;
-  for (int64_t k = 0;; ++k) {
-    const int64_t r = snake_item(k, wid, nwarps);
-    if (r >= rows) break;
-    const int b = nb - 1 - static_cast<int>(r / n_pe);
+  for (int b0 = 0; b0 < hq; b0 += 32)
+    n_pe += __popc(__ballot_sync(0xffffffffu, b0 + lane < hq && route[b0 + lane] == 0));
+  const int T = (nb + kPT - 1) / kPT;
+  const int64_t items = static_cast<int64_t>(n_pe) * T;
+  const bool vec = (nb & 3) == 0 && (reinterpret_cast<uintptr_t>(pbar) & 15u) == 0;  // 16-byte row segments
+  auto fail = [&](uint32_t where) {
+    *reinterpret_cast<volatile int*>(&bars.abort) = 1;
+    report_error(status, CRISP_ERR_TIMEOUT, where);
+  };
+  // phase counters (each role counts its own); `tile` counts tile passes
+  uint32_t a_n = 0, b_n[2] = {0u, 0u}, d_n[2] = {0u, 0u}, x_n = 0, tile = 0;
+  bool ok = true;
+  for (int64_t k = 0; ok; ++k) {
+    const int64_t r = snake_item(k, blockIdx.x, gridDim.x);
+    if (r >= items) break;
+    const int bt = T - 1 - static_cast<int>(r / n_pe);
     const int h = nth_head(route, hq, false, static_cast<int>(r % n_pe));
-    if (!CRISP_CHECK(h < hq && b >= 0, status, 0x413)) return;
-    float* z = pbar + (static_cast<size_t>(h) * nb + b) * nb;
-    float mx = -INFINITY;
-    for (int c = lane; c <= b; c += 32) mx = fmaxf(mx, z[c]);
+    // (checking build) the item's rows and its TMA coordinates lie in the maps
+    if (!CRISP_CHECK(h < hq && bt >= 0 && bt * kPT < nb && h / group < hq / group, status, 0x412)) break;
+    const int g = h / group;
+    const int passes = 2 * (bt + 1);  // tile passes of this item
+    if (warp == 0) {
+      if (lane == 0) {
+        if (!ptx::mbar_wait(&bars.a_empty, (a_n & 1u) ^ 1u, &bars.abort)) { fail(0x415); ok = false; }
+        if (ok) {
+          ptx::mbar_arrive_expect_tx(&bars.a_full, 2 * kPTile);
+          ptx::tma_load_3d(sA, &tq_hi, &bars.a_full, 0, bt * kPT, h);
+          ptx::tma_load_3d(sA + kPHalf, &tq_hi, &bars.a_full, 64, bt * kPT, h);
+          ptx::tma_load_3d(sA + kPTile, &tq_lo, &bars.a_full, 0, bt * kPT, h);
+          ptx::tma_load_3d(sA + kPTile + kPHalf, &tq_lo, &bars.a_full, 64, bt * kPT, h);
+        }
+        for (int t = 0; ok && t < passes; ++t) {
+          const int ct = t % (bt + 1);
+          const int st = static_cast<int>((tile + t) & 1u);
+          if (!ptx::mbar_wait(&bars.b_empty[st], (b_n[st] & 1u) ^ 1u, &bars.abort)) { fail(0x416); ok = false; break; }
+          ++b_n[st];
+          uint8_t* dst = sB + 2 * kPTile * st;
+          ptx::mbar_arrive_expect_tx(&bars.b_full[st], 2 * kPTile);
+          ptx::tma_load_3d(dst, &tk_hi, &bars.b_full[st], 0, ct * kPT, g);
+          ptx::tma_load_3d(dst + kPHalf, &tk_hi, &bars.b_full[st], 64, ct * kPT, g);
+          ptx::tma_load_3d(dst + kPTile, &tk_lo, &bars.b_full[st], 0, ct * kPT, g);
+          ptx::tma_load_3d(dst + kPTile + kPHalf, &tk_lo, &bars.b_full[st], 64, ct * kPT, g);
+        }
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
+        if (!ptx::mbar_wait(&bars.a_full, a_n & 1u, &bars.abort)) { fail(0x417); ok = false; }
+        const uint32_t ah = ptx::smem_u32(sA), al = ptx::smem_u32(sA + kPTile);
+        for (int t = 0; ok && t < passes; ++t) {
+          const int u = static_cast<int>((tile + t) & 1u);  // B stage and accumulator
+          if (!ptx::mbar_wait(&bars.b_full[u], b_n[u] & 1u, &bars.abort) ||
+              !ptx::mbar_wait(&bars.d_empty[u], (d_n[u] & 1u) ^ 1u, &bars.abort)) {
+            fail(0x418);
+            ok = false;
+            break;
+          }
+          ++b_n[u];
+          ++d_n[u];
+          ptx::tc_fence_after();
+          const uint32_t bh = ptx::smem_u32(sB + 2 * kPTile * u), bl = bh + kPTile;
+          const uint32_t d = tmem + u * 128;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float sum = 0.f;
-    for (int c = lane; c <= b; c += 32) sum += ptx::ex2_approx(z[c] - mx);
-    sum = warp_sum(sum);
-    const float inv = 1.0f / sum;
-    for (int c = lane; c < nb; c += 32) z[c] = c <= b ? ptx::ex2_approx(z[c] - mx) * inv : 0.f;
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kPHalf + (kk & 3) * 32;
+            ptx::umma_ss(d, ptx::sdesc_sw128(ah + off, 16, 1024), ptx::sdesc_sw128(bh + off, 16, 1024), idesc, kk > 0);
+            ptx::umma_ss(d, ptx::sdesc_sw128(ah + off, 16, 1024), ptx::sdesc_sw128(bl + off, 16, 1024), idesc, 1);
+            ptx::umma_ss(d, ptx::sdesc_sw128(al + off, 16, 1024), ptx::sdesc_sw128(bh + off, 16, 1024), idesc, 1);
+          }
+          ptx::umma_commit(&bars.b_empty[u]);
+          ptx::umma_commit(&bars.d_full[u]);
+        }
+        ptx::umma_commit(&bars.a_empty);
+      }
+    } else {
+      // Epilogue warp e = warp - 2 reads TMEM lane quarter q = warp % 4 (rows
+      // r0 .. r0 + 31 of the tile, one per lane) and the 64 columns of half
+      // ch of each accumulator.
+      const int e = warp - 2, q = warp & 3, ch = e >> 2;
+      const int r0 = bt * kPT + q * 32, row = r0 + lane;
+      const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+      float* tr = sT + e * kPStage;
+      float* out = pbar + static_cast<size_t>(h) * nb * nb;
+      // zeros right of the row tile: columns [128 (bt + 1), nb) of rows r0 ..
+      // r0 + 31, the two warps of a quarter taking alternate 32-lane runs
+      const int z0 = (bt + 1) * kPT;
+      if (z0 < nb) {
+        const int rows = min(32, nb - r0);
+        for (int rr = 0; rr < rows; ++rr) {
+          float* dst = out + static_cast<size_t>(r0 + rr) * nb;
+          if (!CRISP_CHECK(static_cast<size_t>(h) * nb + r0 + rr < static_cast<size_t>(hq) * nb, status, 0x41b)) break;
+          if (vec) {
+            for (int c = z0 + 4 * (ch * 32 + lane); c < nb; c += 4 * 64)
+              *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+            for (int c = z0 + ch * 32 + lane; c < nb; c += 64) dst[c] = 0.f;
+          }
+        }
+      }
+      float m = -INFINITY, l = 0.f, inv = 0.f;
+      for (int t = 0; t < passes; ++t) {
+        const bool second = t > bt;
+        if (t == bt + 1) {
+          // the two halves' (max, sum) of each row combine into the row's
+          bars.stats[ch][q * 32 + lane] = make_float2(m, l);
+          ptx::mbar_arrive(&bars.xbar);
+          if (ok && !ptx::mbar_wait(&bars.xbar, x_n & 1u, &bars.abort)) {
+            if (lane == 0) fail(0x41a);
+            ok = false;
+          }
+          ++x_n;
+          const float2 a = bars.stats[0][q * 32 + lane], b = bars.stats[1][q * 32 + lane];
+          m = fmaxf(a.x, b.x);  // finite for rows < nb: column 0 is in half 0
+          l = a.y * ptx::ex2_approx(a.x - m) + (b.x == -INFINITY ? 0.f : b.y * ptx::ex2_approx(b.x - m));
+          inv = 1.0f / l;
+        }
+        if (!ok) break;
+        const int ct = t % (bt + 1);
+        const int u = static_cast<int>((tile + t) & 1u);
+        if (!ptx::mbar_wait(&bars.d_full[u], d_n[u] & 1u, &bars.abort)) {
+          if (lane == 0) fail(0x419);
+          ok = false;
+          break;
+        }
+        ++d_n[u];
+        ptx::tc_fence_after();
+        if (!second) {
+#pragma unroll 1
+          for (int pc = 0; pc < 2; ++pc) {
+            const int c0 = ch * 64 + pc * 32, col = ct * kPT + c0;
+            if (r0 >= nb || col >= nb || col > r0 + 31) break;  // past the map, or right of the diagonal
+            uint32_t v[32];
+            ptx::tmem_ld32(tmem + lane_addr + u * 128 + c0, v);
+            float z[32], mp = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              z[j] = col + j <= row ? __fmul_rn(__uint_as_float(v[j]), c_log2) : -INFINITY;
+              mp = fmaxf(mp, z[j]);
+            }
+            if (mp != -INFINITY) {  // this row has entries c <= b in the piece
+              const float mn = fmaxf(m, mp);
+              float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                s0 += ptx::ex2_approx(z[j] - mn);
+                s1 += ptx::ex2_approx(z[j + 1] - mn);
+              }
+              l = (m == -INFINITY ? 0.f : l * ptx::ex2_approx(m - mn)) + (s0 + s1);
+              m = mn;
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int pc = 0; pc < 4; ++pc) {
+            const int c0 = ch * 64 + pc * 16, col = ct * kPT + c0;
+            if (r0 >= nb || col >= nb) break;  // rows or columns past the map
+            const bool above = col > r0 + 31;  // the whole piece lies right of the diagonal
+            uint32_t v[16];
+            if (!above) ptx::tmem_ld16(tmem + lane_addr + u * 128 + c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              float pj[4];
+#pragma unroll
+              for (int x = 0; x < 4; ++x)
+                pj[x] = !above && col + j + x <= row
+                            ? ptx::ex2_approx(__fmul_rn(__uint_as_float(v[j + x]), c_log2) - m) * inv
+                            : 0.f;
+              *reinterpret_cast<float4*>(tr + lane * 20 + j) = make_float4(pj[0], pj[1], pj[2], pj[3]);
+            }
+            __syncwarp();
+            // rows r0 + 8i + lane / 4, columns col + 4 (lane % 4) .. + 3
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = 8 * i + (lane >> 2), cc = 4 * (lane & 3);
+              const float4 p = *reinterpret_cast<const float4*>(tr + rr * 20 + cc);
+              if (r0 + rr < nb && col + cc < nb &&
+                  CRISP_CHECK(static_cast<size_t>(h) * nb + r0 + rr < static_cast<size_t>(hq) * nb, status, 0x41c)) {
+                float* dst = out + static_cast<size_t>(r0 + rr) * nb + col + cc;
+                if (vec) {
+                  *reinterpret_cast<float4*>(dst) = p;
+                } else {
+                  dst[0] = p.x;
+                  if (col + cc + 1 < nb) dst[1] = p.y;
+                  if (col + cc + 2 < nb) dst[2] = p.z;
+                  if (col + cc + 3 < nb) dst[3] = p.w;
+                }
+              }
+            }
+            __syncwarp();
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars.d_empty[u]);
+      }
+    }
+    ++a_n;
+    tile += static_cast<uint32_t>(passes);
+    ok = __syncthreads_and(ok) != 0;
   }
+  if (warp == 1 && lane == 0) {
+    ptx::umma_commit(&bars.drain);
+    const int never = 0;
+    ptx::mbar_wait(&bars.drain, 0, &never);
+  }
+  if (warp == 0 && lane == 0) {
+    // every copy has landed before the CTA exits (consumers may have given up)
+    const int never = 0;
+    if (a_n > 0) ptx::mbar_wait(&bars.a_full, (a_n - 1u) & 1u, &never);
+    for (int i = 0; i < 2; ++i)
+      if (b_n[i] > 0) ptx::mbar_wait(&bars.b_full[i], (b_n[i] - 1u) & 1u, &never);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, 256);
 }
 
 // A6: one warp per row (h, b), no block barrier. Warps are numbered PE rows
@@ -398,8 +561,8 @@ cudaError_t launch_pe_map(const crisp_shape& s, const void* q, const void* k, co
                           char* ws, cudaStream_t st) {
   const ScratchLayout L = scratch_layout(s);
   const int nb = num_blocks(s.seq_len);
-  auto* qbar = reinterpret_cast<float*>(ws + L.qbar);
-  auto* kbar = reinterpret_cast<float*>(ws + L.kbar);
+  auto* qbar = reinterpret_cast<__nv_bfloat16*>(ws + L.qbar);  // hi [hq][nb][128], then lo
+  auto* kbar = reinterpret_cast<__nv_bfloat16*>(ws + L.kbar);  // hi [hkv][nb][128], then lo
   auto* status = reinterpret_cast<DevStatus*>(ws + L.status);
   // Grids of resident CTAs, each looping over its share of the PE heads'
   // items (VS heads cost a route read), so a layer with few PE heads launches
@@ -409,12 +572,17 @@ cudaError_t launch_pe_map(const crisp_shape& s, const void* q, const void* k, co
   pool_kernel<<<resident_grid(pool_kernel, sms, pool_items), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), route, s.hq, s.hkv, s.seq_len, nb,
       s.q_head_stride, s.q_tok_stride, s.kv_head_stride, s.kv_tok_stride, qbar, kbar, status);
+  CUtensorMap tq_hi, tq_lo, tk_hi, tk_lo;
+  const size_t q_half = static_cast<size_t>(s.hq) * nb * kD, k_half = static_cast<size_t>(s.hkv) * nb * kD;
+  if (!encode_bf16_rows(&tq_hi, qbar, s.hq, nb) || !encode_bf16_rows(&tq_lo, qbar + q_half, s.hq, nb) ||
+      !encode_bf16_rows(&tk_hi, kbar, s.hkv, nb) || !encode_bf16_rows(&tk_lo, kbar + k_half, s.hkv, nb))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(pooled_map, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoresSmem);
+  if (e != cudaSuccess) return e;
   const int64_t T = (nb + kPT - 1) / kPT;
-  const int64_t tiles = static_cast<int64_t>(s.hq) * T * (T + 1) / 2;
-  pooled_scores<<<resident_grid(pooled_scores, sms, tiles), 256, 0, st>>>(
-      qbar, kbar, route, s.hq, nb, s.hq / s.hkv, s.scale * 1.4426950408889634f, pbar, status);
-  const int64_t rows = static_cast<int64_t>(s.hq) * nb;
-  pooled_softmax<<<resident_grid(pooled_softmax, sms, (rows + 7) / 8), 256, 0, st>>>(route, s.hq, nb, pbar, status);
+  pooled_map<<<static_cast<unsigned>(std::min<int64_t>(sms, static_cast<int64_t>(s.hq) * T)), kScoresThreads,
+               kScoresSmem, st>>>(tq_hi, tq_lo, tk_hi, tk_lo, route, s.hq, nb, s.hq / s.hkv,
+                                  s.scale * 1.4426950408889634f, pbar, status);
   return cudaGetLastError();
 }
 

@@ -635,7 +635,7 @@ def test_attention_is_deterministic_under_load():
 def test_prefill_layer_replays_from_a_cuda_graph():
     # Every call enqueues on the caller's stream and allocates nothing, so a
     # whole layer can be captured once and replayed (the short-sequence case
-    # is launch-bound: 13 launches for a 2k-token layer).
+    # is launch-bound: 12 launches for a 2k-token layer).
     w = synth.small("graph", 8, 2, 2048, 121)
     q, k, v = w.generate()
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
