@@ -426,12 +426,13 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
 // re-forms the selection keys (quantum << 13 | 8191 - c) from the row. Bitset
 // word i is the ballot of the lanes' keys 32i .. 32i + 31.
 struct PeWarpLayout {
-  int hist, chosen, vals, bytes;  // byte offsets inside one warp's slice
+  int hist, last, chosen, vals, bytes;  // byte offsets inside one warp's slice
 };
 __host__ __device__ inline PeWarpLayout pe_warp_layout(int nb, bool row_in_shared) {
   PeWarpLayout L;
   L.hist = 0;
-  L.chosen = 256 * 8;
+  L.last = 256 * 8;
+  L.chosen = L.last + 256 * 2;
   L.vals = L.chosen + (((nb + 31) / 32 + 3) / 4) * 16;
   L.bytes = L.vals + (row_in_shared ? ((nb + 3) / 4) * 16 : 0);
   return L;
@@ -453,6 +454,7 @@ __global__ void __launch_bounds__(256, 4) select_pe_kernel(const float* __restri
   const PeWarpLayout L = pe_warp_layout(nb, kRowInShared);
   unsigned char* mine = pe_smem + static_cast<size_t>(warp) * L.bytes;
   auto* hist = reinterpret_cast<unsigned long long*>(mine + L.hist);
+  auto* last = reinterpret_cast<unsigned short*>(mine + L.last);
   auto* chosen = reinterpret_cast<uint32_t*>(mine + L.chosen);
   auto* vals = reinterpret_cast<float*>(mine + L.vals);
   const int row = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(256, 4) select_pe_kernel(const float* __restri
     // member of the shortest (mass desc, index asc) prefix.
     const uint64_t x = warp_radix_max_key(
         len, key_of, mass_in_key, [](int) { return true; },
-        [&](unsigned long long f) { return static_cast<unsigned __int128>(gamma_den) * f >= goal; }, hist);
+        [&](unsigned long long f) { return static_cast<unsigned __int128>(gamma_den) * f >= goal; }, hist, last);
     for (int i = 0; i < words; ++i) {
       const int c = 32 * i + lane;
       const uint32_t word = __ballot_sync(0xffffffffu, c < len && key_of(c) >= x);
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(256, 4) select_pe_kernel(const float* __restri
     auto unchosen = [&](int c) { return !((chosen[c >> 5] >> (c & 31)) & 1u); };
     const uint64_t x = warp_radix_max_key(
         len, key_of, [](int, uint64_t) { return 1ull; }, unchosen,
-        [&](unsigned long long cnt) { return cnt >= static_cast<unsigned long long>(need); }, hist);
+        [&](unsigned long long cnt) { return cnt >= static_cast<unsigned long long>(need); }, hist, last);
     for (int i = 0; i < words; ++i) {
       const int c = 32 * i + lane;
       const bool add = c < len && unchosen(c) && key_of(c) >= x;

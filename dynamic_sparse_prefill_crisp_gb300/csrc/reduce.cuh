@@ -133,12 +133,16 @@ __device__ __forceinline__ uint64_t radix_max_key(int len, KeyFn key_of, WeightF
 }
 
 // The same search by one warp on its own (no block barrier): `hist` is the
-// warp's own 256 entries; weight_of(c, key) is given the key already formed.
-// Every lane of the warp calls it with the same arguments and gets the
-// result.
+// warp's own 256 entries and `last` 256 key indexes; weight_of(c, key) is
+// given the key already formed. Every lane of the warp calls it with the
+// same arguments and gets the result. Each pass records the index of one key
+// of each digit (digit 0, summed in registers without atomics, in a register
+// per lane): when the chosen digit holds a single key, that index names the
+// answer without another read of the row.
 template <typename KeyFn, typename WeightFn, typename EligFn, typename ReachFn>
 __device__ __forceinline__ uint64_t warp_radix_max_key(int len, KeyFn key_of, WeightFn weight_of, EligFn eligible,
-                                                       ReachFn reach, unsigned long long* hist) {
+                                                       ReachFn reach, unsigned long long* hist,
+                                                       unsigned short* last) {
   constexpr unsigned long long kOne = 1ull << 40, kWeight = kOne - 1;
   const int lane = threadIdx.x & 31;
   uint64_t prefix = 0;
@@ -148,17 +152,22 @@ __device__ __forceinline__ uint64_t warp_radix_max_key(int len, KeyFn key_of, We
     for (int k = 0; k < 8; ++k) hist[lane + 32 * k] = 0ull;
     __syncwarp();
     unsigned long long w0 = 0;
+    int c0 = 0;  // a key of digit 0 seen by this lane
     for (int c = lane; c < len; c += 32) {
       if (!eligible(c)) continue;
       const uint64_t key = key_of(c);
       if ((key >> (shift + 8)) != prefix) continue;
       const int d = static_cast<int>((key >> shift) & 255u);
       const unsigned long long w = kOne + weight_of(c, key);
-      if (d == 0)
+      if (d == 0) {
         w0 += w;
-      else
+        c0 = c;
+      } else {
         atomicAdd(&hist[d], w);
+        last[d] = static_cast<unsigned short>(c);  // any writer: read only when the digit holds one key
+      }
     }
+    const bool has0 = w0 != 0;
     w0 = warp_sum(w0);
     __syncwarp();
     if (lane == 0) hist[0] = w0;  // digit 0 takes no atomics
@@ -197,14 +206,18 @@ __device__ __forceinline__ uint64_t warp_radix_max_key(int len, KeyFn key_of, We
     prefix = (prefix << 8) | static_cast<uint64_t>(digit);
     above = new_above;
     if (single == 1ull && shift > 0) {
-      uint64_t x = 0;
-      for (int c = lane; c < len; c += 32)
-        if (eligible(c) && (key_of(c) >> shift) == prefix) x = key_of(c);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x |= __shfl_xor_sync(0xffffffffu, x, o);
-      return x;
+      // One eligible key carries the decided digits: the goal is reached at
+      // it and not above it, so it is the answer.
+      int c;
+      if (digit == 0) {
+        const unsigned int own = __ballot_sync(0xffffffffu, has0);  // the one lane that saw it
+        c = __shfl_sync(0xffffffffu, c0, own ? __ffs(own) - 1 : 0);
+      } else {
+        c = last[digit];
+      }
+      return key_of(c);
     }
-    __syncwarp();  // every lane has read hist before the next pass clears it
+    __syncwarp();  // every lane has read hist and last before the next pass writes them
   }
   return prefix;
 }
