@@ -309,7 +309,10 @@ CRISP_API crisp_status crisp_select_vs(const crisp_shape* shape, const crisp_par
  * and k (a short last block averaged over its own tokens),
  * pbar[h][b][c] = softmax over c <= b of scale * qbar_b . kbar_c, and 0 for
  * c > b. Rows of VS heads are not written. q, k bf16; pbar fp32
- * [hq][nb][nb], 16-byte aligned. */
+ * [hq][nb][nb], 16-byte aligned. Precision: the means are summed in fp32 and
+ * held as hi + lo bf16 pairs (16 significant bits); the logits accumulate
+ * hi.hi + hi.lo + lo.hi in fp32 on the tensor cores (lo.lo, 2^-16 of a
+ * product, is left out). */
 CRISP_API crisp_status crisp_pe_pool(const crisp_shape* shape, const void* q, const void* k, const uint8_t* route,
                                      float* pbar, void* ws, size_t ws_bytes, crisp_stream_t stream);
 
