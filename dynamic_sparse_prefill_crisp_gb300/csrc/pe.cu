@@ -144,7 +144,8 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
 // walks the column tiles ct <= bt twice: pass 1 keeps each row's running max
 // and sum of 2^(z - max) (z = scale log2(e) qbar . kbar), pass 2 forms the
 // same products again and writes p = 2^(z - max) / sum for c <= b and 0 for
-// b < c < nb, so the logits never go to memory. TMA double-buffers
+// b < c < nb (the zeros right of the row tile first, while the first
+// products are in flight), so the logits never go to memory. TMA double-buffers
 // B = kbar rows, the MMA thread alternates two TMEM accumulators, and eight
 // epilogue warps (two per TMEM lane quarter, one per 64-column half) read
 // the accumulators; each 32x16 piece of P goes through shared memory so that
@@ -153,17 +154,17 @@ constexpr int kPT = 128;                            // tile edge
 constexpr uint32_t kPTile = kPT * kD * 2;           // 32 KB: one bf16 128x128 operand
 constexpr uint32_t kPHalf = kPTile / 2;             // one 64-feature half
 constexpr int kPStage = 32 * 20;                    // an epilogue warp's 32x16 fp32 transpose (padded rows)
-constexpr int kScoresThreads = 320;                 // TMA warp, MMA warp, 8 epilogue warps
-constexpr uint32_t kScoresSmem = 1024 + 6 * kPTile + 8 * kPStage * 4;  // A, two B stages, eight transposes
+constexpr int kMapThreads = 320;                 // TMA warp, MMA warp, 8 epilogue warps
+constexpr uint32_t kMapSmem = 1024 + 6 * kPTile + 8 * kPStage * 4;  // A, two B stages, eight transposes
 
-struct ScoresBars {
+struct MapBars {
   uint64_t a_full, a_empty, b_full[2], b_empty[2], d_full[2], d_empty[2], xbar, drain;
   uint32_t tmem_base;
   int abort;
   float2 stats[2][kPT];  // (max, sum) of each row of the item's tile, per column half
 };
 
-__global__ void __launch_bounds__(kScoresThreads, 1)
+__global__ void __launch_bounds__(kMapThreads, 1)
     pooled_map(const __grid_constant__ CUtensorMap tq_hi, const __grid_constant__ CUtensorMap tq_lo,
                const __grid_constant__ CUtensorMap tk_hi, const __grid_constant__ CUtensorMap tk_lo,
                const uint8_t* __restrict__ route, int hq, int nb, int group, float c_log2,
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
   uint8_t* sA = base;                 // hi, lo
   uint8_t* sB = base + 2 * kPTile;    // stage s: hi, lo at + 2 * kPTile * s
   float* sT = reinterpret_cast<float*>(base + 6 * kPTile);  // epilogue warp e: sT + e * kPStage
-  __shared__ ScoresBars bars;
+  __shared__ MapBars bars;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     bars.abort = 0;
@@ -579,11 +580,11 @@ cudaError_t launch_pe_map(const crisp_shape& s, const void* q, const void* k, co
   if (!encode_bf16_rows(&tq_hi, qbar, s.hq, nb) || !encode_bf16_rows(&tq_lo, qbar + q_half, s.hq, nb) ||
       !encode_bf16_rows(&tk_hi, kbar, s.hkv, nb) || !encode_bf16_rows(&tk_lo, kbar + k_half, s.hkv, nb))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(pooled_map, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoresSmem);
+  cudaError_t e = cudaFuncSetAttribute(pooled_map, cudaFuncAttributeMaxDynamicSharedMemorySize, kMapSmem);
   if (e != cudaSuccess) return e;
   const int64_t T = (nb + kPT - 1) / kPT;
-  pooled_map<<<static_cast<unsigned>(std::min<int64_t>(sms, static_cast<int64_t>(s.hq) * T)), kScoresThreads,
-               kScoresSmem, st>>>(tq_hi, tq_lo, tk_hi, tk_lo, route, s.hq, nb, s.hq / s.hkv,
+  pooled_map<<<static_cast<unsigned>(std::min<int64_t>(sms, static_cast<int64_t>(s.hq) * T)), kMapThreads,
+               kMapSmem, st>>>(tq_hi, tq_lo, tk_hi, tk_lo, route, s.hq, nb, s.hq / s.hkv,
                                   s.scale * 1.4426950408889634f, pbar, status);
   return cudaGetLastError();
 }
