@@ -233,6 +233,50 @@ def test_custom_scale_and_mixed_layouts():
     check_attention(q, k, v, r["out"], rb, scale=scale)
 
 
+POOLED_CASES = [
+    # hq, hkv, n, seed, scale (0: 1/sqrt(128))
+    (4, 1, 256, 91, 0.0),      # the shortest layer the steps take: two blocks, one row tile
+    (4, 2, 257, 92, 0.0),      # a one-token last block
+    (8, 2, 131201, 93, 0.0),   # nb = 1026: nine row tiles, rows longer than the 1,024 kept in shared memory
+    (4, 1, 4096, 94, 1.0),     # wide pooled logits
+]
+
+
+@pytest.mark.parametrize("hq,hkv,n,seed,scale", POOLED_CASES, ids=["n256", "n257", "nb1026", "scale1"])
+def test_pooled_map_and_pe_selection_every_head(hq, hkv, n, seed, scale):
+    # Every head routed to PE: the tensor-core pooled map against the fp64
+    # estimate at the map tolerance (zeros above the diagonal exactly), and
+    # both PE selection modes bit-exact against the oracle on the GPU's map.
+    w = synth.small("pooled", hq, hkv, n, seed)
+    q, k, _ = w.generate()
+    nb = crisp.num_blocks(n)
+    W = (nb + 31) // 32
+    qd, kd = to_dev(q), to_dev(k)
+    s = crisp.make_shape(hq, hkv, n, qd, kd, None, scale=scale)
+    ws = new_workspace(s)
+    route = torch.zeros((hq,), dtype=torch.uint8, device="cuda")
+    pbar = torch.full((hq, nb, nb), float("nan"), dtype=torch.float32, device="cuda")
+    crisp.pe_pool(s, qd, kd, route, pbar, ws)
+    torch.cuda.synchronize()
+    assert_status_ok(ws)
+    got = pbar.cpu().numpy()
+    assert np.isfinite(got).all()
+    upper = np.triu(np.ones((nb, nb), dtype=bool), 1)
+    assert (got[:, upper] == 0.0).all()
+    check_map(got, oracle.pe_map(q, k, scale=scale if scale > 0 else None))
+    route_h = route.cpu().numpy()
+    for mode in (crisp.PE_GAMMA, crisp.PE_NOISE):
+        params = crisp.params_default()
+        params.pe_mode = mode
+        pebits = empty((hq, nb, W), torch.int32)
+        crisp.select_pe(s, params, pbar, route, pebits, ws)
+        torch.cuda.synchronize()
+        assert_status_ok(ws)
+        ref = oracle.select_pe(got, route_h, pe_mode=mode, gamma=(params.gamma_num, params.gamma_den),
+                               alpha=(params.alpha_num, params.alpha_den), kmin=params.kmin_blocks)
+        assert np.array_equal(ref, pebits.cpu().numpy().view(np.uint32))
+
+
 def test_attention_convenience_call_matches_the_layer():
     # crisp.attention allocates the output and workspace with torch and runs
     # the same layer call: identical bits, ragged length included.
