@@ -304,19 +304,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
         bool go = mbar_wait(&bars.q_full, 0, &bars.abort);
         if (!go) fail(&bars.abort, status, 0x203);
-        const uint32_t qa = smem_u32(sQ);
+        const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
         // S_s = Q K_s^T (8 steps of 16 features) into buffer s.
         auto issue_qk = [&](int s) -> bool {
           if (!mbar_wait(&bars.k_full[s], kn[s] & 1u, &bars.abort)) return false;
           ++kn[s];
           tc_fence_after();
-          const uint32_t ka = smem_u32(sK + s * kSub);
+          const uint64_t dk = sdesc_sw128(smem_u32(sK + s * kSub), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
+            // the start-address field is (address >> 4) in the low 14 bits;
+            // shared addresses stay below 2^18, so adding offset >> 4 never carries
             const uint32_t qoff = (kk >> 2) * kHalf + (kk & 3) * 32;
             const uint32_t koff = (kk >> 2) * kSubHalf + (kk & 3) * 32;
-            umma_ss(tmem + s * kSubKeys, sdesc_sw128(qa + qoff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024),
-                    idesc_qk, kk > 0);
+            umma_ss(tmem + s * kSubKeys, dq + (qoff >> 4), dk + (koff >> 4), idesc_qk, kk > 0);
           }
           umma_commit(&bars.k_empty[s]);
           umma_commit(&bars.s_full[s]);
@@ -330,12 +331,11 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (!mbar_wait(&bars.v_full[s], vn[s] & 1u, &bars.abort)) return false;
           ++vn[s];
           tc_fence_after();
-          const uint32_t va = smem_u32(sV + s * kSub);
+          const uint64_t dv = sdesc_sw128(smem_u32(sV + s * kSub), kSubHalf, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t pa = tmem + s * kSubKeys + (kk >> 1) * 32 + 16 + (kk & 1) * 8;
-            umma_ts(tmem + 128, pa, sdesc_sw128(va + kk * 2048, kSubHalf, 1024), idesc_pv,
-                    (first && kk == 0) ? 0u : 1u);
+            umma_ts(tmem + 128, pa, dv + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
           }
           umma_commit(&bars.v_empty[s]);
           return true;
