@@ -69,6 +69,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* a
   return __all_sync(0xffffffffu, ok);
 }
 
+// Two 16-bit counters (one per slot s = 0, 1) in one register, so that a
+// slot picked at run time costs shifts, not a local-memory array.
+struct SlotCounts {
+  uint32_t v = 0u;
+  __device__ __forceinline__ uint32_t parity(int s) const { return (v >> (16 * s)) & 1u; }
+  __device__ __forceinline__ void inc(int s) { v += 1u << (16 * s); }
+};
+
 __device__ __forceinline__ void fail(int* abort, DevStatus* st, uint32_t where) {
   *reinterpret_cast<volatile int*>(abort) = 1;
   report_error(st, CRISP_ERR_TIMEOUT, where);
@@ -192,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // Phase counters that persist across passes (each role counts its own).
   uint32_t kn[2] = {0u, 0u}, vn[2] = {0u, 0u};  // TMA: loads issued per slot; MMA: loads consumed per slot
-  uint32_t pn[2] = {0u, 0u};                    // MMA: p_full phases consumed per slot
-  uint32_t sn[2] = {0u, 0u};                    // softmax: s_full phases consumed per slot
+  SlotCounts pn;                                // MMA: p_full phases consumed per slot
+  SlotCounts sn;                                // softmax: s_full phases consumed per slot
   uint32_t drains = 0u, o_phase = 0u, x_phase = 0u;
   // Softmax state (per thread: one row, one 32-column chunk).
   const int quarter = warp & 3, chunk = warp >> 2;
@@ -326,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         // O += P_s V_s (4 steps of 16 keys); P_s of chunk c at columns
         // 64s + 32c + 16 .. +15 (bf16 pairs, 8 columns per 16 keys).
         auto issue_pv = [&](int s, bool first) -> bool {
-          if (!mbar_wait(&bars.p_full[s], pn[s] & 1u, &bars.abort)) return false;
-          ++pn[s];
+          if (!mbar_wait(&bars.p_full[s], pn.parity(s), &bars.abort)) return false;
+          pn.inc(s);
           if (!mbar_wait(&bars.v_full[s], vn[s] & 1u, &bars.abort)) return false;
           ++vn[s];
           tc_fence_after();
@@ -359,14 +367,14 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int i = 0; go && i < nsub; ++i) {
             const int s = i & 1;
             if (i >= 2) {
-              go = mbar_wait(&bars.p_full[s], pn[s] & 1u, &bars.abort);
-              if (go) ++pn[s];
+              go = mbar_wait(&bars.p_full[s], pn.parity(s), &bars.abort);
+              if (go) pn.inc(s);
             }
             if (go) go = issue_qk(s);
           }
           for (int s = 0; go && s < 2 && s < nsub; ++s) {
-            go = mbar_wait(&bars.p_full[s], pn[s] & 1u, &bars.abort);
-            if (go) ++pn[s];
+            go = mbar_wait(&bars.p_full[s], pn.parity(s), &bars.abort);
+            if (go) pn.inc(s);
           }
         }
         if (!go) fail(&bars.abort, status, 0x204);
@@ -385,12 +393,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (mode != kMaxOnly) l = 0.f;
       for (int i = 0; ok && i < nsub; ++i) {
         const int s = i & 1, j = i >> 1;
-        if (!warp_wait(&bars.s_full[s], sn[s] & 1u, &bars.abort)) {
+        if (!warp_wait(&bars.s_full[s], sn.parity(s), &bars.abort)) {
           if (lane == 0) fail(&bars.abort, status, 0x207);
           ok = false;
           break;
         }
-        ++sn[s];
+        sn.inc(s);
         tc_fence_after();
         const bool diag = bars.has_diag && j == count - 1;  // ascending order: qb is last
         const int key0 = s * kSubKeys + chunk * 32;          // key index in the block of column 0
