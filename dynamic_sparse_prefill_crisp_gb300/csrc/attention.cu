@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         };
         auto load = [&](bool is_k, int t, int kb) -> bool {
           const int s = t & 1;
-          uint64_t* empty = is_k ? &bars.k_empty[s] : &bars.v_empty[s];
+          // K slot s is free once the scores of its last sub-block are formed
+          uint64_t* empty = is_k ? &bars.s_full[s] : &bars.v_empty[s];
           uint64_t* full = is_k ? &bars.k_full[s] : &bars.v_full[s];
           uint32_t& cnt = is_k ? kn[s] : vn[s];
           if (!mbar_wait(empty, (cnt & 1u) ^ 1u, &bars.abort)) {
@@ -313,12 +314,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         bool go = mbar_wait(&bars.q_full, 0, &bars.abort);
         if (!go) fail(&bars.abort, status, 0x203);
         const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dk0 = sdesc_sw128(smem_u32(sK), 16, 1024), dk1 = dk0 + (kSub >> 4);
+        const uint64_t dv0 = sdesc_sw128(smem_u32(sV), kSubHalf, 1024), dv1 = dv0 + (kSub >> 4);
         // S_s = Q K_s^T (8 steps of 16 features) into buffer s.
         auto issue_qk = [&](int s) -> bool {
           if (!mbar_wait(&bars.k_full[s], kn[s] & 1u, &bars.abort)) return false;
           ++kn[s];
           tc_fence_after();
-          const uint64_t dk = sdesc_sw128(smem_u32(sK + s * kSub), 16, 1024);
+          const uint64_t dk = s ? dk1 : dk0;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             // the start-address field is (address >> 4) in the low 14 bits;
@@ -327,7 +330,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint32_t koff = (kk >> 2) * kSubHalf + (kk & 3) * 32;
             umma_ss(tmem + s * kSubKeys, dq + (qoff >> 4), dk + (koff >> 4), idesc_qk, kk > 0);
           }
-          umma_commit(&bars.k_empty[s]);
           umma_commit(&bars.s_full[s]);
           return true;
         };
@@ -339,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (!mbar_wait(&bars.v_full[s], vn[s] & 1u, &bars.abort)) return false;
           ++vn[s];
           tc_fence_after();
-          const uint64_t dv = sdesc_sw128(smem_u32(sV + s * kSub), kSubHalf, 1024);
+          const uint64_t dv = s ? dv1 : dv0;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t pa = tmem + s * kSubKeys + (kk >> 1) * 32 + 16 + (kk & 1) * 8;
