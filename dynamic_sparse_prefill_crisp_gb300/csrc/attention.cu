@@ -102,6 +102,54 @@ __device__ __forceinline__ void p_exp32(const uint32_t (&sv)[32], float c, float
   sum += (sa0 + sa1) + (sb0 + sb1);
 }
 
+// S = Q K^T over 128 features as eight K = 16 products in one asm block:
+// step kk reads A (Q) and B (K) at descriptor start addresses advanced by
+// 2 (kk % 4) + (kk / 4) * a_half (resp. b_half) 16-byte units; the first
+// step overwrites D. One predicate pair serves all eight.
+template <uint32_t kAHalf, uint32_t kBHalf>
+__device__ __forceinline__ void umma_qk_x8(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred f, t;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 f, %3, %3;\n\t"
+      "setp.eq.b32 t, %3, %3;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+      "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, %4;\n\tadd.s64 b, %2, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, %4 + 2;\n\tadd.s64 b, %2, %5 + 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, %4 + 4;\n\tadd.s64 b, %2, %5 + 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, %1, %4 + 6;\n\tadd.s64 b, %2, %5 + 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t}\n" ::"r"(d),
+      "l"(da), "l"(db), "r"(idesc), "n"(kAHalf), "n"(kBHalf)
+      : "memory");
+}
+
+// O += P V over 64 keys as four K = 16 products in one asm block: step kk
+// reads P from TMEM column pa + 32 (kk / 2) + 8 (kk % 2) and V 16 keys
+// (128 16-byte units) further on; the first step accumulates iff acc0.
+__device__ __forceinline__ void umma_pv_x4(uint32_t d, uint32_t pa, uint64_t dv, uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b32 ta;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %3, %3;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 ta, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
+      "add.u32 ta, %1, 32;\n\tadd.s64 b, %2, 256;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
+      "add.u32 ta, %1, 40;\n\tadd.s64 b, %2, 384;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t}\n" ::"r"(d),
+      "r"(pa), "l"(dv), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
 // Keys above the row on the diagonal block (key index col0 + e > r) -> -inf.
 __device__ __forceinline__ void mask_diag32(int col0, int r, uint32_t (&sv)[32]) {
 #pragma unroll
@@ -322,14 +370,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           ++kn[s];
           tc_fence_after();
           const uint64_t dk = s ? dk1 : dk0;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // the start-address field is (address >> 4) in the low 14 bits;
-            // shared addresses stay below 2^18, so adding offset >> 4 never carries
-            const uint32_t qoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-            const uint32_t koff = (kk >> 2) * kSubHalf + (kk & 3) * 32;
-            umma_ss(tmem + s * kSubKeys, dq + (qoff >> 4), dk + (koff >> 4), idesc_qk, kk > 0);
-          }
+          // the start-address field is (address >> 4) in the low 14 bits;
+          // shared addresses stay below 2^18, so adding offset >> 4 never carries
+          umma_qk_x8<(kHalf >> 4), (kSubHalf >> 4)>(tmem + s * kSubKeys, dq, dk, idesc_qk);
           umma_commit(&bars.s_full[s]);
           return true;
         };
@@ -342,11 +385,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           ++vn[s];
           tc_fence_after();
           const uint64_t dv = s ? dv1 : dv0;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t pa = tmem + s * kSubKeys + (kk >> 1) * 32 + 16 + (kk & 1) * 8;
-            umma_ts(tmem + 128, pa, dv + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
-          }
+          umma_pv_x4(tmem + 128, tmem + s * kSubKeys + 16, dv, idesc_pv, first ? 0u : 1u);
           umma_commit(&bars.v_empty[s]);
           return true;
         };
