@@ -51,7 +51,7 @@ enum Mode : int { kFast = 0, kMaxOnly = 1, kFixed = 2 };
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t k_full[2], v_full[2], v_empty[2];  // a K slot is free again once s_full of its sub-block completes
   uint64_t s_full[2], p_full[2];
   uint64_t o_full, drain;
   uint64_t xbar[4];      // per lane quarter: both warps have written their partial row maxima
@@ -214,7 +214,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&bars.q_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.k_full[s], 1);
-      mbar_init(&bars.k_empty[s], 1);
       mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.v_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
